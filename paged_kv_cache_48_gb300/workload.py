@@ -1,0 +1,373 @@
+"""Seeded synthetic decode workloads for the paged KV-cache path.
+
+This module only draws inputs: sequence lengths, a shuffled physical block
+pool with reference counts, per-sequence block tables, slot mappings, query
+and key/value values, the list of freshly allocated blocks and the initial
+(stale) bytes of the pool.  It performs none of the method's arithmetic (no
+write, zeroing, quantisation or attention), so both the CUDA path and the
+CPU oracle consume exactly the same inputs from here.
+
+Structure follows the vLLM pages:
+ - vLLM concept page (compassingai.com), "15 分钟专家深入" item 2: blocks of
+   16 tokens, a page table per sequence, blocks allocated on demand, shared
+   prompt prefixes pointing at the same physical blocks;
+ - vLLM internals (naphjohn.github.io), §1.1 and Figure 1: blocks scattered
+   anywhere in the pool, reference counts on shared prefix blocks, at most
+   one partially filled block per sequence;
+ - vLLM v0.17.1 notes (admirer.cn), "重点：35219": recycled blocks still hold
+   fp32 bit patterns (NaN/Inf among them) when they are handed out again.
+"""
+from __future__ import annotations
+
+from collections import deque
+from dataclasses import dataclass, field
+
+import numpy as np
+
+BLOCK_SIZE = 16
+
+# Explicit fp32 bit patterns planted in recycled blocks: quiet NaN, +Inf, -Inf.
+STALE_PATTERNS = (0x7FC00000, 0x7F800000, 0xFF800000)
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (nearest, ties to even) and return
+    the 16-bit patterns.  Used only to draw bf16 inputs."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if not np.isfinite(x).all():
+        raise ValueError("bf16_bits draws finite values only")
+    u = x.view(np.uint32)
+    rounded = (u + np.uint32(0x7FFF) + ((u >> 16) & np.uint32(1))) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bf16_values(bits: np.ndarray) -> np.ndarray:
+    """The float32 value of bfloat16 bit patterns (exact)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(
+        np.float32)
+
+
+class BlockPool:
+    """Physical block pool with a seeded shuffled free list and reference
+    counts.  A block with refcount > 1 is shared (a common prompt prefix);
+    freeing drops one reference and returns the block to the pool when the
+    count reaches zero."""
+
+    def __init__(self, num_blocks: int, rng: np.random.Generator):
+        self.num_blocks = int(num_blocks)
+        self.free_list = deque(int(b) for b in rng.permutation(self.num_blocks))
+        self.refcount = np.zeros(self.num_blocks, dtype=np.int32)
+
+    @property
+    def used(self) -> int:
+        return int(np.count_nonzero(self.refcount))
+
+    def allocate(self) -> int:
+        if not self.free_list:
+            raise RuntimeError("block pool exhausted")
+        b = self.free_list.popleft()
+        self.refcount[b] = 1
+        return b
+
+    def share(self, block: int) -> int:
+        if self.refcount[block] <= 0:
+            raise ValueError("sharing a free block")
+        self.refcount[block] += 1
+        return block
+
+    def free(self, block: int) -> None:
+        if self.refcount[block] <= 0:
+            raise ValueError("double free")
+        self.refcount[block] -= 1
+        if self.refcount[block] == 0:
+            self.free_list.append(int(block))
+
+
+@dataclass
+class Workload:
+    """One decode step's inputs plus the history that precedes it."""
+    name: str
+    batch: int
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    kv_dtype: str                 # "bf16" or "fp8_e4m3"
+    num_blocks: int
+    max_blocks: int
+    seq_lens: np.ndarray          # int32 [B]
+    block_tables: np.ndarray      # int32 [B, max_blocks], -1 = unused
+    q: np.ndarray                 # uint16 bf16 bits [B, Hq, d]
+    hist_k: np.ndarray            # uint16 [Th, Hkv, d] written at set-up
+    hist_v: np.ndarray
+    hist_slots: np.ndarray        # int64 [Th]
+    step_k: np.ndarray            # uint16 [Ts, Hkv, d] written in the step
+    step_v: np.ndarray
+    step_slots: np.ndarray        # int64 [Ts]
+    fresh_blocks: np.ndarray      # int32 [n] zeroed in the step
+    init_key: np.ndarray          # uint8 [NB * block_bytes] pool bytes
+    init_value: np.ndarray
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+    scale: float = 0.0
+    block_size: int = BLOCK_SIZE
+    refcount: np.ndarray = field(default=None)   # int32 [NB]
+    groups: list = field(default_factory=list)   # prefix-sharing groups
+    seed: int = 0
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.kv_dtype == "bf16" else 1
+
+    @property
+    def block_bytes(self) -> int:
+        return self.block_size * self.num_kv_heads * self.head_dim * self.elem_bytes
+
+    @property
+    def group_size(self) -> int:
+        return self.num_heads // self.num_kv_heads
+
+    @property
+    def max_seq_len(self) -> int:
+        return int(self.seq_lens.max()) if self.batch else 0
+
+    def kv_read_bytes(self) -> int:
+        """Algorithmic K+V bytes one decode step reads (logical, per
+        sequence; shared prefix blocks count once per sequence)."""
+        return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * \
+            self.head_dim * 2 * self.elem_bytes
+
+    def unique_kv_read_bytes(self) -> int:
+        """K+V bytes of the distinct cached tokens the step reads."""
+        seen = {}
+        for b in range(self.batch):
+            L = int(self.seq_lens[b])
+            for j in range((L + self.block_size - 1) // self.block_size):
+                blk = int(self.block_tables[b, j])
+                n = min(self.block_size, L - j * self.block_size)
+                seen[blk] = max(seen.get(blk, 0), n)
+        return sum(seen.values()) * self.num_kv_heads * self.head_dim * 2 * \
+            self.elem_bytes
+
+
+def _draw_bf16(rng: np.random.Generator, shape) -> np.ndarray:
+    return bf16_bits(rng.standard_normal(size=shape, dtype=np.float32))
+
+
+def make_workload(name: str, batch: int, num_heads: int, num_kv_heads: int,
+                  head_dim: int, len_lo: int, len_hi: int, seed: int,
+                  kv_dtype: str = "bf16", pool_factor: float = 1.2,
+                  seq_lens=None, num_blocks=None, max_len=None,
+                  prefix_groups: int = 0, prefix_len: int = 0,
+                  fresh_policy: str = "new_token") -> Workload:
+    """Draw one workload.
+
+    seq_lens uniform in [len_lo, len_hi] unless given.  The pool holds
+    ceil(pool_factor * blocks needed) blocks (or ``num_blocks``), handed out
+    in a seeded shuffled order.  With ``prefix_groups`` > 0 the batch is cut
+    into that many equal groups whose first ``prefix_len`` tokens (a whole
+    number of blocks) share the same physical blocks; seq_lens then count
+    the prefix plus a private suffix drawn from [len_lo, len_hi].
+
+    fresh_policy:
+      "new_token"  -- a block is fresh when the step's new token (position
+                      L-1) is its first slot;
+      "recycle515" -- the last four logical blocks of every sequence plus the
+                      fifth-last block of sequences 0, 1 and 2.
+    Tokens that live in fresh blocks, and every sequence's new token, are
+    written during the step (after zeroing); all others at set-up.
+    """
+    bs = BLOCK_SIZE
+    rng = np.random.default_rng(seed)
+    if seq_lens is None:
+        lens = rng.integers(len_lo, len_hi + 1, size=batch).astype(np.int64)
+    else:
+        lens = np.asarray(seq_lens, dtype=np.int64)
+    if prefix_groups:
+        assert prefix_len % bs == 0 and batch % prefix_groups == 0
+        lens = lens + prefix_len
+    nblk = (lens + bs - 1) // bs
+    if max_len is None:
+        max_len = int(lens.max()) if batch else 0
+    max_blocks = max(1, (int(max_len) + bs - 1) // bs)
+    prefix_blocks = prefix_len // bs
+    if prefix_groups:
+        needed = prefix_groups * prefix_blocks + int((nblk - prefix_blocks).sum())
+    else:
+        needed = int(nblk.sum())
+    if num_blocks is None:
+        num_blocks = int(np.ceil(pool_factor * needed))
+    pool = BlockPool(num_blocks, rng)
+
+    tables = np.full((batch, max_blocks), -1, dtype=np.int32)
+    groups = []
+    if prefix_groups:
+        per = batch // prefix_groups
+        for gi in range(prefix_groups):
+            shared = [pool.allocate() for _ in range(prefix_blocks)]
+            members = list(range(gi * per, (gi + 1) * per))
+            groups.append({"members": members, "prefix_blocks": shared})
+            for b in members:
+                for j, blk in enumerate(shared):
+                    tables[b, j] = pool.share(blk) if b != members[0] else blk
+                for j in range(prefix_blocks, int(nblk[b])):
+                    tables[b, j] = pool.allocate()
+    else:
+        for b in range(batch):
+            for j in range(int(nblk[b])):
+                tables[b, j] = pool.allocate()
+
+    fresh = []
+    if fresh_policy == "new_token":
+        for b in range(batch):
+            L = int(lens[b])
+            if L > 0 and (L - 1) % bs == 0:
+                fresh.append(int(tables[b, (L - 1) // bs]))
+    elif fresh_policy == "recycle515":
+        for b in range(batch):
+            n = int(nblk[b])
+            take = 5 if b < 3 else 4
+            for j in range(max(0, n - take), n):
+                fresh.append(int(tables[b, j]))
+    elif fresh_policy != "none":
+        raise ValueError(fresh_policy)
+    fresh_set = set(fresh)
+
+    # Token positions: shared prefix tokens once per group, then each
+    # sequence's private tokens.
+    hkd = (num_kv_heads, head_dim)
+    fresh_arr = np.asarray(sorted(fresh_set), dtype=np.int64)
+    hist_parts, step_parts = [], []
+    for grp in groups:
+        t = np.arange(prefix_len, dtype=np.int64)
+        blks = np.asarray(grp["prefix_blocks"], dtype=np.int64)[t // bs]
+        hist_parts.append(blks * bs + t % bs)
+    for b in range(batch):
+        L = int(lens[b])
+        start = prefix_len if prefix_groups else 0
+        t = np.arange(start, L, dtype=np.int64)
+        blks = tables[b, t // bs].astype(np.int64)
+        slots = blks * bs + t % bs
+        in_step = np.isin(blks, fresh_arr) | (t == L - 1)
+        step_parts.append(slots[in_step])
+        hist_parts.append(slots[~in_step])
+    hist_slots = np.concatenate(hist_parts) if hist_parts else \
+        np.zeros(0, np.int64)
+    step_slots = np.concatenate(step_parts) if step_parts else \
+        np.zeros(0, np.int64)
+
+    q = _draw_bf16(rng, (batch, num_heads, head_dim))
+    hist_k = _draw_bf16(rng, (hist_slots.size, *hkd))
+    hist_v = _draw_bf16(rng, (hist_slots.size, *hkd))
+    step_k = _draw_bf16(rng, (step_slots.size, *hkd))
+    step_v = _draw_bf16(rng, (step_slots.size, *hkd))
+
+    k_scale = v_scale = 1.0
+    if kv_dtype == "fp8_e4m3":
+        # per-tensor scale: largest magnitude written maps to 448, the
+        # largest finite E4M3 value.
+        def amax(*arrs):
+            m = 0.0
+            for a in arrs:
+                if a.size:
+                    m = max(m, float(np.abs(bf16_values(a)).max()))
+            return m
+        k_scale = float(np.float32(amax(hist_k, step_k) / 448.0))
+        v_scale = float(np.float32(amax(hist_v, step_v) / 448.0))
+    elif kv_dtype != "bf16":
+        raise ValueError(kv_dtype)
+
+    eb = 2 if kv_dtype == "bf16" else 1
+    block_bytes = bs * num_kv_heads * head_dim * eb
+    # Pool bytes before the step: 0xFF everywhere (NaN in bf16 and in E4M3,
+    # so any read of a slot that is not part of a sequence is visible), and
+    # random fp32 words with planted NaN/Inf in the freshly allocated blocks.
+    init_key = np.full(num_blocks * block_bytes, 0xFF, dtype=np.uint8)
+    init_value = np.full(num_blocks * block_bytes, 0xFF, dtype=np.uint8)
+    for arr in (init_key, init_value):
+        for blk in fresh:
+            words = rng.integers(0, 2**32, size=block_bytes // 4,
+                                 dtype=np.uint64).astype(np.uint32)
+            words[: len(STALE_PATTERNS)] = STALE_PATTERNS
+            pos = rng.integers(0, words.size, size=len(STALE_PATTERNS))
+            words[pos] = STALE_PATTERNS
+            arr[blk * block_bytes:(blk + 1) * block_bytes] = words.view(np.uint8)
+
+    return Workload(
+        name=name, batch=batch, num_heads=num_heads,
+        num_kv_heads=num_kv_heads, head_dim=head_dim, kv_dtype=kv_dtype,
+        num_blocks=num_blocks, max_blocks=max_blocks,
+        seq_lens=lens.astype(np.int32), block_tables=tables, q=q,
+        hist_k=hist_k, hist_v=hist_v, hist_slots=hist_slots,
+        step_k=step_k, step_v=step_v, step_slots=step_slots,
+        fresh_blocks=np.asarray(fresh, dtype=np.int32),
+        init_key=init_key, init_value=init_value, k_scale=k_scale,
+        v_scale=v_scale, scale=1.0 / float(np.sqrt(head_dim)),
+        refcount=pool.refcount.copy(), groups=groups, seed=seed)
+
+
+# ---------------------------------------------------------------------------
+# The five decode workloads, full size and a small variant of each that the
+# fp64 oracle finishes in seconds while still spanning several blocks,
+# several 512-token partitions and a ragged last block.
+# ---------------------------------------------------------------------------
+
+def tiny_mha(seed: int = 0) -> Workload:
+    """4 sequences, lengths {1,17,33,64}, 8 q = 8 kv heads, head_dim 64,
+    a 64-block pool whose blocks are taken in a seeded permuted order."""
+    return make_workload("tiny_mha", 4, 8, 8, 64, 0, 0, seed,
+                         seq_lens=[1, 17, 33, 64], num_blocks=64)
+
+
+def llama8b_gqa(seed: int = 5, small: bool = False) -> Workload:
+    """Llama-8B-shaped GQA decode: 32 q / 8 kv heads, head_dim 128,
+    seq_lens uniform in [512, 4096], pool 20% larger than needed.  The
+    default seed draws 4 sequences whose new token opens a block, the
+    expected count for 64 sequences and 16-token blocks."""
+    if small:
+        return make_workload("llama8b_gqa_small", 8, 32, 8, 128, 20, 700,
+                             seed)
+    return make_workload("llama8b_gqa", 64, 32, 8, 128, 512, 4096, seed,
+                         max_len=4096)
+
+
+def prefix_shared(seed: int = 2, small: bool = False) -> Workload:
+    """16 groups x 16 sequences sharing a 1024-token prefix (64 blocks,
+    refcount 16) plus private suffixes uniform in [32, 512]."""
+    if small:
+        return make_workload("prefix_shared_small", 8, 32, 8, 128, 5, 60,
+                             seed, prefix_groups=2, prefix_len=64)
+    return make_workload("prefix_shared", 256, 32, 8, 128, 32, 512, seed,
+                         prefix_groups=16, prefix_len=1024,
+                         max_len=1024 + 512)
+
+
+def long_context(seed: int = 3, small: bool = False) -> Workload:
+    """Long-context decode: batch 8, seq_lens uniform in [32768, 131072],
+    64 q / 8 kv heads, head_dim 128 (split into 512-token partitions)."""
+    if small:
+        return make_workload("long_context_small", 2, 64, 8, 128, 1500, 3000,
+                             seed)
+    return make_workload("long_context", 8, 64, 8, 128, 32768, 131072, seed,
+                         max_len=131072)
+
+
+def fp8_recycle(seed: int = 4, small: bool = False) -> Workload:
+    """fp8 E4M3 KV with a per-tensor scale, batch 128, 40 q / 8 kv heads,
+    head_dim 128, seq_lens uniform in [1024, 8192]; 515 recycled blocks
+    holding stale fp32 bit patterns are zeroed before the step's writes."""
+    if small:
+        return make_workload("fp8_recycle_small", 6, 40, 8, 128, 40, 300,
+                             seed, kv_dtype="fp8_e4m3",
+                             fresh_policy="recycle515")
+    return make_workload("fp8_recycle", 128, 40, 8, 128, 1024, 8192, seed,
+                         kv_dtype="fp8_e4m3", fresh_policy="recycle515",
+                         max_len=8192)
+
+
+CONFIGS = {
+    "tiny_mha": tiny_mha,
+    "llama8b_gqa": llama8b_gqa,
+    "prefix_shared": prefix_shared,
+    "long_context": long_context,
+    "fp8_recycle": fp8_recycle,
+}

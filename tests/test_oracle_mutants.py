@@ -1,0 +1,104 @@
+"""Plant plausible mistakes in copies of the CPU oracle and check that the
+pins catch every one of them (no GPU).
+
+Each mutant is a one-line textual change of oracle/pagedkv_oracle.c,
+compiled into a temporary library and run against every pin in a child
+process (a mutant that crashes counts as caught).  The real oracle must pass
+every pin (test_oracle_pins.py); each mutant must fail at least one.
+"""
+import subprocess
+import sys
+import textwrap
+from pathlib import Path
+
+import pytest
+
+import oracle
+
+ROOT = Path(__file__).resolve().parent.parent
+
+# (name, original text, mutated text)
+MUTANTS = [
+    ("drop_softmax_scale", "p[t] = a->scale * s;", "p[t] = s;"),
+    ("gqa_head_modulo", "const int kvh = h / group;",
+     "const int kvh = h % a->num_kv_heads;"),
+    ("no_max_subtraction", "p[t] = exp(p[t] - mx);", "p[t] = exp(p[t]);"),
+    ("no_normalisation", "double w = p[t] / denom;", "double w = p[t];"),
+    ("one_token_too_many", "const int L = a->seq_lens[b];",
+     "const int L = a->seq_lens[b] > 0 ? a->seq_lens[b] + 1 : 0;"),
+    ("value_read_from_key_cache",
+     "V[(size_t)t * d + i] = decode_elem(a->value_cache,",
+     "V[(size_t)t * d + i] = decode_elem(a->key_cache,"),
+    ("block_offset_ignored",
+     "(((size_t)blk * bs + (size_t)(t - j * bs)) * a->num_kv_heads +",
+     "(((size_t)blk * bs + (size_t)0) * a->num_kv_heads +"),
+    ("logical_block_as_physical",
+     "int32_t blk = a->block_tables[(size_t)b * a->max_blocks + j];",
+     "int32_t blk = j;"),
+    ("query_from_wrong_head",
+     "const uint16_t *qrow = a->q + ((size_t)b * a->num_heads + h) * d;",
+     "const uint16_t *qrow = a->q + ((size_t)b * a->num_heads + kvh) * d;"),
+    ("fp8_scale_not_applied",
+     "return oracle_e4m3_to_double(cache[idx]) * scale;",
+     "return oracle_e4m3_to_double(cache[idx]);"),
+    ("e4m3_bias_8", "mag = ldexp(1.0 + (double)m / 8.0, e - 7);",
+     "mag = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("e4m3_subnormal_exponent", "mag = ldexp((double)m / 8.0, -6);",
+     "mag = ldexp((double)m / 8.0, -7);"),
+    ("e4m3_ties_up", "code = (lo % 2 == 0) ? lo : lo + 1;", "code = lo + 1;"),
+    ("e4m3_truncate", "else if (a > half)", "else if (a > vhi)"),
+    ("e4m3_overflow_to_nan", "return (uint8_t)(sign | 0x7E);",
+     "return (uint8_t)(sign | 0x7F);"),
+    ("quantise_multiplies", "q = xf / scale;", "q = xf * scale;"),
+    ("bf16_wrong_shift", "uint32_t w = ((uint32_t)bits) << 16;",
+     "uint32_t w = ((uint32_t)bits) << 15;"),
+    ("write_skips_value",
+     "memcpy(value_cache + (base + e) * eb, &vb, 2);", "(void)vb;"),
+    ("write_swaps_block_offset", "off = s % block_size;",
+     "off = (s + 1) % block_size;"),
+    ("zero_skips_value_cache",
+     "memset(value_cache + (size_t)id * block_bytes, 0, block_bytes);",
+     "(void)value_cache;"),
+    ("zero_accepts_negative", "if (id < 0 || id >= num_blocks) {",
+     "if (id >= num_blocks) {"),
+    ("empty_sequence_not_zero", "out_row[i] = 0.0;", "out_row[i] = 1.0;"),
+]
+
+_RUNNER = textwrap.dedent("""
+    import sys
+    sys.path[:0] = [{root!r}, {tests!r}]
+    import oracle, oracle_pins
+    o = oracle.Oracle({lib!r})
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(o)
+        except Exception as e:
+            failed.append(pin.__name__)
+    print("FAILED", len(failed), ",".join(failed))
+""")
+
+
+def test_mutants_are_distinct_edits():
+    src = oracle.SOURCE.read_text()
+    for name, old, new in MUTANTS:
+        assert src.count(old) == 1, f"{name}: anchor not unique/present"
+        assert old != new
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, tmp_path):
+    src = oracle.SOURCE.read_text()
+    assert src.count(old) == 1
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.compile_library(mutated, tmp_path / "libmutant.so")
+    code = _RUNNER.format(root=str(ROOT), tests=str(ROOT / "tests"),
+                          lib=str(lib))
+    proc = subprocess.run([sys.executable, "-c", code], capture_output=True,
+                          text=True, timeout=300)
+    if proc.returncode != 0:
+        return  # the mutant crashed the pins: caught
+    line = [l for l in proc.stdout.splitlines() if l.startswith("FAILED")][-1]
+    n_failed = int(line.split()[1])
+    assert n_failed > 0, f"mutant {name} passed every pin"
