@@ -1,0 +1,401 @@
+"""Decode-step benchmark of the paged KV-cache path on GB300.
+
+One step = one pass of the whole hot path over one batch: zero the blocks
+the step freshly allocates, write each sequence's new token through its
+slot, then paged decode attention (with the split-KV reduce when the
+partitioning splits sequences).  Workload: Llama-8B-shaped GQA decode
+(batch 64, 32 q / 8 kv heads, head_dim 128, bf16 KV, seq_lens uniform in
+[512, 4096], 16-token blocks scattered over a pool 20% larger than needed).
+
+Prints one JSON line.  --impl reference times the fp64 CPU oracle on the
+same workload instead (a bounded sample of sequences per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = ("paged decode attention KV-read GB/s (% of GB300 HBM peak); "
+          "seq-steps/sec")
+L2_NOTE = "inputs larger than L2 (0.59 GB of KV read per step, L2 126 MB)"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE = ROOT / "profiles" / "paged_decode_kernel_llama8b_gqa.md"
+KERNEL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_decode.cu",
+                  "paged_kv_cache_48_gb300/csrc/pkv_device.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--partition-tokens", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-seqs", type=int, default=16)
+    return ap.parse_args()
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        h.update((ROOT / rel).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return float(json.loads(p.read_text())["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    if not PROFILE.exists():
+        return None
+    text = PROFILE.read_text()
+    sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not sha or not val or sha.group(1) != kernel_sha():
+        return None
+    return float(val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() in ("active", "0x1", "1"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_step(W, kc, vc, seqs, n_threads=0):
+    """The oracle's decode step on the sequences `seqs` (all heads)."""
+    import oracle
+    o = oracle.load()
+    dt = oracle.DTYPE_BF16 if W.kv_dtype == "bf16" else oracle.DTYPE_FP8_E4M3
+    o.zero_blocks(kc, vc, W.block_bytes, W.fresh_blocks)
+    o.kv_write(kc, vc, dt, W.block_size, W.num_kv_heads, W.head_dim,
+               W.k_scale, W.v_scale, W.step_k, W.step_v, W.step_slots)
+    pairs = np.array([(b, h) for b in seqs for h in range(W.num_heads)],
+                     dtype=np.int32)
+    out, err = o.attention_decode(W.q, kc, vc, dt, W.k_scale, W.v_scale,
+                                  W.block_size, W.num_kv_heads, W.head_dim,
+                                  W.block_tables, W.seq_lens, W.scale,
+                                  pairs=pairs, n_threads=n_threads)
+    assert err == 0
+    return out
+
+
+def oracle_setup(W):
+    import oracle
+    o = oracle.load()
+    dt = oracle.DTYPE_BF16 if W.kv_dtype == "bf16" else oracle.DTYPE_FP8_E4M3
+    kc, vc = W.init_key.copy(), W.init_value.copy()
+    o.kv_write(kc, vc, dt, W.block_size, W.num_kv_heads, W.head_dim,
+               W.k_scale, W.v_scale, W.hist_k, W.hist_v, W.hist_slots)
+    return kc, vc, o.num_threads()
+
+
+def time_cpu_oracle(W, n_seqs, steps, warmup=0):
+    """Seconds per oracle step on the first n_seqs sequences; returns
+    (value GB/s, seq-steps/s, seconds per step, threads, bytes)."""
+    kc, vc, threads = oracle_setup(W)
+    seqs = list(range(min(n_seqs, W.batch)))
+    kv_bytes = int(W.seq_lens[seqs].astype(np.int64).sum()) * \
+        W.num_kv_heads * W.head_dim * 2 * W.elem_bytes
+    for _ in range(warmup):
+        cpu_oracle_step(W, kc, vc, seqs)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        cpu_oracle_step(W, kc, vc, seqs)
+    dt = (time.perf_counter() - t0) / max(1, steps)
+    return kv_bytes / dt / 1e9, len(seqs) / dt, dt, threads, kv_bytes
+
+
+def run_reference(args):
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return 0
+    from paged_kv_cache_48_gb300 import workload as wl
+    W = wl.llama8b_gqa()
+    gbs, sps, dt, threads, kvb = time_cpu_oracle(W, args.cpu_sample_seqs,
+                                                 args.steps, args.warmup)
+    peak, kind = measured_peak()
+    sample = (f"first {min(args.cpu_sample_seqs, W.batch)} of {W.batch} "
+              f"sequences, all heads, per step ({kvb / 1e6:.1f} MB of KV)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4),
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "seq_steps_per_s": round(sps, 3),
+        "pct_of_hbm_peak": round(100 * gbs / peak, 4),
+        "config": {"workload": W.name, "batch": W.batch,
+                   "num_heads": W.num_heads, "num_kv_heads": W.num_kv_heads,
+                   "head_dim": W.head_dim, "block_size": W.block_size,
+                   "seq_lens": "uniform [512, 4096]", "kv_dtype": W.kv_dtype,
+                   "l2": "host oracle (no L2 flush)"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s",
+                         "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    sys.path.insert(0, str(ROOT / "tests"))
+    from paged_kv_cache_48_gb300 import (PagedKVCache, paged_attention_decode,
+                                         paged_attention_partition_tokens,
+                                         paged_attention_workspace_bytes,
+                                         paged_kv_write, paged_kv_zero_blocks,
+                                         pkv_check)
+    from paged_kv_cache_48_gb300 import workload as wl
+
+    W = wl.llama8b_gqa(seed=5 + 1000 * rank if rank else 5)
+    shape = (W.num_blocks, 16, W.num_kv_heads, W.head_dim)
+    kc = torch.from_numpy(W.init_key).view(torch.bfloat16).reshape(shape).to(dev)
+    vc = torch.from_numpy(W.init_value).view(torch.bfloat16).reshape(shape).to(dev)
+    cache = PagedKVCache(kc, vc, "bf16")
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16)
+    paged_kv_write(bf(W.hist_k).to(dev), bf(W.hist_v).to(dev),
+                   torch.from_numpy(W.hist_slots).to(dev), cache)
+    q = bf(W.q).to(dev)
+    tables = torch.from_numpy(W.block_tables).to(dev)
+    lens = torch.from_numpy(W.seq_lens).to(dev)
+    sk, sv = bf(W.step_k).to(dev), bf(W.step_v).to(dev)
+    slots = torch.from_numpy(W.step_slots).to(dev)
+    fresh = W.fresh_blocks
+    max_len = int(W.max_blocks * 16)  # host bound: the table width
+    pt = paged_attention_partition_tokens(W.batch, W.num_heads,
+                                          W.num_kv_heads, max_len,
+                                          args.partition_tokens)
+    ws_bytes = paged_attention_workspace_bytes(W.batch, W.num_heads,
+                                               W.num_kv_heads, W.head_dim,
+                                               max_len, args.partition_tokens)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    max_parts = -(-max_len // pt)
+    launches_per_step = (1 if fresh.size else 0) + (1 if slots.numel() else 0) \
+        + 1 + (1 if max_parts > 1 else 0)
+
+    def step(ev=None):
+        if fresh.size:
+            paged_kv_zero_blocks(cache, fresh)
+        paged_kv_write(sk, sv, slots, cache)
+        if ev is not None:
+            ev[0].record(stream)
+        paged_attention_decode(q, cache, tables, lens, W.scale, max_len,
+                               out=out, partition_tokens=args.partition_tokens,
+                               workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, detail = pkv_check()
+    if st != 0:
+        raise RuntimeError(f"device error {st} at {detail} during warm-up")
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(K):
+            step(evs[i])
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        elapsed_ms = start.elapsed_time(end)
+
+        # end to end: pinned host inputs -> device, step, output -> host
+        pin = lambda t: t.cpu().pin_memory()
+        h_q, h_tables, h_lens = pin(q), pin(tables), pin(lens)
+        h_sk, h_sv, h_slots = pin(sk), pin(sv), pin(slots)
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        pairs = [(h_q, q), (h_tables, tables), (h_lens, lens), (h_sk, sk),
+                 (h_sv, sv), (h_slots, slots)]
+        h2d = sum(h.numel() * h.element_size() for h, _ in pairs) + fresh.nbytes
+        d2h = h_out.numel() * h_out.element_size()
+        K2 = max(1, K // 2)
+        barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K2):
+            for h, d in pairs:
+                d.copy_(h, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+    st, detail = pkv_check()
+    if st != 0:
+        raise RuntimeError(f"device error {st} at {detail} in the timed region")
+
+    attn_ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
+    if world > 1:
+        t = torch.tensor([elapsed_ms, e2e_ms, attn_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms, e2e_ms, attn_ms = [float(x) for x in t.tolist()]
+
+    kv_bytes = W.kv_read_bytes()
+    ms_per_step = elapsed_ms / K
+    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    e2e_value = world * kv_bytes / (e2e_ms / K2 * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
+    traffic = profiled_traffic()
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "seq_steps_per_s": round(world * W.batch / (ms_per_step * 1e-3), 1),
+        "config": {"workload": W.name, "batch": W.batch,
+                   "num_heads": W.num_heads, "num_kv_heads": W.num_kv_heads,
+                   "head_dim": W.head_dim, "block_size": 16,
+                   "seq_lens": "uniform [512, 4096]", "kv_dtype": "bf16",
+                   "num_blocks": W.num_blocks, "fresh_blocks": int(fresh.size),
+                   "partition_tokens": pt, "kv_read_bytes": kv_bytes,
+                   "l2": L2_NOTE},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": peak_kind,
+                     "kernel": "paged_decode_kernel (+ lse reduce when split)",
+                     "launch_ms": round(attn_ms, 5)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, sps, dt, threads, kvb = time_cpu_oracle(W, args.cpu_sample_seqs,
+                                                     steps=2, warmup=0)
+        line["cpu_baseline"] = {
+            "value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"first {min(args.cpu_sample_seqs, W.batch)} of "
+                       f"{W.batch} sequences, all heads, 2 steps "
+                       f"({kvb / 1e6:.1f} MB of KV per step)")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,165 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 (sm_103a) paged KV-cache decode path.
+ *
+ * The method is PagedAttention as the vLLM pages describe it:
+ *   - vLLM concept page (compassingai.com), "15 分钟专家深入" item 2: the KV
+ *     cache is cut into fixed-size blocks of 16 tokens, each sequence owns a
+ *     page table (block table) of physical block ids, new blocks are filled
+ *     on demand, and a GPU kernel gathers the blocks through the table;
+ *   - same page, "技术原理": gather the blocks named by the table, then
+ *     scores = Q K^T / sqrt(head_dim), softmax, times V;
+ *   - vLLM v0.17.1 notes (admirer.cn), "修复方案": blocks freshly handed to
+ *     attention are zeroed on the GPU before first use, with the block ids
+ *     sent from host memory together with the launch;
+ *   - vLLM internals (naphjohn.github.io), §1.1 and Figure 1: blocks lie
+ *     anywhere in the pool and shared prefixes point at the same block.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers unless a parameter says otherwise.  The
+ *     caller owns all memory; the library allocates nothing per call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *     Every call is asynchronous on that stream.
+ *   - The return value reports errors the host can see before launching
+ *     (null pointers, bad sizes or dtypes, CUDA launch failures).  Errors
+ *     only the device can see (a slot, block id or sequence length out of
+ *     range, an internal wait that timed out) skip the offending item and
+ *     are recorded in a device error word that pkv_check() reads and clears.
+ *     No kernel traps.
+ *   - Layout of both caches: [num_blocks, block_size, num_kv_heads,
+ *     head_dim], row-major and contiguous; block_size must be 16, head_dim
+ *     64 or 128.  Elements are bf16, or OCP E4M3 bytes with one fp32 scale
+ *     per cache (value = decode(byte) * scale).
+ *   - Entry points are thread-safe; calls on the same stream are ordered.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_ARG = 1,       /* null pointer, negative size, bad partition  */
+    PKV_ERR_DTYPE = 2,     /* unknown cache dtype                          */
+    PKV_ERR_SHAPE = 3,     /* block_size != 16, head_dim not 64/128,
+                              num_heads not a multiple of num_kv_heads     */
+    PKV_ERR_CUDA = 4,      /* a CUDA runtime/driver call failed            */
+    PKV_ERR_RANGE = 5,     /* device: slot / block id / seq_len out of range */
+    PKV_ERR_TIMEOUT = 6,   /* device: a bounded wait gave up               */
+    PKV_ERR_WORKSPACE = 7  /* workspace missing or too small               */
+} pkv_status;
+
+typedef enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1 } pkv_dtype;
+
+/* A paged KV cache.  The struct is read during the call only; the buffers
+ * it points at stay owned by the caller. */
+typedef struct {
+    void *key_cache;       /* [num_blocks, block_size, num_kv_heads, head_dim] */
+    void *value_cache;     /* same shape and dtype as key_cache             */
+    int32_t num_blocks;
+    int32_t block_size;    /* must be 16                                    */
+    int32_t num_kv_heads;
+    int32_t head_dim;      /* 64 or 128                                     */
+    int32_t dtype;         /* pkv_dtype                                     */
+    float k_scale;         /* fp8 only: value = decode(byte) * k_scale      */
+    float v_scale;         /* fp8 only                                      */
+} pkv_cache;
+
+/* Slot-mapped KV write.  Source: vLLM concept page (compassingai.com),
+ * "15 分钟专家深入" item 2 (blocks filled on demand as tokens arrive) and its
+ * mention of high-bandwidth KV pack/unpack kernels.
+ *   k, v          bf16 [num_tokens, num_kv_heads, head_dim], contiguous.
+ *   slot_mapping  int64 [num_tokens]; slot s >= 0 writes row s % 16 of
+ *                 block s / 16; s < 0 skips the token (padding);
+ *                 s >= num_blocks * 16 is a device range error (skipped).
+ * bf16 caches receive the bits unchanged.  fp8 caches receive
+ * E4M3(round-to-nearest-even, saturate to +-448)(x / scale) where the
+ * division is IEEE binary32 and scale is k_scale or v_scale.
+ * Tokens must not share a slot (the order between them is unspecified). */
+pkv_status paged_kv_write(const void *k, const void *v,
+                          const int64_t *slot_mapping, int64_t num_tokens,
+                          const pkv_cache *cache, void *stream);
+
+/* Zero freshly allocated blocks.  Source: vLLM v0.17.1 notes (admirer.cn),
+ * "修复方案": only the newly allocated blocks are cleared, every byte of
+ * their K and V segments, before attention first reads them; the ids travel
+ * from host memory with the launch.
+ *   block_ids     int32 [n]; on the host when ids_on_host != 0 (any host
+ *                 memory: the ids are copied into the launch parameters, so
+ *                 the buffer may be reused as soon as the call returns),
+ *                 otherwise on the device.
+ * Ids outside [0, num_blocks) are device range errors (skipped).  No other
+ * block is touched. */
+pkv_status paged_kv_zero_blocks(const pkv_cache *cache,
+                                const int32_t *block_ids, int64_t n,
+                                int ids_on_host, void *stream);
+
+/* Decode attention over a paged cache, one query token per sequence.
+ * Source: vLLM concept page (compassingai.com), "技术原理" pseudocode
+ * (gather by page table, Q K^T / sqrt(d), softmax, times V) and its note on
+ * GQA (fewer KV heads than Q heads); the gather happens inside the kernel
+ * (vLLM internals, naphjohn.github.io, §4.1).
+ *   q             bf16 [batch, num_heads, head_dim].
+ *   block_tables  int32 [batch, max_blocks]; entry j of row b is the
+ *                 physical block of tokens 16j..16j+15 of sequence b.
+ *                 Only entries j < ceil(seq_lens[b] / 16) are read.
+ *   seq_lens      int32 [batch] (device); 0 gives an all-zero output row.
+ *   scale         multiplies Q.K (1/sqrt(head_dim) in the pages).
+ *   out           bf16 [batch, num_heads, head_dim].
+ *   max_seq_len   host upper bound of seq_lens (sizes the grid); a longer
+ *                 sequence is clamped and reported as a range error.
+ *   partition_tokens  0 = automatic; otherwise a multiple of 16: sequences
+ *                 longer than this are split into partitions of that many
+ *                 tokens whose results are merged by a log-sum-exp reduce.
+ *   workspace     device scratch of workspace_bytes, at least
+ *                 paged_attention_workspace_bytes(...) for the same
+ *                 arguments; may be NULL when that function returns 0.
+ * q head h reads kv head h / (num_heads / num_kv_heads).  Positions past
+ * seq_lens[b] are excluded by selection, so stale bits (NaN/Inf) in unused
+ * slots never reach the output.  The result is bitwise deterministic and
+ * independent of where the blocks lie in the pool. */
+pkv_status paged_attention_decode(const void *q, const pkv_cache *cache,
+                                  const int32_t *block_tables,
+                                  int32_t max_blocks, const int32_t *seq_lens,
+                                  int32_t batch, int32_t num_heads,
+                                  float scale, void *out, int32_t max_seq_len,
+                                  int32_t partition_tokens, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace paged_attention_decode needs for these arguments
+ * (0 when no sequence can be split).  Host-only; never fails. */
+size_t paged_attention_workspace_bytes(int32_t batch, int32_t num_heads,
+                                       int32_t num_kv_heads, int32_t head_dim,
+                                       int32_t max_seq_len,
+                                       int32_t partition_tokens);
+
+/* The partition length (tokens) paged_attention_decode uses for these
+ * arguments on the current device; a value >= max_seq_len means no split.
+ * Returns -1 on invalid arguments. */
+int32_t paged_attention_partition_tokens(int32_t batch, int32_t num_heads,
+                                         int32_t num_kv_heads,
+                                         int32_t max_seq_len,
+                                         int32_t partition_tokens);
+
+/* Synchronise `stream`, then read and clear the device error word of the
+ * current device.  Returns PKV_OK, PKV_ERR_RANGE or PKV_ERR_TIMEOUT (the
+ * first error recorded since the last check), or PKV_ERR_CUDA.  When
+ * `detail` is not NULL it receives the offending index (slot, block id or
+ * sequence) of that first error, or -1. */
+pkv_status pkv_check(void *stream, int64_t *detail);
+
+/* Static description of a status code. */
+const char *pkv_status_str(pkv_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

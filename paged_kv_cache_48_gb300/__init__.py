@@ -1,0 +1,19 @@
+"""GB300 (sm_103a) paged KV-cache decode path: slot-mapped KV write,
+zeroing of fresh blocks, and PagedAttention decode with in-kernel
+block-table gather, GQA, split-KV with a log-sum-exp reduce and fp8 E4M3 KV.
+
+The kernels live in ``libpagedkv.so`` (C ABI: include/pagedkv.h); this
+package binds them for PyTorch tensors.  Build with
+``python -m paged_kv_cache_48_gb300.build``.
+"""
+from .ops import (PagedKVCache, PagedKVError, paged_attention_decode,
+                  paged_attention_partition_tokens,
+                  paged_attention_workspace_bytes, paged_kv_write,
+                  paged_kv_zero_blocks, pkv_check, raise_on_device_error)
+
+__all__ = [
+    "PagedKVCache", "PagedKVError", "paged_attention_decode",
+    "paged_attention_partition_tokens", "paged_attention_workspace_bytes",
+    "paged_kv_write", "paged_kv_zero_blocks", "pkv_check",
+    "raise_on_device_error",
+]

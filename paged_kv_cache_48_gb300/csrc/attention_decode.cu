@@ -1,0 +1,706 @@
+// attention_decode.cu -- PagedAttention decode for sm_103a.
+//
+// What it computes (vLLM concept page, compassingai.com, "技术原理"): for
+// every sequence b and query head h, gather the KV blocks named by the
+// sequence's block table, then softmax(scale * q . K^T) . V over the
+// seq_lens[b] cached tokens.  GQA: q head h reads kv head h / group (same
+// page: fewer KV heads than Q heads).  The gather happens inside the kernel
+// (vLLM internals, naphjohn.github.io, §4.1); positions past seq_len are
+// excluded by selection, never multiplied by zero (vLLM v0.17.1 notes,
+// admirer.cn, "重点：35219": 0 x NaN = NaN).
+//
+// Design (one GPU, HBM-bound):
+//  * Grid = (partition, sequence, kv head x query sub-group).  A CTA owns one
+//    kv head of one partition of one sequence and at most 8 of that head's
+//    query heads.  Long sequences are cut into partitions whose
+//    (max, sum, normalised output) triples a second kernel merges with a
+//    log-sum-exp reduction.
+//  * Each of the CTA's warps streams its own subset of the partition's
+//    16-token blocks through a private ring of shared-memory stages.  Lane 0
+//    reads the physical block id from the block table and issues TMA tile
+//    loads (4-D tensor map over [num_blocks, 16, num_kv_heads, head_dim],
+//    box = 16 tokens x 128 bytes, 128-byte swizzle) that complete on the
+//    stage's mbarrier.  The block table indirection is just the 4th TMA
+//    coordinate.
+//  * Per block: S^T = K . Q^T with mma.sync m16n8k16 (16 tokens x 8 query
+//    heads x head_dim), online softmax over tokens with warp shuffles, then
+//    O^T += V^T . P^T (head_dim x 8 x 16 tokens); P^T is formed from the
+//    score fragment with movmatrix.  fp8 E4M3 tiles are decoded to f16 in
+//    registers (exact) and multiplied with an f16 copy of q; k_scale is
+//    folded into the score scale and v_scale into the output.
+//  * The warps' partial states are merged through shared memory.
+// Every reduction has a fixed order, so results are bitwise deterministic
+// and independent of where blocks sit in the pool.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+
+static __device__ unsigned long long g_err_attention = 0ull;
+
+struct DecodeParams {
+  const __nv_bfloat16 *q;      // [B, Hq, D]
+  const int32_t *block_tables;  // [B, max_blocks]
+  const int32_t *seq_lens;      // [B]
+  __nv_bfloat16 *out;           // [B, Hq, D]
+  float *part_o;                // [B, Hq, max_parts, D]
+  float2 *part_ml;              // [B, Hq, max_parts]: (max * log2e, sum)
+  int32_t batch, num_heads, num_kv_heads, group, q_groups;
+  int32_t num_blocks, max_blocks, max_parts, part_tokens;
+  float scale_log2;  // scale * log2(e) (* k_scale for fp8)
+  float v_scale;     // 1 for bf16
+  unsigned long long timeout_ns;
+};
+
+template <bool FP8, int D>
+struct Cfg {
+  static constexpr int ELT = FP8 ? 1 : 2;
+  static constexpr int ROW_BYTES = D * ELT;
+  static constexpr int BOX_BYTES = ROW_BYTES >= 128 ? 128 : ROW_BYTES;
+  static constexpr int NBOX = ROW_BYTES / BOX_BYTES;
+  static constexpr int BOX_ELEMS = BOX_BYTES / ELT;
+  static constexpr int TILE_BYTES = 16 * ROW_BYTES;    // K (or V) of a block-head
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K + V
+  static constexpr int NW = 4;                         // warps per CTA
+  static constexpr int RING_BYTES = 96 * 1024;         // all stages of a CTA
+  static constexpr int S0 = RING_BYTES / (NW * STAGE_BYTES);
+  static constexpr int STAGES = S0 < 2 ? 2 : (S0 > 8 ? 8 : S0);
+  static constexpr int MT = D / 16;                    // 16-row tiles of head_dim
+  static constexpr int OS_STRIDE = D + 4;              // padded row of o_s
+  static constexpr int SMEM_BYTES = NW * STAGES * STAGE_BYTES + 1024;
+  static_assert(8 * OS_STRIDE * 4 <= STAGES * STAGE_BYTES,
+                "combine scratch must fit in a warp's ring");
+};
+
+template <bool FP8>
+__device__ __forceinline__ void mma_kv(float (&d)[4], uint32_t a0, uint32_t a1,
+                                       uint32_t a2, uint32_t a3, uint32_t b0,
+                                       uint32_t b1) {
+  if (FP8)
+    mma_f16(d, a0, a1, a2, a3, b0, b1);
+  else
+    mma_bf16(d, a0, a1, a2, a3, b0, b1);
+}
+
+// Row of head_dim held by output fragment element (m-tile mt, upper half
+// `hi` of the 16 rows) for lane group g = lane / 4.
+template <bool FP8>
+__device__ __forceinline__ int o_row(int mt, int hi, int g) {
+  return FP8 ? 16 * mt + 2 * g + hi : 16 * mt + 8 * hi + g;
+}
+
+template <bool FP8, int D>
+__global__ void __launch_bounds__(Cfg<FP8, D>::NW * 32)
+paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v,
+                    const DecodeParams p) {
+  using C = Cfg<FP8, D>;
+  extern __shared__ uint8_t smem_dyn[];
+  __shared__ uint64_t bars[C::NW][C::STAGES];
+  __shared__ int stage_ok[C::NW][C::STAGES];
+  __shared__ float m_s[C::NW][8];
+  __shared__ float l_s[C::NW][8];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;  // fragment row group
+  const int c = lane & 3;   // fragment column pair
+  const int part = blockIdx.x;
+  const int b = blockIdx.y;
+  const int kvh = blockIdx.z / p.q_groups;
+  const int qg = blockIdx.z - kvh * p.q_groups;
+
+  // ---- sequence extent and this CTA's partition --------------------------
+  int L = __ldg(p.seq_lens + b);
+  {
+    const int cap = min(p.max_blocks * 16, p.max_parts * p.part_tokens);
+    if (L < 0 || L > cap) {
+      if (part == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+        record_error(&g_err_attention, PKV_ERR_RANGE, b);
+      L = L < 0 ? 0 : cap;
+    }
+  }
+  const int nparts = L <= p.part_tokens ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+  if (part >= nparts) return;
+  const int tok0 = part * p.part_tokens;  // multiple of 16
+  const int tok1 = min(L, tok0 + p.part_tokens);
+  const int blk0 = tok0 >> 4;
+  const int nblk = (tok1 - tok0 + 15) >> 4;
+  const int my_n = nblk > warp ? (nblk - warp + C::NW - 1) / C::NW : 0;
+  const int heads_here = min(8, p.group - qg * 8);
+
+  // ---- shared memory ring of this warp -----------------------------------
+  const uint32_t base_u32 = smem_u32(smem_dyn);
+  uint8_t *ring = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32) +
+                  warp * C::STAGES * C::STAGE_BYTES;
+  if (lane == 0) {
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[warp][s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  // ---- query fragments (B operand of S^T = K . Q^T) -----------------------
+  // Lane holds, for query head n = g of the sub-group, the head_dim pairs
+  // that the A fragment of the same k-step pairs with.
+  uint32_t qf[C::MT][2];
+  {
+    const bool valid = g < heads_here;
+    const int head = kvh * p.group + qg * 8 + g;
+    const __nv_bfloat16 *qrow = p.q + ((size_t)b * p.num_heads + head) * D;
+#pragma unroll
+    for (int ks = 0; ks < C::MT; ++ks) {
+      if (!valid) {
+        qf[ks][0] = qf[ks][1] = 0u;
+        continue;
+      }
+      if (!FP8) {
+        qf[ks][0] = __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * ks + 2 * c));
+        qf[ks][1] = __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * ks + 8 + 2 * c));
+      } else {
+        // fp8 tiles give lane 4 consecutive head_dim values per row; the
+        // k index order of the mma is permuted to match (a dot product is
+        // order-free), so q is loaded in the same permuted order.
+        const uint2 four = __ldg(reinterpret_cast<const uint2 *>(qrow + 16 * ks + 4 * c));
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&four.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&four.y));
+        qf[ks][0] = pack_f16x2(f0.x, f0.y);
+        qf[ks][1] = pack_f16x2(f1.x, f1.y);
+      }
+    }
+  }
+
+  // ---- block ids of this warp, 32 at a time in registers -----------------
+  const int32_t *table = p.block_tables + (size_t)b * p.max_blocks + blk0 + warp;
+  int ids_reg = -1;
+  const uint64_t policy = l2_policy_evict_normal();
+  if (lane == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+
+  auto issue = [&](int i) {
+    if ((i & 31) == 0) ids_reg = (i + lane < my_n) ? __ldg(table + (i + lane) * C::NW) : -1;
+    int phys = __shfl_sync(0xffffffffu, ids_reg, i & 31);
+    if (lane == 0) {
+      const int stage = i % C::STAGES;
+      int ok = 1;
+      if (phys < 0 || phys >= p.num_blocks) {
+        record_error(&g_err_attention, PKV_ERR_RANGE, b);
+        phys = 0;
+        ok = 0;
+      }
+      stage_ok[warp][stage] = ok;
+      uint8_t *sk = ring + stage * C::STAGE_BYTES;
+      uint8_t *sv = sk + C::TILE_BYTES;
+      uint64_t *bar = &bars[warp][stage];
+      mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+#pragma unroll
+      for (int bx = 0; bx < C::NBOX; ++bx)
+        tma_load_4d(sk + bx * 16 * C::BOX_BYTES, &tmap_k, bar, bx * C::BOX_ELEMS, kvh, 0,
+                    phys, policy);
+#pragma unroll
+      for (int bx = 0; bx < C::NBOX; ++bx)
+        tma_load_4d(sv + bx * 16 * C::BOX_BYTES, &tmap_v, bar, bx * C::BOX_ELEMS, kvh, 0,
+                    phys, policy);
+    }
+  };
+
+  float o[C::MT][4];
+#pragma unroll
+  for (int mt = 0; mt < C::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  int issued = 0;
+  const int pre = min(C::STAGES, my_n);
+  for (; issued < pre; ++issued) issue(issued);
+
+  // ldmatrix source rows/chunks for this lane (see the fragment layouts of
+  // mma.m16n8k16): K uses (row = lane%8 + 8*bit3, chunk = 2x + bit4),
+  // V^T uses (row = lane%8 + 8*bit4, chunk = 2x + bit3) for bf16 and the K
+  // pattern for fp8.
+  const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int k_chk = lane >> 4;
+  const int v_row = FP8 ? k_row : (lane & 7) + (lane >> 4) * 8;
+  const int v_chk = FP8 ? k_chk : (lane >> 3) & 1;
+
+  bool failed = false;
+  for (int i = 0; i < my_n; ++i) {
+    const int stage = i % C::STAGES;
+    if (!mbar_wait_bounded(&bars[warp][stage], (i / C::STAGES) & 1, p.timeout_ns)) {
+      failed = true;
+      break;
+    }
+    const int j = blk0 + warp + i * C::NW;
+    const int nv = stage_ok[warp][stage] ? min(16, tok1 - j * 16) : 0;
+    const uint32_t sk = smem_u32(ring + stage * C::STAGE_BYTES);
+    const uint32_t sv = sk + C::TILE_BYTES;
+
+    // -- S^T[16 tokens x 8 heads] = K . Q^T --------------------------------
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (!FP8) {
+#pragma unroll
+      for (int ks = 0; ks < C::MT; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * ks + k_chk), a0, a1, a2, a3);
+        mma_kv<FP8>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      }
+    } else {
+#pragma unroll
+      for (int kp = 0; kp < C::MT / 2; ++kp) {
+        uint32_t r0, r1, r2, r3;
+        ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * kp + k_chk), r0, r1, r2, r3);
+        mma_kv<FP8>(sc, e4m3x2_to_f16x2(r0 & 0xffff), e4m3x2_to_f16x2(r1 & 0xffff),
+                    e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0],
+                    qf[2 * kp][1]);
+        mma_kv<FP8>(sc, e4m3x2_to_f16x2(r2 & 0xffff), e4m3x2_to_f16x2(r3 & 0xffff),
+                    e4m3x2_to_f16x2(r2 >> 16), e4m3x2_to_f16x2(r3 >> 16),
+                    qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
+      }
+    }
+
+    // -- online softmax over the block's tokens, per query-head column ----
+    // sc[0], sc[1]: token g, heads 2c, 2c+1; sc[2], sc[3]: token g + 8.
+    const bool v_lo = g < nv, v_hi = g + 8 < nv;
+    const float s0 = v_lo ? sc[0] * p.scale_log2 : -INFINITY;
+    const float s1 = v_lo ? sc[1] * p.scale_log2 : -INFINITY;
+    const float s2 = v_hi ? sc[2] * p.scale_log2 : -INFINITY;
+    const float s3 = v_hi ? sc[3] * p.scale_log2 : -INFINITY;
+    float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+      bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+    }
+    const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
+    const float p0 = exp2f(s0 - mu0), p2 = exp2f(s2 - mu0);
+    const float p1 = exp2f(s1 - mu1), p3 = exp2f(s3 - mu1);
+    l0 = l0 * al0 + (p0 + p2);
+    l1 = l1 * al1 + (p1 + p3);
+    m0 = mn0;
+    m1 = mn1;
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt) {
+      o[mt][0] *= al0;
+      o[mt][1] *= al1;
+      o[mt][2] *= al0;
+      o[mt][3] *= al1;
+    }
+
+    // -- P^T fragment (B operand of O^T += V^T . P^T) ---------------------
+    const uint32_t pb0 = movmatrix_trans(FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
+    const uint32_t pb1 = movmatrix_trans(FP8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
+
+    // V rows past the sequence may hold stale NaN/Inf bits: zero them in
+    // the A fragment (tokens 2c, 2c+1 in regs 0/1, 8+2c, 9+2c in regs 2/3),
+    // so that p = 0 never meets a NaN inside the mma.
+    uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+    if (nv < 16) {
+      vm_lo = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
+      vm_hi = (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
+    }
+
+    // -- O^T[head_dim x 8] += V^T . P^T -----------------------------------
+    if (!FP8) {
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * mt + v_chk), a0, a1, a2, a3);
+        mma_kv<FP8>(o[mt], a0 & vm_lo, a1 & vm_lo, a2 & vm_hi, a3 & vm_hi, pb0, pb1);
+      }
+    } else {
+#pragma unroll
+      for (int qq = 0; qq < C::MT / 2; ++qq) {
+        uint32_t r0, r1, r2, r3;
+        ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * qq + v_chk), r0, r1, r2, r3);
+        // r0/r2: tokens 2c, 2c+1 (rows 0-7); r1/r3: tokens 8+2c, 9+2c.
+        // Each holds [t0 dA, t0 dB, t1 dA, t1 dB]; regroup per head_dim row.
+        const uint32_t x0 = prmt(r0, 0u, 0x3120u), x1 = prmt(r1, 0u, 0x3120u);
+        const uint32_t x2 = prmt(r2, 0u, 0x3120u), x3 = prmt(r3, 0u, 0x3120u);
+        mma_kv<FP8>(o[2 * qq], e4m3x2_to_f16x2(x0 & 0xffff) & vm_lo,
+                    e4m3x2_to_f16x2(x0 >> 16) & vm_lo, e4m3x2_to_f16x2(x1 & 0xffff) & vm_hi,
+                    e4m3x2_to_f16x2(x1 >> 16) & vm_hi, pb0, pb1);
+        mma_kv<FP8>(o[2 * qq + 1], e4m3x2_to_f16x2(x2 & 0xffff) & vm_lo,
+                    e4m3x2_to_f16x2(x2 >> 16) & vm_lo, e4m3x2_to_f16x2(x3 & 0xffff) & vm_hi,
+                    e4m3x2_to_f16x2(x3 >> 16) & vm_hi, pb0, pb1);
+      }
+    }
+
+    __syncwarp();
+    if (issued < my_n) issue(issued++);
+  }
+
+  if (failed) {
+    if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, b);
+    // Let copies still in flight land before the ring is reused or the CTA
+    // exits (bounded as well).
+    for (int i = 0; i < issued; ++i)
+      mbar_wait_bounded(&bars[warp][i % C::STAGES], (i / C::STAGES) & 1, p.timeout_ns);
+    m0 = m1 = -INFINITY;
+  }
+
+  // ---- merge the warps' states -------------------------------------------
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  float *o_s = reinterpret_cast<float *>(ring);  // this warp's ring, now idle
+  if (!failed && my_n > 0) {
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+      for (int hi = 0; hi < 2; ++hi) {
+        const int d = o_row<FP8>(mt, hi, g);
+        o_s[(2 * c) * C::OS_STRIDE + d] = o[mt][2 * hi];
+        o_s[(2 * c + 1) * C::OS_STRIDE + d] = o[mt][2 * hi + 1];
+      }
+    }
+  }
+  if (g == 0) {
+    m_s[warp][2 * c] = m0;
+    m_s[warp][2 * c + 1] = m1;
+    l_s[warp][2 * c] = l0;
+    l_s[warp][2 * c + 1] = l1;
+  }
+  __syncthreads();
+
+  const uint8_t *rings = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32);
+  for (int idx = threadIdx.x; idx < heads_here * D; idx += blockDim.x) {
+    const int h = idx / D;
+    const int d = idx - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < C::NW; ++w) M = fmaxf(M, m_s[w][h]);
+    float lsum = 0.f, acc = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < C::NW; ++w) {
+        const float mw = m_s[w][h];
+        if (mw == -INFINITY) continue;
+        const float e = exp2f(mw - M);
+        lsum += e * l_s[w][h];
+        acc += e * reinterpret_cast<const float *>(
+                       rings + w * C::STAGES * C::STAGE_BYTES)[h * C::OS_STRIDE + d];
+      }
+    }
+    const float res = lsum > 0.f ? acc / lsum * p.v_scale : 0.f;
+    const int head = kvh * p.group + qg * 8 + h;
+    const size_t bh = (size_t)b * p.num_heads + head;
+    if (nparts == 1) {
+      p.out[bh * D + d] = __float2bfloat16_rn(res);
+    } else {
+      p.part_o[(bh * p.max_parts + part) * D + d] = res;
+      if (d == 0) p.part_ml[bh * p.max_parts + part] = make_float2(M, lsum);
+    }
+  }
+}
+
+// Log-sum-exp merge of a split sequence's partitions: one CTA per (query
+// head, sequence), one thread per head_dim element.  Partition j carries
+// m_j (log2 domain), l_j and its normalised output o_j; the result is
+// sum_j 2^(m_j - M) l_j o_j / sum_j 2^(m_j - M) l_j with M = max_j m_j.
+template <int D>
+__global__ void __launch_bounds__(D)
+paged_decode_reduce_kernel(const DecodeParams p) {
+  extern __shared__ float w_s[];  // [max_parts]
+  __shared__ float red[D / 32];
+  const int h = blockIdx.x, b = blockIdx.y;
+  int L = __ldg(p.seq_lens + b);
+  const int cap = min(p.max_blocks * 16, p.max_parts * p.part_tokens);
+  L = L < 0 ? 0 : (L > cap ? cap : L);
+  const int nparts = L <= p.part_tokens ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+  if (nparts <= 1) return;  // the decode kernel wrote the output directly
+  const size_t bh = (size_t)b * p.num_heads + h;
+  const float2 *ml = p.part_ml + bh * p.max_parts;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  float M = -INFINITY;
+  for (int j = tid; j < nparts; j += D) M = fmaxf(M, ml[j].x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+
+  float W = 0.f;
+  for (int j = tid; j < nparts; j += D) {
+    const float2 v = ml[j];
+    const float w = v.x == -INFINITY ? 0.f : exp2f(v.x - M) * v.y;
+    w_s[j] = w;
+    W += w;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+  if (lane == 0) red[warp] = W;
+  __syncthreads();
+  W = 0.f;
+#pragma unroll
+  for (int w = 0; w < D / 32; ++w) W += red[w];
+
+  const float *po = p.part_o + bh * p.max_parts * D + tid;
+  float acc = 0.f;
+  for (int j = 0; j < nparts; ++j) {
+    const float w = w_s[j];
+    if (w != 0.f) acc += w * po[(size_t)j * D];
+  }
+  p.out[bh * D + tid] = __float2bfloat16_rn(W > 0.f ? acc / W : 0.f);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 4-D map over one cache: dims (innermost first) {head_dim, num_kv_heads,
+// 16, num_blocks}, box {box_elems, 1, 16, 1}.
+bool encode_cache_map(CUtensorMap *map, void *base, const pkv_cache *c) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const bool fp8 = c->dtype == PKV_FP8_E4M3;
+  const cuuint64_t elt = fp8 ? 1 : 2;
+  const cuuint64_t row = (cuuint64_t)c->head_dim * elt;
+  const cuuint32_t box_bytes = row >= 128 ? 128 : (cuuint32_t)row;
+  cuuint64_t dims[4] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads, 16,
+                        (cuuint64_t)c->num_blocks};
+  cuuint64_t strides[3] = {row, row * c->num_kv_heads, row * c->num_kv_heads * 16};
+  cuuint32_t box[4] = {(cuuint32_t)(box_bytes / elt), 1, 16, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r =
+      fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base,
+         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Small cache of encoded maps keyed by the cache geometry.
+struct MapEntry {
+  void *key_cache, *value_cache;
+  int32_t num_blocks, num_kv_heads, head_dim, dtype;
+  CUtensorMap k, v;
+};
+
+bool get_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
+  static std::mutex mu;
+  static MapEntry entries[8];
+  static int n_entries = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_entries; ++i) {
+    const MapEntry &e = entries[i];
+    if (e.key_cache == c->key_cache && e.value_cache == c->value_cache &&
+        e.num_blocks == c->num_blocks && e.num_kv_heads == c->num_kv_heads &&
+        e.head_dim == c->head_dim && e.dtype == c->dtype) {
+      *k = e.k;
+      *v = e.v;
+      return true;
+    }
+  }
+  MapEntry e;
+  e.key_cache = c->key_cache;
+  e.value_cache = c->value_cache;
+  e.num_blocks = c->num_blocks;
+  e.num_kv_heads = c->num_kv_heads;
+  e.head_dim = c->head_dim;
+  e.dtype = c->dtype;
+  if (!encode_cache_map(&e.k, c->key_cache, c) || !encode_cache_map(&e.v, c->value_cache, c))
+    return false;
+  entries[next] = e;
+  next = (next + 1) % 8;
+  if (n_entries < 8) ++n_entries;
+  *k = e.k;
+  *v = e.v;
+  return true;
+}
+
+int choose_partition_tokens(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
+                            int32_t max_seq_len, int32_t requested, int sms) {
+  if (requested > 0) return requested;
+  const int64_t whole = std::max<int64_t>(16, ((int64_t)max_seq_len + 15) / 16 * 16);
+  const int group = num_heads / num_kv_heads;
+  const int64_t units = (int64_t)batch * num_kv_heads * ((group + 7) / 8);
+  const int64_t target = (int64_t)sms * 8;  // about 4 waves of 2 CTAs per SM
+  if (units >= target || whole <= 256) return (int)std::min<int64_t>(whole, INT32_MAX / 2);
+  for (int pt = 8192; pt >= 512; pt >>= 1) {
+    if (pt >= whole) continue;
+    if (units * ((whole + pt - 1) / pt) >= target) return pt;
+  }
+  return 256;
+}
+
+template <bool FP8, int D>
+pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
+                         int grid_x, cudaStream_t s) {
+  using C = Cfg<FP8, D>;
+  static int configured_device = -1;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (configured_device != dev) {
+      if (cudaFuncSetAttribute(paged_decode_kernel<FP8, D>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_BYTES) != cudaSuccess)
+        return PKV_ERR_CUDA;
+      configured_device = dev;
+    }
+  }
+  dim3 grid(grid_x, p.batch, p.num_kv_heads * p.q_groups);
+  paged_decode_kernel<FP8, D><<<grid, C::NW * 32, C::SMEM_BYTES, s>>>(mk, mv, p);
+  if (cudaPeekAtLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  if (p.max_parts > 1) {
+    dim3 rgrid(p.num_heads, p.batch);
+    paged_decode_reduce_kernel<D><<<rgrid, D, p.max_parts * sizeof(float), s>>>(p);
+    if (cudaPeekAtLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+size_t workspace_for(int32_t batch, int32_t num_heads, int32_t head_dim, int32_t max_parts) {
+  if (max_parts <= 1) return 0;
+  const size_t rows = (size_t)batch * num_heads * max_parts;
+  const size_t o_bytes = (rows * head_dim * sizeof(float) + 255) / 256 * 256;
+  return o_bytes + rows * sizeof(float2);
+}
+
+}  // namespace
+
+unsigned long long read_and_clear_error_attention(cudaStream_t s, cudaError_t *err) {
+  unsigned long long v = 0ull;
+  *err = cudaMemcpyFromSymbolAsync(&v, g_err_attention, sizeof v, 0, cudaMemcpyDeviceToHost, s);
+  if (*err != cudaSuccess) return 0ull;
+  *err = cudaStreamSynchronize(s);
+  if (*err != cudaSuccess) return 0ull;
+  if (v) {
+    const unsigned long long zero = 0ull;
+    *err = cudaMemcpyToSymbolAsync(g_err_attention, &zero, sizeof zero, 0,
+                                   cudaMemcpyHostToDevice, s);
+    if (*err == cudaSuccess) *err = cudaStreamSynchronize(s);
+  }
+  return v;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int32_t paged_attention_partition_tokens(int32_t batch, int32_t num_heads,
+                                                    int32_t num_kv_heads, int32_t max_seq_len,
+                                                    int32_t partition_tokens) {
+  if (batch < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
+      max_seq_len < 0 || partition_tokens < 0 || partition_tokens % 16)
+    return -1;
+  const int sms = device_sm_count();
+  return choose_partition_tokens(batch, num_heads, num_kv_heads, max_seq_len, partition_tokens,
+                                 sms > 0 ? sms : 148);
+}
+
+extern "C" size_t paged_attention_workspace_bytes(int32_t batch, int32_t num_heads,
+                                                  int32_t num_kv_heads, int32_t head_dim,
+                                                  int32_t max_seq_len,
+                                                  int32_t partition_tokens) {
+  const int32_t pt = paged_attention_partition_tokens(batch, num_heads, num_kv_heads,
+                                                      max_seq_len, partition_tokens);
+  if (pt <= 0 || batch <= 0 || head_dim <= 0) return 0;
+  const int32_t max_parts = (int32_t)(((int64_t)max_seq_len + pt - 1) / pt);
+  return workspace_for(batch, num_heads, head_dim, max_parts);
+}
+
+extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cache,
+                                             const int32_t *block_tables, int32_t max_blocks,
+                                             const int32_t *seq_lens, int32_t batch,
+                                             int32_t num_heads, float scale, void *out,
+                                             int32_t max_seq_len, int32_t partition_tokens,
+                                             void *workspace, size_t workspace_bytes,
+                                             void *stream) {
+  pkv_status st = validate_cache(cache);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || num_heads <= 0 || max_blocks <= 0 || max_seq_len < 0 ||
+      partition_tokens < 0 || partition_tokens % 16 || !std::isfinite(scale))
+    return PKV_ERR_ARG;
+  if (num_heads % cache->num_kv_heads) return PKV_ERR_SHAPE;
+  if (batch == 0) return PKV_OK;
+  if (!q || !out || !block_tables || !seq_lens) return PKV_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(q) & 15) return PKV_ERR_ARG;
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
+  if (fp8 && !(cache->k_scale > 0.f && cache->v_scale > 0.f)) return PKV_ERR_ARG;
+  if (batch > 65535) return PKV_ERR_ARG;
+  const int group = num_heads / cache->num_kv_heads;
+  const int q_groups = (group + 7) / 8;
+  if ((int64_t)cache->num_kv_heads * q_groups > 65535) return PKV_ERR_ARG;
+
+  const int sms = device_sm_count();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  const int pt = choose_partition_tokens(batch, num_heads, cache->num_kv_heads, max_seq_len,
+                                         partition_tokens, sms);
+  const int64_t parts64 = std::max<int64_t>(1, ((int64_t)max_seq_len + pt - 1) / pt);
+  if (parts64 > INT32_MAX / 2) return PKV_ERR_ARG;
+  const int max_parts = (int)parts64;
+  const size_t need = workspace_for(batch, num_heads, cache->head_dim, max_parts);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
+    if ((size_t)max_parts * sizeof(float) > 48 * 1024) return PKV_ERR_ARG;
+  }
+
+  CUtensorMap mk, mv;
+  if (!get_maps(cache, &mk, &mv)) return PKV_ERR_CUDA;
+
+  DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.part_o = need ? static_cast<float *>(workspace) : nullptr;
+  p.part_ml = need ? reinterpret_cast<float2 *>(
+                         static_cast<uint8_t *>(workspace) +
+                         ((size_t)batch * num_heads * max_parts * cache->head_dim * sizeof(float) +
+                          255) / 256 * 256)
+                   : nullptr;
+  p.batch = batch;
+  p.num_heads = num_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.group = group;
+  p.q_groups = q_groups;
+  p.num_blocks = cache->num_blocks;
+  p.max_blocks = max_blocks;
+  p.max_parts = max_parts;
+  p.part_tokens = pt;
+  p.scale_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
+  p.v_scale = fp8 ? cache->v_scale : 1.f;
+  p.timeout_ns = 2000000000ull;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fp8)
+    return cache->head_dim == 128 ? launch_decode<true, 128>(mk, mv, p, max_parts, s)
+                                  : launch_decode<true, 64>(mk, mv, p, max_parts, s);
+  return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, max_parts, s)
+                                : launch_decode<false, 64>(mk, mv, p, max_parts, s);
+}

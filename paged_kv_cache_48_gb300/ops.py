@@ -1,0 +1,213 @@
+"""PyTorch-facing binding of the C ABI (include/pagedkv.h).
+
+Marshalling only: tensors are checked for dtype, shape, device and
+contiguity, their data pointers and torch's current CUDA stream are passed
+to ``libpagedkv.so``, and a non-OK status raises ``PagedKVError``.  Every
+step of the path (write, zeroing, gather, attention, reduce) runs in the
+library's kernels; PyTorch only owns the device memory and the streams.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _native
+from ._native import PagedKVError, PkvCache
+
+BLOCK_SIZE = 16
+_DTYPES = {"bf16": _native.PKV_BF16, "fp8_e4m3": _native.PKV_FP8_E4M3}
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _require(t: torch.Tensor, name: str, dtype, device=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+class PagedKVCache:
+    """Key and value caches of shape [num_blocks, 16, num_kv_heads,
+    head_dim] on one CUDA device, bf16 or fp8 E4M3 (stored as uint8 with a
+    per-tensor fp32 scale each)."""
+
+    def __init__(self, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                 kv_dtype: str = "bf16", k_scale: float = 1.0,
+                 v_scale: float = 1.0):
+        if kv_dtype not in _DTYPES:
+            raise ValueError(f"kv_dtype must be one of {list(_DTYPES)}")
+        elt = torch.bfloat16 if kv_dtype == "bf16" else torch.uint8
+        _require(key_cache, "key_cache", elt, ndim=4)
+        _require(value_cache, "value_cache", elt, device=key_cache.device,
+                 ndim=4)
+        if key_cache.shape != value_cache.shape:
+            raise ValueError("key_cache and value_cache shapes differ")
+        if key_cache.shape[1] != BLOCK_SIZE:
+            raise ValueError("block_size must be 16")
+        if not key_cache.is_cuda:
+            raise ValueError("caches must live on a CUDA device")
+        self.key_cache = key_cache
+        self.value_cache = value_cache
+        self.kv_dtype = kv_dtype
+        self.k_scale = float(k_scale)
+        self.v_scale = float(v_scale)
+        self._struct = PkvCache(
+            key_cache.data_ptr(), value_cache.data_ptr(), key_cache.shape[0],
+            BLOCK_SIZE, key_cache.shape[2], key_cache.shape[3],
+            _DTYPES[kv_dtype], self.k_scale, self.v_scale)
+
+    @classmethod
+    def empty(cls, num_blocks: int, num_kv_heads: int, head_dim: int,
+              kv_dtype: str = "bf16", k_scale: float = 1.0,
+              v_scale: float = 1.0, device="cuda") -> "PagedKVCache":
+        elt = torch.bfloat16 if kv_dtype == "bf16" else torch.uint8
+        shape = (num_blocks, BLOCK_SIZE, num_kv_heads, head_dim)
+        return cls(torch.empty(shape, dtype=elt, device=device),
+                   torch.empty(shape, dtype=elt, device=device), kv_dtype,
+                   k_scale, v_scale)
+
+    @property
+    def device(self) -> torch.device:
+        return self.key_cache.device
+
+    @property
+    def num_blocks(self) -> int:
+        return self.key_cache.shape[0]
+
+    @property
+    def num_kv_heads(self) -> int:
+        return self.key_cache.shape[2]
+
+    @property
+    def head_dim(self) -> int:
+        return self.key_cache.shape[3]
+
+    def c_struct(self) -> PkvCache:
+        return self._struct
+
+
+def paged_kv_write(k: torch.Tensor, v: torch.Tensor,
+                   slot_mapping: torch.Tensor, cache: PagedKVCache,
+                   stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Write tokens' K/V rows ([T, num_kv_heads, head_dim] bf16) into
+    their slots (int64 [T], negative = skip)."""
+    dev = cache.device
+    _require(k, "k", torch.bfloat16, dev, 3)
+    _require(v, "v", torch.bfloat16, dev, 3)
+    _require(slot_mapping, "slot_mapping", torch.int64, dev, 1)
+    T = k.shape[0]
+    if v.shape != k.shape or slot_mapping.shape[0] != T or \
+            k.shape[1:] != (cache.num_kv_heads, cache.head_dim):
+        raise ValueError("k, v, slot_mapping shapes do not match the cache")
+    st = _native.lib().paged_kv_write(
+        k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+        ctypes.byref(cache.c_struct()), _stream_handle(stream, dev))
+    _native.check("paged_kv_write", st)
+
+
+def paged_kv_zero_blocks(cache: PagedKVCache, block_ids,
+                         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Zero every byte of the K and V segments of the given blocks.  Host
+    ids (numpy array, list or CPU tensor) ride in the launch parameters;
+    a CUDA int32 tensor is read by the kernel directly."""
+    dev = cache.device
+    if isinstance(block_ids, torch.Tensor) and block_ids.is_cuda:
+        _require(block_ids, "block_ids", torch.int32, dev, 1)
+        ptr, n, on_host, keep = block_ids.data_ptr(), block_ids.numel(), 0, None
+    else:
+        if isinstance(block_ids, torch.Tensor):
+            block_ids = block_ids.numpy()
+        keep = np.ascontiguousarray(block_ids, dtype=np.int32).reshape(-1)
+        ptr, n, on_host = keep.ctypes.data, keep.size, 1
+    st = _native.lib().paged_kv_zero_blocks(
+        ctypes.byref(cache.c_struct()), ptr, n, on_host,
+        _stream_handle(stream, dev))
+    del keep
+    _native.check("paged_kv_zero_blocks", st)
+
+
+def paged_attention_workspace_bytes(batch: int, num_heads: int,
+                                    num_kv_heads: int, head_dim: int,
+                                    max_seq_len: int,
+                                    partition_tokens: int = 0) -> int:
+    return int(_native.lib().paged_attention_workspace_bytes(
+        batch, num_heads, num_kv_heads, head_dim, max_seq_len,
+        partition_tokens))
+
+
+def paged_attention_partition_tokens(batch: int, num_heads: int,
+                                     num_kv_heads: int, max_seq_len: int,
+                                     partition_tokens: int = 0) -> int:
+    return int(_native.lib().paged_attention_partition_tokens(
+        batch, num_heads, num_kv_heads, max_seq_len, partition_tokens))
+
+
+def paged_attention_decode(q: torch.Tensor, cache: PagedKVCache,
+                           block_tables: torch.Tensor,
+                           seq_lens: torch.Tensor, scale: float,
+                           max_seq_len: int, out: Optional[torch.Tensor] = None,
+                           partition_tokens: int = 0,
+                           workspace: Optional[torch.Tensor] = None,
+                           stream: Optional[torch.cuda.Stream] = None
+                           ) -> torch.Tensor:
+    """Decode attention: q [B, Hq, d] bf16, block_tables int32 [B,
+    max_blocks], seq_lens int32 [B] (device), max_seq_len a host bound of
+    seq_lens.  Returns out [B, Hq, d] bf16."""
+    dev = cache.device
+    _require(q, "q", torch.bfloat16, dev, 3)
+    _require(block_tables, "block_tables", torch.int32, dev, 2)
+    _require(seq_lens, "seq_lens", torch.int32, dev, 1)
+    B, Hq, d = q.shape
+    if d != cache.head_dim or block_tables.shape[0] != B or \
+            seq_lens.shape[0] != B:
+        raise ValueError("q, block_tables, seq_lens shapes do not match")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _require(out, "out", torch.bfloat16, dev, 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    need = paged_attention_workspace_bytes(B, Hq, cache.num_kv_heads, d,
+                                           max_seq_len, partition_tokens)
+    ws_ptr, ws_bytes = None, 0
+    if need:
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        _require(workspace, "workspace", torch.uint8, dev, 1)
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+    st = _native.lib().paged_attention_decode(
+        q.data_ptr(), ctypes.byref(cache.c_struct()), block_tables.data_ptr(),
+        block_tables.shape[1], seq_lens.data_ptr(), B, Hq, float(scale),
+        out.data_ptr(), int(max_seq_len), int(partition_tokens), ws_ptr,
+        ws_bytes, _stream_handle(stream, dev))
+    _native.check("paged_attention_decode", st)
+    return out
+
+
+def pkv_check(stream: Optional[torch.cuda.Stream] = None, device=None):
+    """Synchronise the stream and return (status, detail) from the device
+    error word, clearing it."""
+    detail = ctypes.c_int64(-1)
+    st = _native.lib().pkv_check(_stream_handle(stream, device),
+                                 ctypes.byref(detail))
+    return int(st), int(detail.value)
+
+
+def raise_on_device_error(stream: Optional[torch.cuda.Stream] = None,
+                          device=None) -> None:
+    st, detail = pkv_check(stream, device)
+    if st != _native.PKV_OK:
+        raise PagedKVError("device check", st, detail)

@@ -21,3 +21,18 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+@pytest.fixture(autouse=True)
+def _gpu_ready(request):
+    """GPU tests need a CUDA device and the built library; fail loudly
+    (never skip to a fallback) when either is missing."""
+    if request.node.get_closest_marker("gpu") is None:
+        yield
+        return
+    import torch
+    from paged_kv_cache_48_gb300 import _native
+    assert torch.cuda.is_available(), "gpu test without a CUDA device"
+    _native.lib()
+    yield
+    torch.cuda.synchronize()

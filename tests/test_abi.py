@@ -1,0 +1,72 @@
+"""The C ABI library builds, loads and exports every declared entry point;
+host-side argument checks answer without touching a GPU (no compute)."""
+import ctypes
+
+import pytest
+
+from paged_kv_cache_48_gb300 import _native, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _native.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _native.declared_functions()
+    assert {"paged_kv_write", "paged_kv_zero_blocks", "paged_attention_decode",
+            "paged_attention_workspace_bytes", "pkv_check"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _native._SIGNATURES, f"{n} has no binding signature"
+
+
+def test_status_strings_and_version(lib):
+    for code, name in _native.STATUS_NAMES.items():
+        s = lib.pkv_status_str(code)
+        assert s and s != b"unknown status", name
+    assert lib.pkv_status_str(99) == b"unknown status"
+    assert lib.pkv_version() >= 100
+
+
+def _cache(**kw):
+    c = _native.PkvCache(16, 16, 4, 16, 2, 128, 0, 1.0, 1.0)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("key_cache", None, 1),
+    ("block_size", 32, 3),
+    ("head_dim", 96, 3),
+    ("dtype", 7, 2),
+    ("num_blocks", 0, 3),
+    ("key_cache", 24, 1),      # not 16-byte aligned
+])
+def test_cache_validation_before_any_cuda_call(lib, field, value, status):
+    c = _cache(**{field: value})
+    st = lib.paged_kv_write(16, 16, 16, 1, ctypes.byref(c), None)
+    assert st == status
+    st = lib.paged_kv_zero_blocks(ctypes.byref(c), 16, 1, 1, None)
+    assert st == status
+
+
+def test_argument_validation(lib):
+    c = _cache()
+    assert lib.paged_kv_write(None, 16, 16, 1, ctypes.byref(c), None) == 1
+    assert lib.paged_kv_write(16, 16, 16, -1, ctypes.byref(c), None) == 1
+    assert lib.paged_kv_write(16, 16, 16, 0, ctypes.byref(c), None) == 0
+    assert lib.paged_kv_zero_blocks(ctypes.byref(c), None, 3, 1, None) == 1
+    assert lib.paged_kv_zero_blocks(ctypes.byref(c), None, 0, 1, None) == 0
+    # num_heads not a multiple of num_kv_heads
+    assert lib.paged_attention_decode(16, ctypes.byref(c), 16, 4, 16, 2, 3,
+                                      0.1, 16, 64, 0, None, 0, None) == 3
+    # partition length not a multiple of 16
+    assert lib.paged_attention_decode(16, ctypes.byref(c), 16, 4, 16, 2, 4,
+                                      0.1, 16, 64, 24, None, 0, None) == 1
+    # empty batch is a no-op
+    assert lib.paged_attention_decode(16, ctypes.byref(c), 16, 4, 16, 0, 4,
+                                      0.1, 16, 64, 0, None, 0, None) == 0
+    assert lib.paged_attention_partition_tokens(8, 64, 8, 1000, 17) == -1
