@@ -56,6 +56,26 @@ def dist_info():
     return world, rank, local
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings over the process group (the
+    slowest rank sets the whole-job time); identity without one."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or \
+            dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64,
+                     device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_gbs(world: int, bytes_per_rank: int, ms_per_step: float) -> float:
+    """Aggregate throughput: every rank moves bytes_per_rank per step and
+    the job's step time is the slowest rank's."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def kernel_sha() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -335,15 +355,13 @@ def run_ours(args):
         raise RuntimeError(f"device error {st} at {detail} in the timed region")
 
     attn_ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
-    if world > 1:
-        t = torch.tensor([elapsed_ms, e2e_ms, attn_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms, e2e_ms, attn_ms = [float(x) for x in t.tolist()]
+    elapsed_ms, e2e_ms, attn_ms = max_over_ranks([elapsed_ms, e2e_ms, attn_ms],
+                                                 device=dev)
 
     kv_bytes = W.kv_read_bytes()
     ms_per_step = elapsed_ms / K
-    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
-    e2e_value = world * kv_bytes / (e2e_ms / K2 * 1e-3) / 1e9
+    value = whole_job_gbs(world, kv_bytes, ms_per_step)
+    e2e_value = whole_job_gbs(world, kv_bytes, e2e_ms / K2)
     peak, peak_kind = measured_peak()
     achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
     traffic = profiled_traffic()

@@ -65,7 +65,7 @@ def test_fp8_write_extremes_bit_exact():
 def test_write_skips_negative_and_reports_out_of_range():
     W = wl.tiny_mha()
     G = _pool(W)
-    before = G.cache.key_cache.clone()
+    before = G.cache.key_cache.view(torch.uint8).clone()  # NaN canaries: compare bytes
     T = 4
     k = torch.zeros((T, W.num_kv_heads, W.head_dim), dtype=torch.bfloat16,
                     device="cuda")
@@ -74,7 +74,7 @@ def test_write_skips_negative_and_reports_out_of_range():
     paged_kv_write(k, k, slots, G.cache)
     st, detail = pkv_check()
     assert st == PKV_ERR_RANGE and detail in (2, 3)
-    assert torch.equal(G.cache.key_cache, before)
+    assert torch.equal(G.cache.key_cache.view(torch.uint8), before)
     assert pkv_check()[0] == PKV_OK  # cleared
 
 
