@@ -145,6 +145,39 @@ int32_t paged_attention_partition_tokens(int32_t batch, int32_t num_heads,
                                          int32_t max_seq_len,
                                          int32_t partition_tokens);
 
+/* Size of the fixed device scratch area used by
+ * paged_attention_decode_noalloc (16 MiB). */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* paged_attention_decode for callers that cannot allocate device memory
+ * (code running where cudaMalloc is forbidden or unavailable: inside an
+ * allocator or allocation callback, under a device-memory budget already
+ * fully handed out, or in a runtime without its own device allocator).
+ * The paper has no counterpart to this entry point; it exists for such
+ * callers only.
+ *   Arguments are those of paged_attention_decode without the workspace:
+ *   the split-KV partials go to a library-owned __device__ array of
+ *   PKV_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
+ *   until the process exits.  Calls whose scratch need
+ *   (paged_attention_workspace_bytes for the same arguments) exceeds that
+ *   size return PKV_ERR_WORKSPACE without launching anything.  The call
+ *   allocates nothing.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) and caches it: make that first call before any
+ *   stream capture.  All calls share the array and it keeps the last
+ *   call's contents (nothing in it needs to start at zero); calls whose
+ *   kernels overlap on the GPU race on it, so order them on one stream or
+ *   with events. */
+pkv_status paged_attention_decode_noalloc(const void *q, const pkv_cache *cache,
+                                          const int32_t *block_tables,
+                                          int32_t max_blocks,
+                                          const int32_t *seq_lens,
+                                          int32_t batch, int32_t num_heads,
+                                          float scale, void *out,
+                                          int32_t max_seq_len,
+                                          int32_t partition_tokens,
+                                          void *stream);
+
 /* Synchronise `stream`, then read and clear the device error word of the
  * current device.  Returns PKV_OK, PKV_ERR_RANGE or PKV_ERR_TIMEOUT (the
  * first error recorded since the last check), or PKV_ERR_CUDA.  When

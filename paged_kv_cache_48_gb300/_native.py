@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_ARG", 2: "PKV_ERR_DTYPE",
                 6: "PKV_ERR_TIMEOUT", 7: "PKV_ERR_WORKSPACE"}
 PKV_BF16 = 0
 PKV_FP8_E4M3 = 1
+PKV_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class PkvCache(ctypes.Structure):
@@ -46,6 +47,10 @@ _SIGNATURES = {
         _P, ctypes.POINTER(PkvCache), _P, ctypes.c_int32, _P, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_float, _P, ctypes.c_int32, ctypes.c_int32,
         _P, ctypes.c_size_t, _P]),
+    "paged_attention_decode_noalloc": (ctypes.c_int, [
+        _P, ctypes.POINTER(PkvCache), _P, ctypes.c_int32, _P, ctypes.c_int32,
+        ctypes.c_int32, ctypes.c_float, _P, ctypes.c_int32, ctypes.c_int32,
+        _P]),
     "paged_attention_workspace_bytes": (ctypes.c_size_t, [
         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_int32]),
