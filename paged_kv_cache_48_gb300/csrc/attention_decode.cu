@@ -9,26 +9,29 @@
 // excluded by selection, never multiplied by zero (vLLM v0.17.1 notes,
 // admirer.cn, "重点：35219": 0 x NaN = NaN).
 //
-// Design (one GPU, HBM-bound):
-//  * Grid = (partition, sequence, kv head x query sub-group).  A CTA owns one
-//    kv head of one partition of one sequence and at most 8 of that head's
-//    query heads.  Long sequences are cut into partitions whose
-//    (max, sum, normalised output) triples a second kernel merges with a
-//    log-sum-exp reduction.
-//  * Each of the CTA's warps streams its own subset of the partition's
-//    16-token blocks through a private ring of shared-memory stages.  Lane 0
-//    reads the physical block id from the block table and issues TMA tile
-//    loads (4-D tensor map over [num_blocks, 16, num_kv_heads, head_dim],
-//    box = 16 tokens x 128 bytes, 128-byte swizzle) that complete on the
-//    stage's mbarrier.  The block table indirection is just the 4th TMA
-//    coordinate.
-//  * Per block: S^T = K . Q^T with mma.sync m16n8k16 (16 tokens x 8 query
-//    heads x head_dim), online softmax over tokens with warp shuffles, then
-//    O^T += V^T . P^T (head_dim x 8 x 16 tokens); P^T is formed from the
-//    score fragment with movmatrix.  fp8 E4M3 tiles are decoded to f16 in
-//    registers (exact) and multiplied with an f16 copy of q; k_scale is
-//    folded into the score scale and v_scale into the output.
-//  * The warps' partial states are merged through shared memory.
+// Work unit: an "item" is one kv head (and up to 8 of its query heads) of
+// one sequence; its KV is a chain of 16-token blocks.  Every warp streams
+// blocks through a private ring of shared-memory stages: lane 0 reads the
+// physical block id from the block table and issues TMA tile loads (4-D
+// tensor map over [num_blocks, 16, num_kv_heads, head_dim], box = 16 tokens
+// x 128 bytes, 128-byte swizzle) that complete on the stage's mbarrier.  The
+// block-table indirection is simply the 4th TMA coordinate.  Per block:
+// S^T = K . Q^T with mma.sync m16n8k16 (16 tokens x 8 query heads x
+// head_dim), an online softmax over tokens with warp shuffles, then
+// O^T += V^T . P^T (P^T formed with movmatrix).  fp8 E4M3 tiles are decoded
+// to f16 in registers (exact) and multiplied with an f16 copy of q; k_scale
+// is folded into the score scale and v_scale into the output.
+//
+// Two schedules share that per-block code:
+//  * balanced stream (automatic): a persistent grid; the concatenated block
+//    chains of all items are cut into one equal contiguous range per warp.
+//    A warp's range covers pieces of one or more items; a piece that is a
+//    whole item writes the output, other pieces write (max, sum, output)
+//    partials that a log-sum-exp merge combines.
+//  * fixed partitions (explicit partition length): one CTA per
+//    (partition, sequence, kv head); its warps share the partition's blocks
+//    and merge through shared memory; split sequences are merged by the same
+//    kind of log-sum-exp reduce.
 // Every reduction has a fixed order, so results are bitwise deterministic
 // and independent of where blocks sit in the pool.
 #include <cudaTypedefs.h>
@@ -50,10 +53,15 @@ struct DecodeParams {
   const int32_t *block_tables;  // [B, max_blocks]
   const int32_t *seq_lens;      // [B]
   __nv_bfloat16 *out;           // [B, Hq, D]
-  float *part_o;                // [B, Hq, max_parts, D]
-  float2 *part_ml;              // [B, Hq, max_parts]: (max * log2e, sum)
-  int32_t batch, num_heads, num_kv_heads, group, q_groups;
-  int32_t num_blocks, max_blocks, max_parts, part_tokens;
+  // fixed partitions: [B, Hq, max_parts, D] and [B, Hq, max_parts]
+  float *part_o;
+  float2 *part_ml;  // (max in log2 units, sum)
+  // balanced stream: pieces [(warps + items), hp, D], [(warps + items), hp]
+  float *piece_o;
+  float2 *piece_ml;
+  unsigned long long *meta;  // [items]: first warp | last warp << 32
+  int32_t batch, num_heads, num_kv_heads, group, q_groups, hp;
+  int32_t num_blocks, max_blocks, max_seq_len, max_parts, part_tokens;
   float scale_log2;  // scale * log2(e) (* k_scale for fp8)
   float v_scale;     // 1 for bf16
   unsigned long long timeout_ns;
@@ -79,6 +87,17 @@ struct Cfg {
                 "combine scratch must fit in a warp's ring");
 };
 
+__device__ __forceinline__ int clamp_len(int L, int cap) {
+  return L < 0 ? 0 : (L > cap ? cap : L);
+}
+
+// Row of head_dim held by output fragment element (m-tile mt, upper half
+// `hi` of the 16 rows) for lane group g = lane / 4.
+template <bool FP8>
+__device__ __forceinline__ int o_row(int mt, int hi, int g) {
+  return FP8 ? 16 * mt + 2 * g + hi : 16 * mt + 8 * hi + g;
+}
+
 template <bool FP8>
 __device__ __forceinline__ void mma_kv(float (&d)[4], uint32_t a0, uint32_t a1,
                                        uint32_t a2, uint32_t a3, uint32_t b0,
@@ -89,13 +108,466 @@ __device__ __forceinline__ void mma_kv(float (&d)[4], uint32_t a0, uint32_t a1,
     mma_bf16(d, a0, a1, a2, a3, b0, b1);
 }
 
-// Row of head_dim held by output fragment element (m-tile mt, upper half
-// `hi` of the 16 rows) for lane group g = lane / 4.
-template <bool FP8>
-__device__ __forceinline__ int o_row(int mt, int hi, int g) {
-  return FP8 ? 16 * mt + 2 * g + hi : 16 * mt + 8 * hi + g;
+// Online-softmax state of one warp over one piece of an item.  Lane
+// (g = lane/4, c = lane%4) holds columns (query heads) 2c and 2c+1: the
+// running max and sum (log2 domain) and O^T rows o_row(mt, hi, g).
+template <bool FP8, int D>
+struct WarpState {
+  float o[Cfg<FP8, D>::MT][4];
+  float m0, m1, l0, l1;
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int mt = 0; mt < Cfg<FP8, D>::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+  }
+  // Sum of l over the lanes that share a column.
+  __device__ __forceinline__ void reduce_l() {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+  }
+};
+
+// B-operand fragments of S^T = K . Q^T for query heads qh0 .. qh0+7 (heads
+// at or past `valid` are zero).  fp8 tiles hand each lane 4 consecutive
+// head_dim values per row, so the k order of the mma is permuted to match
+// (a dot product does not depend on it) and q is loaded in that order.
+template <bool FP8, int D>
+__device__ __forceinline__ void load_q(uint32_t (&qf)[Cfg<FP8, D>::MT][2],
+                                       const __nv_bfloat16 *q_item, int valid, int lane) {
+  const int g = lane >> 2, c = lane & 3;
+  const __nv_bfloat16 *qrow = q_item + (size_t)g * D;
+#pragma unroll
+  for (int ks = 0; ks < Cfg<FP8, D>::MT; ++ks) {
+    if (g >= valid) {
+      qf[ks][0] = qf[ks][1] = 0u;
+      continue;
+    }
+    if (!FP8) {
+      qf[ks][0] = __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * ks + 2 * c));
+      qf[ks][1] = __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * ks + 8 + 2 * c));
+    } else {
+      const uint2 four = __ldg(reinterpret_cast<const uint2 *>(qrow + 16 * ks + 4 * c));
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&four.x));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&four.y));
+      qf[ks][0] = pack_f16x2(f0.x, f0.y);
+      qf[ks][1] = pack_f16x2(f1.x, f1.y);
+    }
+  }
 }
 
+// One 16-token block: scores, online softmax update and P.V accumulation.
+// sk/sv: shared addresses of the K and V tiles; nv: valid tokens (0..16).
+template <bool FP8, int D>
+__device__ __forceinline__ void attend_block(uint32_t sk, uint32_t sv, int nv,
+                                             const uint32_t (&qf)[Cfg<FP8, D>::MT][2],
+                                             float scale_log2, WarpState<FP8, D> &st,
+                                             int lane) {
+  using C = Cfg<FP8, D>;
+  const int g = lane >> 2, c = lane & 3;
+  // ldmatrix source rows/chunks for this lane (fragment layouts of
+  // mma.m16n8k16): K uses (row = lane%8 + 8*bit3, chunk = 2x + bit4), V^T
+  // uses (row = lane%8 + 8*bit4, chunk = 2x + bit3) for bf16 and the K
+  // pattern for fp8.
+  const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int k_chk = lane >> 4;
+  const int v_row = FP8 ? k_row : (lane & 7) + (lane >> 4) * 8;
+  const int v_chk = FP8 ? k_chk : (lane >> 3) & 1;
+
+  // -- S^T[16 tokens x 8 heads] = K . Q^T ----------------------------------
+  float sc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (!FP8) {
+#pragma unroll
+    for (int ks = 0; ks < C::MT; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * ks + k_chk), a0, a1, a2, a3);
+      mma_kv<FP8>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+    }
+  } else {
+#pragma unroll
+    for (int kp = 0; kp < C::MT / 2; ++kp) {
+      uint32_t r0, r1, r2, r3;
+      ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * kp + k_chk), r0, r1, r2, r3);
+      mma_kv<FP8>(sc, e4m3x2_to_f16x2(r0 & 0xffff), e4m3x2_to_f16x2(r1 & 0xffff),
+                  e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0],
+                  qf[2 * kp][1]);
+      mma_kv<FP8>(sc, e4m3x2_to_f16x2(r2 & 0xffff), e4m3x2_to_f16x2(r3 & 0xffff),
+                  e4m3x2_to_f16x2(r2 >> 16), e4m3x2_to_f16x2(r3 >> 16), qf[2 * kp + 1][0],
+                  qf[2 * kp + 1][1]);
+    }
+  }
+
+  // -- online softmax per query-head column -------------------------------
+  // sc[0], sc[1]: token g, heads 2c, 2c+1; sc[2], sc[3]: token g + 8.
+  const bool v_lo = g < nv, v_hi = g + 8 < nv;
+  const float s0 = v_lo ? sc[0] * scale_log2 : -INFINITY;
+  const float s1 = v_lo ? sc[1] * scale_log2 : -INFINITY;
+  const float s2 = v_hi ? sc[2] * scale_log2 : -INFINITY;
+  const float s3 = v_hi ? sc[3] * scale_log2 : -INFINITY;
+  float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+  }
+  const float mn0 = fmaxf(st.m0, bm0), mn1 = fmaxf(st.m1, bm1);
+  const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+  const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float al0 = exp2f(st.m0 - mu0), al1 = exp2f(st.m1 - mu1);
+  const float p0 = exp2f(s0 - mu0), p2 = exp2f(s2 - mu0);
+  const float p1 = exp2f(s1 - mu1), p3 = exp2f(s3 - mu1);
+  st.l0 = st.l0 * al0 + (p0 + p2);
+  st.l1 = st.l1 * al1 + (p1 + p3);
+  st.m0 = mn0;
+  st.m1 = mn1;
+#pragma unroll
+  for (int mt = 0; mt < C::MT; ++mt) {
+    st.o[mt][0] *= al0;
+    st.o[mt][1] *= al1;
+    st.o[mt][2] *= al0;
+    st.o[mt][3] *= al1;
+  }
+
+  // -- P^T fragment (B operand of O^T += V^T . P^T) -----------------------
+  const uint32_t pb0 = movmatrix_trans(FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
+  const uint32_t pb1 = movmatrix_trans(FP8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
+
+  // V rows past the sequence may hold stale NaN/Inf bits: zero them in the
+  // A fragment (tokens 2c, 2c+1 in regs 0/1, 8+2c, 9+2c in regs 2/3), so
+  // that p = 0 never meets a NaN inside the mma.
+  uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+  if (nv < 16) {
+    vm_lo = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
+    vm_hi = (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
+  }
+
+  // -- O^T[head_dim x 8] += V^T . P^T -------------------------------------
+  if (!FP8) {
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt) {
+      uint32_t a0, a1, a2, a3;
+      ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * mt + v_chk), a0, a1, a2, a3);
+      mma_kv<FP8>(st.o[mt], a0 & vm_lo, a1 & vm_lo, a2 & vm_hi, a3 & vm_hi, pb0, pb1);
+    }
+  } else {
+#pragma unroll
+    for (int qq = 0; qq < C::MT / 2; ++qq) {
+      uint32_t r0, r1, r2, r3;
+      ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * qq + v_chk), r0, r1, r2, r3);
+      // r0/r2: tokens 2c, 2c+1 (rows 0-7); r1/r3: tokens 8+2c, 9+2c.  Each
+      // holds [t0 dA, t0 dB, t1 dA, t1 dB]; regroup per head_dim row.
+      const uint32_t x0 = prmt(r0, 0u, 0x3120u), x1 = prmt(r1, 0u, 0x3120u);
+      const uint32_t x2 = prmt(r2, 0u, 0x3120u), x3 = prmt(r3, 0u, 0x3120u);
+      mma_kv<FP8>(st.o[2 * qq], e4m3x2_to_f16x2(x0 & 0xffff) & vm_lo,
+                  e4m3x2_to_f16x2(x0 >> 16) & vm_lo, e4m3x2_to_f16x2(x1 & 0xffff) & vm_hi,
+                  e4m3x2_to_f16x2(x1 >> 16) & vm_hi, pb0, pb1);
+      mma_kv<FP8>(st.o[2 * qq + 1], e4m3x2_to_f16x2(x2 & 0xffff) & vm_lo,
+                  e4m3x2_to_f16x2(x2 >> 16) & vm_lo, e4m3x2_to_f16x2(x3 & 0xffff) & vm_hi,
+                  e4m3x2_to_f16x2(x3 >> 16) & vm_hi, pb0, pb1);
+    }
+  }
+}
+
+// Lane 0 issues the TMA loads of one block-head (K and V) into a stage.
+template <bool FP8, int D>
+__device__ __forceinline__ void issue_block(uint8_t *stage, uint64_t *bar,
+                                            const CUtensorMap *tk, const CUtensorMap *tv,
+                                            int kvh, int phys, uint64_t policy) {
+  using C = Cfg<FP8, D>;
+  mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+#pragma unroll
+  for (int bx = 0; bx < C::NBOX; ++bx)
+    tma_load_4d(stage + bx * 16 * C::BOX_BYTES, tk, bar, bx * C::BOX_ELEMS, kvh, 0, phys, policy);
+#pragma unroll
+  for (int bx = 0; bx < C::NBOX; ++bx)
+    tma_load_4d(stage + C::TILE_BYTES + bx * 16 * C::BOX_BYTES, tv, bar, bx * C::BOX_ELEMS, kvh,
+                0, phys, policy);
+}
+
+// ===========================================================================
+// Balanced stream schedule
+// ===========================================================================
+
+// Position in the concatenated block chains of all items (item = (b, hq)
+// with hq = kv head * q_groups + query sub-group; items ordered b-major).
+struct Cursor {
+  int b, L, n, hq, j;  // sequence, its clamped length, its blocks, item, block
+  long long base;      // index of (b, hq = 0, j = 0) in the stream
+};
+
+__device__ __forceinline__ int blocks_of(const DecodeParams &p, int b, int cap) {
+  return (clamp_len(__ldg(p.seq_lens + b), cap) + 15) >> 4;
+}
+
+// Moves a cursor to the next block of the stream (skipping empty
+// sequences).  Only called while the stream has a next block.
+__device__ __forceinline__ void advance(Cursor &cu, const DecodeParams &p, int HQ, int cap) {
+  if (++cu.j < cu.n) return;
+  cu.j = 0;
+  if (++cu.hq < HQ) return;
+  cu.hq = 0;
+  cu.base += (long long)cu.n * HQ;
+  do {
+    ++cu.b;
+    cu.L = clamp_len(__ldg(p.seq_lens + cu.b), cap);
+    cu.n = (cu.L + 15) >> 4;
+  } while (cu.n == 0 && cu.b + 1 < p.batch);
+}
+
+template <bool FP8, int D>
+__global__ void __launch_bounds__(Cfg<FP8, D>::NW * 32)
+paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                           const __grid_constant__ CUtensorMap tmap_v,
+                           const DecodeParams p) {
+  using C = Cfg<FP8, D>;
+  extern __shared__ uint8_t smem_dyn[];
+  __shared__ uint64_t bars[C::NW][C::STAGES];
+  __shared__ int stage_ok[C::NW][C::STAGES];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const uint32_t base_u32 = smem_u32(smem_dyn);
+  uint8_t *ring = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32) +
+                  warp * C::STAGES * C::STAGE_BYTES;
+  if (lane == 0) {
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[warp][s], 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  __syncwarp();
+  grid_dependency_wait();
+  allow_dependent_launch();
+
+  const int HQ = p.num_kv_heads * p.q_groups;
+  const int cap = min(p.max_blocks * 16, p.max_seq_len);
+  const long long W = (long long)gridDim.x * C::NW;
+  const long long w = (long long)blockIdx.x * C::NW + warp;
+
+  // -- total blocks T of the stream; record out-of-range lengths once ------
+  long long T = 0;
+  for (int b0 = 0; b0 < p.batch; b0 += 32) {
+    const int b = b0 + lane;
+    if (b < p.batch) {
+      const int L = __ldg(p.seq_lens + b);
+      if (w == 0 && (L < 0 || L > cap)) record_error(&g_err_attention, PKV_ERR_RANGE, b);
+      T += (clamp_len(L, cap) + 15) >> 4;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) T += __shfl_xor_sync(0xffffffffu, T, off);
+  T *= HQ;
+  const long long start = w * T / W, end = (w + 1) * T / W;
+  if (start >= end) return;
+
+  // -- locate the first block of this warp's range -------------------------
+  Cursor cu;
+  {
+    long long run = 0;  // blocks per item of sequences before b0
+    for (int b0 = 0;; b0 += 32) {
+      const int b = b0 + lane;
+      const int n = b < p.batch ? blocks_of(p, b, cap) : 0;
+      int incl = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const bool past = b < p.batch && (run + incl) * HQ > start;
+      const unsigned mask = __ballot_sync(0xffffffffu, past);
+      if (mask) {
+        const int src = __ffs(mask) - 1;
+        cu.b = b0 + src;
+        cu.n = __shfl_sync(0xffffffffu, n, src);
+        cu.base = (run + __shfl_sync(0xffffffffu, incl - n, src)) * HQ;
+        break;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    cu.L = clamp_len(__ldg(p.seq_lens + cu.b), cap);
+    const long long off = start - cu.base;
+    cu.hq = (int)(off / cu.n);
+    cu.j = (int)(off - (long long)cu.hq * cu.n);
+  }
+  const long long total = end - start;
+
+  // -- issue side: cursor, 32-entry window of block ids ---------------------
+  Cursor ci = cu;
+  int win_b = -1, win_j = -1, ids = 0;
+  const uint64_t policy = l2_policy_evict_normal();
+  long long issued = 0;
+  auto issue_next = [&]() {
+    const int jw = ci.j & ~31;
+    if (ci.b != win_b || jw != win_j) {
+      win_b = ci.b;
+      win_j = jw;
+      const int jj = jw + lane;
+      ids = jj < ci.n ? __ldg(p.block_tables + (size_t)ci.b * p.max_blocks + jj) : -1;
+    }
+    int phys = __shfl_sync(0xffffffffu, ids, ci.j & 31);
+    if (lane == 0) {
+      const int stage = (int)(issued % C::STAGES);
+      int ok = 1;
+      if (phys < 0 || phys >= p.num_blocks) {
+        record_error(&g_err_attention, PKV_ERR_RANGE, ci.b);
+        phys = 0;
+        ok = 0;
+      }
+      stage_ok[warp][stage] = ok;
+      issue_block<FP8, D>(ring + stage * C::STAGE_BYTES, &bars[warp][stage], &tmap_k, &tmap_v,
+                          ci.hq / p.q_groups, phys, policy);
+    }
+    ++issued;
+    if (issued < total) advance(ci, p, HQ, cap);
+  };
+
+  const int pre = (int)(total < C::STAGES ? total : (long long)C::STAGES);
+  for (int i = 0; i < pre; ++i) issue_next();
+
+  // -- compute side ---------------------------------------------------------
+  WarpState<FP8, D> st;
+  st.reset();
+  uint32_t qf[C::MT][2];
+  int piece_j0 = cu.j;
+  int kvh = cu.hq / p.q_groups, qg = cu.hq - kvh * p.q_groups;
+  int heads_here = min(8, p.group - qg * 8);
+  load_q<FP8, D>(qf, p.q + ((size_t)cu.b * p.num_heads + kvh * p.group + qg * 8) * D, heads_here,
+                 lane);
+
+  bool failed = false;
+  for (long long i = 0; i < total; ++i) {
+    const int stage = (int)(i % C::STAGES);
+    if (!mbar_wait_bounded(&bars[warp][stage], (uint32_t)((i / C::STAGES) & 1), p.timeout_ns)) {
+      failed = true;
+      break;
+    }
+    const int nv = stage_ok[warp][stage] ? min(16, cu.L - cu.j * 16) : 0;
+    const uint32_t sk = smem_u32(ring + stage * C::STAGE_BYTES);
+    attend_block<FP8, D>(sk, sk + C::TILE_BYTES, nv, qf, p.scale_log2, st, lane);
+    __syncwarp();
+    if (issued < total) issue_next();
+
+    // -- end of a piece: the item's last block or the range's last block ----
+    const bool last_of_item = cu.j == cu.n - 1;
+    if (last_of_item || i == total - 1) {
+      st.reduce_l();
+      const long long s = (long long)cu.b * HQ + cu.hq;
+      if (piece_j0 == 0) {
+        // first piece of the item records which warps hold its pieces
+        const long long ps = cu.base + (long long)cu.hq * cu.n;
+        const long long wl = ((ps + cu.n) * W - 1) / T;
+        if (lane == 0) p.meta[s] = (unsigned long long)w | ((unsigned long long)wl << 32);
+      }
+      const bool whole = piece_j0 == 0 && last_of_item;
+      const float inv0 = st.l0 > 0.f ? p.v_scale / st.l0 : 0.f;
+      const float inv1 = st.l1 > 0.f ? p.v_scale / st.l1 : 0.f;
+      if (whole) {
+        __nv_bfloat16 *orow =
+            p.out + ((size_t)cu.b * p.num_heads + kvh * p.group + qg * 8) * D;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            const int d = o_row<FP8>(mt, hi, g);
+            if (2 * c < heads_here)
+              orow[(size_t)(2 * c) * D + d] = __float2bfloat16_rn(st.o[mt][2 * hi] * inv0);
+            if (2 * c + 1 < heads_here)
+              orow[(size_t)(2 * c + 1) * D + d] = __float2bfloat16_rn(st.o[mt][2 * hi + 1] * inv1);
+          }
+        }
+      } else {
+        const long long slot = w + s;
+        float *po = p.piece_o + (size_t)slot * p.hp * D;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+          for (int hi = 0; hi < 2; ++hi) {
+            const int d = o_row<FP8>(mt, hi, g);
+            if (2 * c < heads_here) po[(size_t)(2 * c) * D + d] = st.o[mt][2 * hi] * inv0;
+            if (2 * c + 1 < heads_here) po[(size_t)(2 * c + 1) * D + d] = st.o[mt][2 * hi + 1] * inv1;
+          }
+        }
+        if (g == 0) {
+          if (2 * c < heads_here) p.piece_ml[slot * p.hp + 2 * c] = make_float2(st.m0, st.l0);
+          if (2 * c + 1 < heads_here)
+            p.piece_ml[slot * p.hp + 2 * c + 1] = make_float2(st.m1, st.l1);
+        }
+      }
+      if (i + 1 < total) {
+        advance(cu, p, HQ, cap);
+        st.reset();
+        piece_j0 = cu.j;  // 0: a new item starts
+        kvh = cu.hq / p.q_groups;
+        qg = cu.hq - kvh * p.q_groups;
+        heads_here = min(8, p.group - qg * 8);
+        load_q<FP8, D>(qf, p.q + ((size_t)cu.b * p.num_heads + kvh * p.group + qg * 8) * D,
+                       heads_here, lane);
+      }
+    } else {
+      advance(cu, p, HQ, cap);
+    }
+  }
+
+  if (failed) {
+    if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, cu.b);
+    // Let copies still in flight land before the CTA exits (bounded too).
+    for (long long i = 0; i < issued; ++i)
+      mbar_wait_bounded(&bars[warp][i % C::STAGES], (uint32_t)((i / C::STAGES) & 1),
+                        p.timeout_ns);
+  }
+}
+
+// Merge of the stream schedule's pieces: one warp per (sequence, query
+// head).  Items held by one warp were written by the decode kernel; empty
+// sequences get zeros here.  result = sum_w 2^(m_w - M) l_w o_w /
+// sum_w 2^(m_w - M) l_w over the item's pieces, in warp order.
+template <int D>
+__global__ void __launch_bounds__(256) paged_decode_stream_reduce_kernel(const DecodeParams p) {
+  grid_dependency_wait();
+  allow_dependent_launch();
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= (long long)p.batch * p.num_heads) return;
+  const int b = (int)(row / p.num_heads);
+  const int h = (int)(row - (long long)b * p.num_heads);
+  const int cap = min(p.max_blocks * 16, p.max_seq_len);
+  __nv_bfloat16 *orow = p.out + (size_t)row * D;
+  if (clamp_len(__ldg(p.seq_lens + b), cap) == 0) {
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) orow[lane + 32 * k] = __float2bfloat16_rn(0.f);
+    return;
+  }
+  const int kvh = h / p.group, hl = h - kvh * p.group;
+  const int qg = hl >> 3, hh = hl & 7;
+  const long long s = (long long)b * p.num_kv_heads * p.q_groups + kvh * p.q_groups + qg;
+  const unsigned long long meta = p.meta[s];
+  const long long wf = (long long)(meta & 0xffffffffull), wl = (long long)(meta >> 32);
+  if (wf == wl) return;
+  float M = -INFINITY;
+  for (long long w = wf; w <= wl; ++w) M = fmaxf(M, p.piece_ml[(w + s) * p.hp + hh].x);
+  float wsum = 0.f, acc[D / 32];
+#pragma unroll
+  for (int k = 0; k < D / 32; ++k) acc[k] = 0.f;
+  for (long long w = wf; w <= wl; ++w) {
+    const float2 ml = p.piece_ml[(w + s) * p.hp + hh];
+    const float e = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M) * ml.y;
+    wsum += e;
+    const float *po = p.piece_o + ((size_t)(w + s) * p.hp + hh) * D;
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) acc[k] += e * po[lane + 32 * k];
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+  for (int k = 0; k < D / 32; ++k) orow[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
+}
+
+// ===========================================================================
+// Fixed-partition schedule
+// ===========================================================================
 template <bool FP8, int D>
 __global__ void __launch_bounds__(Cfg<FP8, D>::NW * 32)
 paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -110,21 +582,34 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = lane >> 2;  // fragment row group
-  const int c = lane & 3;   // fragment column pair
+  const int g = lane >> 2;
+  const int c = lane & 3;
   const int part = blockIdx.x;
   const int b = blockIdx.y;
   const int kvh = blockIdx.z / p.q_groups;
   const int qg = blockIdx.z - kvh * p.q_groups;
 
+  const uint32_t base_u32 = smem_u32(smem_dyn);
+  uint8_t *rings = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32);
+  uint8_t *ring = rings + warp * C::STAGES * C::STAGE_BYTES;
+  if (lane == 0) {
+    for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[warp][s], 1);
+    fence_barrier_init();
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  __syncwarp();
+  grid_dependency_wait();
+  allow_dependent_launch();
+
   // ---- sequence extent and this CTA's partition --------------------------
   int L = __ldg(p.seq_lens + b);
   {
-    const int cap = min(p.max_blocks * 16, p.max_parts * p.part_tokens);
+    const int cap = min(p.max_blocks * 16, p.max_seq_len);
     if (L < 0 || L > cap) {
       if (part == 0 && blockIdx.z == 0 && threadIdx.x == 0)
         record_error(&g_err_attention, PKV_ERR_RANGE, b);
-      L = L < 0 ? 0 : cap;
+      L = clamp_len(L, cap);
     }
   }
   const int nparts = L <= p.part_tokens ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
@@ -136,55 +621,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int my_n = nblk > warp ? (nblk - warp + C::NW - 1) / C::NW : 0;
   const int heads_here = min(8, p.group - qg * 8);
 
-  // ---- shared memory ring of this warp -----------------------------------
-  const uint32_t base_u32 = smem_u32(smem_dyn);
-  uint8_t *ring = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32) +
-                  warp * C::STAGES * C::STAGE_BYTES;
-  if (lane == 0) {
-    for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[warp][s], 1);
-    fence_barrier_init();
-  }
-  __syncwarp();
-
-  // ---- query fragments (B operand of S^T = K . Q^T) -----------------------
-  // Lane holds, for query head n = g of the sub-group, the head_dim pairs
-  // that the A fragment of the same k-step pairs with.
   uint32_t qf[C::MT][2];
-  {
-    const bool valid = g < heads_here;
-    const int head = kvh * p.group + qg * 8 + g;
-    const __nv_bfloat16 *qrow = p.q + ((size_t)b * p.num_heads + head) * D;
-#pragma unroll
-    for (int ks = 0; ks < C::MT; ++ks) {
-      if (!valid) {
-        qf[ks][0] = qf[ks][1] = 0u;
-        continue;
-      }
-      if (!FP8) {
-        qf[ks][0] = __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * ks + 2 * c));
-        qf[ks][1] = __ldg(reinterpret_cast<const unsigned int *>(qrow + 16 * ks + 8 + 2 * c));
-      } else {
-        // fp8 tiles give lane 4 consecutive head_dim values per row; the
-        // k index order of the mma is permuted to match (a dot product is
-        // order-free), so q is loaded in the same permuted order.
-        const uint2 four = __ldg(reinterpret_cast<const uint2 *>(qrow + 16 * ks + 4 * c));
-        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&four.x));
-        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&four.y));
-        qf[ks][0] = pack_f16x2(f0.x, f0.y);
-        qf[ks][1] = pack_f16x2(f1.x, f1.y);
-      }
-    }
-  }
+  load_q<FP8, D>(qf, p.q + ((size_t)b * p.num_heads + kvh * p.group + qg * 8) * D, heads_here,
+                 lane);
 
   // ---- block ids of this warp, 32 at a time in registers -----------------
   const int32_t *table = p.block_tables + (size_t)b * p.max_blocks + blk0 + warp;
   int ids_reg = -1;
   const uint64_t policy = l2_policy_evict_normal();
-  if (lane == 0) {
-    prefetch_tensormap(&tmap_k);
-    prefetch_tensormap(&tmap_v);
-  }
-
   auto issue = [&](int i) {
     if ((i & 31) == 0) ids_reg = (i + lane < my_n) ? __ldg(table + (i + lane) * C::NW) : -1;
     int phys = __shfl_sync(0xffffffffu, ids_reg, i & 31);
@@ -197,38 +641,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
         ok = 0;
       }
       stage_ok[warp][stage] = ok;
-      uint8_t *sk = ring + stage * C::STAGE_BYTES;
-      uint8_t *sv = sk + C::TILE_BYTES;
-      uint64_t *bar = &bars[warp][stage];
-      mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
-#pragma unroll
-      for (int bx = 0; bx < C::NBOX; ++bx)
-        tma_load_4d(sk + bx * 16 * C::BOX_BYTES, &tmap_k, bar, bx * C::BOX_ELEMS, kvh, 0,
-                    phys, policy);
-#pragma unroll
-      for (int bx = 0; bx < C::NBOX; ++bx)
-        tma_load_4d(sv + bx * 16 * C::BOX_BYTES, &tmap_v, bar, bx * C::BOX_ELEMS, kvh, 0,
-                    phys, policy);
+      issue_block<FP8, D>(ring + stage * C::STAGE_BYTES, &bars[warp][stage], &tmap_k, &tmap_v,
+                          kvh, phys, policy);
     }
   };
 
-  float o[C::MT][4];
-#pragma unroll
-  for (int mt = 0; mt < C::MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
+  WarpState<FP8, D> st;
+  st.reset();
   int issued = 0;
   const int pre = min(C::STAGES, my_n);
   for (; issued < pre; ++issued) issue(issued);
-
-  // ldmatrix source rows/chunks for this lane (see the fragment layouts of
-  // mma.m16n8k16): K uses (row = lane%8 + 8*bit3, chunk = 2x + bit4),
-  // V^T uses (row = lane%8 + 8*bit4, chunk = 2x + bit3) for bf16 and the K
-  // pattern for fp8.
-  const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8;
-  const int k_chk = lane >> 4;
-  const int v_row = FP8 ? k_row : (lane & 7) + (lane >> 4) * 8;
-  const int v_chk = FP8 ? k_chk : (lane >> 3) & 1;
 
   bool failed = false;
   for (int i = 0; i < my_n; ++i) {
@@ -240,120 +662,20 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const int j = blk0 + warp + i * C::NW;
     const int nv = stage_ok[warp][stage] ? min(16, tok1 - j * 16) : 0;
     const uint32_t sk = smem_u32(ring + stage * C::STAGE_BYTES);
-    const uint32_t sv = sk + C::TILE_BYTES;
-
-    // -- S^T[16 tokens x 8 heads] = K . Q^T --------------------------------
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (!FP8) {
-#pragma unroll
-      for (int ks = 0; ks < C::MT; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * ks + k_chk), a0, a1, a2, a3);
-        mma_kv<FP8>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-      }
-    } else {
-#pragma unroll
-      for (int kp = 0; kp < C::MT / 2; ++kp) {
-        uint32_t r0, r1, r2, r3;
-        ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * kp + k_chk), r0, r1, r2, r3);
-        mma_kv<FP8>(sc, e4m3x2_to_f16x2(r0 & 0xffff), e4m3x2_to_f16x2(r1 & 0xffff),
-                    e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0],
-                    qf[2 * kp][1]);
-        mma_kv<FP8>(sc, e4m3x2_to_f16x2(r2 & 0xffff), e4m3x2_to_f16x2(r3 & 0xffff),
-                    e4m3x2_to_f16x2(r2 >> 16), e4m3x2_to_f16x2(r3 >> 16),
-                    qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
-      }
-    }
-
-    // -- online softmax over the block's tokens, per query-head column ----
-    // sc[0], sc[1]: token g, heads 2c, 2c+1; sc[2], sc[3]: token g + 8.
-    const bool v_lo = g < nv, v_hi = g + 8 < nv;
-    const float s0 = v_lo ? sc[0] * p.scale_log2 : -INFINITY;
-    const float s1 = v_lo ? sc[1] * p.scale_log2 : -INFINITY;
-    const float s2 = v_hi ? sc[2] * p.scale_log2 : -INFINITY;
-    const float s3 = v_hi ? sc[3] * p.scale_log2 : -INFINITY;
-    float bm0 = fmaxf(s0, s2), bm1 = fmaxf(s1, s3);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-      bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-    }
-    const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = exp2f(m0 - mu0), al1 = exp2f(m1 - mu1);
-    const float p0 = exp2f(s0 - mu0), p2 = exp2f(s2 - mu0);
-    const float p1 = exp2f(s1 - mu1), p3 = exp2f(s3 - mu1);
-    l0 = l0 * al0 + (p0 + p2);
-    l1 = l1 * al1 + (p1 + p3);
-    m0 = mn0;
-    m1 = mn1;
-#pragma unroll
-    for (int mt = 0; mt < C::MT; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
-    }
-
-    // -- P^T fragment (B operand of O^T += V^T . P^T) ---------------------
-    const uint32_t pb0 = movmatrix_trans(FP8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1));
-    const uint32_t pb1 = movmatrix_trans(FP8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3));
-
-    // V rows past the sequence may hold stale NaN/Inf bits: zero them in
-    // the A fragment (tokens 2c, 2c+1 in regs 0/1, 8+2c, 9+2c in regs 2/3),
-    // so that p = 0 never meets a NaN inside the mma.
-    uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-    if (nv < 16) {
-      vm_lo = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
-      vm_hi = (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
-    }
-
-    // -- O^T[head_dim x 8] += V^T . P^T -----------------------------------
-    if (!FP8) {
-#pragma unroll
-      for (int mt = 0; mt < C::MT; ++mt) {
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * mt + v_chk), a0, a1, a2, a3);
-        mma_kv<FP8>(o[mt], a0 & vm_lo, a1 & vm_lo, a2 & vm_hi, a3 & vm_hi, pb0, pb1);
-      }
-    } else {
-#pragma unroll
-      for (int qq = 0; qq < C::MT / 2; ++qq) {
-        uint32_t r0, r1, r2, r3;
-        ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * qq + v_chk), r0, r1, r2, r3);
-        // r0/r2: tokens 2c, 2c+1 (rows 0-7); r1/r3: tokens 8+2c, 9+2c.
-        // Each holds [t0 dA, t0 dB, t1 dA, t1 dB]; regroup per head_dim row.
-        const uint32_t x0 = prmt(r0, 0u, 0x3120u), x1 = prmt(r1, 0u, 0x3120u);
-        const uint32_t x2 = prmt(r2, 0u, 0x3120u), x3 = prmt(r3, 0u, 0x3120u);
-        mma_kv<FP8>(o[2 * qq], e4m3x2_to_f16x2(x0 & 0xffff) & vm_lo,
-                    e4m3x2_to_f16x2(x0 >> 16) & vm_lo, e4m3x2_to_f16x2(x1 & 0xffff) & vm_hi,
-                    e4m3x2_to_f16x2(x1 >> 16) & vm_hi, pb0, pb1);
-        mma_kv<FP8>(o[2 * qq + 1], e4m3x2_to_f16x2(x2 & 0xffff) & vm_lo,
-                    e4m3x2_to_f16x2(x2 >> 16) & vm_lo, e4m3x2_to_f16x2(x3 & 0xffff) & vm_hi,
-                    e4m3x2_to_f16x2(x3 >> 16) & vm_hi, pb0, pb1);
-      }
-    }
-
+    attend_block<FP8, D>(sk, sk + C::TILE_BYTES, nv, qf, p.scale_log2, st, lane);
     __syncwarp();
     if (issued < my_n) issue(issued++);
   }
 
   if (failed) {
     if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, b);
-    // Let copies still in flight land before the ring is reused or the CTA
-    // exits (bounded as well).
     for (int i = 0; i < issued; ++i)
       mbar_wait_bounded(&bars[warp][i % C::STAGES], (i / C::STAGES) & 1, p.timeout_ns);
-    m0 = m1 = -INFINITY;
+    st.m0 = st.m1 = -INFINITY;
   }
 
   // ---- merge the warps' states -------------------------------------------
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
+  st.reduce_l();
   float *o_s = reinterpret_cast<float *>(ring);  // this warp's ring, now idle
   if (!failed && my_n > 0) {
 #pragma unroll
@@ -361,20 +683,19 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
       for (int hi = 0; hi < 2; ++hi) {
         const int d = o_row<FP8>(mt, hi, g);
-        o_s[(2 * c) * C::OS_STRIDE + d] = o[mt][2 * hi];
-        o_s[(2 * c + 1) * C::OS_STRIDE + d] = o[mt][2 * hi + 1];
+        o_s[(2 * c) * C::OS_STRIDE + d] = st.o[mt][2 * hi];
+        o_s[(2 * c + 1) * C::OS_STRIDE + d] = st.o[mt][2 * hi + 1];
       }
     }
   }
   if (g == 0) {
-    m_s[warp][2 * c] = m0;
-    m_s[warp][2 * c + 1] = m1;
-    l_s[warp][2 * c] = l0;
-    l_s[warp][2 * c + 1] = l1;
+    m_s[warp][2 * c] = st.m0;
+    m_s[warp][2 * c + 1] = st.m1;
+    l_s[warp][2 * c] = st.l0;
+    l_s[warp][2 * c + 1] = st.l1;
   }
   __syncthreads();
 
-  const uint8_t *rings = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32);
   for (int idx = threadIdx.x; idx < heads_here * D; idx += blockDim.x) {
     const int h = idx / D;
     const int d = idx - h * D;
@@ -414,10 +735,11 @@ __global__ void __launch_bounds__(D)
 paged_decode_reduce_kernel(const DecodeParams p) {
   extern __shared__ float w_s[];  // [max_parts]
   __shared__ float red[D / 32];
+  grid_dependency_wait();
+  allow_dependent_launch();
   const int h = blockIdx.x, b = blockIdx.y;
-  int L = __ldg(p.seq_lens + b);
-  const int cap = min(p.max_blocks * 16, p.max_parts * p.part_tokens);
-  L = L < 0 ? 0 : (L > cap ? cap : L);
+  const int cap = min(p.max_blocks * 16, p.max_seq_len);
+  const int L = clamp_len(__ldg(p.seq_lens + b), cap);
   const int nparts = L <= p.part_tokens ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
   if (nparts <= 1) return;  // the decode kernel wrote the output directly
   const size_t bh = (size_t)b * p.num_heads + h;
@@ -539,55 +861,103 @@ bool get_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
   return true;
 }
 
-int choose_partition_tokens(int32_t batch, int32_t num_heads, int32_t num_kv_heads,
-                            int32_t max_seq_len, int32_t requested, int sms) {
-  if (requested > 0) return requested;
-  const int64_t whole = std::max<int64_t>(16, ((int64_t)max_seq_len + 15) / 16 * 16);
-  const int group = num_heads / num_kv_heads;
-  const int64_t units = (int64_t)batch * num_kv_heads * ((group + 7) / 8);
-  const int64_t target = (int64_t)sms * 8;  // about 4 waves of 2 CTAs per SM
-  if (units >= target || whole <= 256) return (int)std::min<int64_t>(whole, INT32_MAX / 2);
-  for (int pt = 8192; pt >= 512; pt >>= 1) {
-    if (pt >= whole) continue;
-    if (units * ((whole + pt - 1) / pt) >= target) return pt;
-  }
-  return 256;
+constexpr int kStreamCtasPerSm = 2;  // two 96 KiB rings per SM
+
+// Warps of the balanced stream schedule on the current device.
+int64_t stream_warps(int sms) { return (int64_t)sms * kStreamCtasPerSm * 4; }
+
+struct StreamLayout {
+  size_t o_off, ml_off, meta_off, bytes;
+};
+
+StreamLayout stream_layout(int64_t batch, int64_t num_heads, int64_t num_kv_heads,
+                           int64_t head_dim, int sms) {
+  const int64_t group = num_heads / num_kv_heads;
+  const int64_t q_groups = (group + 7) / 8;
+  const int64_t hp = std::min<int64_t>(8, group);
+  const int64_t items = batch * num_kv_heads * q_groups;
+  const int64_t slots = stream_warps(sms) + items;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  StreamLayout l;
+  l.o_off = 0;
+  l.ml_off = up((size_t)slots * hp * head_dim * sizeof(float));
+  l.meta_off = l.ml_off + up((size_t)slots * hp * sizeof(float2));
+  l.bytes = l.meta_off + up((size_t)items * sizeof(unsigned long long));
+  return l;
 }
 
-template <bool FP8, int D>
-pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                         int grid_x, cudaStream_t s) {
-  using C = Cfg<FP8, D>;
-  static int configured_device = -1;
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (configured_device != dev) {
-      if (cudaFuncSetAttribute(paged_decode_kernel<FP8, D>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::SMEM_BYTES) != cudaSuccess)
-        return PKV_ERR_CUDA;
-      configured_device = dev;
-    }
-  }
-  dim3 grid(grid_x, p.batch, p.num_kv_heads * p.q_groups);
-  paged_decode_kernel<FP8, D><<<grid, C::NW * 32, C::SMEM_BYTES, s>>>(mk, mv, p);
-  if (cudaPeekAtLastError() != cudaSuccess) return PKV_ERR_CUDA;
-  if (p.max_parts > 1) {
-    dim3 rgrid(p.num_heads, p.batch);
-    paged_decode_reduce_kernel<D><<<rgrid, D, p.max_parts * sizeof(float), s>>>(p);
-    if (cudaPeekAtLastError() != cudaSuccess) return PKV_ERR_CUDA;
-  }
-  return PKV_OK;
-}
-
-size_t workspace_for(int32_t batch, int32_t num_heads, int32_t head_dim, int32_t max_parts) {
+size_t partition_workspace(int32_t batch, int32_t num_heads, int32_t head_dim, int32_t max_parts) {
   if (max_parts <= 1) return 0;
   const size_t rows = (size_t)batch * num_heads * max_parts;
   const size_t o_bytes = (rows * head_dim * sizeof(float) + 255) / 256 * 256;
   return o_bytes + rows * sizeof(float2);
+}
+
+// Launch with programmatic stream serialisation (see grid_dependency_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <bool FP8, int D>
+pkv_status configure_smem() {
+  using C = Cfg<FP8, D>;
+  static int configured[64] = {0};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(paged_decode_kernel<FP8, D>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(paged_decode_stream_kernel<FP8, D>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    configured[dev] = 1;
+  }
+  return PKV_OK;
+}
+
+template <bool FP8, int D>
+pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
+                         bool stream_schedule, int sms, cudaStream_t s) {
+  using C = Cfg<FP8, D>;
+  pkv_status st = configure_smem<FP8, D>();
+  if (st != PKV_OK) return st;
+  if (stream_schedule) {
+    const int ctas = sms * kStreamCtasPerSm;
+    if (launch_pdl(paged_decode_stream_kernel<FP8, D>, dim3(ctas), dim3(C::NW * 32),
+                   C::SMEM_BYTES, s, mk, mv, p) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    const long long rows = (long long)p.batch * p.num_heads;
+    if (launch_pdl(paged_decode_stream_reduce_kernel<D>, dim3((unsigned)((rows + 7) / 8)),
+                   dim3(256), 0, s, p) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    return PKV_OK;
+  }
+  dim3 grid(p.max_parts, p.batch, p.num_kv_heads * p.q_groups);
+  if (launch_pdl(paged_decode_kernel<FP8, D>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s, mk, mv,
+                 p) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (p.max_parts > 1) {
+    if (launch_pdl(paged_decode_reduce_kernel<D>, dim3(p.num_heads, p.batch), dim3(D),
+                   p.max_parts * sizeof(float), s, p) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
 }
 
 }  // namespace
@@ -617,20 +987,25 @@ extern "C" int32_t paged_attention_partition_tokens(int32_t batch, int32_t num_h
   if (batch < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
       max_seq_len < 0 || partition_tokens < 0 || partition_tokens % 16)
     return -1;
-  const int sms = device_sm_count();
-  return choose_partition_tokens(batch, num_heads, num_kv_heads, max_seq_len, partition_tokens,
-                                 sms > 0 ? sms : 148);
+  return partition_tokens;  // 0: balanced stream schedule
 }
 
 extern "C" size_t paged_attention_workspace_bytes(int32_t batch, int32_t num_heads,
                                                   int32_t num_kv_heads, int32_t head_dim,
                                                   int32_t max_seq_len,
                                                   int32_t partition_tokens) {
-  const int32_t pt = paged_attention_partition_tokens(batch, num_heads, num_kv_heads,
-                                                      max_seq_len, partition_tokens);
-  if (pt <= 0 || batch <= 0 || head_dim <= 0) return 0;
-  const int32_t max_parts = (int32_t)(((int64_t)max_seq_len + pt - 1) / pt);
-  return workspace_for(batch, num_heads, head_dim, max_parts);
+  if (paged_attention_partition_tokens(batch, num_heads, num_kv_heads, max_seq_len,
+                                       partition_tokens) < 0 ||
+      batch <= 0 || head_dim <= 0)
+    return 0;
+  if (partition_tokens == 0) {
+    const int sms = device_sm_count();
+    return stream_layout(batch, num_heads, num_kv_heads, head_dim, sms > 0 ? sms : 148).bytes;
+  }
+  const int64_t parts = std::max<int64_t>(1, ((int64_t)max_seq_len + partition_tokens - 1) /
+                                                 partition_tokens);
+  if (parts > INT32_MAX / 2) return 0;
+  return partition_workspace(batch, num_heads, head_dim, (int32_t)parts);
 }
 
 extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cache,
@@ -655,52 +1030,68 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
   const int group = num_heads / cache->num_kv_heads;
   const int q_groups = (group + 7) / 8;
   if ((int64_t)cache->num_kv_heads * q_groups > 65535) return PKV_ERR_ARG;
-
   const int sms = device_sm_count();
   if (sms <= 0) return PKV_ERR_CUDA;
-  const int pt = choose_partition_tokens(batch, num_heads, cache->num_kv_heads, max_seq_len,
-                                         partition_tokens, sms);
-  const int64_t parts64 = std::max<int64_t>(1, ((int64_t)max_seq_len + pt - 1) / pt);
-  if (parts64 > INT32_MAX / 2) return PKV_ERR_ARG;
-  const int max_parts = (int)parts64;
-  const size_t need = workspace_for(batch, num_heads, cache->head_dim, max_parts);
+  const bool stream_schedule = partition_tokens == 0;
+
+  DecodeParams p;
+  std::memset(&p, 0, sizeof p);
+  const size_t need = paged_attention_workspace_bytes(batch, num_heads, cache->num_kv_heads,
+                                                      cache->head_dim, max_seq_len,
+                                                      partition_tokens);
   if (need > 0) {
     if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
-    if ((size_t)max_parts * sizeof(float) > 48 * 1024) return PKV_ERR_ARG;
+  }
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  if (stream_schedule) {
+    const StreamLayout l =
+        stream_layout(batch, num_heads, cache->num_kv_heads, cache->head_dim, sms);
+    p.piece_o = reinterpret_cast<float *>(ws + l.o_off);
+    p.piece_ml = reinterpret_cast<float2 *>(ws + l.ml_off);
+    p.meta = reinterpret_cast<unsigned long long *>(ws + l.meta_off);
+    p.max_parts = 1;
+    p.part_tokens = 0;
+  } else {
+    const int64_t parts64 =
+        std::max<int64_t>(1, ((int64_t)max_seq_len + partition_tokens - 1) / partition_tokens);
+    if (parts64 > INT32_MAX / 2) return PKV_ERR_ARG;
+    p.max_parts = (int)parts64;
+    p.part_tokens = partition_tokens;
+    if (need > 0) {
+      if ((size_t)p.max_parts * sizeof(float) > 48 * 1024) return PKV_ERR_ARG;
+      p.part_o = reinterpret_cast<float *>(ws);
+      p.part_ml = reinterpret_cast<float2 *>(
+          ws + ((size_t)batch * num_heads * p.max_parts * cache->head_dim * sizeof(float) + 255) /
+                   256 * 256);
+    }
   }
 
   CUtensorMap mk, mv;
   if (!get_maps(cache, &mk, &mv)) return PKV_ERR_CUDA;
 
-  DecodeParams p;
   p.q = static_cast<const __nv_bfloat16 *>(q);
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
   p.out = static_cast<__nv_bfloat16 *>(out);
-  p.part_o = need ? static_cast<float *>(workspace) : nullptr;
-  p.part_ml = need ? reinterpret_cast<float2 *>(
-                         static_cast<uint8_t *>(workspace) +
-                         ((size_t)batch * num_heads * max_parts * cache->head_dim * sizeof(float) +
-                          255) / 256 * 256)
-                   : nullptr;
   p.batch = batch;
   p.num_heads = num_heads;
   p.num_kv_heads = cache->num_kv_heads;
   p.group = group;
   p.q_groups = q_groups;
+  p.hp = std::min(8, group);
   p.num_blocks = cache->num_blocks;
   p.max_blocks = max_blocks;
-  p.max_parts = max_parts;
-  p.part_tokens = pt;
+  p.max_seq_len = max_seq_len;
   p.scale_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
   p.v_scale = fp8 ? cache->v_scale : 1.f;
   p.timeout_ns = 2000000000ull;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (fp8)
-    return cache->head_dim == 128 ? launch_decode<true, 128>(mk, mv, p, max_parts, s)
-                                  : launch_decode<true, 64>(mk, mv, p, max_parts, s);
-  return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, max_parts, s)
-                                : launch_decode<false, 64>(mk, mv, p, max_parts, s);
+    return cache->head_dim == 128
+               ? launch_decode<true, 128>(mk, mv, p, stream_schedule, sms, s)
+               : launch_decode<true, 64>(mk, mv, p, stream_schedule, sms, s);
+  return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, stream_schedule, sms, s)
+                                : launch_decode<false, 64>(mk, mv, p, stream_schedule, sms, s);
 }

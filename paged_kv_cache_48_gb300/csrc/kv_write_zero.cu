@@ -12,6 +12,7 @@
 // sized in multiples of the SM count, no shared memory.
 #include <algorithm>
 #include <cstring>
+#include <utility>
 
 #include "pkv_device.cuh"
 #include "pkv_host.h"
@@ -33,6 +34,8 @@ kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                 int vecs_per_row, uint8_t *__restrict__ key_cache,
                 uint8_t *__restrict__ value_cache, int64_t num_slots,
                 float k_scale, float v_scale) {
+  grid_dependency_wait();
+  allow_dependent_launch();
   const int64_t total = num_tokens * vecs_per_row;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
        idx < total; idx += (int64_t)gridDim.x * blockDim.x) {
@@ -109,6 +112,8 @@ __global__ void __launch_bounds__(256)
 zero_blocks_kernel(uint4 *__restrict__ key_cache, uint4 *__restrict__ value_cache,
                    int64_t vecs_per_block, int32_t num_blocks,
                    const int32_t *__restrict__ ids, int64_t n) {
+  grid_dependency_wait();
+  allow_dependent_launch();
   for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
     const int32_t id = __ldg(ids + i);
     if (id < 0 || id >= num_blocks) {
@@ -125,6 +130,8 @@ zero_blocks_param_kernel(uint4 *__restrict__ key_cache,
                          uint4 *__restrict__ value_cache,
                          int64_t vecs_per_block, int32_t num_blocks,
                          const __grid_constant__ ZeroIds ids, int64_t id_base) {
+  grid_dependency_wait();
+  allow_dependent_launch();
   for (int i = blockIdx.x; i < ids.n; i += gridDim.x) {
     const int32_t id = ids.ids[i];
     if (id < 0 || id >= num_blocks) {
@@ -139,6 +146,23 @@ zero_blocks_param_kernel(uint4 *__restrict__ key_cache,
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
+// Launch with programmatic stream serialisation (see grid_dependency_wait).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                              cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 unsigned long long read_and_clear_error_write_zero(cudaStream_t s,
                                                    cudaError_t *err) {
   unsigned long long v = 0ull;
@@ -183,20 +207,19 @@ extern "C" pkv_status paged_kv_write(const void *k, const void *v,
   const int grid = (int)std::min<int64_t>(want, (int64_t)sms * 8);
   const int64_t num_slots = (int64_t)cache->num_blocks * cache->block_size;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
   if (fp8)
-    kv_write_kernel<true><<<grid, threads, 0, s>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
-        slot_mapping, num_tokens, vecs_per_row,
-        static_cast<uint8_t *>(cache->key_cache),
-        static_cast<uint8_t *>(cache->value_cache), num_slots, cache->k_scale,
-        cache->v_scale);
+    e = launch_pdl(kv_write_kernel<true>, dim3(grid), dim3(threads), s,
+                   static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
+                   num_tokens, vecs_per_row, static_cast<uint8_t *>(cache->key_cache),
+                   static_cast<uint8_t *>(cache->value_cache), num_slots, cache->k_scale,
+                   cache->v_scale);
   else
-    kv_write_kernel<false><<<grid, threads, 0, s>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
-        slot_mapping, num_tokens, vecs_per_row,
-        static_cast<uint8_t *>(cache->key_cache),
-        static_cast<uint8_t *>(cache->value_cache), num_slots, 1.f, 1.f);
-  return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    e = launch_pdl(kv_write_kernel<false>, dim3(grid), dim3(threads), s,
+                   static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping,
+                   num_tokens, vecs_per_row, static_cast<uint8_t *>(cache->key_cache),
+                   static_cast<uint8_t *>(cache->value_cache), num_slots, 1.f, 1.f);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 extern "C" pkv_status paged_kv_zero_blocks(const pkv_cache *cache,
@@ -219,10 +242,10 @@ extern "C" pkv_status paged_kv_zero_blocks(const pkv_cache *cache,
   const int threads = 256;
   if (!ids_on_host) {
     const int grid = (int)std::min<int64_t>(n, (int64_t)sms * 16);
-    zero_blocks_kernel<<<grid, threads, 0, s>>>(kc, vc, vecs_per_block,
-                                                 cache->num_blocks, block_ids,
-                                                 n);
-    return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return launch_pdl(zero_blocks_kernel, dim3(grid), dim3(threads), s, kc, vc,
+                      vecs_per_block, cache->num_blocks, block_ids, n) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
   }
   // Host ids travel inside the launch parameters, kZeroIdsPerLaunch at a
   // time; the parameter block is copied at launch, so the caller's buffer
@@ -233,9 +256,9 @@ extern "C" pkv_status paged_kv_zero_blocks(const pkv_cache *cache,
     chunk.n = m;
     std::memcpy(chunk.ids, block_ids + base, sizeof(int32_t) * m);
     const int grid = std::min(m, sms * 16);
-    zero_blocks_param_kernel<<<grid, threads, 0, s>>>(
-        kc, vc, vecs_per_block, cache->num_blocks, chunk, base);
-    if (cudaPeekAtLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (launch_pdl(zero_blocks_param_kernel, dim3(grid), dim3(threads), s, kc, vc,
+                   vecs_per_block, cache->num_blocks, chunk, base) != cudaSuccess)
+      return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }

@@ -29,6 +29,21 @@ __device__ __forceinline__ void record_error(unsigned long long *word,
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialisation; it waits for its predecessor in
+// the stream (completion and memory flush) before touching global memory,
+// and immediately lets its own successor start launching, so launch latency
+// overlaps the predecessor's tail.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Shared memory addressing
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

@@ -29,6 +29,11 @@ SMALL = {
                                         kv_dtype="fp8_e4m3",
                                         fresh_policy="recycle515"),
     "mha_d128": lambda: wl.make_workload("mha_d128", 5, 4, 4, 128, 1, 90, 33),
+    # many items per warp under the balanced schedule
+    "many_mid": lambda: wl.make_workload("many_mid", 512, 8, 2, 128, 16, 200, 34),
+    # empty sequences first, in the middle and last (cursor skips them)
+    "gaps": lambda: wl.make_workload("gaps", 7, 8, 2, 128, 0, 0, 35,
+                                     seq_lens=[0, 300, 0, 0, 45, 1, 0]),
 }
 
 _cache = {}
@@ -68,6 +73,9 @@ def test_deterministic_and_split_equivalence():
     a = harness.gpu_step(W, G).clone()
     b = harness.gpu_step(W, G).clone()
     assert torch.equal(a, b)
+    e = harness.gpu_step(W, G, partition_tokens=512).clone()
+    f = harness.gpu_step(W, G, partition_tokens=512).clone()
+    assert torch.equal(e, f)
     whole = ((W.max_seq_len + 15) // 16) * 16
     c = harness.gpu_step(W, G, partition_tokens=whole).clone()
     d = harness.gpu_step(W, G, partition_tokens=whole + 16).clone()
@@ -95,11 +103,12 @@ def _relocate(W, rng):
 
 
 @pytest.mark.parametrize("name", ["llama_small", "fp8_small", "prefix_small"])
-def test_block_placement_does_not_change_bits(name):
+@pytest.mark.parametrize("partition_tokens", [0, 64])
+def test_block_placement_does_not_change_bits(name, partition_tokens):
     W, _ = _case(name)
     W2 = _relocate(W, np.random.default_rng(9))
-    a = harness.run_gpu(W, partition_tokens=64, want_cache=False)["out"]
-    b = harness.run_gpu(W2, partition_tokens=64, want_cache=False)["out"]
+    a = harness.run_gpu(W, partition_tokens=partition_tokens, want_cache=False)["out"]
+    b = harness.run_gpu(W2, partition_tokens=partition_tokens, want_cache=False)["out"]
     assert np.array_equal(a, b)
 
 
@@ -113,12 +122,13 @@ def test_single_key_returns_its_value_exactly():
             assert np.array_equal(res["out"][b, h], v[b, h // 4])
 
 
-def test_empty_sequence_gives_zeros_and_others_unaffected():
+@pytest.mark.parametrize("partition_tokens", [0, 16])
+def test_empty_sequence_gives_zeros_and_others_unaffected(partition_tokens):
     W = wl.make_workload("with_empty", 4, 8, 2, 128, 0, 0, 8,
                          seq_lens=[0, 40, 0, 17])
     kc, vc = harness.oracle_cache(W)
     ref = harness.oracle_out(W, kc, vc)
-    res = harness.run_gpu(W, partition_tokens=16, want_cache=False)
+    res = harness.run_gpu(W, partition_tokens=partition_tokens, want_cache=False)
     assert res["status"] == PKV_OK
     assert np.array_equal(res["out"][[0, 2]], np.zeros_like(res["out"][[0, 2]]))
     harness.assert_close(res["out"], ref, "bf16")
@@ -148,7 +158,6 @@ def test_seq_len_beyond_bound_is_reported():
 
 
 def test_auto_partition_choice_is_reported():
-    pt = paged_attention_partition_tokens(64, 32, 8, 4096, 0)
-    assert pt > 0 and pt % 16 == 0
+    assert paged_attention_partition_tokens(64, 32, 8, 4096, 0) == 0  # balanced
     assert paged_attention_partition_tokens(8, 64, 8, 131072, 512) == 512
     assert paged_attention_partition_tokens(8, 64, 8, 131072, 17) == -1
