@@ -345,7 +345,7 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   const int HQ = p.num_kv_heads * p.q_groups;
   const int cap = min(p.max_blocks * 16, p.max_seq_len);
-  const long long W = (long long)gridDim.x * C::NW;
+  const long long W_grid = (long long)gridDim.x * C::NW;
   const long long w = (long long)blockIdx.x * C::NW + warp;
 
   // -- total blocks T of the stream; record out-of-range lengths once ------
@@ -361,8 +361,12 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) T += __shfl_xor_sync(0xffffffffu, T, off);
   T *= HQ;
+  // Cut the stream into min(warps, T) ranges so that every range is
+  // non-empty: the merge then finds a piece at every warp between an item's
+  // first and last warp.
+  const long long W = T < W_grid ? T : W_grid;
+  if (w >= W) return;
   const long long start = w * T / W, end = (w + 1) * T / W;
-  if (start >= end) return;
 
   // -- locate the first block of this warp's range -------------------------
   Cursor cu;
