@@ -39,6 +39,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "pkv_device.cuh"
@@ -56,11 +57,15 @@ struct DecodeParams {
   // fixed partitions: [B, Hq, max_parts, D] and [B, Hq, max_parts]
   float *part_o;
   float2 *part_ml;  // (max in log2 units, sum)
-  // balanced stream: pieces [(warps + items), hp, D], [(warps + items), hp]
+  // balanced stream: pieces [(ctas + items), item q heads, D] and
+  // [(ctas + items), item q heads]; one ticket word per item
   float *piece_o;
   float2 *piece_ml;
-  unsigned long long *meta;  // [items]: first warp | last warp << 32
-  int32_t batch, num_heads, num_kv_heads, group, q_groups, hp;
+  unsigned long long *tickets;
+  unsigned long long epoch;  // 1 .. 2^40-1, distinct per call
+  int32_t hg;                // kv heads per item (stream schedule)
+  int32_t ring_slots;        // K or V slots in a CTA's ring (stream schedule)
+  int32_t batch, num_heads, num_kv_heads, group, q_groups;
   int32_t num_blocks, max_blocks, max_seq_len, max_parts, part_tokens;
   float scale_log2;  // scale * log2(e) (* k_scale for fp8)
   float v_scale;     // 1 for bf16
@@ -159,26 +164,19 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[Cfg<FP8, D>::MT][2],
   }
 }
 
-// One 16-token block: scores, online softmax update and P.V accumulation.
-// sk/sv: shared addresses of the K and V tiles; nv: valid tokens (0..16).
+// S^T[16 tokens x 8 heads] = K . Q^T for one 16-token block; sk is the
+// shared address of the K tile.  sc[0], sc[1]: token g, heads 2c, 2c+1;
+// sc[2], sc[3]: token g + 8.
 template <bool FP8, int D>
-__device__ __forceinline__ void attend_block(uint32_t sk, uint32_t sv, int nv,
+__device__ __forceinline__ void block_scores(uint32_t sk,
                                              const uint32_t (&qf)[Cfg<FP8, D>::MT][2],
-                                             float scale_log2, WarpState<FP8, D> &st,
-                                             int lane) {
+                                             float (&sc)[4], int lane) {
   using C = Cfg<FP8, D>;
-  const int g = lane >> 2, c = lane & 3;
   // ldmatrix source rows/chunks for this lane (fragment layouts of
-  // mma.m16n8k16): K uses (row = lane%8 + 8*bit3, chunk = 2x + bit4), V^T
-  // uses (row = lane%8 + 8*bit4, chunk = 2x + bit3) for bf16 and the K
-  // pattern for fp8.
+  // mma.m16n8k16): K uses (row = lane%8 + 8*bit3, chunk = 2x + bit4).
   const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8;
   const int k_chk = lane >> 4;
-  const int v_row = FP8 ? k_row : (lane & 7) + (lane >> 4) * 8;
-  const int v_chk = FP8 ? k_chk : (lane >> 3) & 1;
-
-  // -- S^T[16 tokens x 8 heads] = K . Q^T ----------------------------------
-  float sc[4] = {0.f, 0.f, 0.f, 0.f};
+  sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
   if (!FP8) {
 #pragma unroll
     for (int ks = 0; ks < C::MT; ++ks) {
@@ -199,6 +197,20 @@ __device__ __forceinline__ void attend_block(uint32_t sk, uint32_t sv, int nv,
                   qf[2 * kp + 1][1]);
     }
   }
+}
+
+// Online softmax update with one block's scores and P.V accumulation; sv is
+// the shared address of the V tile, nv the block's valid tokens (0..16).
+template <bool FP8, int D>
+__device__ __forceinline__ void block_update(uint32_t sv, int nv, const float (&sc)[4],
+                                             float scale_log2, WarpState<FP8, D> &st,
+                                             int lane) {
+  using C = Cfg<FP8, D>;
+  const int g = lane >> 2, c = lane & 3;
+  // V^T uses (row = lane%8 + 8*bit4, chunk = 2x + bit3) for bf16 and the K
+  // pattern for fp8.
+  const int v_row = FP8 ? (lane & 7) + ((lane >> 3) & 1) * 8 : (lane & 7) + (lane >> 4) * 8;
+  const int v_chk = FP8 ? lane >> 4 : (lane >> 3) & 1;
 
   // -- online softmax per query-head column -------------------------------
   // sc[0], sc[1]: token g, heads 2c, 2c+1; sc[2], sc[3]: token g + 8.
@@ -271,6 +283,17 @@ __device__ __forceinline__ void attend_block(uint32_t sk, uint32_t sv, int nv,
   }
 }
 
+// One 16-token block: scores, online softmax update and P.V accumulation.
+template <bool FP8, int D>
+__device__ __forceinline__ void attend_block(uint32_t sk, uint32_t sv, int nv,
+                                             const uint32_t (&qf)[Cfg<FP8, D>::MT][2],
+                                             float scale_log2, WarpState<FP8, D> &st,
+                                             int lane) {
+  float sc[4];
+  block_scores<FP8, D>(sk, qf, sc, lane);
+  block_update<FP8, D>(sv, nv, sc, scale_log2, st, lane);
+}
+
 // Lane 0 issues the TMA loads of one block-head (K and V) into a stage.
 template <bool FP8, int D>
 __device__ __forceinline__ void issue_block(uint8_t *stage, uint64_t *bar,
@@ -290,26 +313,41 @@ __device__ __forceinline__ void issue_block(uint8_t *stage, uint64_t *bar,
 // ===========================================================================
 // Balanced stream schedule
 // ===========================================================================
+// Item = (sequence b, group kg of hg consecutive kv heads with all their
+// query heads).  The block chains of all items, concatenated b-major, are
+// cut into one equal contiguous range per CTA (one CTA per SM).  In a CTA a
+// producer warp walks its range and, per block, TMA-loads the K tiles of all
+// hg heads into one ring slot and the V tiles into the next, so the whole
+// contiguous K (then V) segment of the block is requested at once.  One
+// consumer warp per (kv head, query sub-group) computes on its head's tiles
+// and releases a slot as soon as it is done with it (K right after the
+// scores).  An item that ends up whole in one CTA writes the output; the
+// pieces of an item split across CTAs are written as (max, sum, output)
+// partials and the CTA that completes the item's last piece merges them
+// (log-sum-exp, pieces in CTA order).  Completion is counted with a ticket
+// word per item: no CTA ever waits for another.
+constexpr int kMaxSlots = 16;
+constexpr int kStreamRingBytes = 192 * 1024;
+constexpr int kMaxConsumerWarps = 8;
 
-// Position in the concatenated block chains of all items (item = (b, hq)
-// with hq = kv head * q_groups + query sub-group; items ordered b-major).
+// Position in the concatenated block chains (item order b-major, then kg).
 struct Cursor {
-  int b, L, n, hq, j;  // sequence, its clamped length, its blocks, item, block
-  long long base;      // index of (b, hq = 0, j = 0) in the stream
+  int b, L, n, kg, j;  // sequence, clamped length, blocks, head group, block
+  long long base;      // stream index of (b, kg = 0, j = 0)
 };
 
 __device__ __forceinline__ int blocks_of(const DecodeParams &p, int b, int cap) {
   return (clamp_len(__ldg(p.seq_lens + b), cap) + 15) >> 4;
 }
 
-// Moves a cursor to the next block of the stream (skipping empty
-// sequences).  Only called while the stream has a next block.
-__device__ __forceinline__ void advance(Cursor &cu, const DecodeParams &p, int HQ, int cap) {
+// Next block of the stream (skipping empty sequences); only called while
+// the stream has a next block.
+__device__ __forceinline__ void advance(Cursor &cu, const DecodeParams &p, int NG, int cap) {
   if (++cu.j < cu.n) return;
   cu.j = 0;
-  if (++cu.hq < HQ) return;
-  cu.hq = 0;
-  cu.base += (long long)cu.n * HQ;
+  if (++cu.kg < NG) return;
+  cu.kg = 0;
+  cu.base += (long long)cu.n * NG;
   do {
     ++cu.b;
     cu.L = clamp_len(__ldg(p.seq_lens + cu.b), cap);
@@ -317,256 +355,312 @@ __device__ __forceinline__ void advance(Cursor &cu, const DecodeParams &p, int H
   } while (cu.n == 0 && cu.b + 1 < p.batch);
 }
 
+// Worker (CTA) of stream position x when T blocks are cut into W ranges
+// [floor(w T / W), floor((w + 1) T / W)).
+__device__ __forceinline__ long long worker_of(long long x, long long W, long long T) {
+  return ((x + 1) * W - 1) / T;
+}
+
 template <bool FP8, int D>
-__global__ void __launch_bounds__(Cfg<FP8, D>::NW * 32)
+__global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1)
 paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v,
                            const DecodeParams p) {
   using C = Cfg<FP8, D>;
   extern __shared__ uint8_t smem_dyn[];
-  __shared__ uint64_t bars[C::NW][C::STAGES];
-  __shared__ int stage_ok[C::NW][C::STAGES];
+  __shared__ uint64_t full_bar[kMaxSlots];
+  __shared__ uint64_t empty_bar[kMaxSlots];
+  __shared__ int slot_ok[kMaxSlots];
+  __shared__ long long sh_T, sh_W, sh_start, sh_end;
+  __shared__ Cursor sh_cu;
+  __shared__ int sh_last;
+  __shared__ int sh_abort;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
+  const int ncw = p.hg * p.q_groups;  // consumer warps; warp ncw produces
+  const int NS = p.ring_slots;
+  const int SLOT = p.hg * C::TILE_BYTES;
+  const int NG = p.num_kv_heads / p.hg;
+  const int HQT = p.hg * p.group;  // query heads per item
+  const int cap = min(p.max_blocks * 16, p.max_seq_len);
   const uint32_t base_u32 = smem_u32(smem_dyn);
-  uint8_t *ring = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32) +
-                  warp * C::STAGES * C::STAGE_BYTES;
-  if (lane == 0) {
-    for (int s = 0; s < C::STAGES; ++s) mbar_init(&bars[warp][s], 1);
+  uint8_t *ring = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], ncw);
+    }
     fence_barrier_init();
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
+    sh_abort = 0;
   }
-  __syncwarp();
+  __syncthreads();
   grid_dependency_wait();
   allow_dependent_launch();
 
-  const int HQ = p.num_kv_heads * p.q_groups;
-  const int cap = min(p.max_blocks * 16, p.max_seq_len);
-  const long long W_grid = (long long)gridDim.x * C::NW;
-  const long long w = (long long)blockIdx.x * C::NW + warp;
-
-  // -- total blocks T of the stream; record out-of-range lengths once ------
-  long long T = 0;
-  for (int b0 = 0; b0 < p.batch; b0 += 32) {
-    const int b = b0 + lane;
-    if (b < p.batch) {
-      const int L = __ldg(p.seq_lens + b);
-      if (w == 0 && (L < 0 || L > cap)) record_error(&g_err_attention, PKV_ERR_RANGE, b);
-      T += (clamp_len(L, cap) + 15) >> 4;
-    }
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) T += __shfl_xor_sync(0xffffffffu, T, off);
-  T *= HQ;
-  // Cut the stream into min(warps, T) ranges so that every range is
-  // non-empty: the merge then finds a piece at every warp between an item's
-  // first and last warp.
-  const long long W = T < W_grid ? T : W_grid;
-  if (w >= W) return;
-  const long long start = w * T / W, end = (w + 1) * T / W;
-
-  // -- locate the first block of this warp's range -------------------------
-  Cursor cu;
-  {
-    long long run = 0;  // blocks per item of sequences before b0
-    for (int b0 = 0;; b0 += 32) {
+  // ---- this CTA's range of the stream -------------------------------------
+  if (warp == 0) {
+    long long T = 0;
+    for (int b0 = 0; b0 < p.batch; b0 += 32) {
       const int b = b0 + lane;
-      const int n = b < p.batch ? blocks_of(p, b, cap) : 0;
-      int incl = n;
+      if (b < p.batch) {
+        const int L = __ldg(p.seq_lens + b);
+        if (blockIdx.x == 0 && (L < 0 || L > cap))
+          record_error(&g_err_attention, PKV_ERR_RANGE, b);
+        T += (clamp_len(L, cap) + 15) >> 4;
+      }
+    }
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
+    for (int off = 16; off > 0; off >>= 1) T += __shfl_xor_sync(0xffffffffu, T, off);
+    T *= NG;
+    // min(CTAs, T) ranges, so that no range is empty
+    const long long W = T < (long long)gridDim.x ? T : (long long)gridDim.x;
+    const long long w = blockIdx.x;
+    const long long start = w < W ? w * T / W : 0, end = w < W ? (w + 1) * T / W : 0;
+    Cursor cu = {0, 0, 0, 0, 0, 0};
+    if (start < end) {
+      long long run = 0;  // blocks per head group of sequences before b0
+      for (int b0 = 0;; b0 += 32) {
+        const int b = b0 + lane;
+        const int n = b < p.batch ? blocks_of(p, b, cap) : 0;
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        const unsigned mask = __ballot_sync(0xffffffffu, b < p.batch && (run + incl) * NG > start);
+        if (mask) {
+          const int src = __ffs(mask) - 1;
+          cu.b = b0 + src;
+          cu.n = __shfl_sync(0xffffffffu, n, src);
+          cu.base = (run + __shfl_sync(0xffffffffu, incl - n, src)) * NG;
+          break;
+        }
+        run += __shfl_sync(0xffffffffu, incl, 31);
       }
-      const bool past = b < p.batch && (run + incl) * HQ > start;
-      const unsigned mask = __ballot_sync(0xffffffffu, past);
-      if (mask) {
-        const int src = __ffs(mask) - 1;
-        cu.b = b0 + src;
-        cu.n = __shfl_sync(0xffffffffu, n, src);
-        cu.base = (run + __shfl_sync(0xffffffffu, incl - n, src)) * HQ;
-        break;
-      }
-      run += __shfl_sync(0xffffffffu, incl, 31);
+      cu.L = clamp_len(__ldg(p.seq_lens + cu.b), cap);
+      const long long off = start - cu.base;
+      cu.kg = (int)(off / cu.n);
+      cu.j = (int)(off - (long long)cu.kg * cu.n);
     }
-    cu.L = clamp_len(__ldg(p.seq_lens + cu.b), cap);
-    const long long off = start - cu.base;
-    cu.hq = (int)(off / cu.n);
-    cu.j = (int)(off - (long long)cu.hq * cu.n);
-  }
-  const long long total = end - start;
-
-  // -- issue side: cursor, 32-entry window of block ids ---------------------
-  Cursor ci = cu;
-  int win_b = -1, win_j = -1, ids = 0;
-  const uint64_t policy = l2_policy_evict_normal();
-  long long issued = 0;
-  auto issue_next = [&]() {
-    const int jw = ci.j & ~31;
-    if (ci.b != win_b || jw != win_j) {
-      win_b = ci.b;
-      win_j = jw;
-      const int jj = jw + lane;
-      ids = jj < ci.n ? __ldg(p.block_tables + (size_t)ci.b * p.max_blocks + jj) : -1;
-    }
-    int phys = __shfl_sync(0xffffffffu, ids, ci.j & 31);
     if (lane == 0) {
-      const int stage = (int)(issued % C::STAGES);
-      int ok = 1;
-      if (phys < 0 || phys >= p.num_blocks) {
-        record_error(&g_err_attention, PKV_ERR_RANGE, ci.b);
-        phys = 0;
-        ok = 0;
-      }
-      stage_ok[warp][stage] = ok;
-      issue_block<FP8, D>(ring + stage * C::STAGE_BYTES, &bars[warp][stage], &tmap_k, &tmap_v,
-                          ci.hq / p.q_groups, phys, policy);
+      sh_T = T;
+      sh_W = W;
+      sh_start = start;
+      sh_end = end;
+      sh_cu = cu;
     }
-    ++issued;
-    if (issued < total) advance(ci, p, HQ, cap);
-  };
+  }
+  // ---- rows of empty sequences are zero ------------------------------------
+  if (warp < ncw) {
+    for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+      if (clamp_len(__ldg(p.seq_lens + b), cap) != 0) continue;
+      for (int h = warp; h < p.num_heads; h += ncw)
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k)
+          p.out[((size_t)b * p.num_heads + h) * D + lane + 32 * k] = __float2bfloat16_rn(0.f);
+    }
+  }
+  __syncthreads();
+  const long long T = sh_T, W = sh_W;
+  const long long total = sh_end - sh_start;
+  if (total <= 0) return;
 
-  const int pre = (int)(total < C::STAGES ? total : (long long)C::STAGES);
-  for (int i = 0; i < pre; ++i) issue_next();
+  if (warp == ncw) {
+    // ======================= producer warp ==================================
+    Cursor ci = sh_cu;
+    int win_b = -1, win_j = -1, ids = 0;
+    const uint64_t policy = l2_policy_evict_normal();
+    long long q = 0;
+    bool stop = false;
+    for (long long x = 0; x < total && !stop; ++x) {
+      const int jw = ci.j & ~31;
+      if (ci.b != win_b || jw != win_j) {
+        win_b = ci.b;
+        win_j = jw;
+        const int jj = jw + lane;
+        ids = jj < ci.n ? __ldg(p.block_tables + (size_t)ci.b * p.max_blocks + jj) : -1;
+      }
+      int phys = __shfl_sync(0xffffffffu, ids, ci.j & 31);
+      const int ok = phys >= 0 && phys < p.num_blocks;
+      if (lane == 0) {
+        if (!ok) {
+          record_error(&g_err_attention, PKV_ERR_RANGE, ci.b);
+          phys = 0;
+        }
+        for (int kv = 0; kv < 2; ++kv, ++q) {
+          const int slot = (int)(q % NS);
+          if (q >= NS && !mbar_wait_bounded(&empty_bar[slot], (uint32_t)((q / NS - 1) & 1),
+                                            p.timeout_ns)) {
+            sh_abort = 1;
+            stop = true;
+            break;
+          }
+          slot_ok[slot] = ok;
+          uint64_t *bar = &full_bar[slot];
+          mbar_arrive_expect_tx(bar, SLOT);
+          uint8_t *dst = ring + (size_t)slot * SLOT;
+          const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
+          for (int hl = 0; hl < p.hg; ++hl)
+#pragma unroll
+            for (int bx = 0; bx < C::NBOX; ++bx)
+              tma_load_4d(dst + hl * C::TILE_BYTES + bx * 16 * C::BOX_BYTES, map, bar,
+                          bx * C::BOX_ELEMS, ci.kg * p.hg + hl, 0, phys, policy);
+        }
+      }
+      stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+      if (x + 1 < total) advance(ci, p, NG, cap);
+    }
+    if (lane == 0) {
+      if (stop) record_error(&g_err_attention, PKV_ERR_TIMEOUT, ci.b);
+      // The copies issued last must land before the CTA may exit, whatever
+      // the consumers did (bounded as well).
+      for (long long r = q > NS ? q - NS : 0; r < q; ++r)
+        mbar_wait_bounded(&full_bar[r % NS], (uint32_t)((r / NS) & 1), p.timeout_ns);
+    }
+    return;
+  }
 
-  // -- compute side ---------------------------------------------------------
+  // ========================= consumer warps =================================
+  const int hl = warp % p.hg;
+  const int qg = warp / p.hg;
+  const int heads_here = min(8, p.group - qg * 8);
+  const int qh_local = hl * p.group + qg * 8;  // first query head within the item
+  Cursor cu = sh_cu;
   WarpState<FP8, D> st;
   st.reset();
   uint32_t qf[C::MT][2];
   int piece_j0 = cu.j;
-  int kvh = cu.hq / p.q_groups, qg = cu.hq - kvh * p.q_groups;
-  int heads_here = min(8, p.group - qg * 8);
-  load_q<FP8, D>(qf, p.q + ((size_t)cu.b * p.num_heads + kvh * p.group + qg * 8) * D, heads_here,
-                 lane);
+  auto item_q = [&]() {
+    return p.q + ((size_t)cu.b * p.num_heads + (size_t)cu.kg * HQT + qh_local) * D;
+  };
+  load_q<FP8, D>(qf, item_q(), heads_here, lane);
 
-  bool failed = false;
-  for (long long i = 0; i < total; ++i) {
-    const int stage = (int)(i % C::STAGES);
-    if (!mbar_wait_bounded(&bars[warp][stage], (uint32_t)((i / C::STAGES) & 1), p.timeout_ns)) {
-      failed = true;
-      break;
+  long long q = 0;
+  for (long long x = 0; x < total; ++x) {
+    // K tile: scores, then release the slot
+    int slot = (int)(q % NS);
+    if (!sh_abort && !mbar_wait_bounded(&full_bar[slot], (uint32_t)((q / NS) & 1), p.timeout_ns)) {
+      sh_abort = 1;
+      if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, cu.b);
     }
-    const int nv = stage_ok[warp][stage] ? min(16, cu.L - cu.j * 16) : 0;
-    const uint32_t sk = smem_u32(ring + stage * C::STAGE_BYTES);
-    attend_block<FP8, D>(sk, sk + C::TILE_BYTES, nv, qf, p.scale_log2, st, lane);
+    const int nv = slot_ok[slot] ? min(16, cu.L - cu.j * 16) : 0;
+    float sc[4];
+    block_scores<FP8, D>(smem_u32(ring + (size_t)slot * SLOT + hl * C::TILE_BYTES), qf, sc, lane);
     __syncwarp();
-    if (issued < total) issue_next();
+    if (lane == 0) mbar_arrive(&empty_bar[slot]);
+    ++q;
+    // V tile: softmax update and P.V, then release the slot
+    slot = (int)(q % NS);
+    if (!sh_abort && !mbar_wait_bounded(&full_bar[slot], (uint32_t)((q / NS) & 1), p.timeout_ns)) {
+      sh_abort = 1;
+      if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, cu.b);
+    }
+    block_update<FP8, D>(smem_u32(ring + (size_t)slot * SLOT + hl * C::TILE_BYTES), nv, sc,
+                         p.scale_log2, st, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[slot]);
+    ++q;
 
-    // -- end of a piece: the item's last block or the range's last block ----
     const bool last_of_item = cu.j == cu.n - 1;
-    if (last_of_item || i == total - 1) {
-      st.reduce_l();
-      const long long s = (long long)cu.b * HQ + cu.hq;
-      if (piece_j0 == 0) {
-        // first piece of the item records which warps hold its pieces
-        const long long ps = cu.base + (long long)cu.hq * cu.n;
-        const long long wl = ((ps + cu.n) * W - 1) / T;
-        if (lane == 0) p.meta[s] = (unsigned long long)w | ((unsigned long long)wl << 32);
-      }
-      const bool whole = piece_j0 == 0 && last_of_item;
-      const float inv0 = st.l0 > 0.f ? p.v_scale / st.l0 : 0.f;
-      const float inv1 = st.l1 > 0.f ? p.v_scale / st.l1 : 0.f;
-      if (whole) {
-        __nv_bfloat16 *orow =
-            p.out + ((size_t)cu.b * p.num_heads + kvh * p.group + qg * 8) * D;
+    if (!last_of_item && x + 1 < total) {
+      advance(cu, p, NG, cap);
+      continue;
+    }
+    // ---- end of a piece: the item's last block or this range's last -------
+    st.reduce_l();
+    const long long s = (long long)cu.b * NG + cu.kg;
+    const size_t out_row0 = (size_t)cu.b * p.num_heads + (size_t)cu.kg * HQT + qh_local;
+    const float inv0 = st.l0 > 0.f ? p.v_scale / st.l0 : 0.f;
+    const float inv1 = st.l1 > 0.f ? p.v_scale / st.l1 : 0.f;
+    if (piece_j0 == 0 && last_of_item) {
+      // whole item in this CTA
+      __nv_bfloat16 *orow = p.out + out_row0 * D;
 #pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
+      for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
-          for (int hi = 0; hi < 2; ++hi) {
-            const int d = o_row<FP8>(mt, hi, g);
-            if (2 * c < heads_here)
-              orow[(size_t)(2 * c) * D + d] = __float2bfloat16_rn(st.o[mt][2 * hi] * inv0);
-            if (2 * c + 1 < heads_here)
-              orow[(size_t)(2 * c + 1) * D + d] = __float2bfloat16_rn(st.o[mt][2 * hi + 1] * inv1);
-          }
-        }
-      } else {
-        const long long slot = w + s;
-        float *po = p.piece_o + (size_t)slot * p.hp * D;
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
-#pragma unroll
-          for (int hi = 0; hi < 2; ++hi) {
-            const int d = o_row<FP8>(mt, hi, g);
-            if (2 * c < heads_here) po[(size_t)(2 * c) * D + d] = st.o[mt][2 * hi] * inv0;
-            if (2 * c + 1 < heads_here) po[(size_t)(2 * c + 1) * D + d] = st.o[mt][2 * hi + 1] * inv1;
-          }
-        }
-        if (g == 0) {
-          if (2 * c < heads_here) p.piece_ml[slot * p.hp + 2 * c] = make_float2(st.m0, st.l0);
+        for (int hi = 0; hi < 2; ++hi) {
+          const int d = o_row<FP8>(mt, hi, g);
+          if (2 * c < heads_here)
+            orow[(size_t)(2 * c) * D + d] = __float2bfloat16_rn(st.o[mt][2 * hi] * inv0);
           if (2 * c + 1 < heads_here)
-            p.piece_ml[slot * p.hp + 2 * c + 1] = make_float2(st.m1, st.l1);
+            orow[(size_t)(2 * c + 1) * D + d] = __float2bfloat16_rn(st.o[mt][2 * hi + 1] * inv1);
         }
-      }
-      if (i + 1 < total) {
-        advance(cu, p, HQ, cap);
-        st.reset();
-        piece_j0 = cu.j;  // 0: a new item starts
-        kvh = cu.hq / p.q_groups;
-        qg = cu.hq - kvh * p.q_groups;
-        heads_here = min(8, p.group - qg * 8);
-        load_q<FP8, D>(qf, p.q + ((size_t)cu.b * p.num_heads + kvh * p.group + qg * 8) * D,
-                       heads_here, lane);
       }
     } else {
-      advance(cu, p, HQ, cap);
+      const long long slot_row = ((long long)blockIdx.x + s) * HQT + qh_local;
+      float *po = p.piece_o + (size_t)slot_row * D;
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          const int d = o_row<FP8>(mt, hi, g);
+          if (2 * c < heads_here) po[(size_t)(2 * c) * D + d] = st.o[mt][2 * hi] * inv0;
+          if (2 * c + 1 < heads_here) po[(size_t)(2 * c + 1) * D + d] = st.o[mt][2 * hi + 1] * inv1;
+        }
+      }
+      if (g == 0) {
+        if (2 * c < heads_here) p.piece_ml[slot_row + 2 * c] = make_float2(st.m0, st.l0);
+        if (2 * c + 1 < heads_here) p.piece_ml[slot_row + 2 * c + 1] = make_float2(st.m1, st.l1);
+      }
+      __threadfence();
+      named_barrier_sync(ncw * 32);
+      if (threadIdx.x == 0) {
+        const long long ps = cu.base + (long long)cu.kg * cu.n;
+        const long long pieces = worker_of(ps + cu.n - 1, W, T) - worker_of(ps, W, T) + 1;
+        unsigned long long *ticket = p.tickets + s;
+        unsigned long long old = atomicAdd(ticket, 0ull), want = 0ull;
+        for (int it = 0; it < (1 << 20); ++it) {
+          want = (old >> 24) == p.epoch ? old + 1ull : ((p.epoch << 24) | 1ull);
+          const unsigned long long got = atomicCAS(ticket, old, want);
+          if (got == old) break;
+          old = got;
+        }
+        const bool last = (long long)(want & 0xffffffull) == pieces;
+        if (last) atomicExch(ticket, 0ull);  // clean for the next call
+        sh_last = last ? 1 : 0;
+      }
+      named_barrier_sync(ncw * 32);
+      if (sh_last) {
+        // merge every piece of the item for this warp's query heads
+        __threadfence();
+        const long long ps = cu.base + (long long)cu.kg * cu.n;
+        const long long wf = worker_of(ps, W, T), wl = worker_of(ps + cu.n - 1, W, T);
+        for (int h = 0; h < heads_here; ++h) {
+          float M = -INFINITY;
+          for (long long w = wf; w <= wl; ++w)
+            M = fmaxf(M, __ldcg(&p.piece_ml[(w + s) * HQT + qh_local + h].x));
+          float wsum = 0.f, acc[D / 32];
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) acc[k] = 0.f;
+          for (long long w = wf; w <= wl; ++w) {
+            const float mw = __ldcg(&p.piece_ml[(w + s) * HQT + qh_local + h].x);
+            const float lw = __ldcg(&p.piece_ml[(w + s) * HQT + qh_local + h].y);
+            const float e = mw == -INFINITY ? 0.f : exp2f(mw - M) * lw;
+            wsum += e;
+            const float *pw = p.piece_o + ((size_t)(w + s) * HQT + qh_local + h) * D;
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) acc[k] += e * __ldcg(pw + lane + 32 * k);
+          }
+          const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+          __nv_bfloat16 *orow = p.out + (out_row0 + h) * D;
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) orow[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
+        }
+      }
+    }
+    if (x + 1 < total) {
+      advance(cu, p, NG, cap);
+      st.reset();
+      piece_j0 = cu.j;  // a new item starts at block 0
+      load_q<FP8, D>(qf, item_q(), heads_here, lane);
     }
   }
-
-  if (failed) {
-    if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, cu.b);
-    // Let copies still in flight land before the CTA exits (bounded too).
-    for (long long i = 0; i < issued; ++i)
-      mbar_wait_bounded(&bars[warp][i % C::STAGES], (uint32_t)((i / C::STAGES) & 1),
-                        p.timeout_ns);
-  }
-}
-
-// Merge of the stream schedule's pieces: one warp per (sequence, query
-// head).  Items held by one warp were written by the decode kernel; empty
-// sequences get zeros here.  result = sum_w 2^(m_w - M) l_w o_w /
-// sum_w 2^(m_w - M) l_w over the item's pieces, in warp order.
-template <int D>
-__global__ void __launch_bounds__(256) paged_decode_stream_reduce_kernel(const DecodeParams p) {
-  grid_dependency_wait();
-  allow_dependent_launch();
-  const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (row >= (long long)p.batch * p.num_heads) return;
-  const int b = (int)(row / p.num_heads);
-  const int h = (int)(row - (long long)b * p.num_heads);
-  const int cap = min(p.max_blocks * 16, p.max_seq_len);
-  __nv_bfloat16 *orow = p.out + (size_t)row * D;
-  if (clamp_len(__ldg(p.seq_lens + b), cap) == 0) {
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) orow[lane + 32 * k] = __float2bfloat16_rn(0.f);
-    return;
-  }
-  const int kvh = h / p.group, hl = h - kvh * p.group;
-  const int qg = hl >> 3, hh = hl & 7;
-  const long long s = (long long)b * p.num_kv_heads * p.q_groups + kvh * p.q_groups + qg;
-  const unsigned long long meta = p.meta[s];
-  const long long wf = (long long)(meta & 0xffffffffull), wl = (long long)(meta >> 32);
-  if (wf == wl) return;
-  float M = -INFINITY;
-  for (long long w = wf; w <= wl; ++w) M = fmaxf(M, p.piece_ml[(w + s) * p.hp + hh].x);
-  float wsum = 0.f, acc[D / 32];
-#pragma unroll
-  for (int k = 0; k < D / 32; ++k) acc[k] = 0.f;
-  for (long long w = wf; w <= wl; ++w) {
-    const float2 ml = p.piece_ml[(w + s) * p.hp + hh];
-    const float e = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M) * ml.y;
-    wsum += e;
-    const float *po = p.piece_o + ((size_t)(w + s) * p.hp + hh) * D;
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) acc[k] += e * po[lane + 32 * k];
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-  for (int k = 0; k < D / 32; ++k) orow[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
 }
 
 // ===========================================================================
@@ -865,28 +959,52 @@ bool get_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
   return true;
 }
 
-constexpr int kStreamCtasPerSm = 2;  // two 96 KiB rings per SM
+// Partition length used when the balanced schedule cannot hold an item's
+// query heads in one CTA (more than 64 query heads per kv head).
+constexpr int kFallbackPartition = 512;
 
-// Warps of the balanced stream schedule on the current device.
-int64_t stream_warps(int sms) { return (int64_t)sms * kStreamCtasPerSm * 4; }
-
-struct StreamLayout {
-  size_t o_off, ml_off, meta_off, bytes;
+// Stream schedule geometry: kv heads per item (largest divisor of Hkv whose
+// consumer warps, hg * query sub-groups, fit in one CTA) and ring slots.
+struct StreamGeom {
+  int hg, q_groups, slots, slot_bytes;
+  bool ok;
 };
 
-StreamLayout stream_layout(int64_t batch, int64_t num_heads, int64_t num_kv_heads,
-                           int64_t head_dim, int sms) {
+StreamGeom stream_geom(int64_t num_heads, int64_t num_kv_heads, int64_t head_dim, int dtype) {
+  StreamGeom gm = {0, 0, 0, 0, false};
+  if (num_kv_heads <= 0 || num_heads % num_kv_heads) return gm;
   const int64_t group = num_heads / num_kv_heads;
-  const int64_t q_groups = (group + 7) / 8;
-  const int64_t hp = std::min<int64_t>(8, group);
-  const int64_t items = batch * num_kv_heads * q_groups;
-  const int64_t slots = stream_warps(sms) + items;
+  gm.q_groups = (int)((group + 7) / 8);
+  if (gm.q_groups > kMaxConsumerWarps) return gm;
+  for (int hg = kMaxConsumerWarps / gm.q_groups; hg >= 1; --hg)
+    if (num_kv_heads % hg == 0) {
+      gm.hg = hg;
+      break;
+    }
+  const int64_t tile = 16 * head_dim * (dtype == PKV_FP8_E4M3 ? 1 : 2);
+  gm.slot_bytes = (int)(gm.hg * tile);
+  gm.slots = (int)std::min<int64_t>(kMaxSlots, kStreamRingBytes / gm.slot_bytes);
+  gm.ok = gm.slots >= 2;
+  return gm;
+}
+
+struct StreamLayout {
+  size_t o_off, ml_off, ticket_off, bytes;
+};
+
+// Pieces: (CTAs + items) slots of the item's query heads; one ticket word
+// per item.
+StreamLayout stream_layout(int64_t batch, int64_t num_heads, int64_t num_kv_heads,
+                           int64_t head_dim, int ctas, const StreamGeom &gm) {
+  const int64_t items = batch * (num_kv_heads / gm.hg);
+  const int64_t hqt = gm.hg * (num_heads / num_kv_heads);
+  const int64_t slots = ctas + items;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   StreamLayout l;
   l.o_off = 0;
-  l.ml_off = up((size_t)slots * hp * head_dim * sizeof(float));
-  l.meta_off = l.ml_off + up((size_t)slots * hp * sizeof(float2));
-  l.bytes = l.meta_off + up((size_t)items * sizeof(unsigned long long));
+  l.ml_off = up((size_t)slots * hqt * head_dim * sizeof(float));
+  l.ticket_off = l.ml_off + up((size_t)slots * hqt * sizeof(float2));
+  l.bytes = l.ticket_off + up((size_t)items * sizeof(unsigned long long));
   return l;
 }
 
@@ -928,7 +1046,7 @@ pkv_status configure_smem() {
                              C::SMEM_BYTES) != cudaSuccess ||
         cudaFuncSetAttribute(paged_decode_stream_kernel<FP8, D>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
+                             kStreamRingBytes + 1024) != cudaSuccess)
       return PKV_ERR_CUDA;
     configured[dev] = 1;
   }
@@ -942,13 +1060,10 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
   pkv_status st = configure_smem<FP8, D>();
   if (st != PKV_OK) return st;
   if (stream_schedule) {
-    const int ctas = sms * kStreamCtasPerSm;
-    if (launch_pdl(paged_decode_stream_kernel<FP8, D>, dim3(ctas), dim3(C::NW * 32),
-                   C::SMEM_BYTES, s, mk, mv, p) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    const long long rows = (long long)p.batch * p.num_heads;
-    if (launch_pdl(paged_decode_stream_reduce_kernel<D>, dim3((unsigned)((rows + 7) / 8)),
-                   dim3(256), 0, s, p) != cudaSuccess)
+    const size_t smem = (size_t)p.ring_slots * p.hg * C::TILE_BYTES + 1024;
+    const int threads = (p.hg * p.q_groups + 1) * 32;
+    if (launch_pdl(paged_decode_stream_kernel<FP8, D>, dim3(sms), dim3(threads), smem, s, mk, mv,
+                   p) != cudaSuccess)
       return PKV_ERR_CUDA;
     return PKV_OK;
   }
@@ -962,6 +1077,17 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
       return PKV_ERR_CUDA;
   }
   return PKV_OK;
+}
+
+// Distinct per call (40 bits, never 0): tags the per-item tickets so that
+// stale ticket words from earlier calls never count.
+unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> counter{0};
+  unsigned long long e;
+  do {
+    e = (counter.fetch_add(1) + 1) & ((1ull << 40) - 1);
+  } while (e == 0);
+  return e;
 }
 
 }  // namespace
@@ -991,6 +1117,8 @@ extern "C" int32_t paged_attention_partition_tokens(int32_t batch, int32_t num_h
   if (batch < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
       max_seq_len < 0 || partition_tokens < 0 || partition_tokens % 16)
     return -1;
+  if (partition_tokens == 0 && !stream_geom(num_heads, num_kv_heads, 128, PKV_BF16).ok)
+    return kFallbackPartition;
   return partition_tokens;  // 0: balanced stream schedule
 }
 
@@ -998,16 +1126,15 @@ extern "C" size_t paged_attention_workspace_bytes(int32_t batch, int32_t num_hea
                                                   int32_t num_kv_heads, int32_t head_dim,
                                                   int32_t max_seq_len,
                                                   int32_t partition_tokens) {
-  if (paged_attention_partition_tokens(batch, num_heads, num_kv_heads, max_seq_len,
-                                       partition_tokens) < 0 ||
-      batch <= 0 || head_dim <= 0)
-    return 0;
-  if (partition_tokens == 0) {
+  const int32_t pt = paged_attention_partition_tokens(batch, num_heads, num_kv_heads, max_seq_len,
+                                                      partition_tokens);
+  if (pt < 0 || batch <= 0 || head_dim <= 0) return 0;
+  if (pt == 0) {
+    const StreamGeom gm = stream_geom(num_heads, num_kv_heads, head_dim, PKV_BF16);
     const int sms = device_sm_count();
-    return stream_layout(batch, num_heads, num_kv_heads, head_dim, sms > 0 ? sms : 148).bytes;
+    return stream_layout(batch, num_heads, num_kv_heads, head_dim, sms > 0 ? sms : 148, gm).bytes;
   }
-  const int64_t parts = std::max<int64_t>(1, ((int64_t)max_seq_len + partition_tokens - 1) /
-                                                 partition_tokens);
+  const int64_t parts = std::max<int64_t>(1, ((int64_t)max_seq_len + pt - 1) / pt);
   if (parts > INT32_MAX / 2) return 0;
   return partition_workspace(batch, num_heads, head_dim, (int32_t)parts);
 }
@@ -1036,6 +1163,9 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
   if ((int64_t)cache->num_kv_heads * q_groups > 65535) return PKV_ERR_ARG;
   const int sms = device_sm_count();
   if (sms <= 0) return PKV_ERR_CUDA;
+  if (partition_tokens == 0 && !stream_geom(num_heads, cache->num_kv_heads, cache->head_dim,
+                                            cache->dtype).ok)
+    partition_tokens = kFallbackPartition;
   const bool stream_schedule = partition_tokens == 0;
 
   DecodeParams p;
@@ -1049,11 +1179,15 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
   }
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   if (stream_schedule) {
+    const StreamGeom gm = stream_geom(num_heads, cache->num_kv_heads, cache->head_dim, cache->dtype);
     const StreamLayout l =
-        stream_layout(batch, num_heads, cache->num_kv_heads, cache->head_dim, sms);
+        stream_layout(batch, num_heads, cache->num_kv_heads, cache->head_dim, sms, gm);
     p.piece_o = reinterpret_cast<float *>(ws + l.o_off);
     p.piece_ml = reinterpret_cast<float2 *>(ws + l.ml_off);
-    p.meta = reinterpret_cast<unsigned long long *>(ws + l.meta_off);
+    p.tickets = reinterpret_cast<unsigned long long *>(ws + l.ticket_off);
+    p.epoch = next_epoch();
+    p.hg = gm.hg;
+    p.ring_slots = gm.slots;
     p.max_parts = 1;
     p.part_tokens = 0;
   } else {
@@ -1083,7 +1217,6 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
   p.num_kv_heads = cache->num_kv_heads;
   p.group = group;
   p.q_groups = q_groups;
-  p.hp = std::min(8, group);
   p.num_blocks = cache->num_blocks;
   p.max_blocks = max_blocks;
   p.max_seq_len = max_seq_len;
