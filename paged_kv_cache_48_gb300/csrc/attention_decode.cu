@@ -170,7 +170,8 @@ __device__ __forceinline__ void load_q(uint32_t (&qf)[Cfg<FP8, D>::MT][2],
 template <bool FP8, int D>
 __device__ __forceinline__ void block_scores(uint32_t sk,
                                              const uint32_t (&qf)[Cfg<FP8, D>::MT][2],
-                                             float (&sc)[4], int lane) {
+                                             float (&sc)[4], int lane,
+                                             uint32_t box_stride = 16 * Cfg<FP8, D>::BOX_BYTES) {
   using C = Cfg<FP8, D>;
   // ldmatrix source rows/chunks for this lane (fragment layouts of
   // mma.m16n8k16): K uses (row = lane%8 + 8*bit3, chunk = 2x + bit4).
@@ -181,14 +182,16 @@ __device__ __forceinline__ void block_scores(uint32_t sk,
 #pragma unroll
     for (int ks = 0; ks < C::MT; ++ks) {
       uint32_t a0, a1, a2, a3;
-      ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * ks + k_chk), a0, a1, a2, a3);
+      ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * ks + k_chk, box_stride), a0, a1, a2,
+                  a3);
       mma_kv<FP8>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
     }
   } else {
 #pragma unroll
     for (int kp = 0; kp < C::MT / 2; ++kp) {
       uint32_t r0, r1, r2, r3;
-      ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * kp + k_chk), r0, r1, r2, r3);
+      ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * kp + k_chk, box_stride), r0, r1, r2,
+                  r3);
       mma_kv<FP8>(sc, e4m3x2_to_f16x2(r0 & 0xffff), e4m3x2_to_f16x2(r1 & 0xffff),
                   e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0],
                   qf[2 * kp][1]);
@@ -203,8 +206,8 @@ __device__ __forceinline__ void block_scores(uint32_t sk,
 // the shared address of the V tile, nv the block's valid tokens (0..16).
 template <bool FP8, int D>
 __device__ __forceinline__ void block_update(uint32_t sv, int nv, const float (&sc)[4],
-                                             float scale_log2, WarpState<FP8, D> &st,
-                                             int lane) {
+                                             float scale_log2, WarpState<FP8, D> &st, int lane,
+                                             uint32_t box_stride = 16 * Cfg<FP8, D>::BOX_BYTES) {
   using C = Cfg<FP8, D>;
   const int g = lane >> 2, c = lane & 3;
   // V^T uses (row = lane%8 + 8*bit4, chunk = 2x + bit3) for bf16 and the K
@@ -261,14 +264,16 @@ __device__ __forceinline__ void block_update(uint32_t sv, int nv, const float (&
 #pragma unroll
     for (int mt = 0; mt < C::MT; ++mt) {
       uint32_t a0, a1, a2, a3;
-      ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * mt + v_chk), a0, a1, a2, a3);
+      ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * mt + v_chk, box_stride), a0,
+                        a1, a2, a3);
       mma_kv<FP8>(st.o[mt], a0 & vm_lo, a1 & vm_lo, a2 & vm_hi, a3 & vm_hi, pb0, pb1);
     }
   } else {
 #pragma unroll
     for (int qq = 0; qq < C::MT / 2; ++qq) {
       uint32_t r0, r1, r2, r3;
-      ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * qq + v_chk), r0, r1, r2, r3);
+      ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * qq + v_chk, box_stride), r0,
+                        r1, r2, r3);
       // r0/r2: tokens 2c, 2c+1 (rows 0-7); r1/r3: tokens 8+2c, 9+2c.  Each
       // holds [t0 dA, t0 dB, t1 dA, t1 dB]; regroup per head_dim row.
       const uint32_t x0 = prmt(r0, 0u, 0x3120u), x1 = prmt(r1, 0u, 0x3120u);
@@ -505,12 +510,9 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
           uint64_t *bar = &full_bar[slot];
           mbar_arrive_expect_tx(bar, SLOT);
           uint8_t *dst = ring + (size_t)slot * SLOT;
-          const CUtensorMap *map = kv ? &tmap_v : &tmap_k;
-          for (int hl = 0; hl < p.hg; ++hl)
-#pragma unroll
-            for (int bx = 0; bx < C::NBOX; ++bx)
-              tma_load_4d(dst + hl * C::TILE_BYTES + bx * 16 * C::BOX_BYTES, map, bar,
-                          bx * C::BOX_ELEMS, ci.kg * p.hg + hl, 0, phys, policy);
+          // one load: all hg heads' tiles of the block, laid out as
+          // [head_dim slice][head][token][BOX_BYTES]
+          tma_load_5d(dst, kv ? &tmap_v : &tmap_k, bar, 0, 0, ci.kg * p.hg, 0, phys, policy);
         }
       }
       stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
@@ -529,6 +531,7 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // ========================= consumer warps =================================
   const int hl = warp % p.hg;
   const int qg = warp / p.hg;
+  const uint32_t box_stride = p.hg * 16 * C::BOX_BYTES;  // between head_dim slices
   const int heads_here = min(8, p.group - qg * 8);
   const int qh_local = hl * p.group + qg * 8;  // first query head within the item
   Cursor cu = sh_cu;
@@ -551,7 +554,8 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     const int nv = slot_ok[slot] ? min(16, cu.L - cu.j * 16) : 0;
     float sc[4];
-    block_scores<FP8, D>(smem_u32(ring + (size_t)slot * SLOT + hl * C::TILE_BYTES), qf, sc, lane);
+    block_scores<FP8, D>(smem_u32(ring + (size_t)slot * SLOT + hl * 16 * C::BOX_BYTES), qf, sc,
+                         lane, box_stride);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[slot]);
     ++q;
@@ -561,8 +565,8 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
       sh_abort = 1;
       if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, cu.b);
     }
-    block_update<FP8, D>(smem_u32(ring + (size_t)slot * SLOT + hl * C::TILE_BYTES), nv, sc,
-                         p.scale_log2, st, lane);
+    block_update<FP8, D>(smem_u32(ring + (size_t)slot * SLOT + hl * 16 * C::BOX_BYTES), nv, sc,
+                         p.scale_log2, st, lane, box_stride);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[slot]);
     ++q;
@@ -920,23 +924,52 @@ bool encode_cache_map(CUtensorMap *map, void *base, const pkv_cache *c) {
   return r == CUDA_SUCCESS;
 }
 
-// Small cache of encoded maps keyed by the cache geometry.
+// 5-D map over one cache for loads of `hg` consecutive kv heads of a block:
+// dims (innermost first) {box_elems, 16 tokens, num_kv_heads, head_dim
+// slices, num_blocks}.  The token stride is larger than the head stride, so
+// one box {box_elems, 16, hg, slices, 1} lands in shared memory as
+// [slice][head][token][box bytes]: every head's 16 tokens are consecutive
+// swizzled rows, exactly the per-head tile layout, and the whole K (or V)
+// segment of the hg heads is requested by a single copy.
+bool encode_group_map(CUtensorMap *map, void *base, const pkv_cache *c, int hg) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const bool fp8 = c->dtype == PKV_FP8_E4M3;
+  const cuuint64_t elt = fp8 ? 1 : 2;
+  const cuuint64_t row = (cuuint64_t)c->head_dim * elt;
+  const cuuint32_t box_bytes = row >= 128 ? 128 : (cuuint32_t)row;
+  const cuuint64_t slices = row / box_bytes;
+  cuuint64_t dims[5] = {box_bytes / elt, 16, (cuuint64_t)c->num_kv_heads, slices,
+                        (cuuint64_t)c->num_blocks};
+  cuuint64_t strides[4] = {row * c->num_kv_heads, row, box_bytes, row * c->num_kv_heads * 16};
+  cuuint32_t box[5] = {(cuuint32_t)(box_bytes / elt), 16, (cuuint32_t)hg, (cuuint32_t)slices, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r =
+      fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base,
+         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Small cache of encoded maps keyed by the cache geometry and the map kind
+// (hg == 0: per-head 4-D maps; hg > 0: 5-D maps over hg heads).
 struct MapEntry {
   void *key_cache, *value_cache;
-  int32_t num_blocks, num_kv_heads, head_dim, dtype;
+  int32_t num_blocks, num_kv_heads, head_dim, dtype, hg;
   CUtensorMap k, v;
 };
 
-bool get_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
+bool get_maps(const pkv_cache *c, int hg, CUtensorMap *k, CUtensorMap *v) {
   static std::mutex mu;
-  static MapEntry entries[8];
+  static MapEntry entries[16];
   static int n_entries = 0, next = 0;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_entries; ++i) {
     const MapEntry &e = entries[i];
     if (e.key_cache == c->key_cache && e.value_cache == c->value_cache &&
         e.num_blocks == c->num_blocks && e.num_kv_heads == c->num_kv_heads &&
-        e.head_dim == c->head_dim && e.dtype == c->dtype) {
+        e.head_dim == c->head_dim && e.dtype == c->dtype && e.hg == hg) {
       *k = e.k;
       *v = e.v;
       return true;
@@ -949,11 +982,15 @@ bool get_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
   e.num_kv_heads = c->num_kv_heads;
   e.head_dim = c->head_dim;
   e.dtype = c->dtype;
-  if (!encode_cache_map(&e.k, c->key_cache, c) || !encode_cache_map(&e.v, c->value_cache, c))
-    return false;
+  e.hg = hg;
+  const bool ok = hg > 0 ? encode_group_map(&e.k, c->key_cache, c, hg) &&
+                               encode_group_map(&e.v, c->value_cache, c, hg)
+                         : encode_cache_map(&e.k, c->key_cache, c) &&
+                               encode_cache_map(&e.v, c->value_cache, c);
+  if (!ok) return false;
   entries[next] = e;
-  next = (next + 1) % 8;
-  if (n_entries < 8) ++n_entries;
+  next = (next + 1) % 16;
+  if (n_entries < 16) ++n_entries;
   *k = e.k;
   *v = e.v;
   return true;
@@ -1206,7 +1243,7 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
   }
 
   CUtensorMap mk, mv;
-  if (!get_maps(cache, &mk, &mv)) return PKV_ERR_CUDA;
+  if (!get_maps(cache, stream_schedule ? p.hg : 0, &mk, &mv)) return PKV_ERR_CUDA;
 
   p.q = static_cast<const __nv_bfloat16 *>(q);
   p.block_tables = block_tables;

@@ -51,22 +51,28 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 }
 
 // Byte offset of 16-byte chunk `chunk` of token row `t` inside a K or V tile
-// that TMA wrote with box {BOX_BYTES/elt, 1, 16, 1}: boxes of 16 rows x
-// BOX_BYTES are stacked; inside a box the 16-byte chunk index is XORed with
-// the row index (128-byte swizzle: 3 bits, 64-byte swizzle: 2 bits of the
-// 128-byte line index).
+// that TMA wrote as boxes of 16 rows x BOX_BYTES, consecutive boxes
+// (head_dim slices) `box_stride` bytes apart: inside a box the 16-byte chunk
+// index is XORed with the row index (128-byte swizzle: 3 bits, 64-byte
+// swizzle: 2 bits of the 128-byte line index).  Box bases are multiples of
+// the swizzle atom, so the XOR only depends on the offset within the box.
 template <int BOX_BYTES>
-__device__ __forceinline__ uint32_t tile_offset(int t, int chunk) {
+__device__ __forceinline__ uint32_t tile_offset(int t, int chunk, uint32_t box_stride) {
   constexpr int CHUNKS = BOX_BYTES / 16;
   const int box = chunk / CHUNKS;
   const int c = chunk % CHUNKS;
-  uint32_t off = box * (16 * BOX_BYTES) + t * BOX_BYTES + c * 16;
+  uint32_t off = t * BOX_BYTES + c * 16;
   if (BOX_BYTES == 128) {
     off ^= ((off >> 7) & 7u) << 4;
   } else {  // 64-byte rows, 64-byte swizzle
     off ^= ((off >> 7) & 3u) << 4;
   }
-  return off;
+  return box * box_stride + off;
+}
+
+template <int BOX_BYTES>
+__device__ __forceinline__ uint32_t tile_offset(int t, int chunk) {
+  return tile_offset<BOX_BYTES>(t, chunk, 16 * BOX_BYTES);
 }
 
 // ---------------------------------------------------------------------------
@@ -147,6 +153,18 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map,
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x),
       "r"(y), "r"(z), "r"(w), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map,
+                                            uint64_t *bar, int c0, int c1, int c2, int c3,
+                                            int c4, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_"
+      "tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5, %6, %7}], [%2], %8;" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(c4), "l"(policy)
       : "memory");
 }
 
