@@ -177,14 +177,15 @@ __device__ __forceinline__ void block_scores(uint32_t sk,
   // mma.m16n8k16): K uses (row = lane%8 + 8*bit3, chunk = 2x + bit4).
   const int k_row = (lane & 7) + ((lane >> 3) & 1) * 8;
   const int k_chk = lane >> 4;
-  sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
+  // Two accumulators over alternating k-steps halve the dependent mma chain.
+  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
   if (!FP8) {
 #pragma unroll
     for (int ks = 0; ks < C::MT; ++ks) {
       uint32_t a0, a1, a2, a3;
       ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * ks + k_chk, box_stride), a0, a1, a2,
                   a3);
-      mma_kv<FP8>(sc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      mma_kv<FP8>((ks & 1) ? sb : sa, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
     }
   } else {
 #pragma unroll
@@ -192,14 +193,16 @@ __device__ __forceinline__ void block_scores(uint32_t sk,
       uint32_t r0, r1, r2, r3;
       ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * kp + k_chk, box_stride), r0, r1, r2,
                   r3);
-      mma_kv<FP8>(sc, e4m3x2_to_f16x2(r0 & 0xffff), e4m3x2_to_f16x2(r1 & 0xffff),
+      mma_kv<FP8>(sa, e4m3x2_to_f16x2(r0 & 0xffff), e4m3x2_to_f16x2(r1 & 0xffff),
                   e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0],
                   qf[2 * kp][1]);
-      mma_kv<FP8>(sc, e4m3x2_to_f16x2(r2 & 0xffff), e4m3x2_to_f16x2(r3 & 0xffff),
+      mma_kv<FP8>(sb, e4m3x2_to_f16x2(r2 & 0xffff), e4m3x2_to_f16x2(r3 & 0xffff),
                   e4m3x2_to_f16x2(r2 >> 16), e4m3x2_to_f16x2(r3 >> 16), qf[2 * kp + 1][0],
                   qf[2 * kp + 1][1]);
     }
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sc[i] = sa[i] + sb[i];
 }
 
 // Online softmax update with one block's scores and P.V accumulation; sv is
@@ -334,6 +337,7 @@ __device__ __forceinline__ void issue_block(uint8_t *stage, uint64_t *bar,
 constexpr int kMaxSlots = 16;
 constexpr int kStreamRingBytes = 192 * 1024;
 constexpr int kMaxConsumerWarps = 8;
+constexpr int kPrefetchBlocks = 4;
 
 // Position in the concatenated block chains (item order b-major, then kg).
 struct Cursor {
@@ -483,7 +487,30 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     const uint64_t policy = l2_policy_evict_normal();
     long long q = 0;
     bool stop = false;
+    // L2 prefetch of the blocks kPrefetchBlocks ahead of the ring: DRAM
+    // requests in flight are then not bounded by the ring, and ring loads
+    // find their lines in L2.
+    Cursor cpf = sh_cu;
+    int pwin_b = -1, pwin_j = -1, pids = 0;
+    long long prefetched = 0;
+    auto prefetch_next = [&]() {
+      const int jw = cpf.j & ~31;
+      if (cpf.b != pwin_b || jw != pwin_j) {
+        pwin_b = cpf.b;
+        pwin_j = jw;
+        const int jj = jw + lane;
+        pids = jj < cpf.n ? __ldg(p.block_tables + (size_t)cpf.b * p.max_blocks + jj) : -1;
+      }
+      const int ph = __shfl_sync(0xffffffffu, pids, cpf.j & 31);
+      if (lane == 0 && ph >= 0 && ph < p.num_blocks) {
+        tma_prefetch_5d(&tmap_k, 0, 0, cpf.kg * p.hg, 0, ph);
+        tma_prefetch_5d(&tmap_v, 0, 0, cpf.kg * p.hg, 0, ph);
+      }
+      if (++prefetched < total) advance(cpf, p, NG, cap);
+    };
+    for (int i = 0; i < kPrefetchBlocks && prefetched < total; ++i) prefetch_next();
     for (long long x = 0; x < total && !stop; ++x) {
+      if (prefetched < total) prefetch_next();
       const int jw = ci.j & ~31;
       if (ci.b != win_b || jw != win_j) {
         win_b = ci.b;
