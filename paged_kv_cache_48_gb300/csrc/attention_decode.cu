@@ -337,7 +337,7 @@ __device__ __forceinline__ void issue_block(uint8_t *stage, uint64_t *bar,
 constexpr int kMaxSlots = 16;
 constexpr int kStreamRingBytes = 192 * 1024;
 constexpr int kMaxConsumerWarps = 8;
-constexpr int kPrefetchBlocks = 4;
+constexpr int kMaxWarpStages = 8;
 
 // Position in the concatenated block chains (item order b-major, then kg).
 struct Cursor {
@@ -371,41 +371,37 @@ __device__ __forceinline__ long long worker_of(long long x, long long W, long lo
 }
 
 template <bool FP8, int D>
-__global__ void __launch_bounds__((kMaxConsumerWarps + 1) * 32, 1)
+__global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
 paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
                            const __grid_constant__ CUtensorMap tmap_v,
                            const DecodeParams p) {
   using C = Cfg<FP8, D>;
   extern __shared__ uint8_t smem_dyn[];
-  __shared__ uint64_t full_bar[kMaxSlots];
-  __shared__ uint64_t empty_bar[kMaxSlots];
-  __shared__ int slot_ok[kMaxSlots];
+  __shared__ uint64_t full_bar[kMaxConsumerWarps][kMaxWarpStages];
+  __shared__ int slot_ok[kMaxConsumerWarps][kMaxWarpStages];
   __shared__ long long sh_T, sh_W, sh_start, sh_end;
   __shared__ Cursor sh_cu;
   __shared__ int sh_last;
-  __shared__ int sh_abort;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int ncw = p.hg * p.q_groups;  // consumer warps; warp ncw produces
-  const int NS = p.ring_slots;
-  const int SLOT = p.hg * C::TILE_BYTES;
+  const int ncw = p.hg * p.q_groups;  // warps: (kv head of the group, query sub-group)
+  const int NSW = p.ring_slots;        // stages (K + V tiles) per warp
   const int NG = p.num_kv_heads / p.hg;
   const int HQT = p.hg * p.group;  // query heads per item
   const int cap = min(p.max_blocks * 16, p.max_seq_len);
   const uint32_t base_u32 = smem_u32(smem_dyn);
-  uint8_t *ring = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32);
+  uint8_t *ring = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32) +
+                  (size_t)warp * NSW * C::STAGE_BYTES;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], ncw);
-    }
+  if (lane == 0) {
+    for (int s = 0; s < NSW; ++s) mbar_init(&full_bar[warp][s], 1);
     fence_barrier_init();
-    prefetch_tensormap(&tmap_k);
-    prefetch_tensormap(&tmap_v);
-    sh_abort = 0;
+    if (warp == 0) {
+      prefetch_tensormap(&tmap_k);
+      prefetch_tensormap(&tmap_v);
+    }
   }
   __syncthreads();
   grid_dependency_wait();
@@ -466,101 +462,59 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
   }
   // ---- rows of empty sequences are zero ------------------------------------
-  if (warp < ncw) {
-    for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
-      if (clamp_len(__ldg(p.seq_lens + b), cap) != 0) continue;
-      for (int h = warp; h < p.num_heads; h += ncw)
+  for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+    if (clamp_len(__ldg(p.seq_lens + b), cap) != 0) continue;
+    for (int h = warp; h < p.num_heads; h += ncw)
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k)
-          p.out[((size_t)b * p.num_heads + h) * D + lane + 32 * k] = __float2bfloat16_rn(0.f);
-    }
+      for (int k = 0; k < D / 32; ++k)
+        p.out[((size_t)b * p.num_heads + h) * D + lane + 32 * k] = __float2bfloat16_rn(0.f);
   }
   __syncthreads();
   const long long T = sh_T, W = sh_W;
   const long long total = sh_end - sh_start;
   if (total <= 0) return;
 
-  if (warp == ncw) {
-    // ======================= producer warp ==================================
-    Cursor ci = sh_cu;
-    int win_b = -1, win_j = -1, ids = 0;
-    const uint64_t policy = l2_policy_evict_normal();
-    long long q = 0;
-    bool stop = false;
-    // L2 prefetch of the blocks kPrefetchBlocks ahead of the ring: DRAM
-    // requests in flight are then not bounded by the ring, and ring loads
-    // find their lines in L2.
-    Cursor cpf = sh_cu;
-    int pwin_b = -1, pwin_j = -1, pids = 0;
-    long long prefetched = 0;
-    auto prefetch_next = [&]() {
-      const int jw = cpf.j & ~31;
-      if (cpf.b != pwin_b || jw != pwin_j) {
-        pwin_b = cpf.b;
-        pwin_j = jw;
-        const int jj = jw + lane;
-        pids = jj < cpf.n ? __ldg(p.block_tables + (size_t)cpf.b * p.max_blocks + jj) : -1;
-      }
-      const int ph = __shfl_sync(0xffffffffu, pids, cpf.j & 31);
-      if (lane == 0 && ph >= 0 && ph < p.num_blocks) {
-        tma_prefetch_5d(&tmap_k, 0, 0, cpf.kg * p.hg, 0, ph);
-        tma_prefetch_5d(&tmap_v, 0, 0, cpf.kg * p.hg, 0, ph);
-      }
-      if (++prefetched < total) advance(cpf, p, NG, cap);
-    };
-    for (int i = 0; i < kPrefetchBlocks && prefetched < total; ++i) prefetch_next();
-    for (long long x = 0; x < total && !stop; ++x) {
-      if (prefetched < total) prefetch_next();
-      const int jw = ci.j & ~31;
-      if (ci.b != win_b || jw != win_j) {
-        win_b = ci.b;
-        win_j = jw;
-        const int jj = jw + lane;
-        ids = jj < ci.n ? __ldg(p.block_tables + (size_t)ci.b * p.max_blocks + jj) : -1;
-      }
-      int phys = __shfl_sync(0xffffffffu, ids, ci.j & 31);
-      const int ok = phys >= 0 && phys < p.num_blocks;
-      if (lane == 0) {
-        if (!ok) {
-          record_error(&g_err_attention, PKV_ERR_RANGE, ci.b);
-          phys = 0;
-        }
-        for (int kv = 0; kv < 2; ++kv, ++q) {
-          const int slot = (int)(q % NS);
-          if (q >= NS && !mbar_wait_bounded(&empty_bar[slot], (uint32_t)((q / NS - 1) & 1),
-                                            p.timeout_ns)) {
-            sh_abort = 1;
-            stop = true;
-            break;
-          }
-          slot_ok[slot] = ok;
-          uint64_t *bar = &full_bar[slot];
-          mbar_arrive_expect_tx(bar, SLOT);
-          uint8_t *dst = ring + (size_t)slot * SLOT;
-          // one load: all hg heads' tiles of the block, laid out as
-          // [head_dim slice][head][token][BOX_BYTES]
-          tma_load_5d(dst, kv ? &tmap_v : &tmap_k, bar, 0, 0, ci.kg * p.hg, 0, phys, policy);
-        }
-      }
-      stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
-      if (x + 1 < total) advance(ci, p, NG, cap);
-    }
-    if (lane == 0) {
-      if (stop) record_error(&g_err_attention, PKV_ERR_TIMEOUT, ci.b);
-      // The copies issued last must land before the CTA may exit, whatever
-      // the consumers did (bounded as well).
-      for (long long r = q > NS ? q - NS : 0; r < q; ++r)
-        mbar_wait_bounded(&full_bar[r % NS], (uint32_t)((r / NS) & 1), p.timeout_ns);
-    }
-    return;
-  }
-
-  // ========================= consumer warps =================================
   const int hl = warp % p.hg;
   const int qg = warp / p.hg;
-  const uint32_t box_stride = p.hg * 16 * C::BOX_BYTES;  // between head_dim slices
   const int heads_here = min(8, p.group - qg * 8);
   const int qh_local = hl * p.group + qg * 8;  // first query head within the item
+
+  // ---- load side: this warp's head of each block of the range --------------
+  Cursor ci = sh_cu;
+  int win_b = -1, win_j = -1, ids = 0;
+  const uint64_t policy = l2_policy_evict_normal();
+  long long issued = 0;
+  auto issue_next = [&]() {
+    const int jw = ci.j & ~31;
+    if (ci.b != win_b || jw != win_j) {
+      win_b = ci.b;
+      win_j = jw;
+      const int jj = jw + lane;
+      ids = jj < ci.n ? __ldg(p.block_tables + (size_t)ci.b * p.max_blocks + jj) : -1;
+    }
+    int phys = __shfl_sync(0xffffffffu, ids, ci.j & 31);
+    if (lane == 0) {
+      const int stage = (int)(issued % NSW);
+      int ok = 1;
+      if (phys < 0 || phys >= p.num_blocks) {
+        record_error(&g_err_attention, PKV_ERR_RANGE, ci.b);
+        phys = 0;
+        ok = 0;
+      }
+      slot_ok[warp][stage] = ok;
+      uint64_t *bar = &full_bar[warp][stage];
+      uint8_t *dst = ring + (size_t)stage * C::STAGE_BYTES;
+      mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+      const int kvh = ci.kg * p.hg + hl;
+      tma_load_5d(dst, &tmap_k, bar, 0, 0, kvh, 0, phys, policy);
+      tma_load_5d(dst + C::TILE_BYTES, &tmap_v, bar, 0, 0, kvh, 0, phys, policy);
+    }
+    if (++issued < total) advance(ci, p, NG, cap);
+  };
+  const int pre = (int)(total < NSW ? total : (long long)NSW);
+  for (int i = 0; i < pre; ++i) issue_next();
+
+  // ---- compute side -------------------------------------------------------
   Cursor cu = sh_cu;
   WarpState<FP8, D> st;
   st.reset();
@@ -571,32 +525,19 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
   };
   load_q<FP8, D>(qf, item_q(), heads_here, lane);
 
-  long long q = 0;
+  bool failed = false;
   for (long long x = 0; x < total; ++x) {
-    // K tile: scores, then release the slot
-    int slot = (int)(q % NS);
-    if (!sh_abort && !mbar_wait_bounded(&full_bar[slot], (uint32_t)((q / NS) & 1), p.timeout_ns)) {
-      sh_abort = 1;
+    const int stage = (int)(x % NSW);
+    if (!failed &&
+        !mbar_wait_bounded(&full_bar[warp][stage], (uint32_t)((x / NSW) & 1), p.timeout_ns)) {
+      failed = true;
       if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, cu.b);
     }
-    const int nv = slot_ok[slot] ? min(16, cu.L - cu.j * 16) : 0;
-    float sc[4];
-    block_scores<FP8, D>(smem_u32(ring + (size_t)slot * SLOT + hl * 16 * C::BOX_BYTES), qf, sc,
-                         lane, box_stride);
+    const int nv = slot_ok[warp][stage] ? min(16, cu.L - cu.j * 16) : 0;
+    const uint32_t sk = smem_u32(ring + (size_t)stage * C::STAGE_BYTES);
+    attend_block<FP8, D>(sk, sk + C::TILE_BYTES, nv, qf, p.scale_log2, st, lane);
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[slot]);
-    ++q;
-    // V tile: softmax update and P.V, then release the slot
-    slot = (int)(q % NS);
-    if (!sh_abort && !mbar_wait_bounded(&full_bar[slot], (uint32_t)((q / NS) & 1), p.timeout_ns)) {
-      sh_abort = 1;
-      if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, cu.b);
-    }
-    block_update<FP8, D>(smem_u32(ring + (size_t)slot * SLOT + hl * 16 * C::BOX_BYTES), nv, sc,
-                         p.scale_log2, st, lane, box_stride);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[slot]);
-    ++q;
+    if (!failed && issued < total) issue_next();
 
     const bool last_of_item = cu.j == cu.n - 1;
     if (!last_of_item && x + 1 < total) {
@@ -640,7 +581,7 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (2 * c + 1 < heads_here) p.piece_ml[slot_row + 2 * c + 1] = make_float2(st.m1, st.l1);
       }
       __threadfence();
-      named_barrier_sync(ncw * 32);
+      __syncthreads();
       if (threadIdx.x == 0) {
         const long long ps = cu.base + (long long)cu.kg * cu.n;
         const long long pieces = worker_of(ps + cu.n - 1, W, T) - worker_of(ps, W, T) + 1;
@@ -656,7 +597,7 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (last) atomicExch(ticket, 0ull);  // clean for the next call
         sh_last = last ? 1 : 0;
       }
-      named_barrier_sync(ncw * 32);
+      __syncthreads();
       if (sh_last) {
         // merge every piece of the item for this warp's query heads
         __threadfence();
@@ -691,6 +632,11 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
       piece_j0 = cu.j;  // a new item starts at block 0
       load_q<FP8, D>(qf, item_q(), heads_here, lane);
     }
+  }
+  if (failed) {
+    // let copies still in flight land before the CTA exits (bounded too)
+    for (long long r = issued > NSW ? issued - NSW : 0; r < issued; ++r)
+      mbar_wait_bounded(&full_bar[warp][r % NSW], (uint32_t)((r / NSW) & 1), p.timeout_ns);
   }
 }
 
@@ -1046,8 +992,9 @@ StreamGeom stream_geom(int64_t num_heads, int64_t num_kv_heads, int64_t head_dim
       break;
     }
   const int64_t tile = 16 * head_dim * (dtype == PKV_FP8_E4M3 ? 1 : 2);
-  gm.slot_bytes = (int)(gm.hg * tile);
-  gm.slots = (int)std::min<int64_t>(kMaxSlots, kStreamRingBytes / gm.slot_bytes);
+  const int64_t warps = (int64_t)gm.hg * gm.q_groups;
+  gm.slot_bytes = (int)(2 * tile);  // one stage: K and V tiles of one head
+  gm.slots = (int)std::min<int64_t>(kMaxWarpStages, kStreamRingBytes / (warps * gm.slot_bytes));
   gm.ok = gm.slots >= 2;
   return gm;
 }
@@ -1124,8 +1071,9 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
   pkv_status st = configure_smem<FP8, D>();
   if (st != PKV_OK) return st;
   if (stream_schedule) {
-    const size_t smem = (size_t)p.ring_slots * p.hg * C::TILE_BYTES + 1024;
-    const int threads = (p.hg * p.q_groups + 1) * 32;
+    const int warps = p.hg * p.q_groups;
+    const size_t smem = (size_t)warps * p.ring_slots * C::STAGE_BYTES + 1024;
+    const int threads = warps * 32;
     if (launch_pdl(paged_decode_stream_kernel<FP8, D>, dim3(sms), dim3(threads), smem, s, mk, mv,
                    p) != cudaSuccess)
       return PKV_ERR_CUDA;
@@ -1270,7 +1218,7 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
   }
 
   CUtensorMap mk, mv;
-  if (!get_maps(cache, stream_schedule ? p.hg : 0, &mk, &mv)) return PKV_ERR_CUDA;
+  if (!get_maps(cache, stream_schedule ? 1 : 0, &mk, &mv)) return PKV_ERR_CUDA;
 
   p.q = static_cast<const __nv_bfloat16 *>(q);
   p.block_tables = block_tables;
