@@ -370,6 +370,80 @@ __device__ __forceinline__ long long worker_of(long long x, long long W, long lo
   return ((x + 1) * W - 1) / T;
 }
 
+// Log-sum-exp merge of item s's pieces (held by CTAs wf..wl, slot w + s)
+// for `heads` query heads starting at item-local head qh0; one warp.  All
+// (max, sum) pairs are loaded at once (lane i: piece i of a chunk of 32),
+// reduced with shuffles, then every lane accumulates its head_dim elements
+// of all heads piece by piece (fixed order: bitwise deterministic).
+template <int D>
+__device__ __forceinline__ void merge_pieces(const DecodeParams &p, long long s, long long wf,
+                                             long long wl, int hqt, int qh0, int heads,
+                                             size_t out_row0, int lane) {
+  constexpr int KD = D / 32;
+  float acc[8][KD];
+  float M[8], wsum[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    M[h] = -INFINITY;
+    wsum[h] = 0.f;
+#pragma unroll
+    for (int k = 0; k < KD; ++k) acc[h][k] = 0.f;
+  }
+  const long long np = wl - wf + 1;
+  // pass 1: maxima
+  for (long long i0 = 0; i0 < np; i0 += 32) {
+    const long long i = i0 + lane;
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      float m = -INFINITY;
+      if (h < heads && i < np) m = __ldcg(&p.piece_ml[(wf + i + s) * hqt + qh0 + h].x);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      M[h] = fmaxf(M[h], m);
+    }
+  }
+  // pass 2: weights (lane i holds piece i0 + i), sums and weighted outputs
+  for (long long i0 = 0; i0 < np; i0 += 32) {
+    const long long i = i0 + lane;
+    float wl_[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      float w = 0.f;
+      if (h < heads && i < np) {
+        const float2 ml = __ldcg(&p.piece_ml[(wf + i + s) * hqt + qh0 + h]);
+        w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M[h]) * ml.y;
+      }
+      wl_[h] = w;
+      float t = w;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+      wsum[h] += t;
+    }
+    const int cnt = (int)(np - i0 < 32 ? np - i0 : 32);
+#pragma unroll 2
+    for (int r = 0; r < cnt; ++r) {
+      const float *po = p.piece_o + ((size_t)(wf + i0 + r + s) * hqt + qh0) * D + lane;
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float w = __shfl_sync(0xffffffffu, wl_[h], r);
+        if (h < heads) {
+#pragma unroll
+          for (int k = 0; k < KD; ++k) acc[h][k] += w * __ldcg(po + (size_t)h * D + 32 * k);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    if (h < heads) {
+      const float inv = wsum[h] > 0.f ? 1.f / wsum[h] : 0.f;
+      __nv_bfloat16 *orow = p.out + (out_row0 + h) * D;
+#pragma unroll
+      for (int k = 0; k < KD; ++k) orow[lane + 32 * k] = __float2bfloat16_rn(acc[h][k] * inv);
+    }
+  }
+}
+
 template <bool FP8, int D>
 __global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
 paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -599,31 +673,10 @@ paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
       __syncthreads();
       if (sh_last) {
-        // merge every piece of the item for this warp's query heads
         __threadfence();
         const long long ps = cu.base + (long long)cu.kg * cu.n;
-        const long long wf = worker_of(ps, W, T), wl = worker_of(ps + cu.n - 1, W, T);
-        for (int h = 0; h < heads_here; ++h) {
-          float M = -INFINITY;
-          for (long long w = wf; w <= wl; ++w)
-            M = fmaxf(M, __ldcg(&p.piece_ml[(w + s) * HQT + qh_local + h].x));
-          float wsum = 0.f, acc[D / 32];
-#pragma unroll
-          for (int k = 0; k < D / 32; ++k) acc[k] = 0.f;
-          for (long long w = wf; w <= wl; ++w) {
-            const float mw = __ldcg(&p.piece_ml[(w + s) * HQT + qh_local + h].x);
-            const float lw = __ldcg(&p.piece_ml[(w + s) * HQT + qh_local + h].y);
-            const float e = mw == -INFINITY ? 0.f : exp2f(mw - M) * lw;
-            wsum += e;
-            const float *pw = p.piece_o + ((size_t)(w + s) * HQT + qh_local + h) * D;
-#pragma unroll
-            for (int k = 0; k < D / 32; ++k) acc[k] += e * __ldcg(pw + lane + 32 * k);
-          }
-          const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-          __nv_bfloat16 *orow = p.out + (out_row0 + h) * D;
-#pragma unroll
-          for (int k = 0; k < D / 32; ++k) orow[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
-        }
+        merge_pieces<D>(p, s, worker_of(ps, W, T), worker_of(ps + cu.n - 1, W, T), HQT,
+                        qh_local, heads_here, out_row0, lane);
       }
     }
     if (x + 1 < total) {
