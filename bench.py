@@ -32,7 +32,7 @@ METRIC = ("paged decode attention KV-read GB/s (% of GB300 HBM peak); "
           "seq-steps/sec")
 L2_NOTE = "inputs larger than L2 (0.59 GB of KV read per step, L2 126 MB)"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE = ROOT / "profiles" / "paged_decode_stream_kernel_llama8b_gqa.md"
+PROFILE = ROOT / "profiles" / "paged_decode_kernel_llama8b_gqa.md"
 KERNEL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_decode.cu",
                   "paged_kv_cache_48_gb300/csrc/pkv_device.cuh"]
 
@@ -283,11 +283,9 @@ def run_ours(args):
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
-    # balanced schedule (pt == 0): decode + merge; fixed partitions: merge
-    # only when some sequence can be split
-    merge = pt == 0 or -(-max_len // pt) > 1
-    launches_per_step = (1 if fresh.size else 0) + (1 if slots.numel() else 0) \
-        + 1 + (1 if merge else 0)
+    # zeroing (when the step opens blocks), the write, the decode kernel (it
+    # merges split sequences itself)
+    launches_per_step = (1 if fresh.size else 0) + (1 if slots.numel() else 0) + 1
 
     def step(ev=None):
         if fresh.size:
@@ -381,16 +379,14 @@ def run_ours(args):
                    "head_dim": W.head_dim, "block_size": 16,
                    "seq_lens": "uniform [512, 4096]", "kv_dtype": "bf16",
                    "num_blocks": W.num_blocks, "fresh_blocks": int(fresh.size),
-                   "schedule": ("balanced stream" if pt == 0 else
-                                f"{pt}-token partitions"),
+                   "partition_tokens": pt,
                    "kv_read_bytes": kv_bytes,
                    "l2": L2_NOTE},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": peak_kind,
-                     "kernel": ("paged_decode_stream_kernel + merge" if pt == 0
-                                else "paged_decode_kernel (+ merge when split)"),
+                     "kernel": "paged_decode_kernel (merges split sequences in-kernel)",
                      "launch_ms": round(attn_ms, 5)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},

@@ -112,13 +112,11 @@ pkv_status paged_kv_zero_blocks(const pkv_cache *cache,
  *   out           bf16 [batch, num_heads, head_dim].
  *   max_seq_len   host upper bound of seq_lens (sizes the grid); a longer
  *                 sequence is clamped and reported as a range error.
- *   partition_tokens  0 = balanced schedule: the block chains of all
- *                 (sequence, kv head) items are cut into equal contiguous
- *                 ranges, one per warp of a persistent grid; items that
- *                 straddle ranges are merged by a log-sum-exp reduce.
- *                 Otherwise a multiple of 16: every sequence is split into
- *                 partitions of that many tokens (one CTA each per kv head)
- *                 whose results the same kind of reduce merges.
+ *   partition_tokens  0 = automatic (see paged_attention_partition_tokens);
+ *                 otherwise a multiple of 16: every sequence is split into
+ *                 partitions of that many tokens, one CTA each per kv head;
+ *                 the CTA that completes a sequence's last partition merges
+ *                 the partitions with a log-sum-exp reduce (no extra launch).
  *   workspace     device scratch of workspace_bytes, at least
  *                 paged_attention_workspace_bytes(...) for the same
  *                 arguments; may be NULL when that function returns 0.
@@ -142,9 +140,11 @@ size_t paged_attention_workspace_bytes(int32_t batch, int32_t num_heads,
                                        int32_t partition_tokens);
 
 /* The partition length (tokens) paged_attention_decode uses for these
- * arguments: 0 for the balanced schedule, otherwise partition_tokens.
- * Returns -1 on invalid arguments (partition_tokens negative or not a
- * multiple of 16, num_heads not a multiple of num_kv_heads). */
+ * arguments: partition_tokens itself when it is positive, otherwise the
+ * automatic choice (a power-of-two multiple of 256 tokens, or the whole
+ * max_seq_len when the sequences alone fill the GPU).  Returns -1 on
+ * invalid arguments (partition_tokens negative or not a multiple of 16,
+ * num_heads not a multiple of num_kv_heads). */
 int32_t paged_attention_partition_tokens(int32_t batch, int32_t num_heads,
                                          int32_t num_kv_heads,
                                          int32_t max_seq_len,

@@ -9,31 +9,26 @@
 // excluded by selection, never multiplied by zero (vLLM v0.17.1 notes,
 // admirer.cn, "重点：35219": 0 x NaN = NaN).
 //
-// Work unit: an "item" is one kv head (and up to 8 of its query heads) of
-// one sequence; its KV is a chain of 16-token blocks.  Every warp streams
-// blocks through a private ring of shared-memory stages: lane 0 reads the
-// physical block id from the block table and issues TMA tile loads (4-D
-// tensor map over [num_blocks, 16, num_kv_heads, head_dim], box = 16 tokens
-// x 128 bytes, 128-byte swizzle) that complete on the stage's mbarrier.  The
-// block-table indirection is simply the 4th TMA coordinate.  Per block:
-// S^T = K . Q^T with mma.sync m16n8k16 (16 tokens x 8 query heads x
-// head_dim), an online softmax over tokens with warp shuffles, then
-// O^T += V^T . P^T (P^T formed with movmatrix).  fp8 E4M3 tiles are decoded
-// to f16 in registers (exact) and multiplied with an f16 copy of q; k_scale
-// is folded into the score scale and v_scale into the output.
-//
-// Two schedules share that per-block code:
-//  * balanced stream (automatic): a persistent grid; the concatenated block
-//    chains of all items are cut into one equal contiguous range per warp.
-//    A warp's range covers pieces of one or more items; a piece that is a
-//    whole item writes the output, other pieces write (max, sum, output)
-//    partials that a log-sum-exp merge combines.
-//  * fixed partitions (explicit partition length): one CTA per
-//    (partition, sequence, kv head); its warps share the partition's blocks
-//    and merge through shared memory; split sequences are merged by the same
-//    kind of log-sum-exp reduce.
-// Every reduction has a fixed order, so results are bitwise deterministic
-// and independent of where blocks sit in the pool.
+// Schedule: one CTA per (kv head, query sub-group of <= 8 heads, partition
+// of a sequence, sequence); the grid is ordered heads-fastest.  The CTA's 4
+// warps take the partition's 16-token blocks round-robin, and each warp
+// streams its blocks through a private ring of shared-memory stages: lane 0
+// reads the physical block id from the block table and issues one TMA load
+// per K and per V tile (5-D tensor map over [num_blocks, 16, num_kv_heads,
+// head_dim] laid out so that one box is the 16 token rows of one head,
+// 128-byte swizzled); the block-table indirection is simply the block
+// coordinate of the load.  Per block: S^T = K . Q^T with mma.sync
+// m16n8k16 (16 tokens x 8 query heads x head_dim), an online softmax over
+// tokens with warp shuffles, then O^T += V^T . P^T (P^T formed with
+// movmatrix).  fp8 E4M3 tiles are decoded to f16 in registers (exact) and
+// multiplied with an f16 copy of q; k_scale is folded into the score scale
+// and v_scale into the output.  The warps merge through shared memory; a
+// sequence split into several partitions is merged by the CTA that
+// completes its last partition (log-sum-exp over the partitions' (max, sum,
+// output) partials, counted with a per-(sequence, kv head) ticket word; no
+// CTA ever waits for another).  Every reduction has a fixed order, so
+// results are bitwise deterministic and independent of where blocks sit in
+// the pool.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -54,17 +49,13 @@ struct DecodeParams {
   const int32_t *block_tables;  // [B, max_blocks]
   const int32_t *seq_lens;      // [B]
   __nv_bfloat16 *out;           // [B, Hq, D]
-  // fixed partitions: [B, Hq, max_parts, D] and [B, Hq, max_parts]
+  // split sequences: partials [B, Hq, max_parts, D] and [B, Hq, max_parts]
+  // (max in log2 units, sum); one ticket word per (sequence, kv head, query
+  // sub-group)
   float *part_o;
-  float2 *part_ml;  // (max in log2 units, sum)
-  // balanced stream: pieces [(ctas + items), item q heads, D] and
-  // [(ctas + items), item q heads]; one ticket word per item
-  float *piece_o;
-  float2 *piece_ml;
+  float2 *part_ml;
   unsigned long long *tickets;
   unsigned long long epoch;  // 1 .. 2^40-1, distinct per call
-  int32_t hg;                // kv heads per item (stream schedule)
-  int32_t ring_slots;        // K or V slots in a CTA's ring (stream schedule)
   int32_t batch, num_heads, num_kv_heads, group, q_groups;
   int32_t num_blocks, max_blocks, max_seq_len, max_parts, part_tokens;
   float scale_log2;  // scale * log2(e) (* k_scale for fp8)
@@ -82,7 +73,7 @@ struct Cfg {
   static constexpr int TILE_BYTES = 16 * ROW_BYTES;    // K (or V) of a block-head
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K + V
   static constexpr int NW = 4;                         // warps per CTA
-  static constexpr int RING_BYTES = 96 * 1024;         // all stages of a CTA
+  static constexpr int RING_BYTES = 64 * 1024;         // all stages of a CTA (3 CTAs/SM)
   static constexpr int S0 = RING_BYTES / (NW * STAGE_BYTES);
   static constexpr int STAGES = S0 < 2 ? 2 : (S0 > 8 ? 8 : S0);
   static constexpr int MT = D / 16;                    // 16-row tiles of head_dim
@@ -241,12 +232,16 @@ __device__ __forceinline__ void block_update(uint32_t sv, int nv, const float (&
   st.l1 = st.l1 * al1 + (p1 + p3);
   st.m0 = mn0;
   st.m1 = mn1;
+  // Once the running maxima settle, alpha is 1 for every column: skip the
+  // rescale then (the result is the same, multiplying by 1 is exact).
+  if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-  for (int mt = 0; mt < C::MT; ++mt) {
-    st.o[mt][0] *= al0;
-    st.o[mt][1] *= al1;
-    st.o[mt][2] *= al0;
-    st.o[mt][3] *= al1;
+    for (int mt = 0; mt < C::MT; ++mt) {
+      st.o[mt][0] *= al0;
+      st.o[mt][1] *= al1;
+      st.o[mt][2] *= al0;
+      st.o[mt][3] *= al1;
+    }
   }
 
   // -- P^T fragment (B operand of O^T += V^T . P^T) -----------------------
@@ -302,399 +297,20 @@ __device__ __forceinline__ void attend_block(uint32_t sk, uint32_t sv, int nv,
   block_update<FP8, D>(sv, nv, sc, scale_log2, st, lane);
 }
 
-// Lane 0 issues the TMA loads of one block-head (K and V) into a stage.
+// Lane 0 issues the TMA loads of one block-head (K and V tiles) into a
+// stage: one box per tile, [head_dim slice][token][BOX_BYTES].
 template <bool FP8, int D>
 __device__ __forceinline__ void issue_block(uint8_t *stage, uint64_t *bar,
                                             const CUtensorMap *tk, const CUtensorMap *tv,
                                             int kvh, int phys, uint64_t policy) {
   using C = Cfg<FP8, D>;
   mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
-#pragma unroll
-  for (int bx = 0; bx < C::NBOX; ++bx)
-    tma_load_4d(stage + bx * 16 * C::BOX_BYTES, tk, bar, bx * C::BOX_ELEMS, kvh, 0, phys, policy);
-#pragma unroll
-  for (int bx = 0; bx < C::NBOX; ++bx)
-    tma_load_4d(stage + C::TILE_BYTES + bx * 16 * C::BOX_BYTES, tv, bar, bx * C::BOX_ELEMS, kvh,
-                0, phys, policy);
+  tma_load_5d(stage, tk, bar, 0, 0, kvh, 0, phys, policy);
+  tma_load_5d(stage + C::TILE_BYTES, tv, bar, 0, 0, kvh, 0, phys, policy);
 }
 
 // ===========================================================================
-// Balanced stream schedule
-// ===========================================================================
-// Item = (sequence b, group kg of hg consecutive kv heads with all their
-// query heads).  The block chains of all items, concatenated b-major, are
-// cut into one equal contiguous range per CTA (one CTA per SM).  In a CTA a
-// producer warp walks its range and, per block, TMA-loads the K tiles of all
-// hg heads into one ring slot and the V tiles into the next, so the whole
-// contiguous K (then V) segment of the block is requested at once.  One
-// consumer warp per (kv head, query sub-group) computes on its head's tiles
-// and releases a slot as soon as it is done with it (K right after the
-// scores).  An item that ends up whole in one CTA writes the output; the
-// pieces of an item split across CTAs are written as (max, sum, output)
-// partials and the CTA that completes the item's last piece merges them
-// (log-sum-exp, pieces in CTA order).  Completion is counted with a ticket
-// word per item: no CTA ever waits for another.
-constexpr int kMaxSlots = 16;
-constexpr int kStreamRingBytes = 192 * 1024;
-constexpr int kMaxConsumerWarps = 8;
-constexpr int kMaxWarpStages = 8;
-
-// Position in the concatenated block chains (item order b-major, then kg).
-struct Cursor {
-  int b, L, n, kg, j;  // sequence, clamped length, blocks, head group, block
-  long long base;      // stream index of (b, kg = 0, j = 0)
-};
-
-__device__ __forceinline__ int blocks_of(const DecodeParams &p, int b, int cap) {
-  return (clamp_len(__ldg(p.seq_lens + b), cap) + 15) >> 4;
-}
-
-// Next block of the stream (skipping empty sequences); only called while
-// the stream has a next block.
-__device__ __forceinline__ void advance(Cursor &cu, const DecodeParams &p, int NG, int cap) {
-  if (++cu.j < cu.n) return;
-  cu.j = 0;
-  if (++cu.kg < NG) return;
-  cu.kg = 0;
-  cu.base += (long long)cu.n * NG;
-  do {
-    ++cu.b;
-    cu.L = clamp_len(__ldg(p.seq_lens + cu.b), cap);
-    cu.n = (cu.L + 15) >> 4;
-  } while (cu.n == 0 && cu.b + 1 < p.batch);
-}
-
-// Worker (CTA) of stream position x when T blocks are cut into W ranges
-// [floor(w T / W), floor((w + 1) T / W)).
-__device__ __forceinline__ long long worker_of(long long x, long long W, long long T) {
-  return ((x + 1) * W - 1) / T;
-}
-
-// Log-sum-exp merge of item s's pieces (held by CTAs wf..wl, slot w + s)
-// for `heads` query heads starting at item-local head qh0; one warp.  All
-// (max, sum) pairs are loaded at once (lane i: piece i of a chunk of 32),
-// reduced with shuffles, then every lane accumulates its head_dim elements
-// of all heads piece by piece (fixed order: bitwise deterministic).
-template <int D>
-__device__ __forceinline__ void merge_pieces(const DecodeParams &p, long long s, long long wf,
-                                             long long wl, int hqt, int qh0, int heads,
-                                             size_t out_row0, int lane) {
-  constexpr int KD = D / 32;
-  float acc[8][KD];
-  float M[8], wsum[8];
-#pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    M[h] = -INFINITY;
-    wsum[h] = 0.f;
-#pragma unroll
-    for (int k = 0; k < KD; ++k) acc[h][k] = 0.f;
-  }
-  const long long np = wl - wf + 1;
-  // pass 1: maxima
-  for (long long i0 = 0; i0 < np; i0 += 32) {
-    const long long i = i0 + lane;
-#pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      float m = -INFINITY;
-      if (h < heads && i < np) m = __ldcg(&p.piece_ml[(wf + i + s) * hqt + qh0 + h].x);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      M[h] = fmaxf(M[h], m);
-    }
-  }
-  // pass 2: weights (lane i holds piece i0 + i), sums and weighted outputs
-  for (long long i0 = 0; i0 < np; i0 += 32) {
-    const long long i = i0 + lane;
-    float wl_[8];
-#pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      float w = 0.f;
-      if (h < heads && i < np) {
-        const float2 ml = __ldcg(&p.piece_ml[(wf + i + s) * hqt + qh0 + h]);
-        w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M[h]) * ml.y;
-      }
-      wl_[h] = w;
-      float t = w;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-      wsum[h] += t;
-    }
-    const int cnt = (int)(np - i0 < 32 ? np - i0 : 32);
-#pragma unroll 2
-    for (int r = 0; r < cnt; ++r) {
-      const float *po = p.piece_o + ((size_t)(wf + i0 + r + s) * hqt + qh0) * D + lane;
-#pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        const float w = __shfl_sync(0xffffffffu, wl_[h], r);
-        if (h < heads) {
-#pragma unroll
-          for (int k = 0; k < KD; ++k) acc[h][k] += w * __ldcg(po + (size_t)h * D + 32 * k);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    if (h < heads) {
-      const float inv = wsum[h] > 0.f ? 1.f / wsum[h] : 0.f;
-      __nv_bfloat16 *orow = p.out + (out_row0 + h) * D;
-#pragma unroll
-      for (int k = 0; k < KD; ++k) orow[lane + 32 * k] = __float2bfloat16_rn(acc[h][k] * inv);
-    }
-  }
-}
-
-template <bool FP8, int D>
-__global__ void __launch_bounds__(kMaxConsumerWarps * 32, 1)
-paged_decode_stream_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                           const __grid_constant__ CUtensorMap tmap_v,
-                           const DecodeParams p) {
-  using C = Cfg<FP8, D>;
-  extern __shared__ uint8_t smem_dyn[];
-  __shared__ uint64_t full_bar[kMaxConsumerWarps][kMaxWarpStages];
-  __shared__ int slot_ok[kMaxConsumerWarps][kMaxWarpStages];
-  __shared__ long long sh_T, sh_W, sh_start, sh_end;
-  __shared__ Cursor sh_cu;
-  __shared__ int sh_last;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int ncw = p.hg * p.q_groups;  // warps: (kv head of the group, query sub-group)
-  const int NSW = p.ring_slots;        // stages (K + V tiles) per warp
-  const int NG = p.num_kv_heads / p.hg;
-  const int HQT = p.hg * p.group;  // query heads per item
-  const int cap = min(p.max_blocks * 16, p.max_seq_len);
-  const uint32_t base_u32 = smem_u32(smem_dyn);
-  uint8_t *ring = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32) +
-                  (size_t)warp * NSW * C::STAGE_BYTES;
-
-  if (lane == 0) {
-    for (int s = 0; s < NSW; ++s) mbar_init(&full_bar[warp][s], 1);
-    fence_barrier_init();
-    if (warp == 0) {
-      prefetch_tensormap(&tmap_k);
-      prefetch_tensormap(&tmap_v);
-    }
-  }
-  __syncthreads();
-  grid_dependency_wait();
-  allow_dependent_launch();
-
-  // ---- this CTA's range of the stream -------------------------------------
-  if (warp == 0) {
-    long long T = 0;
-    for (int b0 = 0; b0 < p.batch; b0 += 32) {
-      const int b = b0 + lane;
-      if (b < p.batch) {
-        const int L = __ldg(p.seq_lens + b);
-        if (blockIdx.x == 0 && (L < 0 || L > cap))
-          record_error(&g_err_attention, PKV_ERR_RANGE, b);
-        T += (clamp_len(L, cap) + 15) >> 4;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) T += __shfl_xor_sync(0xffffffffu, T, off);
-    T *= NG;
-    // min(CTAs, T) ranges, so that no range is empty
-    const long long W = T < (long long)gridDim.x ? T : (long long)gridDim.x;
-    const long long w = blockIdx.x;
-    const long long start = w < W ? w * T / W : 0, end = w < W ? (w + 1) * T / W : 0;
-    Cursor cu = {0, 0, 0, 0, 0, 0};
-    if (start < end) {
-      long long run = 0;  // blocks per head group of sequences before b0
-      for (int b0 = 0;; b0 += 32) {
-        const int b = b0 + lane;
-        const int n = b < p.batch ? blocks_of(p, b, cap) : 0;
-        int incl = n;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += y;
-        }
-        const unsigned mask = __ballot_sync(0xffffffffu, b < p.batch && (run + incl) * NG > start);
-        if (mask) {
-          const int src = __ffs(mask) - 1;
-          cu.b = b0 + src;
-          cu.n = __shfl_sync(0xffffffffu, n, src);
-          cu.base = (run + __shfl_sync(0xffffffffu, incl - n, src)) * NG;
-          break;
-        }
-        run += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      cu.L = clamp_len(__ldg(p.seq_lens + cu.b), cap);
-      const long long off = start - cu.base;
-      cu.kg = (int)(off / cu.n);
-      cu.j = (int)(off - (long long)cu.kg * cu.n);
-    }
-    if (lane == 0) {
-      sh_T = T;
-      sh_W = W;
-      sh_start = start;
-      sh_end = end;
-      sh_cu = cu;
-    }
-  }
-  // ---- rows of empty sequences are zero ------------------------------------
-  for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
-    if (clamp_len(__ldg(p.seq_lens + b), cap) != 0) continue;
-    for (int h = warp; h < p.num_heads; h += ncw)
-#pragma unroll
-      for (int k = 0; k < D / 32; ++k)
-        p.out[((size_t)b * p.num_heads + h) * D + lane + 32 * k] = __float2bfloat16_rn(0.f);
-  }
-  __syncthreads();
-  const long long T = sh_T, W = sh_W;
-  const long long total = sh_end - sh_start;
-  if (total <= 0) return;
-
-  const int hl = warp % p.hg;
-  const int qg = warp / p.hg;
-  const int heads_here = min(8, p.group - qg * 8);
-  const int qh_local = hl * p.group + qg * 8;  // first query head within the item
-
-  // ---- load side: this warp's head of each block of the range --------------
-  Cursor ci = sh_cu;
-  int win_b = -1, win_j = -1, ids = 0;
-  const uint64_t policy = l2_policy_evict_normal();
-  long long issued = 0;
-  auto issue_next = [&]() {
-    const int jw = ci.j & ~31;
-    if (ci.b != win_b || jw != win_j) {
-      win_b = ci.b;
-      win_j = jw;
-      const int jj = jw + lane;
-      ids = jj < ci.n ? __ldg(p.block_tables + (size_t)ci.b * p.max_blocks + jj) : -1;
-    }
-    int phys = __shfl_sync(0xffffffffu, ids, ci.j & 31);
-    if (lane == 0) {
-      const int stage = (int)(issued % NSW);
-      int ok = 1;
-      if (phys < 0 || phys >= p.num_blocks) {
-        record_error(&g_err_attention, PKV_ERR_RANGE, ci.b);
-        phys = 0;
-        ok = 0;
-      }
-      slot_ok[warp][stage] = ok;
-      uint64_t *bar = &full_bar[warp][stage];
-      uint8_t *dst = ring + (size_t)stage * C::STAGE_BYTES;
-      mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
-      const int kvh = ci.kg * p.hg + hl;
-      tma_load_5d(dst, &tmap_k, bar, 0, 0, kvh, 0, phys, policy);
-      tma_load_5d(dst + C::TILE_BYTES, &tmap_v, bar, 0, 0, kvh, 0, phys, policy);
-    }
-    if (++issued < total) advance(ci, p, NG, cap);
-  };
-  const int pre = (int)(total < NSW ? total : (long long)NSW);
-  for (int i = 0; i < pre; ++i) issue_next();
-
-  // ---- compute side -------------------------------------------------------
-  Cursor cu = sh_cu;
-  WarpState<FP8, D> st;
-  st.reset();
-  uint32_t qf[C::MT][2];
-  int piece_j0 = cu.j;
-  auto item_q = [&]() {
-    return p.q + ((size_t)cu.b * p.num_heads + (size_t)cu.kg * HQT + qh_local) * D;
-  };
-  load_q<FP8, D>(qf, item_q(), heads_here, lane);
-
-  bool failed = false;
-  for (long long x = 0; x < total; ++x) {
-    const int stage = (int)(x % NSW);
-    if (!failed &&
-        !mbar_wait_bounded(&full_bar[warp][stage], (uint32_t)((x / NSW) & 1), p.timeout_ns)) {
-      failed = true;
-      if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, cu.b);
-    }
-    const int nv = slot_ok[warp][stage] ? min(16, cu.L - cu.j * 16) : 0;
-    const uint32_t sk = smem_u32(ring + (size_t)stage * C::STAGE_BYTES);
-    attend_block<FP8, D>(sk, sk + C::TILE_BYTES, nv, qf, p.scale_log2, st, lane);
-    __syncwarp();
-    if (!failed && issued < total) issue_next();
-
-    const bool last_of_item = cu.j == cu.n - 1;
-    if (!last_of_item && x + 1 < total) {
-      advance(cu, p, NG, cap);
-      continue;
-    }
-    // ---- end of a piece: the item's last block or this range's last -------
-    st.reduce_l();
-    const long long s = (long long)cu.b * NG + cu.kg;
-    const size_t out_row0 = (size_t)cu.b * p.num_heads + (size_t)cu.kg * HQT + qh_local;
-    const float inv0 = st.l0 > 0.f ? p.v_scale / st.l0 : 0.f;
-    const float inv1 = st.l1 > 0.f ? p.v_scale / st.l1 : 0.f;
-    if (piece_j0 == 0 && last_of_item) {
-      // whole item in this CTA
-      __nv_bfloat16 *orow = p.out + out_row0 * D;
-#pragma unroll
-      for (int mt = 0; mt < C::MT; ++mt) {
-#pragma unroll
-        for (int hi = 0; hi < 2; ++hi) {
-          const int d = o_row<FP8>(mt, hi, g);
-          if (2 * c < heads_here)
-            orow[(size_t)(2 * c) * D + d] = __float2bfloat16_rn(st.o[mt][2 * hi] * inv0);
-          if (2 * c + 1 < heads_here)
-            orow[(size_t)(2 * c + 1) * D + d] = __float2bfloat16_rn(st.o[mt][2 * hi + 1] * inv1);
-        }
-      }
-    } else {
-      const long long slot_row = ((long long)blockIdx.x + s) * HQT + qh_local;
-      float *po = p.piece_o + (size_t)slot_row * D;
-#pragma unroll
-      for (int mt = 0; mt < C::MT; ++mt) {
-#pragma unroll
-        for (int hi = 0; hi < 2; ++hi) {
-          const int d = o_row<FP8>(mt, hi, g);
-          if (2 * c < heads_here) po[(size_t)(2 * c) * D + d] = st.o[mt][2 * hi] * inv0;
-          if (2 * c + 1 < heads_here) po[(size_t)(2 * c + 1) * D + d] = st.o[mt][2 * hi + 1] * inv1;
-        }
-      }
-      if (g == 0) {
-        if (2 * c < heads_here) p.piece_ml[slot_row + 2 * c] = make_float2(st.m0, st.l0);
-        if (2 * c + 1 < heads_here) p.piece_ml[slot_row + 2 * c + 1] = make_float2(st.m1, st.l1);
-      }
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const long long ps = cu.base + (long long)cu.kg * cu.n;
-        const long long pieces = worker_of(ps + cu.n - 1, W, T) - worker_of(ps, W, T) + 1;
-        unsigned long long *ticket = p.tickets + s;
-        unsigned long long old = atomicAdd(ticket, 0ull), want = 0ull;
-        for (int it = 0; it < (1 << 20); ++it) {
-          want = (old >> 24) == p.epoch ? old + 1ull : ((p.epoch << 24) | 1ull);
-          const unsigned long long got = atomicCAS(ticket, old, want);
-          if (got == old) break;
-          old = got;
-        }
-        const bool last = (long long)(want & 0xffffffull) == pieces;
-        if (last) atomicExch(ticket, 0ull);  // clean for the next call
-        sh_last = last ? 1 : 0;
-      }
-      __syncthreads();
-      if (sh_last) {
-        __threadfence();
-        const long long ps = cu.base + (long long)cu.kg * cu.n;
-        merge_pieces<D>(p, s, worker_of(ps, W, T), worker_of(ps + cu.n - 1, W, T), HQT,
-                        qh_local, heads_here, out_row0, lane);
-      }
-    }
-    if (x + 1 < total) {
-      advance(cu, p, NG, cap);
-      st.reset();
-      piece_j0 = cu.j;  // a new item starts at block 0
-      load_q<FP8, D>(qf, item_q(), heads_here, lane);
-    }
-  }
-  if (failed) {
-    // let copies still in flight land before the CTA exits (bounded too)
-    for (long long r = issued > NSW ? issued - NSW : 0; r < issued; ++r)
-      mbar_wait_bounded(&full_bar[warp][r % NSW], (uint32_t)((r / NSW) & 1), p.timeout_ns);
-  }
-}
-
-// ===========================================================================
-// Fixed-partition schedule
+// Decode kernel
 // ===========================================================================
 template <bool FP8, int D>
 __global__ void __launch_bounds__(Cfg<FP8, D>::NW * 32)
@@ -707,15 +323,16 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   __shared__ int stage_ok[C::NW][C::STAGES];
   __shared__ float m_s[C::NW][8];
   __shared__ float l_s[C::NW][8];
+  __shared__ int sh_last;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2;
   const int c = lane & 3;
-  const int part = blockIdx.x;
-  const int b = blockIdx.y;
-  const int kvh = blockIdx.z / p.q_groups;
-  const int qg = blockIdx.z - kvh * p.q_groups;
+  const int kvh = blockIdx.x / p.q_groups;
+  const int qg = blockIdx.x - kvh * p.q_groups;
+  const int part = blockIdx.y;
+  const int b = blockIdx.z;
 
   const uint32_t base_u32 = smem_u32(smem_dyn);
   uint8_t *rings = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32);
@@ -735,7 +352,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   {
     const int cap = min(p.max_blocks * 16, p.max_seq_len);
     if (L < 0 || L > cap) {
-      if (part == 0 && blockIdx.z == 0 && threadIdx.x == 0)
+      if (part == 0 && blockIdx.x == 0 && threadIdx.x == 0)
         record_error(&g_err_attention, PKV_ERR_RANGE, b);
       L = clamp_len(L, cap);
     }
@@ -748,10 +365,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int nblk = (tok1 - tok0 + 15) >> 4;
   const int my_n = nblk > warp ? (nblk - warp + C::NW - 1) / C::NW : 0;
   const int heads_here = min(8, p.group - qg * 8);
+  const size_t row0 = (size_t)b * p.num_heads + (size_t)kvh * p.group + qg * 8;
 
   uint32_t qf[C::MT][2];
-  load_q<FP8, D>(qf, p.q + ((size_t)b * p.num_heads + kvh * p.group + qg * 8) * D, heads_here,
-                 lane);
+  load_q<FP8, D>(qf, p.q + row0 * D, heads_here, lane);
 
   // ---- block ids of this warp, 32 at a time in registers -----------------
   const int32_t *table = p.block_tables + (size_t)b * p.max_blocks + blk0 + warp;
@@ -797,6 +414,8 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   if (failed) {
     if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, b);
+    // let copies still in flight land before the ring is reused or the CTA
+    // exits (bounded as well)
     for (int i = 0; i < issued; ++i)
       mbar_wait_bounded(&bars[warp][i % C::STAGES], (i / C::STAGES) & 1, p.timeout_ns);
     st.m0 = st.m1 = -INFINITY;
@@ -843,70 +462,55 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
       }
     }
     const float res = lsum > 0.f ? acc / lsum * p.v_scale : 0.f;
-    const int head = kvh * p.group + qg * 8 + h;
-    const size_t bh = (size_t)b * p.num_heads + head;
+    const size_t r = row0 + h;
     if (nparts == 1) {
-      p.out[bh * D + d] = __float2bfloat16_rn(res);
+      p.out[r * D + d] = __float2bfloat16_rn(res);
     } else {
-      p.part_o[(bh * p.max_parts + part) * D + d] = res;
-      if (d == 0) p.part_ml[bh * p.max_parts + part] = make_float2(M, lsum);
+      p.part_o[(r * p.max_parts + part) * D + d] = res;
+      if (d == 0) p.part_ml[r * p.max_parts + part] = make_float2(M, lsum);
     }
   }
-}
+  if (nparts == 1) return;
 
-// Log-sum-exp merge of a split sequence's partitions: one CTA per (query
-// head, sequence), one thread per head_dim element.  Partition j carries
-// m_j (log2 domain), l_j and its normalised output o_j; the result is
-// sum_j 2^(m_j - M) l_j o_j / sum_j 2^(m_j - M) l_j with M = max_j m_j.
-template <int D>
-__global__ void __launch_bounds__(D)
-paged_decode_reduce_kernel(const DecodeParams p) {
-  extern __shared__ float w_s[];  // [max_parts]
-  __shared__ float red[D / 32];
-  grid_dependency_wait();
-  allow_dependent_launch();
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int cap = min(p.max_blocks * 16, p.max_seq_len);
-  const int L = clamp_len(__ldg(p.seq_lens + b), cap);
-  const int nparts = L <= p.part_tokens ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
-  if (nparts <= 1) return;  // the decode kernel wrote the output directly
-  const size_t bh = (size_t)b * p.num_heads + h;
-  const float2 *ml = p.part_ml + bh * p.max_parts;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-  float M = -INFINITY;
-  for (int j = tid; j < nparts; j += D) M = fmaxf(M, ml[j].x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (lane == 0) red[warp] = M;
+  // ---- split sequence: the CTA completing the last partition merges ------
+  __threadfence();
   __syncthreads();
-  M = red[0];
-#pragma unroll
-  for (int w = 1; w < D / 32; ++w) M = fmaxf(M, red[w]);
-  __syncthreads();
-
-  float W = 0.f;
-  for (int j = tid; j < nparts; j += D) {
-    const float2 v = ml[j];
-    const float w = v.x == -INFINITY ? 0.f : exp2f(v.x - M) * v.y;
-    w_s[j] = w;
-    W += w;
+  if (threadIdx.x == 0) {
+    unsigned long long *ticket =
+        p.tickets + ((size_t)b * p.num_kv_heads + kvh) * p.q_groups + qg;
+    unsigned long long old = atomicAdd(ticket, 0ull), want = 0ull;
+    for (int it = 0; it < (1 << 20); ++it) {
+      want = (old >> 24) == p.epoch ? old + 1ull : ((p.epoch << 24) | 1ull);
+      const unsigned long long got = atomicCAS(ticket, old, want);
+      if (got == old) break;
+      old = got;
+    }
+    const bool last = (int)(want & 0xffffffull) == nparts;
+    if (last) atomicExch(ticket, 0ull);  // clean for the next call
+    sh_last = last ? 1 : 0;
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
-  if (lane == 0) red[warp] = W;
   __syncthreads();
-  W = 0.f;
-#pragma unroll
-  for (int w = 0; w < D / 32; ++w) W += red[w];
-
-  const float *po = p.part_o + bh * p.max_parts * D + tid;
-  float acc = 0.f;
-  for (int j = 0; j < nparts; ++j) {
-    const float w = w_s[j];
-    if (w != 0.f) acc += w * po[(size_t)j * D];
+  if (!sh_last) return;
+  __threadfence();
+  // One thread per (head, head_dim element); partitions in order.
+  for (int idx = threadIdx.x; idx < heads_here * D; idx += blockDim.x) {
+    const int h = idx / D;
+    const int d = idx - h * D;
+    const size_t r = row0 + h;
+    const float2 *ml = p.part_ml + r * p.max_parts;
+    const float *po = p.part_o + r * p.max_parts * D + d;
+    float M = -INFINITY;
+    for (int j = 0; j < nparts; ++j) M = fmaxf(M, __ldcg(&ml[j].x));
+    float wsum = 0.f, acc = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < nparts; ++j) {
+      const float2 v = __ldcg(&ml[j]);
+      const float w = v.x == -INFINITY ? 0.f : exp2f(v.x - M) * v.y;
+      wsum += w;
+      acc += w * __ldcg(po + (size_t)j * D);
+    }
+    p.out[r * D + d] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
   }
-  p.out[bh * D + tid] = __float2bfloat16_rn(W > 0.f ? acc / W : 0.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -928,36 +532,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 4-D map over one cache: dims (innermost first) {head_dim, num_kv_heads,
-// 16, num_blocks}, box {box_elems, 1, 16, 1}.
+// 5-D map over one cache: dims (innermost first) {box_elems, 16 tokens,
+// num_kv_heads, head_dim slices, num_blocks}.  The token stride is larger
+// than the head stride, so a box {box_elems, 16, 1, slices, 1} -- one head
+// of one block -- lands in shared memory as [slice][token][box bytes]: the
+// 16 tokens are consecutive swizzled rows, conflict-free for ldmatrix, and
+// the whole tile is one copy.
 bool encode_cache_map(CUtensorMap *map, void *base, const pkv_cache *c) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const bool fp8 = c->dtype == PKV_FP8_E4M3;
-  const cuuint64_t elt = fp8 ? 1 : 2;
-  const cuuint64_t row = (cuuint64_t)c->head_dim * elt;
-  const cuuint32_t box_bytes = row >= 128 ? 128 : (cuuint32_t)row;
-  cuuint64_t dims[4] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->num_kv_heads, 16,
-                        (cuuint64_t)c->num_blocks};
-  cuuint64_t strides[3] = {row, row * c->num_kv_heads, row * c->num_kv_heads * 16};
-  cuuint32_t box[4] = {(cuuint32_t)(box_bytes / elt), 1, 16, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r =
-      fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base,
-         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-         box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// 5-D map over one cache for loads of `hg` consecutive kv heads of a block:
-// dims (innermost first) {box_elems, 16 tokens, num_kv_heads, head_dim
-// slices, num_blocks}.  The token stride is larger than the head stride, so
-// one box {box_elems, 16, hg, slices, 1} lands in shared memory as
-// [slice][head][token][box bytes]: every head's 16 tokens are consecutive
-// swizzled rows, exactly the per-head tile layout, and the whole K (or V)
-// segment of the hg heads is requested by a single copy.
-bool encode_group_map(CUtensorMap *map, void *base, const pkv_cache *c, int hg) {
   auto fn = encode_fn();
   if (!fn) return false;
   const bool fp8 = c->dtype == PKV_FP8_E4M3;
@@ -968,7 +549,7 @@ bool encode_group_map(CUtensorMap *map, void *base, const pkv_cache *c, int hg) 
   cuuint64_t dims[5] = {box_bytes / elt, 16, (cuuint64_t)c->num_kv_heads, slices,
                         (cuuint64_t)c->num_blocks};
   cuuint64_t strides[4] = {row * c->num_kv_heads, row, box_bytes, row * c->num_kv_heads * 16};
-  cuuint32_t box[5] = {(cuuint32_t)(box_bytes / elt), 16, (cuuint32_t)hg, (cuuint32_t)slices, 1};
+  cuuint32_t box[5] = {(cuuint32_t)(box_bytes / elt), 16, 1, (cuuint32_t)slices, 1};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   const CUresult r =
       fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base,
@@ -978,24 +559,23 @@ bool encode_group_map(CUtensorMap *map, void *base, const pkv_cache *c, int hg) 
   return r == CUDA_SUCCESS;
 }
 
-// Small cache of encoded maps keyed by the cache geometry and the map kind
-// (hg == 0: per-head 4-D maps; hg > 0: 5-D maps over hg heads).
+// Small cache of encoded maps keyed by the cache geometry.
 struct MapEntry {
   void *key_cache, *value_cache;
-  int32_t num_blocks, num_kv_heads, head_dim, dtype, hg;
+  int32_t num_blocks, num_kv_heads, head_dim, dtype;
   CUtensorMap k, v;
 };
 
-bool get_maps(const pkv_cache *c, int hg, CUtensorMap *k, CUtensorMap *v) {
+bool get_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
   static std::mutex mu;
-  static MapEntry entries[16];
+  static MapEntry entries[8];
   static int n_entries = 0, next = 0;
   std::lock_guard<std::mutex> lock(mu);
   for (int i = 0; i < n_entries; ++i) {
     const MapEntry &e = entries[i];
     if (e.key_cache == c->key_cache && e.value_cache == c->value_cache &&
         e.num_blocks == c->num_blocks && e.num_kv_heads == c->num_kv_heads &&
-        e.head_dim == c->head_dim && e.dtype == c->dtype && e.hg == hg) {
+        e.head_dim == c->head_dim && e.dtype == c->dtype) {
       *k = e.k;
       *v = e.v;
       return true;
@@ -1008,75 +588,47 @@ bool get_maps(const pkv_cache *c, int hg, CUtensorMap *k, CUtensorMap *v) {
   e.num_kv_heads = c->num_kv_heads;
   e.head_dim = c->head_dim;
   e.dtype = c->dtype;
-  e.hg = hg;
-  const bool ok = hg > 0 ? encode_group_map(&e.k, c->key_cache, c, hg) &&
-                               encode_group_map(&e.v, c->value_cache, c, hg)
-                         : encode_cache_map(&e.k, c->key_cache, c) &&
-                               encode_cache_map(&e.v, c->value_cache, c);
-  if (!ok) return false;
+  if (!encode_cache_map(&e.k, c->key_cache, c) || !encode_cache_map(&e.v, c->value_cache, c))
+    return false;
   entries[next] = e;
-  next = (next + 1) % 16;
-  if (n_entries < 16) ++n_entries;
+  next = (next + 1) % 8;
+  if (n_entries < 8) ++n_entries;
   *k = e.k;
   *v = e.v;
   return true;
 }
 
-// Partition length used when the balanced schedule cannot hold an item's
-// query heads in one CTA (more than 64 query heads per kv head).
-constexpr int kFallbackPartition = 512;
+constexpr int kCtasPerSm = 3;  // 64 KiB rings
 
-// Stream schedule geometry: kv heads per item (largest divisor of Hkv whose
-// consumer warps, hg * query sub-groups, fit in one CTA) and ring slots.
-struct StreamGeom {
-  int hg, q_groups, slots, slot_bytes;
-  bool ok;
-};
-
-StreamGeom stream_geom(int64_t num_heads, int64_t num_kv_heads, int64_t head_dim, int dtype) {
-  StreamGeom gm = {0, 0, 0, 0, false};
-  if (num_kv_heads <= 0 || num_heads % num_kv_heads) return gm;
+// Automatic partition length: the longest of 256 * 2^k tokens that still
+// gives about three waves of CTAs for the worst case (every sequence at
+// max_seq_len); no split at all when the sequences alone fill them.
+int auto_partition_tokens(int64_t batch, int64_t num_heads, int64_t num_kv_heads,
+                          int64_t max_seq_len, int sms) {
+  const int64_t whole = std::max<int64_t>(16, (max_seq_len + 15) / 16 * 16);
   const int64_t group = num_heads / num_kv_heads;
-  gm.q_groups = (int)((group + 7) / 8);
-  if (gm.q_groups > kMaxConsumerWarps) return gm;
-  for (int hg = kMaxConsumerWarps / gm.q_groups; hg >= 1; --hg)
-    if (num_kv_heads % hg == 0) {
-      gm.hg = hg;
-      break;
-    }
-  const int64_t tile = 16 * head_dim * (dtype == PKV_FP8_E4M3 ? 1 : 2);
-  const int64_t warps = (int64_t)gm.hg * gm.q_groups;
-  gm.slot_bytes = (int)(2 * tile);  // one stage: K and V tiles of one head
-  gm.slots = (int)std::min<int64_t>(kMaxWarpStages, kStreamRingBytes / (warps * gm.slot_bytes));
-  gm.ok = gm.slots >= 2;
-  return gm;
+  const int64_t units = batch * num_kv_heads * ((group + 7) / 8);
+  const int64_t target = (int64_t)sms * kCtasPerSm * 3;
+  if (units >= target) return (int)std::min<int64_t>(whole, 1 << 30);
+  int64_t pt = 256;
+  while (pt * 2 < whole && units * ((whole + 2 * pt - 1) / (2 * pt)) >= target) pt *= 2;
+  return (int)std::min<int64_t>(pt, whole);
 }
 
-struct StreamLayout {
-  size_t o_off, ml_off, ticket_off, bytes;
+struct PartLayout {
+  size_t ml_off, ticket_off, bytes;
 };
 
-// Pieces: (CTAs + items) slots of the item's query heads; one ticket word
-// per item.
-StreamLayout stream_layout(int64_t batch, int64_t num_heads, int64_t num_kv_heads,
-                           int64_t head_dim, int ctas, const StreamGeom &gm) {
-  const int64_t items = batch * (num_kv_heads / gm.hg);
-  const int64_t hqt = gm.hg * (num_heads / num_kv_heads);
-  const int64_t slots = ctas + items;
+PartLayout part_layout(int64_t batch, int64_t num_heads, int64_t num_kv_heads,
+                       int64_t head_dim, int64_t max_parts) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  StreamLayout l;
-  l.o_off = 0;
-  l.ml_off = up((size_t)slots * hqt * head_dim * sizeof(float));
-  l.ticket_off = l.ml_off + up((size_t)slots * hqt * sizeof(float2));
-  l.bytes = l.ticket_off + up((size_t)items * sizeof(unsigned long long));
-  return l;
-}
-
-size_t partition_workspace(int32_t batch, int32_t num_heads, int32_t head_dim, int32_t max_parts) {
-  if (max_parts <= 1) return 0;
   const size_t rows = (size_t)batch * num_heads * max_parts;
-  const size_t o_bytes = (rows * head_dim * sizeof(float) + 255) / 256 * 256;
-  return o_bytes + rows * sizeof(float2);
+  const int64_t q_groups = (num_heads / num_kv_heads + 7) / 8;
+  PartLayout l;
+  l.ml_off = up(rows * head_dim * sizeof(float));
+  l.ticket_off = l.ml_off + up(rows * sizeof(float2));
+  l.bytes = l.ticket_off + up((size_t)batch * num_kv_heads * q_groups * sizeof(unsigned long long));
+  return l;
 }
 
 // Launch with programmatic stream serialisation (see grid_dependency_wait).
@@ -1097,50 +649,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 template <bool FP8, int D>
-pkv_status configure_smem() {
+pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
+                         cudaStream_t s) {
   using C = Cfg<FP8, D>;
   static int configured[64] = {0};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!configured[dev]) {
-    if (cudaFuncSetAttribute(paged_decode_kernel<FP8, D>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(paged_decode_stream_kernel<FP8, D>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kStreamRingBytes + 1024) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    configured[dev] = 1;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      if (cudaFuncSetAttribute(paged_decode_kernel<FP8, D>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_BYTES) != cudaSuccess)
+        return PKV_ERR_CUDA;
+      configured[dev] = 1;
+    }
   }
-  return PKV_OK;
-}
-
-template <bool FP8, int D>
-pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                         bool stream_schedule, int sms, cudaStream_t s) {
-  using C = Cfg<FP8, D>;
-  pkv_status st = configure_smem<FP8, D>();
-  if (st != PKV_OK) return st;
-  if (stream_schedule) {
-    const int warps = p.hg * p.q_groups;
-    const size_t smem = (size_t)warps * p.ring_slots * C::STAGE_BYTES + 1024;
-    const int threads = warps * 32;
-    if (launch_pdl(paged_decode_stream_kernel<FP8, D>, dim3(sms), dim3(threads), smem, s, mk, mv,
-                   p) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    return PKV_OK;
-  }
-  dim3 grid(p.max_parts, p.batch, p.num_kv_heads * p.q_groups);
+  dim3 grid(p.num_kv_heads * p.q_groups, p.max_parts, p.batch);
   if (launch_pdl(paged_decode_kernel<FP8, D>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s, mk, mv,
                  p) != cudaSuccess)
     return PKV_ERR_CUDA;
-  if (p.max_parts > 1) {
-    if (launch_pdl(paged_decode_reduce_kernel<D>, dim3(p.num_heads, p.batch), dim3(D),
-                   p.max_parts * sizeof(float), s, p) != cudaSuccess)
-      return PKV_ERR_CUDA;
-  }
   return PKV_OK;
 }
 
@@ -1182,9 +711,9 @@ extern "C" int32_t paged_attention_partition_tokens(int32_t batch, int32_t num_h
   if (batch < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
       max_seq_len < 0 || partition_tokens < 0 || partition_tokens % 16)
     return -1;
-  if (partition_tokens == 0 && !stream_geom(num_heads, num_kv_heads, 128, PKV_BF16).ok)
-    return kFallbackPartition;
-  return partition_tokens;  // 0: balanced stream schedule
+  if (partition_tokens > 0) return partition_tokens;
+  const int sms = device_sm_count();
+  return auto_partition_tokens(batch, num_heads, num_kv_heads, max_seq_len, sms > 0 ? sms : 148);
 }
 
 extern "C" size_t paged_attention_workspace_bytes(int32_t batch, int32_t num_heads,
@@ -1193,15 +722,10 @@ extern "C" size_t paged_attention_workspace_bytes(int32_t batch, int32_t num_hea
                                                   int32_t partition_tokens) {
   const int32_t pt = paged_attention_partition_tokens(batch, num_heads, num_kv_heads, max_seq_len,
                                                       partition_tokens);
-  if (pt < 0 || batch <= 0 || head_dim <= 0) return 0;
-  if (pt == 0) {
-    const StreamGeom gm = stream_geom(num_heads, num_kv_heads, head_dim, PKV_BF16);
-    const int sms = device_sm_count();
-    return stream_layout(batch, num_heads, num_kv_heads, head_dim, sms > 0 ? sms : 148, gm).bytes;
-  }
+  if (pt <= 0 || batch <= 0 || head_dim <= 0) return 0;
   const int64_t parts = std::max<int64_t>(1, ((int64_t)max_seq_len + pt - 1) / pt);
-  if (parts > INT32_MAX / 2) return 0;
-  return partition_workspace(batch, num_heads, head_dim, (int32_t)parts);
+  if (parts <= 1 || parts > INT32_MAX / 2) return 0;
+  return part_layout(batch, num_heads, num_kv_heads, head_dim, parts).bytes;
 }
 
 extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cache,
@@ -1225,53 +749,34 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
   if (batch > 65535) return PKV_ERR_ARG;
   const int group = num_heads / cache->num_kv_heads;
   const int q_groups = (group + 7) / 8;
-  if ((int64_t)cache->num_kv_heads * q_groups > 65535) return PKV_ERR_ARG;
-  const int sms = device_sm_count();
-  if (sms <= 0) return PKV_ERR_CUDA;
-  if (partition_tokens == 0 && !stream_geom(num_heads, cache->num_kv_heads, cache->head_dim,
-                                            cache->dtype).ok)
-    partition_tokens = kFallbackPartition;
-  const bool stream_schedule = partition_tokens == 0;
+  if ((int64_t)cache->num_kv_heads * q_groups > INT32_MAX) return PKV_ERR_ARG;
+  const int32_t pt = paged_attention_partition_tokens(batch, num_heads, cache->num_kv_heads,
+                                                      max_seq_len, partition_tokens);
+  if (pt <= 0) return PKV_ERR_ARG;
+  const int64_t parts64 = std::max<int64_t>(1, ((int64_t)max_seq_len + pt - 1) / pt);
+  if (parts64 > 65535) return PKV_ERR_ARG;  // grid.y
 
   DecodeParams p;
   std::memset(&p, 0, sizeof p);
+  p.max_parts = (int)parts64;
+  p.part_tokens = pt;
   const size_t need = paged_attention_workspace_bytes(batch, num_heads, cache->num_kv_heads,
                                                       cache->head_dim, max_seq_len,
                                                       partition_tokens);
   if (need > 0) {
     if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_WORKSPACE;
-  }
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  if (stream_schedule) {
-    const StreamGeom gm = stream_geom(num_heads, cache->num_kv_heads, cache->head_dim, cache->dtype);
-    const StreamLayout l =
-        stream_layout(batch, num_heads, cache->num_kv_heads, cache->head_dim, sms, gm);
-    p.piece_o = reinterpret_cast<float *>(ws + l.o_off);
-    p.piece_ml = reinterpret_cast<float2 *>(ws + l.ml_off);
+    const PartLayout l =
+        part_layout(batch, num_heads, cache->num_kv_heads, cache->head_dim, p.max_parts);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.part_o = reinterpret_cast<float *>(ws);
+    p.part_ml = reinterpret_cast<float2 *>(ws + l.ml_off);
     p.tickets = reinterpret_cast<unsigned long long *>(ws + l.ticket_off);
     p.epoch = next_epoch();
-    p.hg = gm.hg;
-    p.ring_slots = gm.slots;
-    p.max_parts = 1;
-    p.part_tokens = 0;
-  } else {
-    const int64_t parts64 =
-        std::max<int64_t>(1, ((int64_t)max_seq_len + partition_tokens - 1) / partition_tokens);
-    if (parts64 > INT32_MAX / 2) return PKV_ERR_ARG;
-    p.max_parts = (int)parts64;
-    p.part_tokens = partition_tokens;
-    if (need > 0) {
-      if ((size_t)p.max_parts * sizeof(float) > 48 * 1024) return PKV_ERR_ARG;
-      p.part_o = reinterpret_cast<float *>(ws);
-      p.part_ml = reinterpret_cast<float2 *>(
-          ws + ((size_t)batch * num_heads * p.max_parts * cache->head_dim * sizeof(float) + 255) /
-                   256 * 256);
-    }
   }
 
   CUtensorMap mk, mv;
-  if (!get_maps(cache, stream_schedule ? 1 : 0, &mk, &mv)) return PKV_ERR_CUDA;
+  if (!get_maps(cache, &mk, &mv)) return PKV_ERR_CUDA;
 
   p.q = static_cast<const __nv_bfloat16 *>(q);
   p.block_tables = block_tables;
@@ -1291,9 +796,8 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (fp8)
-    return cache->head_dim == 128
-               ? launch_decode<true, 128>(mk, mv, p, stream_schedule, sms, s)
-               : launch_decode<true, 64>(mk, mv, p, stream_schedule, sms, s);
-  return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, stream_schedule, sms, s)
-                                : launch_decode<false, 64>(mk, mv, p, stream_schedule, sms, s);
+    return cache->head_dim == 128 ? launch_decode<true, 128>(mk, mv, p, s)
+                                  : launch_decode<true, 64>(mk, mv, p, s);
+  return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, s)
+                                : launch_decode<false, 64>(mk, mv, p, s);
 }

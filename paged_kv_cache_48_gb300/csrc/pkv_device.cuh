@@ -98,15 +98,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar,
       : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Barrier among the first `threads` threads of the CTA (named barrier 1).
-__device__ __forceinline__ void named_barrier_sync(int threads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -141,21 +132,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar,
 }
 
 // ---------------------------------------------------------------------------
-// TMA: 4-D tiled tensor load into shared memory, completion on an mbarrier.
+// TMA: 5-D tiled tensor load into shared memory, completion on an mbarrier.
 // Coordinates are element indices, innermost first.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map,
-                                            uint64_t *bar, int x, int y, int z,
-                                            int w, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_"
-      "tx::bytes.L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x),
-      "r"(y), "r"(z), "r"(w), "l"(policy)
-      : "memory");
-}
-
 __device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map,
                                             uint64_t *bar, int c0, int c1, int c2, int c3,
                                             int c4, uint64_t policy) {
@@ -165,16 +144,6 @@ __device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map,
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
       "r"(c3), "r"(c4), "l"(policy)
-      : "memory");
-}
-
-// Prefetch a 5-D box into L2 (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_5d(const CUtensorMap *map, int c0, int c1, int c2,
-                                                int c3, int c4) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
       : "memory");
 }
 
