@@ -283,9 +283,11 @@ def run_ours(args):
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
-    # zeroing (when the step opens blocks), the write, the decode kernel (it
-    # merges split sequences itself)
-    launches_per_step = (1 if fresh.size else 0) + (1 if slots.numel() else 0) + 1
+    # zeroing (when the step opens blocks), the write, the decode kernel and
+    # the merge of split sequences (when a sequence can be split)
+    split = -(-max_len // pt) > 1
+    launches_per_step = (1 if fresh.size else 0) + (1 if slots.numel() else 0) + 1 \
+        + (1 if split else 0)
 
     def step(ev=None):
         if fresh.size:
@@ -386,7 +388,7 @@ def run_ours(args):
                      "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": peak_kind,
-                     "kernel": "paged_decode_kernel (merges split sequences in-kernel)",
+                     "kernel": "paged_decode_kernel + paged_decode_merge_kernel",
                      "launch_ms": round(attn_ms, 5)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},

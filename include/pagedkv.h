@@ -115,8 +115,8 @@ pkv_status paged_kv_zero_blocks(const pkv_cache *cache,
  *   partition_tokens  0 = automatic (see paged_attention_partition_tokens);
  *                 otherwise a multiple of 16: every sequence is split into
  *                 partitions of that many tokens, one CTA each per kv head;
- *                 the CTA that completes a sequence's last partition merges
- *                 the partitions with a log-sum-exp reduce (no extra launch).
+ *                 a second kernel merges the partitions of split sequences
+ *                 with a log-sum-exp reduce.
  *   workspace     device scratch of workspace_bytes, at least
  *                 paged_attention_workspace_bytes(...) for the same
  *                 arguments; may be NULL when that function returns 0.

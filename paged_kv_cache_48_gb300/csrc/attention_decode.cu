@@ -23,18 +23,17 @@
 // movmatrix).  fp8 E4M3 tiles are decoded to f16 in registers (exact) and
 // multiplied with an f16 copy of q; k_scale is folded into the score scale
 // and v_scale into the output.  The warps merge through shared memory; a
-// sequence split into several partitions is merged by the CTA that
-// completes its last partition (log-sum-exp over the partitions' (max, sum,
-// output) partials, counted with a per-(sequence, kv head) ticket word; no
-// CTA ever waits for another).  Every reduction has a fixed order, so
-// results are bitwise deterministic and independent of where blocks sit in
-// the pool.
+// sequence split into several partitions writes (max, sum, output)
+// partials that a second kernel merges with a log-sum-exp reduce (one warp
+// per output row, launched with programmatic dependent launch so that it is
+// resident before the decode kernel ends).  Every reduction has a fixed
+// order, so results are bitwise deterministic and independent of where
+// blocks sit in the pool.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cmath>
 #include <cstring>
-#include <atomic>
 #include <mutex>
 
 #include "pkv_device.cuh"
@@ -50,12 +49,9 @@ struct DecodeParams {
   const int32_t *seq_lens;      // [B]
   __nv_bfloat16 *out;           // [B, Hq, D]
   // split sequences: partials [B, Hq, max_parts, D] and [B, Hq, max_parts]
-  // (max in log2 units, sum); one ticket word per (sequence, kv head, query
-  // sub-group)
+  // (max in log2 units, sum)
   float *part_o;
   float2 *part_ml;
-  unsigned long long *tickets;
-  unsigned long long epoch;  // 1 .. 2^40-1, distinct per call
   int32_t batch, num_heads, num_kv_heads, group, q_groups;
   int32_t num_blocks, max_blocks, max_seq_len, max_parts, part_tokens;
   float scale_log2;  // scale * log2(e) (* k_scale for fp8)
@@ -323,7 +319,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   __shared__ int stage_ok[C::NW][C::STAGES];
   __shared__ float m_s[C::NW][8];
   __shared__ float l_s[C::NW][8];
-  __shared__ int sh_last;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -470,47 +465,59 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
       if (d == 0) p.part_ml[r * p.max_parts + part] = make_float2(M, lsum);
     }
   }
-  if (nparts == 1) return;
+}
 
-  // ---- split sequence: the CTA completing the last partition merges ------
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    unsigned long long *ticket =
-        p.tickets + ((size_t)b * p.num_kv_heads + kvh) * p.q_groups + qg;
-    unsigned long long old = atomicAdd(ticket, 0ull), want = 0ull;
-    for (int it = 0; it < (1 << 20); ++it) {
-      want = (old >> 24) == p.epoch ? old + 1ull : ((p.epoch << 24) | 1ull);
-      const unsigned long long got = atomicCAS(ticket, old, want);
-      if (got == old) break;
-      old = got;
+// Log-sum-exp merge of split sequences: one warp per (sequence, query head)
+// row, lane l owning head_dim elements l, l + 32, ...  Partition j carries
+// m_j (log2 domain), l_j and its normalised output o_j; the result is
+// sum_j 2^(m_j - M) l_j o_j / sum_j 2^(m_j - M) l_j with M = max_j m_j.  The
+// (m, l) pairs of up to 32 partitions are loaded at once (one per lane) and
+// reduced with shuffles; outputs accumulate partition by partition.
+template <int D>
+__global__ void __launch_bounds__(256) paged_decode_merge_kernel(const DecodeParams p) {
+  constexpr int KD = D / 32;
+  grid_dependency_wait();
+  allow_dependent_launch();
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= (long long)p.batch * p.num_heads) return;
+  const int b = (int)(row / p.num_heads);
+  const int cap = min(p.max_blocks * 16, p.max_seq_len);
+  const int L = clamp_len(__ldg(p.seq_lens + b), cap);
+  const int nparts = L <= p.part_tokens ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+  if (nparts <= 1) return;  // the decode kernel wrote this row
+  const float2 *ml = p.part_ml + (size_t)row * p.max_parts;
+  const float *po = p.part_o + (size_t)row * p.max_parts * D + lane;
+  float M = -INFINITY;
+  for (int j = lane; j < nparts; j += 32) M = fmaxf(M, ml[j].x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float wsum = 0.f, acc[KD];
+#pragma unroll
+  for (int k = 0; k < KD; ++k) acc[k] = 0.f;
+  for (int j0 = 0; j0 < nparts; j0 += 32) {
+    float w = 0.f;
+    if (j0 + lane < nparts) {
+      const float2 v = ml[j0 + lane];
+      w = v.x == -INFINITY ? 0.f : exp2f(v.x - M) * v.y;
     }
-    const bool last = (int)(want & 0xffffffull) == nparts;
-    if (last) atomicExch(ticket, 0ull);  // clean for the next call
-    sh_last = last ? 1 : 0;
-  }
-  __syncthreads();
-  if (!sh_last) return;
-  __threadfence();
-  // One thread per (head, head_dim element); partitions in order.
-  for (int idx = threadIdx.x; idx < heads_here * D; idx += blockDim.x) {
-    const int h = idx / D;
-    const int d = idx - h * D;
-    const size_t r = row0 + h;
-    const float2 *ml = p.part_ml + r * p.max_parts;
-    const float *po = p.part_o + r * p.max_parts * D + d;
-    float M = -INFINITY;
-    for (int j = 0; j < nparts; ++j) M = fmaxf(M, __ldcg(&ml[j].x));
-    float wsum = 0.f, acc = 0.f;
+    float t = w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    wsum += t;
+    const int cnt = min(32, nparts - j0);
 #pragma unroll 4
-    for (int j = 0; j < nparts; ++j) {
-      const float2 v = __ldcg(&ml[j]);
-      const float w = v.x == -INFINITY ? 0.f : exp2f(v.x - M) * v.y;
-      wsum += w;
-      acc += w * __ldcg(po + (size_t)j * D);
+    for (int r = 0; r < cnt; ++r) {
+      const float wr = __shfl_sync(0xffffffffu, w, r);
+      const float *pj = po + (size_t)(j0 + r) * D;
+#pragma unroll
+      for (int k = 0; k < KD; ++k) acc[k] += wr * pj[32 * k];
     }
-    p.out[r * D + d] = __float2bfloat16_rn(wsum > 0.f ? acc / wsum : 0.f);
   }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16 *orow = p.out + (size_t)row * D + lane;
+#pragma unroll
+  for (int k = 0; k < KD; ++k) orow[32 * k] = __float2bfloat16_rn(acc[k] * inv);
 }
 
 // ---------------------------------------------------------------------------
@@ -616,18 +623,17 @@ int auto_partition_tokens(int64_t batch, int64_t num_heads, int64_t num_kv_heads
 }
 
 struct PartLayout {
-  size_t ml_off, ticket_off, bytes;
+  size_t ml_off, bytes;
 };
 
 PartLayout part_layout(int64_t batch, int64_t num_heads, int64_t num_kv_heads,
                        int64_t head_dim, int64_t max_parts) {
+  (void)num_kv_heads;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t rows = (size_t)batch * num_heads * max_parts;
-  const int64_t q_groups = (num_heads / num_kv_heads + 7) / 8;
   PartLayout l;
   l.ml_off = up(rows * head_dim * sizeof(float));
-  l.ticket_off = l.ml_off + up(rows * sizeof(float2));
-  l.bytes = l.ticket_off + up((size_t)batch * num_kv_heads * q_groups * sizeof(unsigned long long));
+  l.bytes = l.ml_off + up(rows * sizeof(float2));
   return l;
 }
 
@@ -670,18 +676,13 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
   if (launch_pdl(paged_decode_kernel<FP8, D>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s, mk, mv,
                  p) != cudaSuccess)
     return PKV_ERR_CUDA;
+  if (p.max_parts > 1) {
+    const long long rows = (long long)p.batch * p.num_heads;
+    if (launch_pdl(paged_decode_merge_kernel<D>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0,
+                   s, p) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
   return PKV_OK;
-}
-
-// Distinct per call (40 bits, never 0): tags the per-item tickets so that
-// stale ticket words from earlier calls never count.
-unsigned long long next_epoch() {
-  static std::atomic<unsigned long long> counter{0};
-  unsigned long long e;
-  do {
-    e = (counter.fetch_add(1) + 1) & ((1ull << 40) - 1);
-  } while (e == 0);
-  return e;
 }
 
 }  // namespace
@@ -771,8 +772,6 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.part_o = reinterpret_cast<float *>(ws);
     p.part_ml = reinterpret_cast<float2 *>(ws + l.ml_off);
-    p.tickets = reinterpret_cast<unsigned long long *>(ws + l.ticket_off);
-    p.epoch = next_epoch();
   }
 
   CUtensorMap mk, mv;
