@@ -30,7 +30,12 @@ sys.path.insert(0, str(ROOT))
 
 METRIC = ("paged decode attention KV-read GB/s (% of GB300 HBM peak); "
           "seq-steps/sec")
-L2_NOTE = "inputs larger than L2 (0.59 GB of KV read per step, L2 126 MB)"
+L2_BYTES = 126 * 2**20
+SEQ_LENS = {"llama8b_gqa": "uniform [512, 4096]",
+            "prefix_shared": "1024 shared + uniform [32, 512]",
+            "long_context": "uniform [32768, 131072]",
+            "fp8_recycle": "uniform [1024, 8192]",
+            "tiny_mha": "{1, 17, 33, 64}"}
 FALLBACK_HBM_GBS = 6800.0
 PROFILE = ROOT / "profiles" / "paged_decode_kernel_llama8b_gqa.md"
 KERNEL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_decode.cu",
@@ -46,6 +51,11 @@ def parse_args():
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
+    ap.add_argument("--workload", default="llama8b_gqa",
+                    choices=["llama8b_gqa", "prefix_shared", "long_context",
+                             "fp8_recycle", "tiny_mha"],
+                    help="decode workload; the headline metric is quoted on "
+                         "llama8b_gqa, the others are reported for context")
     return ap.parse_args()
 
 
@@ -211,7 +221,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     from paged_kv_cache_48_gb300 import workload as wl
-    W = wl.llama8b_gqa()
+    W = wl.CONFIGS[args.workload]()
     gbs, sps, dt, threads, kvb = time_cpu_oracle(W, args.cpu_sample_seqs,
                                                  args.steps, args.warmup)
     peak, kind = measured_peak()
@@ -228,7 +238,7 @@ def run_reference(args):
         "config": {"workload": W.name, "batch": W.batch,
                    "num_heads": W.num_heads, "num_kv_heads": W.num_kv_heads,
                    "head_dim": W.head_dim, "block_size": W.block_size,
-                   "seq_lens": "uniform [512, 4096]", "kv_dtype": W.kv_dtype,
+                   "seq_lens": SEQ_LENS[W.name], "kv_dtype": W.kv_dtype,
                    "l2": "host oracle (no L2 flush)"},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s",
                          "cores": threads, "kind": "oracle",
@@ -251,7 +261,6 @@ def run_ours(args):
         torch.cuda.set_device(0)
     dev = torch.device("cuda", torch.cuda.current_device())
 
-    sys.path.insert(0, str(ROOT / "tests"))
     from paged_kv_cache_48_gb300 import (PagedKVCache, paged_attention_decode,
                                          paged_attention_partition_tokens,
                                          paged_attention_workspace_bytes,
@@ -259,14 +268,20 @@ def run_ours(args):
                                          pkv_check)
     from paged_kv_cache_48_gb300 import workload as wl
 
-    W = wl.llama8b_gqa(seed=5 + 1000 * rank if rank else 5)
+    make = wl.CONFIGS[args.workload]
+    W = make() if rank == 0 else make(seed=1000 + rank)
+    fp8 = W.kv_dtype == "fp8_e4m3"
+    elt = torch.uint8 if fp8 else torch.bfloat16
     shape = (W.num_blocks, 16, W.num_kv_heads, W.head_dim)
-    kc = torch.from_numpy(W.init_key).view(torch.bfloat16).reshape(shape).to(dev)
-    vc = torch.from_numpy(W.init_value).view(torch.bfloat16).reshape(shape).to(dev)
-    cache = PagedKVCache(kc, vc, "bf16")
+    kc = torch.from_numpy(W.init_key).view(elt).reshape(shape).to(dev)
+    vc = torch.from_numpy(W.init_value).view(elt).reshape(shape).to(dev)
+    cache = PagedKVCache(kc, vc, W.kv_dtype, W.k_scale, W.v_scale)
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16)
-    paged_kv_write(bf(W.hist_k).to(dev), bf(W.hist_v).to(dev),
-                   torch.from_numpy(W.hist_slots).to(dev), cache)
+    chunk = 1 << 18
+    for s0 in range(0, W.hist_slots.size, chunk):
+        s1 = min(W.hist_slots.size, s0 + chunk)
+        paged_kv_write(bf(W.hist_k[s0:s1]).to(dev), bf(W.hist_v[s0:s1]).to(dev),
+                       torch.from_numpy(W.hist_slots[s0:s1]).to(dev), cache)
     q = bf(W.q).to(dev)
     tables = torch.from_numpy(W.block_tables).to(dev)
     lens = torch.from_numpy(W.seq_lens).to(dev)
@@ -286,13 +301,19 @@ def run_ours(args):
     # zeroing (when the step opens blocks), the write, the decode kernel and
     # the merge of split sequences (when a sequence can be split)
     split = -(-max_len // pt) > 1
-    launches_per_step = (1 if fresh.size else 0) + (1 if slots.numel() else 0) + 1 \
-        + (1 if split else 0)
+    launches_per_step = (1 if fresh.size else 0) + (1 if slots.numel() else 0) \
+        + 1 + (1 if split else 0)
+    kv_bytes = W.kv_read_bytes()
+    # Workloads whose KV fits in twice the L2 are timed step by step with an
+    # L2 flush (a 512 MiB write) between steps, outside the timed events.
+    flush = kv_bytes < 2 * L2_BYTES
+    scrub = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev) if flush else None
 
     def step(ev=None):
         if fresh.size:
             paged_kv_zero_blocks(cache, fresh)
-        paged_kv_write(sk, sv, slots, cache)
+        if slots.numel():
+            paged_kv_write(sk, sv, slots, cache)
         if ev is not None:
             ev[0].record(stream)
         paged_attention_decode(q, cache, tables, lens, W.scale, max_len,
@@ -305,6 +326,28 @@ def run_ours(args):
         if world > 1:
             torch.distributed.barrier()
 
+    def timed_loop(n, body):
+        """Device time of n calls of body(): one event pair around the loop,
+        or per call with an L2 flush in between when flushing."""
+        if not flush:
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(n):
+                body(i)
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b)
+        pairs = [(torch.cuda.Event(enable_timing=True),
+                  torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            scrub.zero_()
+            pairs[i][0].record(stream)
+            body(i)
+            pairs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(x.elapsed_time(y) for x, y in pairs)
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -315,43 +358,33 @@ def run_ours(args):
     K = args.steps
     evs = [(torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clocks:
         barrier()
         torch.cuda.synchronize()
-        start.record(stream)
-        for i in range(K):
-            step(evs[i])
-        end.record(stream)
-        torch.cuda.synchronize()
+        elapsed_ms = timed_loop(K, lambda i: step(evs[i]))
         barrier()
-        elapsed_ms = start.elapsed_time(end)
 
         # end to end: pinned host inputs -> device, step, output -> host
         pin = lambda t: t.cpu().pin_memory()
         h_q, h_tables, h_lens = pin(q), pin(tables), pin(lens)
         h_sk, h_sv, h_slots = pin(sk), pin(sv), pin(slots)
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        pairs = [(h_q, q), (h_tables, tables), (h_lens, lens), (h_sk, sk),
-                 (h_sv, sv), (h_slots, slots)]
-        h2d = sum(h.numel() * h.element_size() for h, _ in pairs) + fresh.nbytes
+        copies = [(h_q, q), (h_tables, tables), (h_lens, lens), (h_sk, sk),
+                  (h_sv, sv), (h_slots, slots)]
+        h2d = sum(h.numel() * h.element_size() for h, _ in copies) + fresh.nbytes
         d2h = h_out.numel() * h_out.element_size()
         K2 = max(1, K // 2)
-        barrier()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(K2):
-            for h, d in pairs:
+
+        def e2e_step(i):
+            for h, d in copies:
                 d.copy_(h, non_blocking=True)
             step()
             h_out.copy_(out, non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
+
         barrier()
-        e2e_ms = e0.elapsed_time(e1)
+        torch.cuda.synchronize()
+        e2e_ms = timed_loop(K2, e2e_step)
+        barrier()
     st, detail = pkv_check()
     if st != 0:
         raise RuntimeError(f"device error {st} at {detail} in the timed region")
@@ -360,30 +393,35 @@ def run_ours(args):
     elapsed_ms, e2e_ms, attn_ms = max_over_ranks([elapsed_ms, e2e_ms, attn_ms],
                                                  device=dev)
 
-    kv_bytes = W.kv_read_bytes()
     ms_per_step = elapsed_ms / K
     value = whole_job_gbs(world, kv_bytes, ms_per_step)
     e2e_value = whole_job_gbs(world, kv_bytes, e2e_ms / K2)
     peak, peak_kind = measured_peak()
     achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
-    traffic = profiled_traffic()
+    traffic = profiled_traffic() if args.workload == "llama8b_gqa" else None
+    l2 = (f"L2 flushed between steps ({kv_bytes / 1e6:.1f} MB of KV per step)"
+          if flush else
+          f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV read per step, "
+          "L2 126 MB)")
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 KV, f16 mma, fp32 accumulate" if fp8 else "bf16",
         "data": "synthetic",
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "seq_steps_per_s": round(world * W.batch / (ms_per_step * 1e-3), 1),
         "config": {"workload": W.name, "batch": W.batch,
                    "num_heads": W.num_heads, "num_kv_heads": W.num_kv_heads,
                    "head_dim": W.head_dim, "block_size": 16,
-                   "seq_lens": "uniform [512, 4096]", "kv_dtype": "bf16",
+                   "seq_lens": SEQ_LENS[W.name], "kv_dtype": W.kv_dtype,
                    "num_blocks": W.num_blocks, "fresh_blocks": int(fresh.size),
-                   "partition_tokens": pt,
-                   "kv_read_bytes": kv_bytes,
-                   "l2": L2_NOTE},
+                   "step_tokens_written": int(slots.numel()),
+                   "partition_tokens": pt, "kv_read_bytes": kv_bytes,
+                   "unique_kv_read_bytes": W.unique_kv_read_bytes(),
+                   "l2": l2},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
