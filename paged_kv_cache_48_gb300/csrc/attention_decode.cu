@@ -488,30 +488,50 @@ __global__ void __launch_bounds__(256) paged_decode_merge_kernel(const DecodePar
   if (nparts <= 1) return;  // the decode kernel wrote this row
   const float2 *ml = p.part_ml + (size_t)row * p.max_parts;
   const float *po = p.part_o + (size_t)row * p.max_parts * D + lane;
-  float M = -INFINITY;
-  for (int j = lane; j < nparts; j += 32) M = fmaxf(M, ml[j].x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   float wsum = 0.f, acc[KD];
 #pragma unroll
   for (int k = 0; k < KD; ++k) acc[k] = 0.f;
-  for (int j0 = 0; j0 < nparts; j0 += 32) {
-    float w = 0.f;
-    if (j0 + lane < nparts) {
-      const float2 v = ml[j0 + lane];
-      w = v.x == -INFINITY ? 0.f : exp2f(v.x - M) * v.y;
-    }
+  if (nparts <= 32) {
+    // common case: lane j holds partition j's (m, l); one load round trip
+    const float2 v = lane < nparts ? ml[lane] : make_float2(-INFINITY, 0.f);
+    float M = v.x;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float w = v.x == -INFINITY ? 0.f : exp2f(v.x - M) * v.y;
     float t = w;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-    wsum += t;
-    const int cnt = min(32, nparts - j0);
+    wsum = t;
 #pragma unroll 4
-    for (int r = 0; r < cnt; ++r) {
+    for (int r = 0; r < nparts; ++r) {
       const float wr = __shfl_sync(0xffffffffu, w, r);
-      const float *pj = po + (size_t)(j0 + r) * D;
+      const float *pj = po + (size_t)r * D;
 #pragma unroll
       for (int k = 0; k < KD; ++k) acc[k] += wr * pj[32 * k];
+    }
+  } else {
+    float M = -INFINITY;
+    for (int j = lane; j < nparts; j += 32) M = fmaxf(M, ml[j].x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    for (int j0 = 0; j0 < nparts; j0 += 32) {
+      float w = 0.f;
+      if (j0 + lane < nparts) {
+        const float2 v = ml[j0 + lane];
+        w = v.x == -INFINITY ? 0.f : exp2f(v.x - M) * v.y;
+      }
+      float t = w;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+      wsum += t;
+      const int cnt = min(32, nparts - j0);
+#pragma unroll 4
+      for (int r = 0; r < cnt; ++r) {
+        const float wr = __shfl_sync(0xffffffffu, w, r);
+        const float *pj = po + (size_t)(j0 + r) * D;
+#pragma unroll
+        for (int k = 0; k < KD; ++k) acc[k] += wr * pj[32 * k];
+      }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
