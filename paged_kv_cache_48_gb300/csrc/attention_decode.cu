@@ -180,12 +180,13 @@ __device__ __forceinline__ void block_scores(uint32_t sk,
       uint32_t r0, r1, r2, r3;
       ldmatrix_x4(sk + tile_offset<C::BOX_BYTES>(k_row, 2 * kp + k_chk, box_stride), r0, r1, r2,
                   r3);
-      mma_kv<FP8>(sa, e4m3x2_to_f16x2(r0 & 0xffff), e4m3x2_to_f16x2(r1 & 0xffff),
-                  e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0],
-                  qf[2 * kp][1]);
-      mma_kv<FP8>(sb, e4m3x2_to_f16x2(r2 & 0xffff), e4m3x2_to_f16x2(r3 & 0xffff),
-                  e4m3x2_to_f16x2(r2 >> 16), e4m3x2_to_f16x2(r3 >> 16), qf[2 * kp + 1][0],
-                  qf[2 * kp + 1][1]);
+      uint32_t a0l, a0h, a1l, a1h, a2l, a2h, a3l, a3h;
+      e4m3x4_to_f16x2x2(r0, a0l, a0h);
+      e4m3x4_to_f16x2x2(r1, a1l, a1h);
+      e4m3x4_to_f16x2x2(r2, a2l, a2h);
+      e4m3x4_to_f16x2x2(r3, a3l, a3h);
+      mma_kv<FP8>(sa, a0l, a1l, a0h, a1h, qf[2 * kp][0], qf[2 * kp][1]);
+      mma_kv<FP8>(sb, a2l, a3l, a2h, a3h, qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
     }
   }
 #pragma unroll
@@ -194,7 +195,7 @@ __device__ __forceinline__ void block_scores(uint32_t sk,
 
 // Online softmax update with one block's scores and P.V accumulation; sv is
 // the shared address of the V tile, nv the block's valid tokens (0..16).
-template <bool FP8, int D>
+template <bool FP8, int D, bool FULL>
 __device__ __forceinline__ void block_update(uint32_t sv, int nv, const float (&sc)[4],
                                              float scale_log2, WarpState<FP8, D> &st, int lane,
                                              uint32_t box_stride = 16 * Cfg<FP8, D>::BOX_BYTES) {
@@ -207,7 +208,7 @@ __device__ __forceinline__ void block_update(uint32_t sv, int nv, const float (&
 
   // -- online softmax per query-head column -------------------------------
   // sc[0], sc[1]: token g, heads 2c, 2c+1; sc[2], sc[3]: token g + 8.
-  const bool v_lo = g < nv, v_hi = g + 8 < nv;
+  const bool v_lo = FULL || g < nv, v_hi = FULL || g + 8 < nv;
   const float s0 = v_lo ? sc[0] * scale_log2 : -INFINITY;
   const float s1 = v_lo ? sc[1] * scale_log2 : -INFINITY;
   const float s2 = v_hi ? sc[2] * scale_log2 : -INFINITY;
@@ -248,10 +249,11 @@ __device__ __forceinline__ void block_update(uint32_t sv, int nv, const float (&
   // A fragment (tokens 2c, 2c+1 in regs 0/1, 8+2c, 9+2c in regs 2/3), so
   // that p = 0 never meets a NaN inside the mma.
   uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-  if (nv < 16) {
+  if (!FULL) {
     vm_lo = (2 * c < nv ? 0x0000ffffu : 0u) | (2 * c + 1 < nv ? 0xffff0000u : 0u);
     vm_hi = (2 * c + 8 < nv ? 0x0000ffffu : 0u) | (2 * c + 9 < nv ? 0xffff0000u : 0u);
   }
+  auto mask = [&](uint32_t x, uint32_t m) { return FULL ? x : (x & m); };
 
   // -- O^T[head_dim x 8] += V^T . P^T -------------------------------------
   if (!FP8) {
@@ -260,7 +262,8 @@ __device__ __forceinline__ void block_update(uint32_t sv, int nv, const float (&
       uint32_t a0, a1, a2, a3;
       ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * mt + v_chk, box_stride), a0,
                         a1, a2, a3);
-      mma_kv<FP8>(st.o[mt], a0 & vm_lo, a1 & vm_lo, a2 & vm_hi, a3 & vm_hi, pb0, pb1);
+      mma_kv<FP8>(st.o[mt], mask(a0, vm_lo), mask(a1, vm_lo), mask(a2, vm_hi), mask(a3, vm_hi),
+                  pb0, pb1);
     }
   } else {
 #pragma unroll
@@ -272,12 +275,15 @@ __device__ __forceinline__ void block_update(uint32_t sv, int nv, const float (&
       // holds [t0 dA, t0 dB, t1 dA, t1 dB]; regroup per head_dim row.
       const uint32_t x0 = prmt(r0, 0u, 0x3120u), x1 = prmt(r1, 0u, 0x3120u);
       const uint32_t x2 = prmt(r2, 0u, 0x3120u), x3 = prmt(r3, 0u, 0x3120u);
-      mma_kv<FP8>(st.o[2 * qq], e4m3x2_to_f16x2(x0 & 0xffff) & vm_lo,
-                  e4m3x2_to_f16x2(x0 >> 16) & vm_lo, e4m3x2_to_f16x2(x1 & 0xffff) & vm_hi,
-                  e4m3x2_to_f16x2(x1 >> 16) & vm_hi, pb0, pb1);
-      mma_kv<FP8>(st.o[2 * qq + 1], e4m3x2_to_f16x2(x2 & 0xffff) & vm_lo,
-                  e4m3x2_to_f16x2(x2 >> 16) & vm_lo, e4m3x2_to_f16x2(x3 & 0xffff) & vm_hi,
-                  e4m3x2_to_f16x2(x3 >> 16) & vm_hi, pb0, pb1);
+      uint32_t c0l, c0h, c1l, c1h, c2l, c2h, c3l, c3h;
+      e4m3x4_to_f16x2x2(x0, c0l, c0h);
+      e4m3x4_to_f16x2x2(x1, c1l, c1h);
+      e4m3x4_to_f16x2x2(x2, c2l, c2h);
+      e4m3x4_to_f16x2x2(x3, c3l, c3h);
+      mma_kv<FP8>(st.o[2 * qq], mask(c0l, vm_lo), mask(c0h, vm_lo), mask(c1l, vm_hi),
+                  mask(c1h, vm_hi), pb0, pb1);
+      mma_kv<FP8>(st.o[2 * qq + 1], mask(c2l, vm_lo), mask(c2h, vm_lo), mask(c3l, vm_hi),
+                  mask(c3h, vm_hi), pb0, pb1);
     }
   }
 }
@@ -290,7 +296,10 @@ __device__ __forceinline__ void attend_block(uint32_t sk, uint32_t sv, int nv,
                                              int lane) {
   float sc[4];
   block_scores<FP8, D>(sk, qf, sc, lane);
-  block_update<FP8, D>(sv, nv, sc, scale_log2, st, lane);
+  if (nv == 16)
+    block_update<FP8, D, true>(sv, nv, sc, scale_log2, st, lane);
+  else
+    block_update<FP8, D, false>(sv, nv, sc, scale_log2, st, lane);
 }
 
 // Lane 0 issues the TMA loads of one block-head (K and V tiles) into a

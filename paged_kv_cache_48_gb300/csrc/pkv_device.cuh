@@ -223,8 +223,22 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0,
 // Two E4M3 bytes (low byte = first element) -> f16x2 (low half = first
 // element).  Every E4M3 value, NaN included, is exactly representable.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+  uint32_t d;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(two));
+  return d;
+}
+
+// Four E4M3 bytes of a register -> two f16x2 (bytes 0,1 -> lo; 2,3 -> hi),
+// reading the register's 16-bit halves directly.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t &lo, uint32_t &hi) {
+  asm("{\n"
+      ".reg .b16 a, b;\n"
+      "mov.b32 {a, b}, %2;\n"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n"
+      "}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
