@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
+    ap.add_argument("--graph", action="store_true",
+                    help="replay the decode step as one captured CUDA graph")
     ap.add_argument("--workload", default="llama8b_gqa",
                     choices=["llama8b_gqa", "prefix_shared", "long_context",
                              "fp8_recycle", "tiny_mha"],
@@ -250,6 +252,15 @@ def run_reference(args):
     return 0
 
 
+def _replay(graph, ev, stream):
+    """One graph replay; with `ev`, the pair brackets the whole step."""
+    if ev is not None:
+        ev[0].record(stream)
+    graph.replay()
+    if ev is not None:
+        ev[1].record(stream)
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_info()
@@ -355,13 +366,30 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device error {st} at {detail} during warm-up")
 
+    run_step = step
+    if args.graph:
+        # The whole step as one CUDA graph (zeroing ids ride in the captured
+        # launch parameters), replayed once per step.
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                step()
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        run_step = lambda ev=None: _replay(graph, ev, stream)
+        for _ in range(args.warmup):
+            run_step()
+        torch.cuda.synchronize()
+
     K = args.steps
     evs = [(torch.cuda.Event(enable_timing=True),
             torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     with ClockSampler(dev.index) as clocks:
         barrier()
         torch.cuda.synchronize()
-        elapsed_ms = timed_loop(K, lambda i: step(evs[i]))
+        elapsed_ms = timed_loop(K, lambda i: run_step(evs[i]))
         barrier()
 
         # end to end: pinned host inputs -> device, step, output -> host
@@ -378,7 +406,7 @@ def run_ours(args):
         def e2e_step(i):
             for h, d in copies:
                 d.copy_(h, non_blocking=True)
-            step()
+            run_step()
             h_out.copy_(out, non_blocking=True)
 
         barrier()
@@ -389,6 +417,8 @@ def run_ours(args):
     if st != 0:
         raise RuntimeError(f"device error {st} at {detail} in the timed region")
 
+    # per-step event pairs: the decode call alone, or the whole replayed
+    # step with --graph
     attn_ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
     elapsed_ms, e2e_ms, attn_ms = max_over_ranks([elapsed_ms, e2e_ms, attn_ms],
                                                  device=dev)
@@ -420,6 +450,7 @@ def run_ours(args):
                    "num_blocks": W.num_blocks, "fresh_blocks": int(fresh.size),
                    "step_tokens_written": int(slots.numel()),
                    "partition_tokens": pt, "kv_read_bytes": kv_bytes,
+                   "cuda_graph": bool(args.graph),
                    "unique_kv_read_bytes": W.unique_kv_read_bytes(),
                    "l2": l2},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
