@@ -81,6 +81,16 @@ class Oracle:
             ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, ctypes.c_double,
             _P, _P, ctypes.c_long, ctypes.c_int]
         lib.oracle_attention_decode.restype = ctypes.c_long
+        for name in ("oracle_copy_blocks",):
+            fn = getattr(lib, name)
+            fn.argtypes = [_P, _P, ctypes.c_size_t, ctypes.c_int, _P, _P,
+                           ctypes.c_long]
+            fn.restype = ctypes.c_long
+        for name in ("oracle_swap_out", "oracle_swap_in"):
+            fn = getattr(lib, name)
+            fn.argtypes = [_P, _P, ctypes.c_size_t, ctypes.c_int, _P,
+                           ctypes.c_long, _P, _P]
+            fn.restype = ctypes.c_long
         lib.oracle_num_threads.argtypes = [ctypes.c_int]
         lib.oracle_num_threads.restype = ctypes.c_int
         self.lib = lib
@@ -133,6 +143,40 @@ class Oracle:
         return self.lib.oracle_zero_blocks(
             key_cache.ctypes.data, value_cache.ctypes.data, block_bytes,
             num_blocks, ids.ctypes.data, ids.size)
+
+    def copy_blocks(self, key_cache, value_cache, block_bytes, src, dst):
+        """In-place copy of blocks src[i] -> dst[i] (in order)."""
+        _check_c(key_cache, np.uint8)
+        _check_c(value_cache, np.uint8)
+        s = np.ascontiguousarray(src, dtype=np.int32)
+        d = np.ascontiguousarray(dst, dtype=np.int32)
+        assert s.shape == d.shape
+        return self.lib.oracle_copy_blocks(
+            key_cache.ctypes.data, value_cache.ctypes.data, block_bytes,
+            key_cache.size // block_bytes, s.ctypes.data, d.ctypes.data,
+            s.size)
+
+    def swap_out(self, key_cache, value_cache, block_bytes, ids):
+        """Returns (out_k, out_v, errors): the blocks packed in id order."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        out_k = np.zeros(ids.size * block_bytes, np.uint8)
+        out_v = np.zeros(ids.size * block_bytes, np.uint8)
+        err = self.lib.oracle_swap_out(
+            key_cache.ctypes.data, value_cache.ctypes.data, block_bytes,
+            key_cache.size // block_bytes, ids.ctypes.data, ids.size,
+            out_k.ctypes.data, out_v.ctypes.data)
+        return out_k, out_v, err
+
+    def swap_in(self, key_cache, value_cache, block_bytes, ids, in_k, in_v):
+        _check_c(key_cache, np.uint8)
+        _check_c(value_cache, np.uint8)
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        in_k = np.ascontiguousarray(in_k, dtype=np.uint8)
+        in_v = np.ascontiguousarray(in_v, dtype=np.uint8)
+        return self.lib.oracle_swap_in(
+            key_cache.ctypes.data, value_cache.ctypes.data, block_bytes,
+            key_cache.size // block_bytes, ids.ctypes.data, ids.size,
+            in_k.ctypes.data, in_v.ctypes.data)
 
     def attention_decode(self, q: np.ndarray, key_cache: np.ndarray,
                          value_cache: np.ndarray, dtype: int,

@@ -214,6 +214,75 @@ long oracle_zero_blocks(uint8_t *key_cache, uint8_t *value_cache,
 }
 
 /* ------------------------------------------------------------------ */
+/* Block copy (copy-on-write) and swap to / from host memory           */
+/* ------------------------------------------------------------------ */
+
+/* Copy-on-write of shared blocks (vLLM internals, naphjohn.github.io,
+ * §1.1: shared prefixes are copied when written): for i = 0 .. n-1 in
+ * order, every byte of block dst[i] of both caches becomes the byte of
+ * block src[i].  Pairs with an id outside [0, num_blocks) are skipped and
+ * counted. */
+long oracle_copy_blocks(uint8_t *key_cache, uint8_t *value_cache,
+                        size_t block_bytes, int num_blocks,
+                        const int32_t *src, const int32_t *dst, long n)
+{
+    long i, errors = 0;
+    for (i = 0; i < n; ++i) {
+        if (src[i] < 0 || src[i] >= num_blocks || dst[i] < 0 ||
+            dst[i] >= num_blocks) {
+            ++errors;
+            continue;
+        }
+        memmove(key_cache + (size_t)dst[i] * block_bytes,
+                key_cache + (size_t)src[i] * block_bytes, block_bytes);
+        memmove(value_cache + (size_t)dst[i] * block_bytes,
+                value_cache + (size_t)src[i] * block_bytes, block_bytes);
+    }
+    return errors;
+}
+
+/* Swap out for preemption (vLLM concept page, compassingai.com,
+ * "15 分钟专家深入" item 1: KV blocks of preempted sequences move to CPU
+ * memory): out_k[i] / out_v[i] (block_bytes each, packed) receive block
+ * ids[i] of each cache.  Out-of-range ids leave their slot untouched. */
+long oracle_swap_out(const uint8_t *key_cache, const uint8_t *value_cache,
+                     size_t block_bytes, int num_blocks, const int32_t *ids,
+                     long n, uint8_t *out_k, uint8_t *out_v)
+{
+    long i, errors = 0;
+    for (i = 0; i < n; ++i) {
+        if (ids[i] < 0 || ids[i] >= num_blocks) {
+            ++errors;
+            continue;
+        }
+        memcpy(out_k + (size_t)i * block_bytes,
+               key_cache + (size_t)ids[i] * block_bytes, block_bytes);
+        memcpy(out_v + (size_t)i * block_bytes,
+               value_cache + (size_t)ids[i] * block_bytes, block_bytes);
+    }
+    return errors;
+}
+
+/* Swap in: block ids[i] of each cache receives in_k[i] / in_v[i]. */
+long oracle_swap_in(uint8_t *key_cache, uint8_t *value_cache,
+                    size_t block_bytes, int num_blocks, const int32_t *ids,
+                    long n, const uint8_t *in_k, const uint8_t *in_v)
+{
+    long i, errors = 0;
+    for (i = 0; i < n; ++i) {
+        if (ids[i] < 0 || ids[i] >= num_blocks) {
+            ++errors;
+            continue;
+        }
+        memcpy(key_cache + (size_t)ids[i] * block_bytes,
+               in_k + (size_t)i * block_bytes, block_bytes);
+        memcpy(value_cache + (size_t)ids[i] * block_bytes,
+               in_v + (size_t)i * block_bytes, block_bytes);
+    }
+    return errors;
+}
+
+/* ------------------------------------------------------------------ */
 /* Decode attention                                                    */
 /* ------------------------------------------------------------------ */
 

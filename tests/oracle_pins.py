@@ -253,6 +253,46 @@ def pin_zero_blocks_is_slice_assignment(oracle):
     assert np.array_equal(kc, ref_k) and np.array_equal(vc, ref_v)
 
 
+def pin_copy_blocks_is_ordered_block_assignment(oracle):
+    rng = np.random.default_rng(28)
+    NB, bb = 10, 64
+    kc = rng.integers(0, 256, NB * bb, dtype=np.uint8)
+    vc = rng.integers(0, 256, NB * bb, dtype=np.uint8)
+    src = np.array([3, 7, 3, 0], np.int32)
+    dst = np.array([5, 1, 9, 7], np.int32)  # block 7 is read, then written
+    rk = kc.reshape(NB, bb).copy()
+    rv = vc.reshape(NB, bb).copy()
+    for a, b in zip(src, dst):  # numpy row assignment, in order
+        rk[b] = rk[a]
+        rv[b] = rv[a]
+    assert oracle.copy_blocks(kc, vc, bb, src, dst) == 0
+    assert np.array_equal(kc.reshape(NB, bb), rk)
+    assert np.array_equal(vc.reshape(NB, bb), rv)
+    assert oracle.copy_blocks(kc, vc, bb, np.array([NB], np.int32),
+                              np.array([0], np.int32)) == 1
+    assert np.array_equal(kc.reshape(NB, bb), rk)
+
+
+def pin_swap_round_trip_is_gather_then_scatter(oracle):
+    rng = np.random.default_rng(29)
+    NB, bb = 12, 32
+    kc = rng.integers(0, 256, NB * bb, dtype=np.uint8)
+    vc = rng.integers(0, 256, NB * bb, dtype=np.uint8)
+    ids = np.array([4, 11, 0, 6], np.int32)
+    ok, ov, err = oracle.swap_out(kc, vc, bb, ids)
+    assert err == 0
+    assert np.array_equal(ok.reshape(-1, bb), kc.reshape(NB, bb)[ids])
+    assert np.array_equal(ov.reshape(-1, bb), vc.reshape(NB, bb)[ids])
+    # swap the same data back in elsewhere: equals copying the blocks
+    k2, v2 = kc.copy(), vc.copy()
+    dst = np.array([1, 2, 3, 5], np.int32)
+    assert oracle.swap_in(k2, v2, bb, dst, ok, ov) == 0
+    k3, v3 = kc.copy(), vc.copy()
+    assert oracle.copy_blocks(k3, v3, bb, ids, dst) == 0
+    assert np.array_equal(k2, k3) and np.array_equal(v2, v3)
+    assert oracle.swap_out(kc, vc, bb, np.array([-1], np.int32))[2] == 1
+
+
 # ---------------------------------------------------------------------------
 # attention: closed forms
 # ---------------------------------------------------------------------------

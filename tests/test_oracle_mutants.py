@@ -62,6 +62,14 @@ MUTANTS = [
     ("zero_accepts_negative", "if (id < 0 || id >= num_blocks) {",
      "if (id >= num_blocks) {"),
     ("empty_sequence_not_zero", "out_row[i] = 0.0;", "out_row[i] = 1.0;"),
+    ("copy_value_from_key",
+     "                value_cache + (size_t)src[i] * block_bytes, block_bytes);",
+     "                key_cache + (size_t)src[i] * block_bytes, block_bytes);"),
+    ("swap_out_wrong_slot", "memcpy(out_k + (size_t)i * block_bytes,",
+     "memcpy(out_k + (size_t)(n - 1 - i) * block_bytes,"),
+    ("swap_in_skips_value",
+     "        memcpy(value_cache + (size_t)ids[i] * block_bytes,\n               in_v + (size_t)i * block_bytes, block_bytes);",
+     "        (void)in_v;"),
 ]
 
 _RUNNER = textwrap.dedent("""
