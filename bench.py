@@ -51,6 +51,11 @@ def parse_args():
     ap.add_argument("--partition-tokens", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
+    ap.add_argument("--kernel", default="decode",
+                    choices=["decode", "zero_blocks", "copy_blocks", "swap"],
+                    help="decode: the decode step (headline); the others time "
+                         "the block-movement entry points on the workload's "
+                         "pool")
     ap.add_argument("--graph", action="store_true",
                     help="replay the decode step as one captured CUDA graph")
     ap.add_argument("--workload", default="llama8b_gqa",
@@ -480,10 +485,118 @@ def run_ours(args):
     return 0
 
 
+def run_blocks(args):
+    """Zeroing, block copy and swap on the workload's cache geometry.
+
+    zero_blocks: 920 MiB and 53.7 MB of blocks (the sizes the vLLM v0.17.1
+    notes time for prefill and decode steps), write bandwidth;
+    copy_blocks: 4096 disjoint pairs, read + write bandwidth (the measured
+    copy peak counts the same way);
+    swap: 4096 blocks out to pinned host memory and back in, against a
+    plain pinned-memory copy of the same bytes."""
+    import torch
+    from paged_kv_cache_48_gb300 import (PagedKVCache, paged_kv_copy_blocks,
+                                         paged_kv_swap_in, paged_kv_swap_out,
+                                         paged_kv_zero_blocks, pkv_check)
+    from paged_kv_cache_48_gb300 import workload as wl
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    W = wl.CONFIGS[args.workload]()
+    elt = torch.uint8 if W.kv_dtype == "fp8_e4m3" else torch.bfloat16
+    bb = W.block_bytes                      # per cache
+    NB = max(W.num_blocks, 2 * 14720, 8192)
+    shape = (NB, 16, W.num_kv_heads, W.head_dim)
+    cache = PagedKVCache(torch.zeros(shape, dtype=elt, device=dev),
+                         torch.zeros(shape, dtype=elt, device=dev),
+                         W.kv_dtype, W.k_scale, W.v_scale)
+    rng = np.random.default_rng(7)
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = measured_peak()
+
+    def time_ms(fn, reps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    reps = max(10, min(args.steps, 200))
+    lines = []
+    if args.kernel == "zero_blocks":
+        for label, total in (("920 MiB (prefill step)", 920 * 2**20),
+                             ("53.7 MB (decode step)", int(30 * 1.79 * 2**20))):
+            n = max(1, total // (2 * bb))
+            ids = rng.permutation(NB)[:n].astype(np.int32)
+            ms = time_ms(lambda: paged_kv_zero_blocks(cache, ids), reps)
+            gbs = 2 * n * bb / (ms * 1e-3) / 1e9
+            lines.append({"metric": f"zero fresh blocks: {label}",
+                          "value": round(ms * 1e3, 2), "unit": "us",
+                          "higher_is_better": False, "blocks": int(n),
+                          "bytes": 2 * n * bb, "GB_per_s": round(gbs, 1),
+                          "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                                       "peak": peak, "unit": "GB/s",
+                                       "frac": round(gbs / peak, 4),
+                                       "peak_kind": peak_kind}})
+    elif args.kernel == "copy_blocks":
+        perm = rng.permutation(NB).astype(np.int32)
+        src, dst = perm[:4096], perm[4096:8192]
+        ms = time_ms(lambda: paged_kv_copy_blocks(cache, src, dst), reps)
+        moved = 2 * 2 * 4096 * bb          # K and V, read and written
+        gbs = moved / (ms * 1e-3) / 1e9
+        lines.append({"metric": "copy 4096 blocks (copy-on-write)",
+                      "value": round(gbs, 1), "unit": "GB/s (read+write)",
+                      "higher_is_better": True, "ms": round(ms, 4),
+                      "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                                   "peak": peak, "unit": "GB/s",
+                                   "frac": round(gbs / peak, 4),
+                                   "peak_kind": peak_kind}})
+    else:
+        n = 4096
+        ids = rng.permutation(NB)[:n].astype(np.int32)
+        hk = torch.empty(n * bb, dtype=torch.uint8).pin_memory()
+        hv = torch.empty(n * bb, dtype=torch.uint8).pin_memory()
+        ms_out = time_ms(lambda: paged_kv_swap_out(cache, ids, hk, hv), reps)
+        ms_in = time_ms(lambda: paged_kv_swap_in(cache, ids, hk, hv), reps)
+        dbuf = torch.empty(2 * n * bb, dtype=torch.uint8, device=dev)
+        hbuf = torch.empty(2 * n * bb, dtype=torch.uint8).pin_memory()
+        ms_d2h = time_ms(lambda: hbuf.copy_(dbuf, non_blocking=True), reps)
+        ms_h2d = time_ms(lambda: dbuf.copy_(hbuf, non_blocking=True), reps)
+        nbytes = 2 * n * bb
+        for label, ms, ref in (("swap out 4096 blocks to pinned host memory", ms_out, ms_d2h),
+                               ("swap in 4096 blocks from pinned host memory", ms_in, ms_h2d)):
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            ref_gbs = nbytes / (ref * 1e-3) / 1e9
+            lines.append({"metric": label, "value": round(gbs, 1),
+                          "unit": "GB/s", "higher_is_better": True,
+                          "ms": round(ms, 4),
+                          "roofline": {"bound": "host link",
+                                       "achieved": round(gbs, 1),
+                                       "peak": round(ref_gbs, 1), "unit": "GB/s",
+                                       "frac": round(gbs / ref_gbs, 4),
+                                       "peak_kind": "pinned cudaMemcpy of the same bytes, measured here"}})
+    st, detail = pkv_check()
+    if st != 0:
+        raise RuntimeError(f"device error {st} at {detail}")
+    for line in lines:
+        line.update({"kernel": args.kernel, "n_gpus": 1, "data": "synthetic",
+                     "config": {"workload": W.name, "block_bytes_per_cache": bb,
+                                "kv_dtype": W.kv_dtype}})
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.kernel != "decode":
+        return run_blocks(args)
     return run_ours(args)
 
 

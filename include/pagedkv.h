@@ -98,6 +98,40 @@ pkv_status paged_kv_zero_blocks(const pkv_cache *cache,
                                 const int32_t *block_ids, int64_t n,
                                 int ids_on_host, void *stream);
 
+/* Copy whole blocks: for each i, every byte of key_cache[dst_ids[i]] and
+ * value_cache[dst_ids[i]] becomes the byte of block src_ids[i].  Source:
+ * vLLM internals (naphjohn.github.io), §1.1 (copy-on-write of a shared
+ * prefix block that one sequence must modify).
+ *   src_ids, dst_ids  int32 [n]; on the host when ids_on_host != 0 (copied
+ *                 into the launch parameters), otherwise on the device.
+ * Pairs are applied concurrently: no block may appear twice among the
+ * destinations, nor as both a source and a destination.  Out-of-range ids
+ * are device range errors (the pair is skipped). */
+pkv_status paged_kv_copy_blocks(const pkv_cache *cache, const int32_t *src_ids,
+                                const int32_t *dst_ids, int64_t n,
+                                int ids_on_host, void *stream);
+
+/* Swap blocks out to host memory: host_k[i] / host_v[i] (block_bytes =
+ * 16 * num_kv_heads * head_dim * elt each, packed in list order) receive
+ * block block_ids[i] of each cache.  Source: vLLM concept page
+ * (compassingai.com), "15 分钟专家深入" item 1 (preempted sequences' KV
+ * swapped out to CPU memory, swapped back in later).
+ *   host_k, host_v  PINNED host memory (cudaHostAlloc / cudaHostRegister),
+ *                 n * block_bytes each; the GPU writes them directly.
+ *                 Pageable memory is rejected with PKV_ERR_ARG.
+ * Ids as for paged_kv_copy_blocks; out-of-range ids are device range
+ * errors (their slots are left untouched).  The host buffers are complete
+ * once the stream reaches this point (e.g. after pkv_check). */
+pkv_status paged_kv_swap_out(const pkv_cache *cache, const int32_t *block_ids,
+                             int64_t n, int ids_on_host, void *host_k,
+                             void *host_v, void *stream);
+
+/* Swap blocks in from pinned host memory: block block_ids[i] of each cache
+ * receives host_k[i] / host_v[i].  Same conventions as paged_kv_swap_out. */
+pkv_status paged_kv_swap_in(const pkv_cache *cache, const int32_t *block_ids,
+                            int64_t n, int ids_on_host, const void *host_k,
+                            const void *host_v, void *stream);
+
 /* Decode attention over a paged cache, one query token per sequence.
  * Source: vLLM concept page (compassingai.com), "技术原理" pseudocode
  * (gather by page table, Q K^T / sqrt(d), softmax, times V) and its note on

@@ -43,11 +43,12 @@ using namespace pkv;
 extern "C" pkv_status pkv_check(void *stream, int64_t *detail) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (detail) *detail = -1;
-  cudaError_t e1 = cudaSuccess, e2 = cudaSuccess;
+  cudaError_t e1 = cudaSuccess, e2 = cudaSuccess, e3 = cudaSuccess;
   const unsigned long long w1 = read_and_clear_error_write_zero(s, &e1);
   const unsigned long long w2 = read_and_clear_error_attention(s, &e2);
-  if (e1 != cudaSuccess || e2 != cudaSuccess) return PKV_ERR_CUDA;
-  const unsigned long long w = w1 ? w1 : w2;
+  const unsigned long long w3 = read_and_clear_error_blocks(s, &e3);
+  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return PKV_ERR_CUDA;
+  const unsigned long long w = w1 ? w1 : (w2 ? w2 : w3);
   if (!w) return PKV_OK;
   if (detail) *detail = (int64_t)(w & 0x00FFFFFFFFFFFFFFull) - 1;
   return static_cast<pkv_status>(w >> 56);

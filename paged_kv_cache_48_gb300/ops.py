@@ -95,6 +95,12 @@ class PagedKVCache:
     def head_dim(self) -> int:
         return self.key_cache.shape[3]
 
+    @property
+    def block_bytes(self) -> int:
+        """Bytes of one block of one cache."""
+        return BLOCK_SIZE * self.num_kv_heads * self.head_dim * \
+            self.key_cache.element_size()
+
     def c_struct(self) -> PkvCache:
         return self._struct
 
@@ -137,6 +143,72 @@ def paged_kv_zero_blocks(cache: PagedKVCache, block_ids,
         _stream_handle(stream, dev))
     del keep
     _native.check("paged_kv_zero_blocks", st)
+
+
+def _block_ids(ids, dev):
+    """(pointer, count, ids_on_host, keep-alive) for a block-id list."""
+    if isinstance(ids, torch.Tensor) and ids.is_cuda:
+        _require(ids, "block ids", torch.int32, dev, 1)
+        return ids.data_ptr(), ids.numel(), 0, ids
+    if isinstance(ids, torch.Tensor):
+        ids = ids.numpy()
+    keep = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    return keep.ctypes.data, keep.size, 1, keep
+
+
+def paged_kv_copy_blocks(cache: PagedKVCache, src_ids, dst_ids,
+                         stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy blocks src_ids[i] -> dst_ids[i] in both caches (copy-on-write
+    of shared blocks).  Ids: host arrays/lists or CUDA int32 tensors."""
+    dev = cache.device
+    sp, sn, s_host, s_keep = _block_ids(src_ids, dev)
+    dp, dn, d_host, d_keep = _block_ids(dst_ids, dev)
+    if sn != dn or s_host != d_host:
+        raise ValueError("src_ids and dst_ids must match in length and place")
+    st = _native.lib().paged_kv_copy_blocks(
+        ctypes.byref(cache.c_struct()), sp, dp, sn, s_host,
+        _stream_handle(stream, dev))
+    del s_keep, d_keep
+    _native.check("paged_kv_copy_blocks", st)
+
+
+def _check_pinned(t: torch.Tensor, name: str, nbytes: int):
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
+        raise ValueError(f"{name} must be a pinned CPU tensor")
+    if not t.is_contiguous() or t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} must be contiguous with >= {nbytes} bytes")
+
+
+def paged_kv_swap_out(cache: PagedKVCache, block_ids, host_k: torch.Tensor,
+                      host_v: torch.Tensor,
+                      stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy blocks to pinned host tensors (packed in id order)."""
+    dev = cache.device
+    p, n, on_host, keep = _block_ids(block_ids, dev)
+    nbytes = n * cache.block_bytes
+    _check_pinned(host_k, "host_k", nbytes)
+    _check_pinned(host_v, "host_v", nbytes)
+    st = _native.lib().paged_kv_swap_out(
+        ctypes.byref(cache.c_struct()), p, n, on_host, host_k.data_ptr(),
+        host_v.data_ptr(), _stream_handle(stream, dev))
+    del keep
+    _native.check("paged_kv_swap_out", st)
+
+
+def paged_kv_swap_in(cache: PagedKVCache, block_ids, host_k: torch.Tensor,
+                     host_v: torch.Tensor,
+                     stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy packed blocks from pinned host tensors into the cache."""
+    dev = cache.device
+    p, n, on_host, keep = _block_ids(block_ids, dev)
+    nbytes = n * cache.block_bytes
+    _check_pinned(host_k, "host_k", nbytes)
+    _check_pinned(host_v, "host_v", nbytes)
+    st = _native.lib().paged_kv_swap_in(
+        ctypes.byref(cache.c_struct()), p, n, on_host, host_k.data_ptr(),
+        host_v.data_ptr(), _stream_handle(stream, dev))
+    del keep
+    _native.check("paged_kv_swap_in", st)
 
 
 def paged_attention_workspace_bytes(batch: int, num_heads: int,
