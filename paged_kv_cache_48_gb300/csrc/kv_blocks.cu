@@ -111,15 +111,18 @@ static int64_t block_vecs(const pkv_cache *c) {
          (c->dtype == PKV_FP8_E4M3 ? 1 : 2) / 16;
 }
 
-// Device view of a pinned host buffer; nullptr when `p` is not pinned
-// (pageable memory must never reach a kernel).
+// Device view of a pinned (page-locked, registered) host buffer; nullptr
+// for anything else.  Pageable memory is refused on every platform, also
+// where the GPU could reach it through the host page tables.
 static void *device_view(const void *p) {
-  void *d = nullptr;
-  if (!p || cudaHostGetDevicePointer(&d, const_cast<void *>(p), 0) != cudaSuccess) {
-    cudaGetLastError();  // clear the sticky-free error of the failed query
+  if (!p) return nullptr;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
     return nullptr;
   }
-  return d;
+  if (attr.type != cudaMemoryTypeHost || !attr.devicePointer) return nullptr;
+  return attr.devicePointer;
 }
 
 unsigned long long read_and_clear_error_blocks(cudaStream_t s, cudaError_t *err) {
