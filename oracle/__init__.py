@@ -91,6 +91,10 @@ class Oracle:
             fn.argtypes = [_P, _P, ctypes.c_size_t, ctypes.c_int, _P,
                            ctypes.c_long, _P, _P]
             fn.restype = ctypes.c_long
+        lib.oracle_prepare_inputs.argtypes = [
+            _P, _P, ctypes.c_int, _P, ctypes.c_int, _P, _P, ctypes.c_int,
+            ctypes.c_int, ctypes.c_long, _P, _P, _P, _P, _P, _P]
+        lib.oracle_prepare_inputs.restype = ctypes.c_long
         lib.oracle_num_threads.argtypes = [ctypes.c_int]
         lib.oracle_num_threads.restype = ctypes.c_int
         self.lib = lib
@@ -177,6 +181,33 @@ class Oracle:
             key_cache.ctypes.data, value_cache.ctypes.data, block_bytes,
             key_cache.size // block_bytes, ids.ctypes.data, ids.size,
             in_k.ctypes.data, in_v.ctypes.data)
+
+    def prepare_inputs(self, idx_mapping, num_scheduled, state_block_table,
+                       state_num_computed, state_token_ids, total_tokens):
+        """Step inputs gathered from the request state table.  Returns a
+        dict of arrays and the error count."""
+        idx = np.ascontiguousarray(idx_mapping, dtype=np.int32)
+        ns = np.ascontiguousarray(num_scheduled, dtype=np.int32)
+        sbt = np.ascontiguousarray(state_block_table, dtype=np.int32)
+        snc = np.ascontiguousarray(state_num_computed, dtype=np.int32)
+        tok = np.ascontiguousarray(state_token_ids, dtype=np.int32)
+        B = idx.size
+        R, MB = sbt.shape
+        ML = tok.shape[1]
+        T = int(total_tokens)
+        out = {"block_tables": np.full((B, MB), -7, np.int32),
+               "seq_lens": np.full(B, -7, np.int32),
+               "query_start_loc": np.full(B + 1, -7, np.int32),
+               "positions": np.full(T, -7, np.int32),
+               "input_ids": np.full(T, -7, np.int32),
+               "slot_mapping": np.full(T, -7, np.int64)}
+        err = self.lib.oracle_prepare_inputs(
+            idx.ctypes.data, ns.ctypes.data, B, sbt.ctypes.data, MB,
+            snc.ctypes.data, tok.ctypes.data, ML, R, T,
+            out["block_tables"].ctypes.data, out["seq_lens"].ctypes.data,
+            out["query_start_loc"].ctypes.data, out["positions"].ctypes.data,
+            out["input_ids"].ctypes.data, out["slot_mapping"].ctypes.data)
+        return out, err
 
     def attention_decode(self, q: np.ndarray, key_cache: np.ndarray,
                          value_cache: np.ndarray, dtype: int,

@@ -283,6 +283,80 @@ long oracle_swap_in(uint8_t *key_cache, uint8_t *value_cache,
 }
 
 /* ------------------------------------------------------------------ */
+/* Step input preparation from a persistent request state table        */
+/* ------------------------------------------------------------------ */
+
+/* Model Runner V2 summary (papercache.org), Figure 2 and "GPU原生的输入准备":
+ * every active request keeps a stable row of a state table; each step
+ * gathers the rows of the scheduled requests, in batch order, into the
+ * step's inputs.  For batch entry b with state row r = idx_mapping[b],
+ * n = num_scheduled[b] new tokens and c = num_computed[r] tokens already
+ * in the cache:
+ *   block_tables[b][:]  = state_block_table[r][:]
+ *   seq_lens[b]         = c + n
+ *   query_start_loc[b]  = n_0 + ... + n_{b-1}   (entry batch = total)
+ *   for t = query_start_loc[b] + i, i < n:
+ *     positions[t]      = c + i
+ *     input_ids[t]      = state_token_ids[r][c + i]
+ *     slot_mapping[t]   = state_block_table[r][(c+i)/16]*16 + (c+i)%16
+ * Entries with an out-of-range row, or positions past the table or the
+ * token buffer, are counted as errors and left as they were (their tokens'
+ * slots become -1).  Returns the error count. */
+long oracle_prepare_inputs(const int32_t *idx_mapping,
+                           const int32_t *num_scheduled, int batch,
+                           const int32_t *state_block_table, int max_blocks,
+                           const int32_t *state_num_computed,
+                           const int32_t *state_token_ids, int max_model_len,
+                           int num_rows, long total_tokens,
+                           int32_t *block_tables, int32_t *seq_lens,
+                           int32_t *query_start_loc, int32_t *positions,
+                           int32_t *input_ids, int64_t *slot_mapping)
+{
+    long errors = 0, t0 = 0;
+    int b, i, j;
+    for (b = 0; b < batch; ++b) {
+        int r = idx_mapping[b];
+        int n = num_scheduled[b];
+        query_start_loc[b] = (int32_t)t0;
+        if (n < 0 || t0 + n > total_tokens) {
+            ++errors;
+            continue;
+        }
+        if (r < 0 || r >= num_rows) {
+            ++errors;
+            for (i = 0; i < n; ++i)
+                slot_mapping[t0 + i] = -1;
+            t0 += n;
+            continue;
+        }
+        {
+            int c = state_num_computed[r];
+            for (j = 0; j < max_blocks; ++j)
+                block_tables[(size_t)b * max_blocks + j] =
+                    state_block_table[(size_t)r * max_blocks + j];
+            seq_lens[b] = c + n;
+            for (i = 0; i < n; ++i) {
+                long t = t0 + i;
+                int pos = c + i;
+                positions[t] = pos;
+                if (pos >= max_blocks * 16 || pos >= max_model_len) {
+                    ++errors;
+                    slot_mapping[t] = -1;
+                    continue;
+                }
+                input_ids[t] = state_token_ids[(size_t)r * max_model_len + pos];
+                slot_mapping[t] =
+                    (int64_t)state_block_table[(size_t)r * max_blocks + pos / 16] *
+                        16 + pos % 16;
+            }
+        }
+        t0 += n;
+    }
+    query_start_loc[batch] = (int32_t)t0;
+    return errors;
+}
+
+/* ------------------------------------------------------------------ */
 /* Decode attention                                                    */
 /* ------------------------------------------------------------------ */
 

@@ -293,6 +293,53 @@ def pin_swap_round_trip_is_gather_then_scatter(oracle):
     assert oracle.swap_out(kc, vc, bb, np.array([-1], np.int32))[2] == 1
 
 
+def _state_table(rng, R=12, MB=8, ML=128):
+    sbt = rng.permutation(R * MB + 10)[:R * MB].astype(np.int32).reshape(R, MB)
+    snc = rng.integers(0, 100, R).astype(np.int32)
+    tok = rng.integers(0, 50000, (R, ML)).astype(np.int32)
+    return sbt, snc, tok
+
+
+def pin_prepare_inputs_is_gather_and_cumsum(oracle):
+    rng = np.random.default_rng(30)
+    sbt, snc, tok = _state_table(rng)
+    idx = np.array([7, 2, 11, 0, 5], np.int32)
+    ns = np.array([1, 17, 1, 0, 9], np.int32)
+    T = int(ns.sum())
+    out, err = oracle.prepare_inputs(idx, ns, sbt, snc, tok, T)
+    assert err == 0
+    qsl = np.concatenate([[0], np.cumsum(ns)])
+    assert np.array_equal(out["query_start_loc"], qsl)
+    assert np.array_equal(out["block_tables"], sbt[idx])
+    assert np.array_equal(out["seq_lens"], snc[idx] + ns)
+    rows = np.repeat(idx, ns)
+    pos = np.concatenate([snc[r] + np.arange(n) for r, n in zip(idx, ns)])
+    assert np.array_equal(out["positions"], pos)
+    assert np.array_equal(out["input_ids"], tok[rows, pos])
+    assert np.array_equal(out["slot_mapping"],
+                          sbt[rows, pos // 16].astype(np.int64) * 16 + pos % 16)
+    # every new token's slot lies inside its request's last needed block
+    last = qsl[1:] - 1
+    for b in range(idx.size):
+        if ns[b]:
+            L = out["seq_lens"][b]
+            assert out["slot_mapping"][last[b]] == sbt[idx[b], (L - 1) // 16] * 16 + (L - 1) % 16
+
+
+def pin_prepare_inputs_range_errors(oracle):
+    rng = np.random.default_rng(31)
+    sbt, snc, tok = _state_table(rng, R=4, MB=2, ML=40)
+    snc[:] = [0, 30, 5, 31]
+    idx = np.array([0, 9, 1, 3], np.int32)       # row 9 does not exist
+    ns = np.array([2, 3, 4, 1], np.int32)          # row 1: positions 30..33 > 32
+    out, err = oracle.prepare_inputs(idx, ns, sbt, snc, tok, int(ns.sum()))
+    assert err == 1 + 2                            # bad row, positions 32 and 33
+    sl = out["slot_mapping"]
+    assert list(sl[2:5]) == [-1, -1, -1]           # the bad row's tokens
+    assert sl[5] >= 0 and sl[6] >= 0 and sl[7] == -1 and sl[8] == -1
+    assert sl[9] == sbt[3, 1] * 16 + 15
+
+
 # ---------------------------------------------------------------------------
 # attention: closed forms
 # ---------------------------------------------------------------------------

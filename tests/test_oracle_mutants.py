@@ -70,6 +70,15 @@ MUTANTS = [
     ("swap_in_skips_value",
      "        memcpy(value_cache + (size_t)ids[i] * block_bytes,\n               in_v + (size_t)i * block_bytes, block_bytes);",
      "        (void)in_v;"),
+    ("prepare_positions_from_zero", "                int pos = c + i;",
+     "                int pos = i;"),
+    ("prepare_table_of_batch_index",
+     "                    (int64_t)state_block_table[(size_t)r * max_blocks + pos / 16] *",
+     "                    (int64_t)state_block_table[(size_t)b * max_blocks + pos / 16] *"),
+    ("prepare_seq_len_without_new", "            seq_lens[b] = c + n;",
+     "            seq_lens[b] = c;"),
+    ("prepare_start_loc_inclusive", "        query_start_loc[b] = (int32_t)t0;",
+     "        query_start_loc[b] = (int32_t)(t0 + n);"),
 ]
 
 _RUNNER = textwrap.dedent("""
