@@ -52,7 +52,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
     ap.add_argument("--kernel", default="decode",
-                    choices=["decode", "zero_blocks", "copy_blocks", "swap"],
+                    choices=["decode", "zero_blocks", "copy_blocks", "swap",
+                             "input_prep"],
                     help="decode: the decode step (headline); the others time "
                          "the block-movement entry points on the workload's "
                          "pool")
@@ -591,8 +592,67 @@ def run_blocks(args):
     return 0
 
 
+def run_input_prep(args):
+    """Step input preparation from a persistent state table: µs per call on
+    the GPU against the oracle's host loop, for a decode batch (64 x 1
+    token) and a mixed chunked-prefill batch (8 x 512 + 56 x 1 tokens)."""
+    import torch
+    import oracle
+    from paged_kv_cache_48_gb300 import paged_prepare_inputs, pkv_check
+    torch.cuda.set_device(0)
+    rng = np.random.default_rng(9)
+    R, MB, ML, B = 512, 256, 4096, 64
+    sbt = rng.permutation(R * MB).astype(np.int32).reshape(R, MB)
+    snc = rng.integers(0, 3000, R).astype(np.int32)
+    tok = rng.integers(0, 151000, (R, ML)).astype(np.int32)
+    idx = rng.permutation(R)[:B].astype(np.int32)
+    c = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    g_sbt, g_snc, g_tok, g_idx = c(sbt), c(snc), c(tok), c(idx)
+    o = oracle.load()
+    stream = torch.cuda.current_stream()
+    for label, ns in (("decode batch, 64 x 1 token", np.ones(B, np.int32)),
+                      ("chunked batch, 8 x 512 + 56 x 1 tokens",
+                       np.array([512] * 8 + [1] * 56, np.int32))):
+        T = int(ns.sum())
+        g_ns = c(ns)
+        f = lambda: paged_prepare_inputs(g_idx, g_ns, g_sbt, g_snc, g_tok, T)
+        for _ in range(max(3, args.warmup)):
+            f()
+        torch.cuda.synchronize()
+        reps = 500
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            f()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) / reps * 1e3
+        t0 = time.perf_counter()
+        n_cpu = 200
+        for _ in range(n_cpu):
+            o.prepare_inputs(idx, ns, sbt, snc, tok, T)
+        cpu_us = (time.perf_counter() - t0) / n_cpu * 1e6
+        print(json.dumps({
+            "kernel": "input_prep", "metric": f"step input preparation: {label}",
+            "value": round(us, 2), "unit": "us", "higher_is_better": False,
+            "tokens": T, "gpu_launches_per_call": 2,
+            "cpu_baseline": {"value": round(cpu_us, 2), "unit": "us", "cores": 1,
+                             "kind": "oracle",
+                             "sample": "the same call, host loop, 200 repetitions"},
+            "data": "synthetic",
+            "config": {"state_rows": R, "max_blocks": MB, "max_model_len": ML,
+                       "batch": B}}), flush=True)
+    st, detail = pkv_check()
+    if st != 0:
+        raise RuntimeError(f"device error {st} at {detail}")
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.kernel == "input_prep":
+        return run_input_prep(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.kernel != "decode":

@@ -132,6 +132,40 @@ pkv_status paged_kv_swap_in(const pkv_cache *cache, const int32_t *block_ids,
                             int64_t n, int ids_on_host, const void *host_k,
                             const void *host_v, void *stream);
 
+/* Build one step's attention inputs on the GPU from a persistent request
+ * state table.  Source: Model Runner V2 summary (papercache.org), Figure 2
+ * and its section on GPU-native input preparation: each active request
+ * keeps a stable row; every step gathers the scheduled rows, in batch
+ * order, into the step's inputs, without CPU-side tensor work.
+ *   idx_mapping        int32 [batch]: state row of each batch entry.
+ *   num_scheduled      int32 [batch]: new tokens of each entry this step
+ *                      (1 for decode, a chunk length for chunked prefill).
+ *   state_block_table  int32 [num_rows, max_blocks].
+ *   state_num_computed int32 [num_rows]: tokens already in the cache.
+ *   state_token_ids    int32 [num_rows, max_model_len].
+ *   total_tokens       host bound: capacity of the per-token outputs.
+ * Outputs (device):
+ *   block_tables    int32 [batch, max_blocks] = state rows, gathered;
+ *   seq_lens        int32 [batch] = num_computed + num_scheduled;
+ *   query_start_loc int32 [batch + 1] = exclusive prefix sum of
+ *                   num_scheduled (last entry = total);
+ *   positions, input_ids  int32 [total_tokens];
+ *   slot_mapping    int64 [total_tokens]: the cache slot of each new token.
+ * Device range errors (row out of range, position past the table or the
+ * token buffer, more tokens than total_tokens, negative counts) skip the
+ * affected outputs (slots become -1) and are reported by pkv_check(). */
+pkv_status paged_prepare_inputs(const int32_t *idx_mapping,
+                                const int32_t *num_scheduled, int32_t batch,
+                                const int32_t *state_block_table,
+                                int32_t max_blocks,
+                                const int32_t *state_num_computed,
+                                const int32_t *state_token_ids,
+                                int32_t max_model_len, int32_t num_rows,
+                                int64_t total_tokens, int32_t *block_tables,
+                                int32_t *seq_lens, int32_t *query_start_loc,
+                                int32_t *positions, int32_t *input_ids,
+                                int64_t *slot_mapping, void *stream);
+
 /* Decode attention over a paged cache, one query token per sequence.
  * Source: vLLM concept page (compassingai.com), "技术原理" pseudocode
  * (gather by page table, Q K^T / sqrt(d), softmax, times V) and its note on

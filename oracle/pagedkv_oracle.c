@@ -299,9 +299,12 @@ long oracle_swap_in(uint8_t *key_cache, uint8_t *value_cache,
  *     positions[t]      = c + i
  *     input_ids[t]      = state_token_ids[r][c + i]
  *     slot_mapping[t]   = state_block_table[r][(c+i)/16]*16 + (c+i)%16
- * Entries with an out-of-range row, or positions past the table or the
- * token buffer, are counted as errors and left as they were (their tokens'
- * slots become -1).  Returns the error count. */
+ * Errors are counted and the offending outputs skipped: a negative count
+ * schedules nothing; an entry whose tokens do not fit in total_tokens
+ * writes nothing (its start offset still advances); an out-of-range row
+ * writes slot -1 for its tokens and nothing else; a position past the
+ * table or the token buffer writes its position and slot -1.  Returns the
+ * error count. */
 long oracle_prepare_inputs(const int32_t *idx_mapping,
                            const int32_t *num_scheduled, int batch,
                            const int32_t *state_block_table, int max_blocks,
@@ -317,9 +320,14 @@ long oracle_prepare_inputs(const int32_t *idx_mapping,
     for (b = 0; b < batch; ++b) {
         int r = idx_mapping[b];
         int n = num_scheduled[b];
-        query_start_loc[b] = (int32_t)t0;
-        if (n < 0 || t0 + n > total_tokens) {
+        if (n < 0) { /* a negative count schedules nothing */
             ++errors;
+            n = 0;
+        }
+        query_start_loc[b] = (int32_t)t0;
+        if (t0 + n > total_tokens) { /* no room left in the outputs */
+            ++errors;
+            t0 += n;
             continue;
         }
         if (r < 0 || r >= num_rows) {

@@ -10,12 +10,14 @@ from .ops import (PagedKVCache, PagedKVError, paged_attention_decode,
                   paged_attention_partition_tokens,
                   paged_attention_workspace_bytes, paged_kv_copy_blocks,
                   paged_kv_swap_in, paged_kv_swap_out, paged_kv_write,
-                  paged_kv_zero_blocks, pkv_check, raise_on_device_error)
+                  paged_kv_zero_blocks, paged_prepare_inputs, pkv_check,
+                  raise_on_device_error)
 
 __all__ = [
     "PagedKVCache", "PagedKVError", "paged_attention_decode",
     "paged_attention_partition_tokens", "paged_attention_workspace_bytes",
     "paged_kv_copy_blocks", "paged_kv_swap_in", "paged_kv_swap_out",
-    "paged_kv_write", "paged_kv_zero_blocks", "pkv_check",
+    "paged_kv_write", "paged_kv_zero_blocks", "paged_prepare_inputs",
+    "pkv_check",
     "raise_on_device_error",
 ]

@@ -51,6 +51,9 @@ _SIGNATURES = {
     "paged_kv_swap_in": (ctypes.c_int, [ctypes.POINTER(PkvCache), _P,
                                         ctypes.c_int64, ctypes.c_int, _P, _P,
                                         _P]),
+    "paged_prepare_inputs": (ctypes.c_int, [
+        _P, _P, ctypes.c_int32, _P, ctypes.c_int32, _P, _P, ctypes.c_int32,
+        ctypes.c_int32, ctypes.c_int64, _P, _P, _P, _P, _P, _P, _P]),
     "paged_attention_decode": (ctypes.c_int, [
         _P, ctypes.POINTER(PkvCache), _P, ctypes.c_int32, _P, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_float, _P, ctypes.c_int32, ctypes.c_int32,

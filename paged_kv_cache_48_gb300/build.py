@@ -18,7 +18,7 @@ CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIBRARY = PKG / "libpagedkv.so"
 SOURCES = ["kv_write_zero.cu", "attention_decode.cu", "pkv_api.cu",
-           "attention_noalloc.cu", "kv_blocks.cu"]
+           "attention_noalloc.cu", "kv_blocks.cu", "input_prep.cu"]
 HEADERS = ["pkv_device.cuh", "pkv_host.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

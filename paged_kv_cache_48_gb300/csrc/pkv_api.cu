@@ -43,12 +43,15 @@ using namespace pkv;
 extern "C" pkv_status pkv_check(void *stream, int64_t *detail) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (detail) *detail = -1;
-  cudaError_t e1 = cudaSuccess, e2 = cudaSuccess, e3 = cudaSuccess;
-  const unsigned long long w1 = read_and_clear_error_write_zero(s, &e1);
-  const unsigned long long w2 = read_and_clear_error_attention(s, &e2);
-  const unsigned long long w3 = read_and_clear_error_blocks(s, &e3);
-  if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) return PKV_ERR_CUDA;
-  const unsigned long long w = w1 ? w1 : (w2 ? w2 : w3);
+  cudaError_t e[4] = {cudaSuccess, cudaSuccess, cudaSuccess, cudaSuccess};
+  const unsigned long long words[4] = {
+      read_and_clear_error_write_zero(s, &e[0]), read_and_clear_error_attention(s, &e[1]),
+      read_and_clear_error_blocks(s, &e[2]), read_and_clear_error_prep(s, &e[3])};
+  unsigned long long w = 0ull;
+  for (int i = 0; i < 4; ++i) {
+    if (e[i] != cudaSuccess) return PKV_ERR_CUDA;
+    if (!w) w = words[i];
+  }
   if (!w) return PKV_OK;
   if (detail) *detail = (int64_t)(w & 0x00FFFFFFFFFFFFFFull) - 1;
   return static_cast<pkv_status>(w >> 56);

@@ -24,5 +24,6 @@ unsigned long long read_and_clear_error_write_zero(cudaStream_t s,
 unsigned long long read_and_clear_error_attention(cudaStream_t s,
                                                   cudaError_t *err);
 unsigned long long read_and_clear_error_blocks(cudaStream_t s, cudaError_t *err);
+unsigned long long read_and_clear_error_prep(cudaStream_t s, cudaError_t *err);
 
 }  // namespace pkv

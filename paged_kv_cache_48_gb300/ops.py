@@ -211,6 +211,46 @@ def paged_kv_swap_in(cache: PagedKVCache, block_ids, host_k: torch.Tensor,
     _native.check("paged_kv_swap_in", st)
 
 
+def paged_prepare_inputs(idx_mapping: torch.Tensor,
+                         num_scheduled: torch.Tensor,
+                         state_block_table: torch.Tensor,
+                         state_num_computed: torch.Tensor,
+                         state_token_ids: torch.Tensor, total_tokens: int,
+                         stream: Optional[torch.cuda.Stream] = None) -> dict:
+    """Gather one step's inputs from the persistent request state table
+    (all int32 CUDA tensors).  Returns block_tables, seq_lens,
+    query_start_loc, positions, input_ids and slot_mapping."""
+    dev = state_block_table.device
+    for t, n, nd in ((idx_mapping, "idx_mapping", 1),
+                     (num_scheduled, "num_scheduled", 1),
+                     (state_block_table, "state_block_table", 2),
+                     (state_num_computed, "state_num_computed", 1),
+                     (state_token_ids, "state_token_ids", 2)):
+        _require(t, n, torch.int32, dev, nd)
+    B = idx_mapping.shape[0]
+    R, MB = state_block_table.shape
+    if num_scheduled.shape[0] != B or state_num_computed.shape[0] != R or \
+            state_token_ids.shape[0] != R:
+        raise ValueError("state table and batch shapes do not match")
+    T = int(total_tokens)
+    out = {"block_tables": torch.empty((B, MB), dtype=torch.int32, device=dev),
+           "seq_lens": torch.empty(B, dtype=torch.int32, device=dev),
+           "query_start_loc": torch.empty(B + 1, dtype=torch.int32, device=dev),
+           "positions": torch.empty(T, dtype=torch.int32, device=dev),
+           "input_ids": torch.empty(T, dtype=torch.int32, device=dev),
+           "slot_mapping": torch.empty(T, dtype=torch.int64, device=dev)}
+    st = _native.lib().paged_prepare_inputs(
+        idx_mapping.data_ptr(), num_scheduled.data_ptr(), B,
+        state_block_table.data_ptr(), MB, state_num_computed.data_ptr(),
+        state_token_ids.data_ptr(), state_token_ids.shape[1], R, T,
+        out["block_tables"].data_ptr(), out["seq_lens"].data_ptr(),
+        out["query_start_loc"].data_ptr(), out["positions"].data_ptr(),
+        out["input_ids"].data_ptr(), out["slot_mapping"].data_ptr(),
+        _stream_handle(stream, dev))
+    _native.check("paged_prepare_inputs", st)
+    return out
+
+
 def paged_attention_workspace_bytes(batch: int, num_heads: int,
                                     num_kv_heads: int, head_dim: int,
                                     max_seq_len: int,
