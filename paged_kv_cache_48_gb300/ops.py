@@ -216,10 +216,12 @@ def paged_prepare_inputs(idx_mapping: torch.Tensor,
                          state_block_table: torch.Tensor,
                          state_num_computed: torch.Tensor,
                          state_token_ids: torch.Tensor, total_tokens: int,
+                         out: Optional[dict] = None,
                          stream: Optional[torch.cuda.Stream] = None) -> dict:
     """Gather one step's inputs from the persistent request state table
     (all int32 CUDA tensors).  Returns block_tables, seq_lens,
-    query_start_loc, positions, input_ids and slot_mapping."""
+    query_start_loc, positions, input_ids and slot_mapping (written into
+    ``out`` when given, e.g. a previous call's result)."""
     dev = state_block_table.device
     for t, n, nd in ((idx_mapping, "idx_mapping", 1),
                      (num_scheduled, "num_scheduled", 1),
@@ -233,12 +235,20 @@ def paged_prepare_inputs(idx_mapping: torch.Tensor,
             state_token_ids.shape[0] != R:
         raise ValueError("state table and batch shapes do not match")
     T = int(total_tokens)
-    out = {"block_tables": torch.empty((B, MB), dtype=torch.int32, device=dev),
-           "seq_lens": torch.empty(B, dtype=torch.int32, device=dev),
-           "query_start_loc": torch.empty(B + 1, dtype=torch.int32, device=dev),
-           "positions": torch.empty(T, dtype=torch.int32, device=dev),
-           "input_ids": torch.empty(T, dtype=torch.int32, device=dev),
-           "slot_mapping": torch.empty(T, dtype=torch.int64, device=dev)}
+    shapes = {"block_tables": ((B, MB), torch.int32),
+              "seq_lens": ((B,), torch.int32),
+              "query_start_loc": ((B + 1,), torch.int32),
+              "positions": ((T,), torch.int32),
+              "input_ids": ((T,), torch.int32),
+              "slot_mapping": ((T,), torch.int64)}
+    if out is None:
+        out = {k: torch.empty(sh, dtype=dt, device=dev)
+               for k, (sh, dt) in shapes.items()}
+    else:
+        for k, (sh, dt) in shapes.items():
+            _require(out[k], k, dt, dev, len(sh))
+            if tuple(out[k].shape) != sh:
+                raise ValueError(f"out[{k!r}] must have shape {sh}")
     st = _native.lib().paged_prepare_inputs(
         idx_mapping.data_ptr(), num_scheduled.data_ptr(), B,
         state_block_table.data_ptr(), MB, state_num_computed.data_ptr(),
