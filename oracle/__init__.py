@@ -81,6 +81,12 @@ class Oracle:
             ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, ctypes.c_double,
             _P, _P, ctypes.c_long, ctypes.c_int]
         lib.oracle_attention_decode.restype = ctypes.c_long
+        lib.oracle_attention_prefill.argtypes = [
+            _P, _P, _P, ctypes.c_int, ctypes.c_double, ctypes.c_double,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P,
+            ctypes.c_int, _P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+            _P, _P, ctypes.c_long, ctypes.c_int]
+        lib.oracle_attention_prefill.restype = ctypes.c_long
         for name in ("oracle_copy_blocks",):
             fn = getattr(lib, name)
             fn.argtypes = [_P, _P, ctypes.c_size_t, ctypes.c_int, _P, _P,
@@ -241,6 +247,46 @@ class Oracle:
             num_kv_heads, head_dim, tables.ctypes.data, tables.shape[1],
             lens.ctypes.data, B, Hq, float(scale), out.ctypes.data, pp,
             n_pairs, int(n_threads))
+        return out, err
+
+    def attention_prefill(self, q: np.ndarray, key_cache: np.ndarray,
+                          value_cache: np.ndarray, dtype: int,
+                          k_scale: float, v_scale: float, block_size: int,
+                          num_kv_heads: int, head_dim: int,
+                          block_tables: np.ndarray, seq_lens: np.ndarray,
+                          query_start_loc: np.ndarray, scale: float,
+                          rows=None, n_threads: int = 0):
+        """fp64 prefill / chunked-prefill attention (causal within each
+        sequence's chunk).  q: uint16 bf16 bits [T, Hq, d]; query_start_loc
+        int [B+1].  Returns (out float64 [T, Hq, d], error_count).  With
+        ``rows`` (int array [n, 2] of (token, head)) only those rows are
+        computed; the others stay 0."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        T, Hq, d = q.shape
+        assert d == head_dim
+        tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+        lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        qsl = np.ascontiguousarray(query_start_loc, dtype=np.int32)
+        B = lens.shape[0]
+        assert tables.shape[0] == B and qsl.shape == (B + 1,)
+        assert B == 0 or qsl[B] == T
+        _check_c(key_cache, np.uint8)
+        _check_c(value_cache, np.uint8)
+        eb = 2 if dtype == DTYPE_BF16 else 1
+        num_blocks = key_cache.size // (block_size * num_kv_heads * head_dim * eb)
+        out = np.zeros((T, Hq, d), dtype=np.float64)
+        if rows is None:
+            rp, n_rows = None, 0
+        else:
+            rows = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 2)
+            rp, n_rows = rows.ctypes.data, rows.shape[0]
+        err = self.lib.oracle_attention_prefill(
+            q.ctypes.data, key_cache.ctypes.data, value_cache.ctypes.data,
+            dtype, float(k_scale), float(v_scale), num_blocks, block_size,
+            num_kv_heads, head_dim, tables.ctypes.data,
+            tables.shape[1] if tables.ndim == 2 else 0, lens.ctypes.data,
+            qsl.ctypes.data, B, Hq, float(scale), out.ctypes.data, rp, n_rows,
+            int(n_threads))
         return out, err
 
 

@@ -382,18 +382,17 @@ typedef struct {
     double scale;
 } attn_args;
 
-/* One (sequence b, query head h) of the pages' PagedAttention pseudocode.
- * Returns 0, or 1 on an out-of-range block id / sequence length (the row is
- * then left as zeros). */
-static int attend_one(const attn_args *a, int b, int h, double *out_row,
-                      double *K, double *V, double *p)
+/* The pages' PagedAttention pseudocode for one query row qrow of q head h
+ * against the first L tokens of sequence b.  Returns 0, or 1 on an
+ * out-of-range block id / sequence length (the row is then left as
+ * zeros). */
+static int attend_row(const attn_args *a, const uint16_t *qrow, int b, int h,
+                      int L, double *out_row, double *K, double *V, double *p)
 {
     const int d = a->head_dim, bs = a->block_size;
     const int group = a->num_heads / a->num_kv_heads;
     const int kvh = h / group;
-    const int L = a->seq_lens[b];
     const int nblk = (L + bs - 1) / bs;
-    const uint16_t *qrow = a->q + ((size_t)b * a->num_heads + h) * d;
     double qd[1024];
     int t, j, i;
     double mx, denom;
@@ -522,7 +521,8 @@ long oracle_attention_decode(const uint16_t *q, const uint8_t *key_cache,
                 ++errors;
                 continue;
             }
-            errors += attend_one(&a, bb, hh,
+            errors += attend_row(&a, q + ((size_t)bb * num_heads + hh) * head_dim,
+                                 bb, hh, seq_lens[bb],
                                  out + ((size_t)bb * num_heads + hh) * head_dim,
                                  K, V, p);
         }
@@ -530,6 +530,128 @@ long oracle_attention_decode(const uint16_t *q, const uint8_t *key_cache,
         free(V);
         free(p);
     }
+    return errors;
+}
+
+/* Prefill / chunked-prefill attention.  vLLM concept page
+ * (compassingai.com), "Continuous Batching" with chunked prefill: a long
+ * prompt is cut into chunks that share steps with decoding sequences, and
+ * every token is inferred incrementally from the tokens before it.  The
+ * reading taken here: sequence b brings n_b = query_start_loc[b+1] -
+ * query_start_loc[b] query tokens (rows query_start_loc[b] .. +n_b-1 of q,
+ * [T, Hq, d]), whose K/V are already in the cache as its last n_b tokens
+ * (seq_lens[b] = c_b + n_b, c_b tokens computed in earlier steps).  Query
+ * token i sits at position c_b + i and attends to the key positions
+ * 0 .. c_b + i, through the pseudocode's gather / scores / softmax / PV; a
+ * decode step is the case n_b = 1.
+ * out is [T, Hq, d] doubles.  With rows != NULL only those n_rows (token,
+ * head) rows are computed.  A sequence with n_b < 0 or c_b < 0 is a range
+ * error and its rows stay 0; returns the error count (a bad sequence
+ * counts once per computed row). */
+long oracle_attention_prefill(const uint16_t *q, const uint8_t *key_cache,
+                              const uint8_t *value_cache, int dtype,
+                              double k_scale, double v_scale, int num_blocks,
+                              int block_size, int num_kv_heads, int head_dim,
+                              const int32_t *block_tables, int max_blocks,
+                              const int32_t *seq_lens,
+                              const int32_t *query_start_loc, int batch,
+                              int num_heads, double scale, double *out,
+                              const int32_t *rows, long n_rows, int n_threads)
+{
+    attn_args a;
+    long total, errors = 0, idx, T;
+    int max_len = 0, b;
+    int32_t *seq_of; /* sequence of each query token, -1 when none */
+
+    if (head_dim > 1024 || num_kv_heads <= 0 || num_heads % num_kv_heads ||
+        batch < 0)
+        return -1;
+    T = batch > 0 ? query_start_loc[batch] : 0;
+    if (T < 0)
+        return -1;
+    a.q = q;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.dtype = dtype;
+    a.k_scale = dtype == ORACLE_DTYPE_BF16 ? 1.0 : k_scale;
+    a.v_scale = dtype == ORACLE_DTYPE_BF16 ? 1.0 : v_scale;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks;
+    a.seq_lens = seq_lens;
+    a.num_heads = num_heads;
+    a.scale = scale;
+    seq_of = (int32_t *)malloc((size_t)(T > 0 ? T : 1) * sizeof(int32_t));
+    if (!seq_of)
+        return -1;
+    for (idx = 0; idx < T; ++idx)
+        seq_of[idx] = -1;
+    for (b = 0; b < batch; ++b) {
+        long t;
+        if (seq_lens[b] > max_len)
+            max_len = seq_lens[b];
+        for (t = query_start_loc[b]; t < query_start_loc[b + 1]; ++t)
+            if (t >= 0 && t < T)
+                seq_of[t] = b;
+    }
+    if (max_len > max_blocks * block_size)
+        max_len = max_blocks * block_size;
+    total = rows ? n_rows : T * num_heads;
+
+#ifdef _OPENMP
+    if (n_threads > 0)
+        omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel reduction(+ : errors)
+    {
+        size_t n = (size_t)(max_len > 0 ? max_len : 1);
+        double *K = (double *)malloc(n * head_dim * sizeof(double));
+        double *V = (double *)malloc(n * head_dim * sizeof(double));
+        double *p = (double *)malloc(n * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (idx = 0; idx < total; ++idx) {
+            long t;
+            int hh, bb, nq, c, i, k;
+            double *orow;
+            if (rows) {
+                t = rows[2 * idx];
+                hh = rows[2 * idx + 1];
+            } else {
+                t = idx / num_heads;
+                hh = (int)(idx % num_heads);
+            }
+            if (t < 0 || t >= T || hh < 0 || hh >= num_heads || !K || !V || !p) {
+                ++errors;
+                continue;
+            }
+            orow = out + ((size_t)t * num_heads + hh) * head_dim;
+            for (k = 0; k < head_dim; ++k)
+                orow[k] = 0.0;
+            bb = seq_of[t];
+            if (bb < 0) { /* a token that no sequence owns */
+                ++errors;
+                continue;
+            }
+            nq = query_start_loc[bb + 1] - query_start_loc[bb];
+            c = seq_lens[bb] - nq; /* tokens before this chunk */
+            i = (int)(t - query_start_loc[bb]);
+            if (c < 0) {
+                ++errors;
+                continue;
+            }
+            errors += attend_row(&a, q + ((size_t)t * num_heads + hh) * head_dim,
+                                 bb, hh, c + i + 1, orow, K, V, p);
+        }
+        free(K);
+        free(V);
+        free(p);
+    }
+    free(seq_of);
     return errors;
 }
 

@@ -587,5 +587,121 @@ def pin_range_errors_reported(oracle):
     assert np.array_equal(out, np.zeros_like(out))
 
 
+# ---------------------------------------------------------------------------
+# prefill / chunked prefill (causal within each sequence's chunk)
+# ---------------------------------------------------------------------------
+
+def _prefill_case(seed, lens, nq, Hq=6, Hkv=2, d=16, permute=True):
+    """Sequences of lens[b] tokens whose last nq[b] are this step's query
+    tokens; blocks placed at seeded random physical ids."""
+    rng = np.random.default_rng(seed)
+    K = [_rand_bf16(rng, (L, Hkv, d)) for L in lens]
+    V = [_rand_bf16(rng, (L, Hkv, d)) for L in lens]
+    nb = [(L + BS - 1) // BS for L in lens]
+    ids = rng.permutation(sum(nb) + 5) if permute else np.arange(sum(nb) + 5)
+    tables, nxt = [], 0
+    for n in nb:
+        tables.append([int(x) for x in ids[nxt:nxt + n]])
+        nxt += n
+    kc, vc = _paged_from_contiguous(K, V, tables, sum(nb) + 5)
+    qsl = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    q = _rand_bf16(rng, (int(qsl[-1]), Hq, d))
+    return K, V, q, kc, vc, _tables_array(tables, max(nb)), qsl
+
+
+def _causal_sdpa_reference(q_bits, K, V, lens, qsl, scale):
+    """torch SDPA in float64 per sequence with an explicit boolean mask:
+    query i of sequence b (position lens[b] - n_b + i) may see key t iff
+    t <= that position."""
+    T, Hq, d = q_bits.shape
+    out = np.zeros((T, Hq, d))
+    for b, L in enumerate(lens):
+        a, e = int(qsl[b]), int(qsl[b + 1])
+        n = e - a
+        if n == 0:
+            continue
+        qb = torch.from_numpy(bf16_values(q_bits[a:e]).astype(np.float64))
+        kb = torch.from_numpy(bf16_values(K[b]).astype(np.float64))
+        vb = torch.from_numpy(bf16_values(V[b]).astype(np.float64))
+        g = Hq // kb.shape[1]
+        kb = kb.permute(1, 0, 2).repeat_interleave(g, dim=0)  # [Hq, L, d]
+        vb = vb.permute(1, 0, 2).repeat_interleave(g, dim=0)
+        pos = torch.arange(L - n, L)[:, None]
+        mask = torch.arange(L)[None, :] <= pos                 # [n, L]
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qb.permute(1, 0, 2), kb, vb, attn_mask=mask, scale=scale)
+        out[a:e] = o.permute(1, 0, 2).numpy()
+    return out
+
+
+def _run_prefill(oracle, q, kc, vc, tables, lens, qsl, Hkv, d, scale, rows=None):
+    out, err = oracle.attention_prefill(q, kc, vc, BF16, 1.0, 1.0, BS, Hkv, d,
+                                        tables, np.array(lens, np.int32), qsl,
+                                        scale, rows=rows)
+    return out, err
+
+
+def pin_prefill_matches_causal_sdpa(oracle):
+    """Whole prompts, chunks after a history, a one-token (decode) entry and
+    an empty entry, against torch SDPA with an explicit causal mask."""
+    lens, nq = (5, 16, 41, 33, 7), (5, 3, 20, 1, 0)
+    K, V, q, kc, vc, tables, qsl = _prefill_case(40, lens, nq)
+    scale = 1.0 / math.sqrt(16)
+    out, err = _run_prefill(oracle, q, kc, vc, tables, lens, qsl, 2, 16, scale)
+    assert err == 0
+    ref = _causal_sdpa_reference(q, K, V, lens, qsl, scale)
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_prefill_first_prompt_token_returns_its_value(oracle):
+    """A prompt's first token attends to itself alone: its output is exactly
+    its own V row (per kv head of its group)."""
+    lens, nq = (9, 20), (9, 20)
+    K, V, q, kc, vc, tables, qsl = _prefill_case(41, lens, nq, Hq=4, Hkv=2)
+    out, err = _run_prefill(oracle, q, kc, vc, tables, lens, qsl, 2, 16, 0.3)
+    assert err == 0
+    for b in range(2):
+        for h in range(4):
+            assert np.array_equal(out[qsl[b], h], bf16_values(V[b][0, h // 2]))
+
+
+def pin_prefill_ignores_keys_after_each_position(oracle):
+    """Changing the K/V of the chunk's last token changes the last query row
+    only; every earlier row of the chunk is bit-identical."""
+    lens, nq = (30,), (12,)
+    K, V, q, kc, vc, tables, qsl = _prefill_case(42, lens, nq, permute=False)
+    out1, _ = _run_prefill(oracle, q, kc, vc, tables, lens, qsl, 2, 16, 0.25)
+    K2 = [K[0].copy()]
+    V2 = [V[0].copy()]
+    rng = np.random.default_rng(43)
+    K2[0][-1] = _rand_bf16(rng, K2[0][-1].shape)
+    V2[0][-1] = _rand_bf16(rng, V2[0][-1].shape)
+    kc2, vc2 = _paged_from_contiguous(K2, V2, [list(tables[0][tables[0] >= 0])],
+                                      kc.size // (BS * 2 * 16 * 2))
+    out2, _ = _run_prefill(oracle, q, kc2, vc2, tables, lens, qsl, 2, 16, 0.25)
+    assert np.array_equal(out1[:-1], out2[:-1])
+    assert not np.allclose(out1[-1], out2[-1])
+
+
+def pin_prefill_rows_subset_and_range_errors(oracle):
+    """A selected (token, head) subset equals the same rows of the full
+    result; a sequence whose chunk is longer than its length is an error
+    and its rows stay zero."""
+    lens, nq = (21, 18), (6, 4)
+    K, V, q, kc, vc, tables, qsl = _prefill_case(44, lens, nq)
+    full, err = _run_prefill(oracle, q, kc, vc, tables, lens, qsl, 2, 16, 0.2)
+    assert err == 0
+    rows = np.array([[0, 5], [3, 0], [9, 2], [7, 4]], np.int32)
+    part, err = _run_prefill(oracle, q, kc, vc, tables, lens, qsl, 2, 16, 0.2,
+                             rows=rows)
+    assert err == 0
+    for t, h in rows:
+        assert np.array_equal(part[t, h], full[t, h])
+    bad, err = _run_prefill(oracle, q, kc, vc, tables, (21, 3), qsl, 2, 16, 0.2)
+    assert err == 4 * 6
+    assert np.array_equal(bad[6:], np.zeros_like(bad[6:]))
+    assert np.array_equal(bad[:6], full[:6])
+
+
 ALL_PINS = [obj for name, obj in sorted(globals().items())
             if name.startswith("pin_") and callable(obj)]

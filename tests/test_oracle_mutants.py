@@ -24,8 +24,8 @@ MUTANTS = [
      "const int kvh = h % a->num_kv_heads;"),
     ("no_max_subtraction", "p[t] = exp(p[t] - mx);", "p[t] = exp(p[t]);"),
     ("no_normalisation", "double w = p[t] / denom;", "double w = p[t];"),
-    ("one_token_too_many", "const int L = a->seq_lens[b];",
-     "const int L = a->seq_lens[b] > 0 ? a->seq_lens[b] + 1 : 0;"),
+    ("one_token_too_many", "bb, hh, seq_lens[bb],",
+     "bb, hh, seq_lens[bb] > 0 ? seq_lens[bb] + 1 : 0,"),
     ("value_read_from_key_cache",
      "V[(size_t)t * d + i] = decode_elem(a->value_cache,",
      "V[(size_t)t * d + i] = decode_elem(a->key_cache,"),
@@ -36,8 +36,15 @@ MUTANTS = [
      "int32_t blk = a->block_tables[(size_t)b * a->max_blocks + j];",
      "int32_t blk = j;"),
     ("query_from_wrong_head",
-     "const uint16_t *qrow = a->q + ((size_t)b * a->num_heads + h) * d;",
-     "const uint16_t *qrow = a->q + ((size_t)b * a->num_heads + kvh) * d;"),
+     "errors += attend_row(&a, q + ((size_t)bb * num_heads + hh) * head_dim,",
+     "errors += attend_row(&a, q + ((size_t)bb * num_heads + hh / (num_heads / num_kv_heads)) * head_dim,"),
+    ("prefill_not_causal", "bb, hh, c + i + 1, orow", "bb, hh, seq_lens[bb], orow"),
+    ("prefill_causal_off_by_one", "bb, hh, c + i + 1, orow", "bb, hh, c + i, orow"),
+    ("prefill_history_ignored", "c = seq_lens[bb] - nq; /* tokens before this chunk */",
+     "c = 0;"),
+    ("prefill_query_row_of_sequence",
+     "errors += attend_row(&a, q + ((size_t)t * num_heads + hh) * head_dim,",
+     "errors += attend_row(&a, q + ((size_t)query_start_loc[bb] * num_heads + hh) * head_dim,"),
     ("fp8_scale_not_applied",
      "return oracle_e4m3_to_double(cache[idx]) * scale;",
      "return oracle_e4m3_to_double(cache[idx]);"),
