@@ -200,6 +200,38 @@ pkv_status paged_attention_decode(const void *q, const pkv_cache *cache,
                                   int32_t partition_tokens, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
+/* Prefill / chunked-prefill attention over a paged cache: several query
+ * tokens per sequence, causal within the sequence.  Source: vLLM concept
+ * page (compassingai.com), "Continuous Batching" (chunked prefill: a long
+ * prompt is cut into chunks that are interleaved with decode steps) and the
+ * "技术原理" pseudocode (gather, Q K^T scaled, softmax, times V).
+ *   q             bf16 [num_tokens, num_heads, head_dim], the query tokens
+ *                 of all sequences back to back.
+ *   query_start_loc int32 [batch + 1] (device): sequence b owns rows
+ *                 query_start_loc[b] .. query_start_loc[b+1] - 1 of q and
+ *                 out; n_b = that count (the output of
+ *                 paged_prepare_inputs has this layout).
+ *   seq_lens      int32 [batch] (device): c_b + n_b, where c_b tokens were
+ *                 cached by earlier steps; the chunk's own K/V must already
+ *                 be in the cache (paged_kv_write) as its last n_b tokens.
+ *   block_tables, max_blocks, scale: as for paged_attention_decode.
+ *   out           bf16 [num_tokens, num_heads, head_dim].
+ *   max_query_len host upper bound of every n_b (sizes the grid); rows of
+ *                 tokens past it are not computed.
+ * Query row i of sequence b is at position c_b + i and attends to the key
+ * positions 0 .. c_b + i; a one-token chunk is a decode step.  The cache
+ * must be bf16 (PKV_ERR_DTYPE otherwise) and num_heads / num_kv_heads at
+ * most 128.  Device-detected errors (n_b < 0, c_b < 0, a needed block id
+ * outside the pool, seq_lens[b] > 16 * max_blocks) are reported by
+ * pkv_check(); the affected rows are zeroed where they lie inside q. */
+pkv_status paged_attention_prefill(const void *q, const pkv_cache *cache,
+                                   const int32_t *block_tables,
+                                   int32_t max_blocks, const int32_t *seq_lens,
+                                   const int32_t *query_start_loc,
+                                   int32_t batch, int32_t num_heads,
+                                   int64_t num_tokens, float scale, void *out,
+                                   int32_t max_query_len, void *stream);
+
 /* Bytes of workspace paged_attention_decode needs for these arguments
  * (0 when no sequence can be split).  Host-only; never fails. */
 size_t paged_attention_workspace_bytes(int32_t batch, int32_t num_heads,

@@ -18,8 +18,9 @@ CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIBRARY = PKG / "libpagedkv.so"
 SOURCES = ["kv_write_zero.cu", "attention_decode.cu", "pkv_api.cu",
-           "attention_noalloc.cu", "kv_blocks.cu", "input_prep.cu"]
-HEADERS = ["pkv_device.cuh", "pkv_host.h"]
+           "attention_noalloc.cu", "kv_blocks.cu", "input_prep.cu",
+           "attention_prefill.cu"]
+HEADERS = ["pkv_device.cuh", "pkv_host.h", "tcgen05.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

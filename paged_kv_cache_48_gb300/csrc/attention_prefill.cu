@@ -1,0 +1,614 @@
+// attention_prefill.cu -- paged prefill / chunked-prefill attention on the
+// fifth-generation tensor cores (tcgen05, sm_103a).
+//
+// What it computes (vLLM concept page, "Continuous Batching" with chunked
+// prefill, and the PagedAttention pseudocode of its "技术原理" section):
+// sequence b brings n_b = query_start_loc[b+1] - query_start_loc[b] query
+// tokens whose K/V already sit in the cache as its last n_b tokens
+// (seq_lens[b] = c_b + n_b).  Query token i of the chunk is at position
+// c_b + i and attends to key positions 0 .. c_b + i, gathered through the
+// sequence's block table, with scores scale * q.k, a softmax and a weighted
+// sum of V.
+//
+// One CTA owns one (query tile, kv head, sequence).  Its 128 M-rows are the
+// (token, q head) pairs of TQ = floor(128 / g) consecutive chunk tokens times
+// the g q heads of the kv head's group (grouped-query attention packed along
+// M), so every K/V tile the CTA loads serves all of them.  Per key tile of
+// 128 positions (8 cache blocks):
+//   S  = Q K^T     tcgen05.mma, M 128 x N 128 x K head_dim, fp32 in TMEM
+//   P  = exp2(S * scale * log2 e - m)   four softmax warps, one TMEM lane
+//                  (one M-row) per thread, bf16 P written to shared memory
+//   O += P V       tcgen05.mma, M 128 x N head_dim x K 128, fp32 in TMEM
+// Warp roles: warp 0 issues the TMA loads (Q once; K and V one 16-token
+// block and 64-element head_dim slice per copy, at the block id the table
+// names), warp 1 owns TMEM and issues the MMAs from one thread, warps 2-5
+// run the online softmax and the epilogue.  S(i+1) is issued as soon as the
+// softmax warps have read S(i) into registers, so the tensor core computes
+// the next scores while the current probabilities are formed; O is rescaled
+// in TMEM only when a row's running maximum grows by more than 2^8 (the
+// probabilities stay below 256, exact in fp32 and safe in bf16; the final
+// division by l uses the same maximum, so the result is unchanged).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+#include "tcgen05.cuh"
+
+namespace pkv {
+
+__device__ unsigned long long g_err_prefill = 0ull;
+
+struct PrefillParams {
+  const int32_t *block_tables;     // [batch, max_blocks]
+  const int32_t *seq_lens;         // [batch]
+  const int32_t *query_start_loc;  // [batch + 1]
+  __nv_bfloat16 *out;              // [num_tokens, num_heads, head_dim]
+  long long num_tokens;
+  int batch, num_heads, num_kv_heads, group, tile_tokens;
+  int num_blocks, max_blocks;
+  float scale_log2;
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct PrefillCfg {
+  static constexpr int SLICES = D / 64;          // 64-element head_dim slices
+  static constexpr int SLICE_BYTES = 128 * 128;  // 128 rows x 128 bytes
+  static constexpr int STAGES = 2;
+  static constexpr int KEYS = 128;               // keys per tile (8 blocks)
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + SLICES * SLICE_BYTES;
+  static constexpr int V_OFF = K_OFF + STAGES * SLICES * SLICE_BYTES;
+  static constexpr int P_OFF = V_OFF + STAGES * SLICES * SLICE_BYTES;
+  static constexpr int BAR_OFF = P_OFF + 2 * SLICE_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + alignment slack
+  static constexpr uint32_t TMEM_COLS = 256;               // S: 0..127, O: 128..
+  static constexpr uint32_t S_COL = 0, O_COL = 128;
+  static constexpr int THREADS = 192;
+};
+
+struct PrefillBars {
+  uint64_t q_full;
+  uint64_t k_full[2], v_full[2], kv_empty[2];
+  uint64_t v_fix;   // last tile: stale V rows past the keys zeroed
+  uint64_t s_full;  // S(i) in TMEM
+  uint64_t s_free;  // S(i) read by the softmax warps
+  uint64_t p_full;  // P(i) in shared memory, O rescaled
+  uint64_t o_done;  // O += P(i) V(i) complete
+  uint32_t tmem_slot;
+  int abort_flag;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
+                                              const PrefillParams &p, volatile int *abort_flag) {
+  if (*abort_flag) return false;
+  if (mbar_wait_bounded(bar, parity, p.timeout_ns)) return true;
+  record_error(&g_err_prefill, PKV_ERR_TIMEOUT, -1);
+  *abort_flag = 1;
+  return false;
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+                         const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+  using C = PrefillCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  PrefillBars &bars = *reinterpret_cast<PrefillBars *>(smem + C::BAR_OFF);
+  volatile int *abort_flag = &bars.abort_flag;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int qt = gridDim.x - 1 - blockIdx.x;  // longest tiles first
+  const int g = p.group, TQ = p.tile_tokens;
+
+  grid_dependency_wait();
+  allow_dependent_launch();
+
+  const int q0 = p.query_start_loc[b];
+  const int n_b = p.query_start_loc[b + 1] - q0;
+  const int L = p.seq_lens[b];
+  const int c = L - n_b;  // tokens before this chunk
+  const int j0 = qt * TQ;
+  if (j0 >= n_b && n_b >= 0) return;  // this tile has no query token
+  const bool bad_seq = n_b < 0 || c < 0 || L > p.max_blocks * 16 || q0 < 0 ||
+                       (long long)q0 + n_b > p.num_tokens;
+  const int j_last = min(j0 + TQ, n_b) - 1;
+  const int kv_len = c + j_last + 1;  // keys any row of this tile sees
+  const int n_tiles = (kv_len + C::KEYS - 1) / C::KEYS;
+  const int nblk = (kv_len + 15) / 16;
+
+  // every block id this tile reads must be inside the pool
+  int bad = bad_seq ? 1 : 0;
+  if (!bad) {
+    const int32_t *row = p.block_tables + (size_t)b * p.max_blocks;
+    for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+      const int32_t id = row[j];
+      if (id < 0 || id >= p.num_blocks) {
+        bad = 1;
+        record_error(&g_err_prefill, PKV_ERR_RANGE, (long long)b * p.max_blocks + j);
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    record_error(&g_err_prefill, PKV_ERR_RANGE, b);
+  }
+  if (__syncthreads_or(bad)) {
+    // zero this tile's output rows of a valid token range, then leave
+    if (!bad_seq) {
+      const int rows = (j_last - j0 + 1) * g;
+      for (int idx = threadIdx.x; idx < rows * (D / 8); idx += blockDim.x) {
+        const int r = idx / (D / 8), ch = idx % (D / 8);
+        const long long tok = (long long)q0 + j0 + r / g;
+        const int h = kvh * g + r % g;
+        *reinterpret_cast<uint4 *>(p.out + ((size_t)tok * p.num_heads + h) * D + ch * 8) =
+            make_uint4(0, 0, 0, 0);
+      }
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.q_full, 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
+    }
+    mbar_init(&bars.v_fix, 1);
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.s_free, 4);
+    mbar_init(&bars.p_full, 4);
+    mbar_init(&bars.o_done, 1);
+    bars.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(smem_u32(&bars.tmem_slot), C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars.tmem_slot;
+
+  const uint32_t sQ = smem_u32(smem + C::Q_OFF);
+  const uint32_t sK = smem_u32(smem + C::K_OFF);
+  const uint32_t sV = smem_u32(smem + C::V_OFF);
+  const uint32_t sP = smem_u32(smem + C::P_OFF);
+  constexpr uint32_t STAGE_BYTES = C::SLICES * C::SLICE_BYTES;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const int32_t *row = p.block_tables + (size_t)b * p.max_blocks;
+    if (lane == 0) {
+      prefetch_tensormap(&qmap);
+      prefetch_tensormap(&kmap);
+      prefetch_tensormap(&vmap);
+      mbar_arrive_expect_tx(&bars.q_full, C::SLICES * 128 * g * TQ);
+      for (int s = 0; s < C::SLICES; ++s)
+        tc::tma_load_4d(sQ + s * C::SLICE_BYTES, &qmap, smem_u32(&bars.q_full), 0, kvh * g, s,
+                        q0 + j0);
+      const uint64_t pol = l2_policy_evict_normal();
+      for (int i = 0; i < n_tiles; ++i) {
+        const int st = i % C::STAGES;
+        if (i >= C::STAGES &&
+            !wait_or_abort(&bars.kv_empty[st], ((i / C::STAGES) - 1) & 1, p, abort_flag))
+          break;
+        const int nv = min(8, nblk - 8 * i);
+        const uint32_t bytes = nv * C::SLICES * 2048;
+        mbar_arrive_expect_tx(&bars.k_full[st], bytes);
+        for (int j = 0; j < nv; ++j) {
+          const int blk = row[8 * i + j];
+          for (int s = 0; s < C::SLICES; ++s)
+            tma_load_5d(smem + C::K_OFF + st * STAGE_BYTES + s * C::SLICE_BYTES + j * 2048, &kmap,
+                        &bars.k_full[st], 0, 0, kvh, s, blk, pol);
+        }
+        mbar_arrive_expect_tx(&bars.v_full[st], bytes);
+        for (int j = 0; j < nv; ++j) {
+          const int blk = row[8 * i + j];
+          for (int s = 0; s < C::SLICES; ++s)
+            tma_load_5d(smem + C::V_OFF + st * STAGE_BYTES + s * C::SLICE_BYTES + j * 2048, &vmap,
+                        &bars.v_full[st], 0, 0, kvh, s, blk, pol);
+        }
+      }
+    }
+    __syncwarp();
+    // The last tile's V rows past kv_len hold bytes that are not part of
+    // the sequence (stale cache contents or an older stage): zero them so
+    // that a zero probability never meets a NaN.
+    const int last = n_tiles - 1, st = last % C::STAGES;
+    if (wait_or_abort(&bars.v_full[st], (last / C::STAGES) & 1, p, abort_flag)) {
+      const int first = kv_len - last * C::KEYS;
+      uint8_t *vbase = smem + C::V_OFF + st * STAGE_BYTES;
+      for (int idx = first * 8 + lane; idx < C::KEYS * 8; idx += 32)
+        for (int s = 0; s < C::SLICES; ++s)
+          *reinterpret_cast<uint4 *>(vbase + s * C::SLICE_BYTES + idx * 16) =
+              make_uint4(0, 0, 0, 0);
+      tc::fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(smem_u32(&bars.v_fix));
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16_f32(128, C::KEYS, false, false);
+      constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
+      auto issue_s = [&](int i) {
+        const int st = i % C::STAGES;
+        const uint32_t kb = sK + st * STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k / 4) * C::SLICE_BYTES + (k % 4) * 32;
+          tc::mma_bf16_ss(tmem + C::S_COL,
+                          tc::smem_desc(sQ + off, 16, 1024, tc::kSwizzle128B),
+                          tc::smem_desc(kb + off, 16, 1024, tc::kSwizzle128B), idS, k > 0);
+        }
+        tc::mma_commit(smem_u32(&bars.s_full));
+      };
+      bool ok = wait_or_abort(&bars.q_full, 0, p, abort_flag) &&
+                wait_or_abort(&bars.k_full[0], 0, p, abort_flag);
+      if (ok) {
+        tc::fence_after_sync();
+        issue_s(0);
+      }
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int st = i % C::STAGES;
+        if (i + 1 < n_tiles) {
+          const int st1 = (i + 1) % C::STAGES;
+          ok = wait_or_abort(&bars.k_full[st1], ((i + 1) / C::STAGES) & 1, p, abort_flag) &&
+               wait_or_abort(&bars.s_free, i & 1, p, abort_flag);
+          if (!ok) break;
+          tc::fence_after_sync();
+          issue_s(i + 1);
+        }
+        ok = wait_or_abort(&bars.p_full, i & 1, p, abort_flag) &&
+             wait_or_abort(&bars.v_full[st], (i / C::STAGES) & 1, p, abort_flag) &&
+             (i + 1 < n_tiles || wait_or_abort(&bars.v_fix, 0, p, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t vb = sV + st * STAGE_BYTES;
+#pragma unroll
+        for (int k = 0; k < C::KEYS / 16; ++k) {
+          tc::mma_bf16_ss(
+              tmem + C::O_COL,
+              tc::smem_desc(sP + (k / 4) * C::SLICE_BYTES + (k % 4) * 32, 16, 1024,
+                            tc::kSwizzle128B),
+              tc::smem_desc(vb + k * 2048, C::SLICE_BYTES, 1024, tc::kSwizzle128B), idO,
+              (i > 0 || k > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(smem_u32(&bars.kv_empty[st]));
+        tc::mma_commit(smem_u32(&bars.o_done));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp % 4;
+    const int r = quarter * 32 + lane;  // M-row = TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int jr = j0 + r / g;
+    const bool row_valid = r < TQ * g && jr < n_b;
+    const int lim = row_valid ? c + jr : kv_len - 1;  // last key this row sees
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < n_tiles; ++i) {
+      if (!(ok = wait_or_abort(&bars.s_full, i & 1, p, abort_flag))) break;
+      tc::fence_after_sync();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tc::tmem_ld_32x32b_x32(lane_addr + C::S_COL + q * 32, sr[q]);
+      tc::tmem_wait_ld();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(smem_u32(&bars.s_free));
+
+      const int key0 = i * C::KEYS;
+      const bool full = key0 + C::KEYS - 1 <= lim;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float x = __uint_as_float(sr[q][e]) * p.scale_log2;
+          if (!full && key0 + q * 32 + e > lim) x = -INFINITY;
+          sr[q][e] = __float_as_uint(x);
+          mt = fmaxf(mt, x);
+        }
+      const bool rescale = mt > m_used + 8.f;
+      const float m_new = rescale ? mt : m_used;
+      const float alpha = rescale ? exp2f(m_used - m_new) : 1.f;  // 0 on the first tile
+      float ls = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float pe = exp2f(__uint_as_float(sr[q][e]) - m_new);
+          sr[q][e] = __float_as_uint(pe);
+          ls += pe;
+        }
+      l = l * alpha + ls;
+      m_used = m_new;
+      // P(i-1) V(i-1) must be done before P is overwritten and O rescaled
+      if (i > 0) {
+        if (!(ok = wait_or_abort(&bars.o_done, (i - 1) & 1, p, abort_flag))) break;
+        tc::fence_after_sync();
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            tc::tmem_ld_32x32b_x32(lane_addr + C::O_COL + q * 32, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tc::tmem_st_32x32b_x32(lane_addr + C::O_COL + q * 32, o);
+          }
+          tc::tmem_wait_st();
+        }
+      }
+      // P row r, bf16, 128-byte swizzled K-major: keys 64 s .. 64 s + 63 in
+      // slice s, 16-byte chunk ch of the row at chunk (ch ^ (r % 8)).
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int ch16 = q * 4 + h;  // 16-byte chunk index over 128 keys
+          const int s = ch16 / 8, ch = ch16 % 8;
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(sr[q][8 * h + 0]), __uint_as_float(sr[q][8 * h + 1]));
+          v.y = pack_bf16x2(__uint_as_float(sr[q][8 * h + 2]), __uint_as_float(sr[q][8 * h + 3]));
+          v.z = pack_bf16x2(__uint_as_float(sr[q][8 * h + 4]), __uint_as_float(sr[q][8 * h + 5]));
+          v.w = pack_bf16x2(__uint_as_float(sr[q][8 * h + 6]), __uint_as_float(sr[q][8 * h + 7]));
+          *reinterpret_cast<uint4 *>(smem + C::P_OFF + s * C::SLICE_BYTES + r * 128 +
+                                     ((ch ^ (r & 7)) * 16)) = v;
+        }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(smem_u32(&bars.p_full));
+    }
+    // epilogue: O / l -> bf16 rows of out
+    if (ok && wait_or_abort(&bars.o_done, (n_tiles - 1) & 1, p, abort_flag)) {
+      tc::fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16 *orow =
+          p.out + ((size_t)(q0 + jr) * p.num_heads + kvh * g + r % g) * D;
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t o[32];
+        tc::tmem_ld_32x32b_x32(lane_addr + C::O_COL + q * 32, o);
+        tc::tmem_wait_ld();
+        if (row_valid) {
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * h + 0]) * inv, __uint_as_float(o[8 * h + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * h + 2]) * inv, __uint_as_float(o[8 * h + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * h + 4]) * inv, __uint_as_float(o[8 * h + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * h + 6]) * inv, __uint_as_float(o[8 * h + 7]) * inv);
+            *reinterpret_cast<uint4 *>(orow + q * 32 + h * 8) = v;
+          }
+        }
+      }
+    }
+  }
+
+  // Before TMEM is released every MMA this CTA issued must have completed:
+  // the last o_done phase covers all of them (commits track every earlier
+  // MMA of the issuing thread).  On an abort, wait for it with a bound.
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    if (*abort_flag && lane == 0) mbar_wait_bounded(&bars.o_done, (n_tiles - 1) & 1, p.timeout_ns);
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 prefill_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// K or V cache: dims {64, 16 tokens, num_kv_heads, head_dim / 64, num_blocks},
+// box {64, 16, 1, 1, 1}: one 64-element head_dim slice of one kv head of
+// one block lands as 16 consecutive 128-byte swizzled rows.
+bool encode_prefill_cache_map(CUtensorMap *map, void *base, const pkv_cache *c) {
+  auto fn = prefill_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t row = (cuuint64_t)c->head_dim * 2;
+  cuuint64_t dims[5] = {64, 16, (cuuint64_t)c->num_kv_heads, (cuuint64_t)c->head_dim / 64,
+                        (cuuint64_t)c->num_blocks};
+  cuuint64_t strides[4] = {row * c->num_kv_heads, row, 128, row * c->num_kv_heads * 16};
+  cuuint32_t box[5] = {64, 16, 1, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Queries [num_tokens, num_heads, head_dim]: dims {64, num_heads,
+// head_dim / 64, num_tokens}, box {64, g, 1, TQ}: the g heads of one kv
+// head's group for TQ consecutive tokens, token-major, one 128-byte row per
+// (token, head).  Rows past num_tokens read as zeros.
+bool encode_query_map(CUtensorMap *map, const void *q, long long num_tokens, int num_heads,
+                      int head_dim, int g, int tq) {
+  auto fn = prefill_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t row = (cuuint64_t)head_dim * 2;
+  cuuint64_t dims[4] = {64, (cuuint64_t)num_heads, (cuuint64_t)head_dim / 64,
+                        (cuuint64_t)num_tokens};
+  cuuint64_t strides[3] = {row, 128, row * num_heads};
+  cuuint32_t box[4] = {64, (cuuint32_t)g, 1, (cuuint32_t)tq};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct PrefillMapEntry {
+  void *key_cache, *value_cache;
+  int32_t num_blocks, num_kv_heads, head_dim;
+  CUtensorMap k, v;
+};
+
+bool get_prefill_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
+  static std::mutex mu;
+  static PrefillMapEntry entries[8];
+  static int n_entries = 0, next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_entries; ++i) {
+    const PrefillMapEntry &e = entries[i];
+    if (e.key_cache == c->key_cache && e.value_cache == c->value_cache &&
+        e.num_blocks == c->num_blocks && e.num_kv_heads == c->num_kv_heads &&
+        e.head_dim == c->head_dim) {
+      *k = e.k;
+      *v = e.v;
+      return true;
+    }
+  }
+  PrefillMapEntry e;
+  e.key_cache = c->key_cache;
+  e.value_cache = c->value_cache;
+  e.num_blocks = c->num_blocks;
+  e.num_kv_heads = c->num_kv_heads;
+  e.head_dim = c->head_dim;
+  if (!encode_prefill_cache_map(&e.k, c->key_cache, c) ||
+      !encode_prefill_cache_map(&e.v, c->value_cache, c))
+    return false;
+  entries[next] = e;
+  next = (next + 1) % 8;
+  if (n_entries < 8) ++n_entries;
+  *k = e.k;
+  *v = e.v;
+  return true;
+}
+
+template <int D>
+pkv_status launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                          const PrefillParams &p, int q_tiles, cudaStream_t s) {
+  using C = PrefillCfg<D>;
+  static int configured[64] = {0};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev]) {
+      if (cudaFuncSetAttribute(paged_prefill_kernel<D>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::SMEM_BYTES) != cudaSuccess)
+        return PKV_ERR_CUDA;
+      configured[dev] = 1;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(q_tiles, p.num_kv_heads, p.batch);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D>, mq, mk, mv, p) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+}  // namespace
+
+unsigned long long read_and_clear_error_prefill(cudaStream_t s, cudaError_t *err) {
+  unsigned long long v = 0ull;
+  *err = cudaMemcpyFromSymbolAsync(&v, g_err_prefill, sizeof v, 0, cudaMemcpyDeviceToHost, s);
+  if (*err != cudaSuccess) return 0ull;
+  *err = cudaStreamSynchronize(s);
+  if (*err != cudaSuccess) return 0ull;
+  if (v) {
+    const unsigned long long zero = 0ull;
+    *err = cudaMemcpyToSymbolAsync(g_err_prefill, &zero, sizeof zero, 0, cudaMemcpyHostToDevice,
+                                   s);
+    if (*err == cudaSuccess) *err = cudaStreamSynchronize(s);
+  }
+  return v;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" pkv_status paged_attention_prefill(const void *q, const pkv_cache *cache,
+                                              const int32_t *block_tables, int32_t max_blocks,
+                                              const int32_t *seq_lens,
+                                              const int32_t *query_start_loc, int32_t batch,
+                                              int32_t num_heads, int64_t num_tokens, float scale,
+                                              void *out, int32_t max_query_len, void *stream) {
+  pkv_status st = validate_cache(cache);
+  if (st != PKV_OK) return st;
+  if (cache->dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (batch < 0 || num_heads <= 0 || max_blocks <= 0 || num_tokens < 0 || max_query_len < 0 ||
+      !std::isfinite(scale))
+    return PKV_ERR_ARG;
+  if (num_heads % cache->num_kv_heads) return PKV_ERR_SHAPE;
+  const int g = num_heads / cache->num_kv_heads;
+  if (g > 128) return PKV_ERR_SHAPE;
+  if (batch == 0 || num_tokens == 0 || max_query_len == 0) return PKV_OK;
+  if (!q || !out || !block_tables || !seq_lens || !query_start_loc) return PKV_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return PKV_ERR_ARG;
+  if (batch > 65535 || cache->num_kv_heads > 65535 || num_tokens > INT32_MAX) return PKV_ERR_ARG;
+  const int tq = 128 / g;
+  const int64_t q_tiles = ((int64_t)max_query_len + tq - 1) / tq;
+  if (q_tiles > INT32_MAX) return PKV_ERR_ARG;
+
+  CUtensorMap mq, mk, mv;
+  if (!encode_query_map(&mq, q, num_tokens, num_heads, cache->head_dim, g, tq))
+    return PKV_ERR_CUDA;
+  if (!get_prefill_maps(cache, &mk, &mv)) return PKV_ERR_CUDA;
+
+  PrefillParams p;
+  std::memset(&p, 0, sizeof p);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.query_start_loc = query_start_loc;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.num_tokens = num_tokens;
+  p.batch = batch;
+  p.num_heads = num_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.group = g;
+  p.tile_tokens = tq;
+  p.num_blocks = cache->num_blocks;
+  p.max_blocks = max_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = 2000000000ull;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cache->head_dim == 128 ? launch_prefill<128>(mq, mk, mv, p, (int)q_tiles, s)
+                                : launch_prefill<64>(mq, mk, mv, p, (int)q_tiles, s);
+}

@@ -43,12 +43,13 @@ using namespace pkv;
 extern "C" pkv_status pkv_check(void *stream, int64_t *detail) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (detail) *detail = -1;
-  cudaError_t e[4] = {cudaSuccess, cudaSuccess, cudaSuccess, cudaSuccess};
-  const unsigned long long words[4] = {
+  cudaError_t e[5] = {cudaSuccess, cudaSuccess, cudaSuccess, cudaSuccess, cudaSuccess};
+  const unsigned long long words[5] = {
       read_and_clear_error_write_zero(s, &e[0]), read_and_clear_error_attention(s, &e[1]),
-      read_and_clear_error_blocks(s, &e[2]), read_and_clear_error_prep(s, &e[3])};
+      read_and_clear_error_blocks(s, &e[2]), read_and_clear_error_prep(s, &e[3]),
+      read_and_clear_error_prefill(s, &e[4])};
   unsigned long long w = 0ull;
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 5; ++i) {
     if (e[i] != cudaSuccess) return PKV_ERR_CUDA;
     if (!w) w = words[i];
   }

@@ -25,5 +25,6 @@ unsigned long long read_and_clear_error_attention(cudaStream_t s,
                                                   cudaError_t *err);
 unsigned long long read_and_clear_error_blocks(cudaStream_t s, cudaError_t *err);
 unsigned long long read_and_clear_error_prep(cudaStream_t s, cudaError_t *err);
+unsigned long long read_and_clear_error_prefill(cudaStream_t s, cudaError_t *err);
 
 }  // namespace pkv

@@ -319,6 +319,44 @@ def paged_attention_decode(q: torch.Tensor, cache: PagedKVCache,
     return out
 
 
+def paged_attention_prefill(q: torch.Tensor, cache: PagedKVCache,
+                            block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                            query_start_loc: torch.Tensor, scale: float,
+                            max_query_len: int,
+                            out: Optional[torch.Tensor] = None,
+                            stream: Optional[torch.cuda.Stream] = None
+                            ) -> torch.Tensor:
+    """Prefill / chunked-prefill attention, causal within each sequence:
+    q [T, Hq, d] bf16 (all sequences' query tokens back to back),
+    query_start_loc int32 [B+1], seq_lens int32 [B] (cached tokens
+    including the chunk), max_query_len a host bound of the chunk lengths.
+    Returns out [T, Hq, d] bf16."""
+    dev = cache.device
+    _require(q, "q", torch.bfloat16, dev, 3)
+    _require(block_tables, "block_tables", torch.int32, dev, 2)
+    _require(seq_lens, "seq_lens", torch.int32, dev, 1)
+    _require(query_start_loc, "query_start_loc", torch.int32, dev, 1)
+    T, Hq, d = q.shape
+    B = seq_lens.shape[0]
+    if d != cache.head_dim or block_tables.shape[0] != B or \
+            query_start_loc.shape[0] != B + 1:
+        raise ValueError("q, block_tables, seq_lens, query_start_loc shapes "
+                         "do not match")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _require(out, "out", torch.bfloat16, dev, 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    st = _native.lib().paged_attention_prefill(
+        q.data_ptr(), ctypes.byref(cache.c_struct()), block_tables.data_ptr(),
+        block_tables.shape[1], seq_lens.data_ptr(), query_start_loc.data_ptr(),
+        B, Hq, T, float(scale), out.data_ptr(), int(max_query_len),
+        _stream_handle(stream, dev))
+    _native.check("paged_attention_prefill", st)
+    return out
+
+
 def pkv_check(stream: Optional[torch.cuda.Stream] = None, device=None):
     """Synchronise the stream and return (status, detail) from the device
     error word, clearing it."""

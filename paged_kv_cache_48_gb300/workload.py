@@ -371,3 +371,144 @@ CONFIGS = {
     "long_context": long_context,
     "fp8_recycle": fp8_recycle,
 }
+
+
+# ---------------------------------------------------------------------------
+# Chunked-prefill workloads (vLLM concept page, "Continuous Batching":
+# long prompts are cut into chunks that run inside ordinary steps).  Each
+# sequence has `history` tokens cached by earlier steps and brings a chunk of
+# `chunk` new tokens whose K/V the step writes before attention reads them.
+# ---------------------------------------------------------------------------
+
+@dataclass
+class PrefillWorkload:
+    """One chunked-prefill step: the cached history and the chunk's tokens."""
+    name: str
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    num_blocks: int
+    max_blocks: int
+    history: np.ndarray           # int32 [B] tokens cached before the step
+    chunk: np.ndarray             # int32 [B] query tokens of the step
+    block_tables: np.ndarray      # int32 [B, max_blocks], -1 = unused
+    q: np.ndarray                 # uint16 bf16 bits [T, Hq, d]
+    hist_k: np.ndarray            # uint16 [Th, Hkv, d] in the pool at set-up
+    hist_v: np.ndarray
+    hist_slots: np.ndarray        # int64 [Th]
+    step_k: np.ndarray            # uint16 [T, Hkv, d] written in the step
+    step_v: np.ndarray
+    step_slots: np.ndarray        # int64 [T]
+    init_key: np.ndarray          # uint8 pool bytes before set-up
+    init_value: np.ndarray
+    scale: float = 0.0
+    kv_dtype: str = "bf16"
+    block_size: int = BLOCK_SIZE
+    seed: int = 0
+
+    @property
+    def batch(self) -> int:
+        return int(self.chunk.shape[0])
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.chunk.sum())
+
+    @property
+    def seq_lens(self) -> np.ndarray:
+        return (self.history + self.chunk).astype(np.int32)
+
+    @property
+    def query_start_loc(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.chunk)]).astype(np.int32)
+
+    @property
+    def max_query_len(self) -> int:
+        return int(self.chunk.max()) if self.batch else 0
+
+    @property
+    def block_bytes(self) -> int:
+        return self.block_size * self.num_kv_heads * self.head_dim * 2
+
+    def attention_flops(self) -> int:
+        """Algorithmic multiply-add flops of the step's attention: every
+        (query token, q head) row sees history + i + 1 keys and spends
+        2 d flops on each score and 2 d on each value row."""
+        n = self.chunk.astype(np.int64)
+        keys = n * self.history.astype(np.int64) + n * (n + 1) // 2
+        return int(keys.sum()) * self.num_heads * 4 * self.head_dim
+
+
+def make_prefill_workload(name: str, history, chunk, num_heads: int,
+                          num_kv_heads: int, head_dim: int, seed: int,
+                          pool_factor: float = 1.2) -> PrefillWorkload:
+    """Draw a chunked-prefill step: blocks for every sequence taken from a
+    shuffled pool 20% larger than needed, the whole pool first filled with
+    0xFF bytes (bf16 NaN) so that any read of an unwritten slot shows,
+    history K/V drawn N(0,1) in place, the chunk's K/V and q drawn N(0,1)."""
+    rng = np.random.default_rng(seed)
+    history = np.asarray(history, dtype=np.int32)
+    chunk = np.asarray(chunk, dtype=np.int32)
+    lens = history + chunk
+    nblk = (lens + BLOCK_SIZE - 1) // BLOCK_SIZE
+    max_blocks = max(1, int(nblk.max()) if len(nblk) else 1)
+    num_blocks = max(8, int(np.ceil(pool_factor * int(nblk.sum()))))
+    pool = BlockPool(num_blocks, rng)
+    tables = np.full((len(lens), max_blocks), -1, dtype=np.int32)
+    for b, n in enumerate(nblk):
+        for j in range(int(n)):
+            tables[b, j] = pool.allocate()
+    Hkv, d = num_kv_heads, head_dim
+
+    def slots_of(b, lo, hi):
+        t = np.arange(lo, hi, dtype=np.int64)
+        return tables[b, t // BLOCK_SIZE].astype(np.int64) * BLOCK_SIZE + t % BLOCK_SIZE
+
+    hist_slots = np.concatenate([slots_of(b, 0, int(history[b]))
+                                 for b in range(len(lens))] or [np.zeros(0, np.int64)])
+    step_slots = np.concatenate([slots_of(b, int(history[b]), int(lens[b]))
+                                 for b in range(len(lens))] or [np.zeros(0, np.int64)])
+    Th, T = hist_slots.size, step_slots.size
+    pool_bytes = num_blocks * BLOCK_SIZE * Hkv * d * 2
+    return PrefillWorkload(
+        name=name, num_heads=num_heads, num_kv_heads=Hkv, head_dim=d,
+        num_blocks=num_blocks, max_blocks=max_blocks, history=history,
+        chunk=chunk, block_tables=tables,
+        q=_draw_bf16(rng, (T, num_heads, d)),
+        hist_k=_draw_bf16(rng, (Th, Hkv, d)), hist_v=_draw_bf16(rng, (Th, Hkv, d)),
+        hist_slots=hist_slots,
+        step_k=_draw_bf16(rng, (T, Hkv, d)), step_v=_draw_bf16(rng, (T, Hkv, d)),
+        step_slots=step_slots,
+        init_key=np.full(pool_bytes, 0xFF, dtype=np.uint8),
+        init_value=np.full(pool_bytes, 0xFF, dtype=np.uint8),
+        scale=1.0 / float(np.sqrt(d)), seed=seed)
+
+
+def prefill_8k(seed: int = 6, small: bool = False) -> PrefillWorkload:
+    """Prefill step of about 8K tokens (the vLLM v0.17.1 notes' prefill
+    batch size): 8 fresh prompts of 1024 tokens, Llama-8B shape (32 q /
+    8 kv heads, head_dim 128)."""
+    if small:
+        return make_prefill_workload("prefill_8k_small", [0, 0, 0],
+                                     [300, 129, 17], 32, 8, 128, seed)
+    return make_prefill_workload("prefill_8k", [0] * 8, [1024] * 8, 32, 8, 128,
+                                 seed)
+
+
+def chunked_prefill_8k(seed: int = 7, small: bool = False) -> PrefillWorkload:
+    """Chunked prefill of about 8K tokens: 8 chunks of 1024 tokens, each
+    after a history uniform in [1024, 7168] tokens, Llama-8B shape."""
+    rng = np.random.default_rng(seed)
+    if small:
+        hist = [int(x) for x in rng.integers(50, 600, 4)]
+        return make_prefill_workload("chunked_prefill_8k_small", hist,
+                                     [200, 37, 1, 130], 32, 8, 128, seed)
+    hist = [int(x) for x in rng.integers(1024, 7169, 8)]
+    return make_prefill_workload("chunked_prefill_8k", hist, [1024] * 8, 32, 8,
+                                 128, seed)
+
+
+PREFILL_CONFIGS = {
+    "prefill_8k": prefill_8k,
+    "chunked_prefill_8k": chunked_prefill_8k,
+}

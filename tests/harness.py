@@ -14,9 +14,9 @@ import torch
 
 import oracle
 from paged_kv_cache_48_gb300 import (PagedKVCache, paged_attention_decode,
-                                     paged_kv_write, paged_kv_zero_blocks,
-                                     pkv_check)
-from paged_kv_cache_48_gb300.workload import Workload
+                                     paged_attention_prefill, paged_kv_write,
+                                     paged_kv_zero_blocks, pkv_check)
+from paged_kv_cache_48_gb300.workload import PrefillWorkload, Workload
 
 # Tolerances of the parity bar: |gpu - ref| <= ATOL + RTOL * |ref| per
 # element, bf16 KV 1e-2 / 1e-2, fp8 KV 3e-2 / 3e-2.
@@ -133,3 +133,72 @@ def assert_close(gpu: np.ndarray, ref: np.ndarray, kv_dtype: str, mask=None):
         f"{int(bad.sum())} of {bad.size} elements out of tolerance; "
         f"max abs err {err.max():.3e}")
     return float(err.max())
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill
+# ---------------------------------------------------------------------------
+
+@dataclass
+class PrefillGpuState:
+    cache: PagedKVCache
+    q: torch.Tensor
+    tables: torch.Tensor
+    seq_lens: torch.Tensor
+    qsl: torch.Tensor
+    step_k: torch.Tensor
+    step_v: torch.Tensor
+    step_slots: torch.Tensor
+
+
+def upload_prefill(W: PrefillWorkload, device="cuda") -> PrefillGpuState:
+    """Pool bytes to the device and the history written through
+    paged_kv_write; the chunk's K/V stay pending for the step."""
+    shape = (W.num_blocks, W.block_size, W.num_kv_heads, W.head_dim)
+    kc = torch.from_numpy(W.init_key).view(torch.bfloat16).reshape(shape).to(device)
+    vc = torch.from_numpy(W.init_value).view(torch.bfloat16).reshape(shape).to(device)
+    cache = PagedKVCache(kc, vc, "bf16")
+    if W.hist_slots.size:
+        chunk = 1 << 18
+        for s in range(0, W.hist_slots.size, chunk):
+            e = min(W.hist_slots.size, s + chunk)
+            paged_kv_write(_u16_to_bf16(W.hist_k[s:e], device),
+                           _u16_to_bf16(W.hist_v[s:e], device),
+                           torch.from_numpy(W.hist_slots[s:e]).to(device), cache)
+    return PrefillGpuState(
+        cache=cache, q=_u16_to_bf16(W.q, device),
+        tables=torch.from_numpy(W.block_tables).to(device),
+        seq_lens=torch.from_numpy(W.seq_lens).to(device),
+        qsl=torch.from_numpy(W.query_start_loc).to(device),
+        step_k=_u16_to_bf16(W.step_k, device),
+        step_v=_u16_to_bf16(W.step_v, device),
+        step_slots=torch.from_numpy(W.step_slots).to(device))
+
+
+def gpu_prefill_step(W: PrefillWorkload, G: PrefillGpuState, out=None):
+    """One chunked-prefill step: write the chunk's K/V, then attend."""
+    if G.step_slots.numel():
+        paged_kv_write(G.step_k, G.step_v, G.step_slots, G.cache)
+    return paged_attention_prefill(G.q, G.cache, G.tables, G.seq_lens, G.qsl,
+                                   W.scale, max_query_len=W.max_query_len,
+                                   out=out)
+
+
+def oracle_prefill_cache(W: PrefillWorkload):
+    o = oracle.load()
+    kc = W.init_key.copy()
+    vc = W.init_value.copy()
+    for k, v, sl in ((W.hist_k, W.hist_v, W.hist_slots),
+                     (W.step_k, W.step_v, W.step_slots)):
+        assert o.kv_write(kc, vc, oracle.DTYPE_BF16, W.block_size,
+                          W.num_kv_heads, W.head_dim, 1.0, 1.0, k, v, sl) == 0
+    return kc, vc
+
+
+def oracle_prefill_out(W: PrefillWorkload, kc, vc, rows=None, n_threads=0):
+    out, err = oracle.load().attention_prefill(
+        W.q, kc, vc, oracle.DTYPE_BF16, 1.0, 1.0, W.block_size,
+        W.num_kv_heads, W.head_dim, W.block_tables, W.seq_lens,
+        W.query_start_loc, W.scale, rows=rows, n_threads=n_threads)
+    assert err == 0
+    return out

@@ -1,0 +1,146 @@
+"""Chunked-prefill attention on the tcgen05 path against the fp64 oracle.
+
+Every case writes the history and then the chunk's K/V through
+paged_kv_write into a pool whose unwritten bytes are 0xFF (bf16 NaN), runs
+paged_attention_prefill and compares every row with the oracle on the same
+seeded inputs (|gpu - ref| <= 1e-2 + 1e-2 |ref|).  Shapes span several
+128-key tiles, several query tiles, ragged tails, one-token chunks, empty
+chunks and group sizes 1, 4, 5 and 8.
+"""
+import numpy as np
+import pytest
+import torch
+
+import harness
+import oracle
+from paged_kv_cache_48_gb300 import (PagedKVCache, PagedKVError,
+                                     paged_attention_decode,
+                                     paged_attention_prefill, pkv_check)
+from paged_kv_cache_48_gb300 import workload as wl
+
+pytestmark = pytest.mark.gpu
+PKV_OK, PKV_ERR_DTYPE, PKV_ERR_RANGE = 0, 2, 5
+
+CASES = {
+    # name: (history, chunk, Hq, Hkv, d)
+    "mha_d64": ([0, 5, 40, 100], [150, 11, 1, 64], 8, 8, 64),
+    "gqa4_chunks": ([569, 393, 426, 543], [200, 37, 1, 130], 32, 8, 128),
+    "gqa4_prompts": ([0, 0, 0], [300, 129, 17], 32, 8, 128),
+    "gqa5": ([0, 200, 333], [77, 130, 26], 40, 8, 128),
+    "gqa8_long": ([1500, 0], [40, 257], 64, 8, 128),
+    "tile_edges": ([0, 128, 0, 112], [128, 128, 256, 16], 32, 8, 128),
+    "with_empty": ([10, 0, 64], [0, 33, 0], 32, 8, 64),
+}
+
+
+def _run_case(W):
+    G = harness.upload_prefill(W)
+    out = harness.gpu_prefill_step(W, G)
+    st, detail = pkv_check()
+    assert st == PKV_OK, (st, detail)
+    return out.float().cpu().numpy(), G
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_prefill_matches_oracle(name):
+    hist, chunk, Hq, Hkv, d = CASES[name]
+    W = wl.make_prefill_workload(name, hist, chunk, Hq, Hkv, d, seed=len(name))
+    gpu, _ = _run_case(W)
+    kc, vc = harness.oracle_prefill_cache(W)
+    ref = harness.oracle_prefill_out(W, kc, vc)
+    harness.assert_close(gpu, ref, "bf16")
+
+
+@pytest.mark.parametrize("cfg", ["prefill_8k", "chunked_prefill_8k"])
+def test_prefill_small_configs(cfg):
+    W = wl.PREFILL_CONFIGS[cfg](small=True)
+    gpu, _ = _run_case(W)
+    kc, vc = harness.oracle_prefill_cache(W)
+    harness.assert_close(gpu, harness.oracle_prefill_out(W, kc, vc), "bf16")
+
+
+def test_prefill_is_deterministic_and_chunking_invariant():
+    """Two runs are bitwise equal, and a 300-token prompt computed as one
+    chunk or as chunks of 200 + 100 gives bitwise-equal rows (each row's
+    arithmetic depends only on its own query and the fixed key tiles)."""
+    W = wl.make_prefill_workload("one", [0], [300], 32, 8, 128, seed=9)
+    a, G = _run_case(W)
+    b = paged_attention_prefill(G.q, G.cache, G.tables, G.seq_lens, G.qsl,
+                                W.scale, W.max_query_len).float().cpu().numpy()
+    assert np.array_equal(a, b)
+    # same cache, same queries, the prompt cut in two steps
+    qsl1 = torch.tensor([0, 200], dtype=torch.int32, device="cuda")
+    qsl2 = torch.tensor([0, 100], dtype=torch.int32, device="cuda")
+    o1 = paged_attention_prefill(G.q[:200].contiguous(), G.cache, G.tables,
+                                 torch.tensor([200], dtype=torch.int32, device="cuda"),
+                                 qsl1, W.scale, 200)
+    o2 = paged_attention_prefill(G.q[200:].contiguous(), G.cache, G.tables,
+                                 torch.tensor([300], dtype=torch.int32, device="cuda"),
+                                 qsl2, W.scale, 100)
+    assert pkv_check()[0] == PKV_OK
+    assert np.array_equal(torch.cat([o1, o2]).float().cpu().numpy(), a)
+
+
+def test_prefill_one_token_chunks_match_decode():
+    """Chunks of one token are decode steps: both kernels match the oracle
+    on the same cache."""
+    W = wl.make_prefill_workload("dec", [17, 300, 1023, 0], [1, 1, 1, 1], 32, 8,
+                                 128, seed=3)
+    gpu, G = _run_case(W)
+    dec = paged_attention_decode(G.q, G.cache, G.tables, G.seq_lens, W.scale,
+                                 max_seq_len=int(W.seq_lens.max()))
+    assert pkv_check()[0] == PKV_OK
+    kc, vc = harness.oracle_prefill_cache(W)
+    ref = harness.oracle_prefill_out(W, kc, vc)
+    harness.assert_close(gpu, ref, "bf16")
+    harness.assert_close(dec.float().cpu().numpy(), ref, "bf16")
+
+
+def test_prefill_bad_block_id_is_reported_and_rows_zeroed():
+    W = wl.make_prefill_workload("bad", [40, 0], [20, 30], 32, 8, 128, seed=4)
+    G = harness.upload_prefill(W)
+    harness.gpu_prefill_step(W, G)
+    assert pkv_check()[0] == PKV_OK
+    tables = W.block_tables.copy()
+    tables[1, 1] = W.num_blocks + 3
+    out = torch.full_like(G.q, 7.0)
+    paged_attention_prefill(G.q, G.cache, torch.from_numpy(tables).cuda(),
+                            G.seq_lens, G.qsl, W.scale, W.max_query_len, out=out)
+    st, detail = pkv_check()
+    assert st == PKV_ERR_RANGE and detail == 1 * W.max_blocks + 1
+    o = out.float().cpu().numpy()
+    assert np.all(o[20:] == 0.0)
+    kc, vc = harness.oracle_prefill_cache(W)
+    ref = harness.oracle_prefill_out(W, kc, vc)
+    harness.assert_close(o[:20], ref[:20], "bf16")
+
+
+def test_prefill_rejects_fp8_cache():
+    kc = torch.zeros((4, 16, 1, 64), dtype=torch.uint8, device="cuda")
+    cache = PagedKVCache(kc, kc.clone(), "fp8_e4m3", 1.0, 1.0)
+    q = torch.zeros((2, 1, 64), dtype=torch.bfloat16, device="cuda")
+    i32 = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
+    with pytest.raises(PagedKVError) as e:
+        paged_attention_prefill(q, cache, i32([[0]]), i32([2]), i32([0, 2]),
+                                0.1, 2)
+    assert e.value.status == PKV_ERR_DTYPE
+
+
+def test_prefill_full_size_sampled_rows():
+    """The full 8K-token chunked-prefill step in the bench's launch
+    configuration; rows sampled across every sequence (first, last and
+    seeded random tokens, all heads of a group) against the oracle."""
+    W = wl.chunked_prefill_8k()
+    gpu, _ = _run_case(W)
+    rng = np.random.default_rng(0)
+    qsl = W.query_start_loc
+    toks = set()
+    for b in range(W.batch):
+        toks.update([int(qsl[b]), int(qsl[b + 1]) - 1])
+        toks.update(int(t) for t in rng.integers(qsl[b], qsl[b + 1], 3))
+    rows = np.array([[t, h] for t in sorted(toks) for h in (0, 5, 17, 31)],
+                    np.int32)
+    kc, vc = harness.oracle_prefill_cache(W)
+    ref = harness.oracle_prefill_out(W, kc, vc, rows=rows)
+    harness.assert_close(gpu[rows[:, 0], rows[:, 1]], ref[rows[:, 0], rows[:, 1]],
+                         "bf16")
