@@ -53,7 +53,7 @@ def parse_args():
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
     ap.add_argument("--kernel", default="decode",
                     choices=["decode", "zero_blocks", "copy_blocks", "swap",
-                             "input_prep"],
+                             "input_prep", "prefill"],
                     help="decode: the decode step (headline); the others time "
                          "the block-movement entry points on the workload's "
                          "pool")
@@ -61,9 +61,12 @@ def parse_args():
                     help="replay the decode step as one captured CUDA graph")
     ap.add_argument("--workload", default="llama8b_gqa",
                     choices=["llama8b_gqa", "prefix_shared", "long_context",
-                             "fp8_recycle", "tiny_mha"],
-                    help="decode workload; the headline metric is quoted on "
-                         "llama8b_gqa, the others are reported for context")
+                             "fp8_recycle", "tiny_mha", "prefill_8k",
+                             "chunked_prefill_8k"],
+                    help="decode workload (the headline metric is quoted on "
+                         "llama8b_gqa, the others are reported for context); "
+                         "with --kernel prefill, prefill_8k or "
+                         "chunked_prefill_8k")
     return ap.parse_args()
 
 
@@ -99,6 +102,18 @@ def kernel_sha() -> str:
     for rel in KERNEL_SOURCES:
         h.update((ROOT / rel).read_bytes())
     return h.hexdigest()[:16]
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the burst figure, for a kernel
+    timed on its own."""
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return float(json.loads(p.read_text())["bf16_tflops"]), "measured"
+        except Exception:
+            pass
+    return 1900.0, "fallback"
 
 
 def measured_peak():
@@ -668,10 +683,149 @@ def run_input_prep(args):
     return 0
 
 
+def run_prefill(args):
+    """Chunked-prefill step (write the chunk's K/V, then causal attention
+    over the paged cache) on the 8K-token workloads: TFLOP/s of the
+    attention's algorithmic flops against the measured bf16 tensor peak,
+    with the oracle timed on a bounded sample of rows."""
+    import torch
+    import oracle
+    from paged_kv_cache_48_gb300 import (PagedKVCache, paged_attention_prefill,
+                                         paged_kv_write, pkv_check)
+    from paged_kv_cache_48_gb300 import workload as wl
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    name = args.workload if args.workload in wl.PREFILL_CONFIGS else \
+        "chunked_prefill_8k"
+    W = wl.PREFILL_CONFIGS[name]()
+    shape = (W.num_blocks, 16, W.num_kv_heads, W.head_dim)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16)
+    cache = PagedKVCache(
+        torch.from_numpy(W.init_key).view(torch.bfloat16).reshape(shape).to(dev),
+        torch.from_numpy(W.init_value).view(torch.bfloat16).reshape(shape).to(dev),
+        "bf16")
+    if W.hist_slots.size:
+        paged_kv_write(bf(W.hist_k).to(dev), bf(W.hist_v).to(dev),
+                       torch.from_numpy(W.hist_slots).to(dev), cache)
+    q, k, v = bf(W.q).to(dev), bf(W.step_k).to(dev), bf(W.step_v).to(dev)
+    slots = torch.from_numpy(W.step_slots).to(dev)
+    tables = torch.from_numpy(W.block_tables).to(dev)
+    lens = torch.from_numpy(W.seq_lens).to(dev)
+    qsl = torch.from_numpy(W.query_start_loc).to(dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    flops = W.attention_flops()
+    mql = W.max_query_len
+
+    def step():
+        paged_kv_write(k, v, slots, cache)
+        paged_attention_prefill(q, cache, tables, lens, qsl, W.scale, mql, out=out)
+
+    def attend():
+        paged_attention_prefill(q, cache, tables, lens, qsl, W.scale, mql, out=out)
+
+    def time_ms(fn, reps):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    reps = max(10, min(args.steps, 500))
+    with ClockSampler(0) as clk:
+        step_ms = time_ms(step, reps)
+        attn_ms = time_ms(attend, reps)
+    st, detail = pkv_check()
+    if st != 0:
+        raise RuntimeError(f"device error {st} at {detail}")
+
+    # end to end: pinned host inputs in, the output back, every step
+    h_q = bf(W.q).pin_memory()
+    h_k, h_v = bf(W.step_k).pin_memory(), bf(W.step_v).pin_memory()
+    h_slots = torch.from_numpy(W.step_slots).pin_memory()
+    h_out = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        q.copy_(h_q, non_blocking=True)
+        k.copy_(h_k, non_blocking=True)
+        v.copy_(h_v, non_blocking=True)
+        slots.copy_(h_slots, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_ms = time_ms(e2e_step, max(10, reps // 4))
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_slots))
+    d2h = h_out.numel() * h_out.element_size()
+
+    peak, peak_kind = measured_tensor_peak()
+    tflops = flops / (step_ms * 1e-3) / 1e12
+    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
+    line = {
+        "kernel": "prefill", "metric": f"chunked-prefill attention TFLOP/s ({name})",
+        "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": reps, "warmup": max(3, args.warmup),
+        "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": name, "batch": W.batch, "num_tokens": W.num_tokens,
+                   "history": [int(x) for x in W.history],
+                   "chunk": [int(x) for x in W.chunk],
+                   "num_heads": W.num_heads, "num_kv_heads": W.num_kv_heads,
+                   "head_dim": W.head_dim, "block_size": 16,
+                   "l2": "inputs larger than L2 (queries + pool)"},
+        "attention_flops": flops,
+        "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2),
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(attn_tflops / peak, 4), "traffic": None,
+                     "peak_kind": peak_kind + " bf16 burst",
+                     "kernel_ms": round(attn_ms, 4)},
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2),
+                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * reps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        kc, vc = W.init_key.copy(), W.init_value.copy()
+        o = oracle.load()
+        for kk, vv, sl in ((W.hist_k, W.hist_v, W.hist_slots),
+                           (W.step_k, W.step_v, W.step_slots)):
+            o.kv_write(kc, vc, oracle.DTYPE_BF16, 16, W.num_kv_heads,
+                       W.head_dim, 1.0, 1.0, kk, vv, sl)
+        rng = np.random.default_rng(1)
+        toks = rng.choice(W.num_tokens, size=128, replace=False)
+        rows = np.array([[t, h] for t in toks for h in range(W.num_heads)],
+                        np.int32)
+        qsl_h = W.query_start_loc
+        seq = np.searchsorted(qsl_h, toks, side="right") - 1
+        keys = (W.history[seq] + (toks - qsl_h[seq]) + 1).astype(np.int64)
+        sample_flops = int(keys.sum()) * W.num_heads * 4 * W.head_dim
+        t0 = time.perf_counter()
+        o.attention_prefill(W.q, kc, vc, oracle.DTYPE_BF16, 1.0, 1.0, 16,
+                            W.num_kv_heads, W.head_dim, W.block_tables,
+                            W.seq_lens, qsl_h, W.scale, rows=rows)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {
+            "value": round(sample_flops / dt / 1e12, 6), "unit": "TFLOP/s",
+            "cores": o.num_threads(0), "kind": "oracle",
+            "sample": f"{rows.shape[0]} (token, head) rows of 128 random tokens, "
+                      f"{dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.kernel == "input_prep":
         return run_input_prep(args)
+    if args.kernel == "prefill":
+        return run_prefill(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.kernel != "decode":

@@ -214,7 +214,8 @@ pkv_status paged_attention_decode(const void *q, const pkv_cache *cache,
  *   seq_lens      int32 [batch] (device): c_b + n_b, where c_b tokens were
  *                 cached by earlier steps; the chunk's own K/V must already
  *                 be in the cache (paged_kv_write) as its last n_b tokens.
- *   block_tables, max_blocks, scale: as for paged_attention_decode.
+ *   block_tables, max_blocks: as for paged_attention_decode.
+ *   scale         multiplies Q.K; must be positive (1/sqrt(head_dim)).
  *   out           bf16 [num_tokens, num_heads, head_dim].
  *   max_query_len host upper bound of every n_b (sizes the grid); rows of
  *                 tokens past it are not computed.

@@ -62,12 +62,16 @@ template <int D>
 struct PrefillCfg {
   static constexpr int SLICES = D / 64;          // 64-element head_dim slices
   static constexpr int SLICE_BYTES = 128 * 128;  // 128 rows x 128 bytes
-  static constexpr int STAGES = 2;
+  static constexpr int TILE_BYTES = SLICES * SLICE_BYTES;
+  // K is released as soon as Q K^T has read it, V only after P V: K runs
+  // one tile ahead of V and gets the deeper ring.
+  static constexpr int KSTAGES = 3;
+  static constexpr int VSTAGES = 2;
   static constexpr int KEYS = 128;               // keys per tile (8 blocks)
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + SLICES * SLICE_BYTES;
-  static constexpr int V_OFF = K_OFF + STAGES * SLICES * SLICE_BYTES;
-  static constexpr int P_OFF = V_OFF + STAGES * SLICES * SLICE_BYTES;
+  static constexpr int K_OFF = Q_OFF + TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + KSTAGES * TILE_BYTES;
+  static constexpr int P_OFF = V_OFF + VSTAGES * TILE_BYTES;
   static constexpr int BAR_OFF = P_OFF + 2 * SLICE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + alignment slack
   static constexpr uint32_t TMEM_COLS = 256;               // S: 0..127, O: 128..
@@ -77,7 +81,8 @@ struct PrefillCfg {
 
 struct PrefillBars {
   uint64_t q_full;
-  uint64_t k_full[2], v_full[2], kv_empty[2];
+  uint64_t k_full[3], k_empty[3];
+  uint64_t v_full[2], v_empty[2];
   uint64_t v_fix;   // last tile: stale V rows past the keys zeroed
   uint64_t s_full;  // S(i) in TMEM
   uint64_t s_free;  // S(i) read by the softmax warps
@@ -86,6 +91,12 @@ struct PrefillBars {
   uint32_t tmem_slot;
   int abort_flag;
 };
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
                                               const PrefillParams &p, volatile int *abort_flag) {
@@ -160,10 +171,13 @@ __global__ void __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.q_full, 1);
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < C::KSTAGES; ++s) {
       mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_empty[s], 1);
+    }
+    for (int s = 0; s < C::VSTAGES; ++s) {
       mbar_init(&bars.v_full[s], 1);
-      mbar_init(&bars.kv_empty[s], 1);
+      mbar_init(&bars.v_empty[s], 1);
     }
     mbar_init(&bars.v_fix, 1);
     mbar_init(&bars.s_full, 1);
@@ -186,7 +200,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sK = smem_u32(smem + C::K_OFF);
   const uint32_t sV = smem_u32(smem + C::V_OFF);
   const uint32_t sP = smem_u32(smem + C::P_OFF);
-  constexpr uint32_t STAGE_BYTES = C::SLICES * C::SLICE_BYTES;
+  constexpr uint32_t STAGE_BYTES = C::TILE_BYTES;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -200,35 +214,38 @@ __global__ void __launch_bounds__(192, 1)
         tc::tma_load_4d(sQ + s * C::SLICE_BYTES, &qmap, smem_u32(&bars.q_full), 0, kvh * g, s,
                         q0 + j0);
       const uint64_t pol = l2_policy_evict_normal();
-      for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % C::STAGES;
-        if (i >= C::STAGES &&
-            !wait_or_abort(&bars.kv_empty[st], ((i / C::STAGES) - 1) & 1, p, abort_flag))
-          break;
+      // K(i + 1) is issued before V(i): Q K^T of the next tile needs its
+      // keys while the current tile's probabilities are still being formed.
+      auto issue = [&](bool is_k, int i) -> bool {
+        const int stages = is_k ? C::KSTAGES : C::VSTAGES;
+        const int st = i % stages;
+        uint64_t *empty = is_k ? &bars.k_empty[st] : &bars.v_empty[st];
+        uint64_t *full = is_k ? &bars.k_full[st] : &bars.v_full[st];
+        if (i >= stages && !wait_or_abort(empty, ((i / stages) - 1) & 1, p, abort_flag))
+          return false;
         const int nv = min(8, nblk - 8 * i);
-        const uint32_t bytes = nv * C::SLICES * 2048;
-        mbar_arrive_expect_tx(&bars.k_full[st], bytes);
+        mbar_arrive_expect_tx(full, nv * C::SLICES * 2048);
+        uint8_t *dst = smem + (is_k ? C::K_OFF : C::V_OFF) + st * STAGE_BYTES;
         for (int j = 0; j < nv; ++j) {
           const int blk = row[8 * i + j];
           for (int s = 0; s < C::SLICES; ++s)
-            tma_load_5d(smem + C::K_OFF + st * STAGE_BYTES + s * C::SLICE_BYTES + j * 2048, &kmap,
-                        &bars.k_full[st], 0, 0, kvh, s, blk, pol);
+            tma_load_5d(dst + s * C::SLICE_BYTES + j * 2048, is_k ? &kmap : &vmap, full, 0, 0,
+                        kvh, s, blk, pol);
         }
-        mbar_arrive_expect_tx(&bars.v_full[st], bytes);
-        for (int j = 0; j < nv; ++j) {
-          const int blk = row[8 * i + j];
-          for (int s = 0; s < C::SLICES; ++s)
-            tma_load_5d(smem + C::V_OFF + st * STAGE_BYTES + s * C::SLICE_BYTES + j * 2048, &vmap,
-                        &bars.v_full[st], 0, 0, kvh, s, blk, pol);
-        }
+        return true;
+      };
+      bool go = issue(true, 0);
+      for (int i = 0; go && i < n_tiles; ++i) {
+        if (i + 1 < n_tiles) go = issue(true, i + 1);
+        go = go && issue(false, i);
       }
     }
     __syncwarp();
     // The last tile's V rows past kv_len hold bytes that are not part of
     // the sequence (stale cache contents or an older stage): zero them so
     // that a zero probability never meets a NaN.
-    const int last = n_tiles - 1, st = last % C::STAGES;
-    if (wait_or_abort(&bars.v_full[st], (last / C::STAGES) & 1, p, abort_flag)) {
+    const int last = n_tiles - 1, st = last % C::VSTAGES;
+    if (wait_or_abort(&bars.v_full[st], (last / C::VSTAGES) & 1, p, abort_flag)) {
       const int first = kv_len - last * C::KEYS;
       uint8_t *vbase = smem + C::V_OFF + st * STAGE_BYTES;
       for (int idx = first * 8 + lane; idx < C::KEYS * 8; idx += 32)
@@ -245,7 +262,7 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t idS = tc::idesc_bf16_f32(128, C::KEYS, false, false);
       constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
       auto issue_s = [&](int i) {
-        const int st = i % C::STAGES;
+        const int st = i % C::KSTAGES;
         const uint32_t kb = sK + st * STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
@@ -255,6 +272,7 @@ __global__ void __launch_bounds__(192, 1)
                           tc::smem_desc(kb + off, 16, 1024, tc::kSwizzle128B), idS, k > 0);
         }
         tc::mma_commit(smem_u32(&bars.s_full));
+        tc::mma_commit(smem_u32(&bars.k_empty[st]));
       };
       bool ok = wait_or_abort(&bars.q_full, 0, p, abort_flag) &&
                 wait_or_abort(&bars.k_full[0], 0, p, abort_flag);
@@ -263,17 +281,17 @@ __global__ void __launch_bounds__(192, 1)
         issue_s(0);
       }
       for (int i = 0; ok && i < n_tiles; ++i) {
-        const int st = i % C::STAGES;
+        const int st = i % C::VSTAGES;
         if (i + 1 < n_tiles) {
-          const int st1 = (i + 1) % C::STAGES;
-          ok = wait_or_abort(&bars.k_full[st1], ((i + 1) / C::STAGES) & 1, p, abort_flag) &&
+          const int st1 = (i + 1) % C::KSTAGES;
+          ok = wait_or_abort(&bars.k_full[st1], ((i + 1) / C::KSTAGES) & 1, p, abort_flag) &&
                wait_or_abort(&bars.s_free, i & 1, p, abort_flag);
           if (!ok) break;
           tc::fence_after_sync();
           issue_s(i + 1);
         }
         ok = wait_or_abort(&bars.p_full, i & 1, p, abort_flag) &&
-             wait_or_abort(&bars.v_full[st], (i / C::STAGES) & 1, p, abort_flag) &&
+             wait_or_abort(&bars.v_full[st], (i / C::VSTAGES) & 1, p, abort_flag) &&
              (i + 1 < n_tiles || wait_or_abort(&bars.v_fix, 0, p, abort_flag));
         if (!ok) break;
         tc::fence_after_sync();
@@ -287,7 +305,7 @@ __global__ void __launch_bounds__(192, 1)
               tc::smem_desc(vb + k * 2048, C::SLICE_BYTES, 1024, tc::kSwizzle128B), idO,
               (i > 0 || k > 0) ? 1u : 0u);
         }
-        tc::mma_commit(smem_u32(&bars.kv_empty[st]));
+        tc::mma_commit(smem_u32(&bars.v_empty[st]));
         tc::mma_commit(smem_u32(&bars.o_done));
       }
     }
@@ -314,37 +332,49 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) tc::mbar_arrive(smem_u32(&bars.s_free));
 
       const int key0 = i * C::KEYS;
-      const bool full = key0 + C::KEYS - 1 <= lim;
-      float mt = -INFINITY;
+      if (key0 + C::KEYS - 1 > lim) {
+        // keys past this row's last visible position are excluded by
+        // selection (a stale NaN in the cache becomes -inf, never a factor)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (key0 + q * 32 + e > lim) sr[q][e] = __float_as_uint(-INFINITY);
+      }
+      // Row maximum of the raw scores in eight independent chains (the
+      // scale is positive, so it commutes with the maximum).
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(sr[q][e]) * p.scale_log2;
-          if (!full && key0 + q * 32 + e > lim) x = -INFINITY;
-          sr[q][e] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
-        }
+        for (int e = 0; e < 32; ++e) mx[e % 8] = fmaxf(mx[e % 8], __uint_as_float(sr[q][e]));
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                       p.scale_log2;
       const bool rescale = mt > m_used + 8.f;
       const float m_new = rescale ? mt : m_used;
-      const float alpha = rescale ? exp2f(m_used - m_new) : 1.f;  // 0 on the first tile
-      float ls = 0.f;
+      const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;  // 0 on the first tile
+      float ls[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float pe = exp2f(__uint_as_float(sr[q][e]) - m_new);
+          const float pe = fast_exp2(fmaf(__uint_as_float(sr[q][e]), p.scale_log2, -m_new));
           sr[q][e] = __float_as_uint(pe);
-          ls += pe;
+          ls[e % 8] += pe;
         }
-      l = l * alpha + ls;
+      l = l * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
       m_used = m_new;
       // P(i-1) V(i-1) must be done before P is overwritten and O rescaled
       if (i > 0) {
         if (!(ok = wait_or_abort(&bars.o_done, (i - 1) & 1, p, abort_flag))) break;
         tc::fence_after_sync();
         if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll
+#pragma unroll 1
           for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
             tc::tmem_ld_32x32b_x32(lane_addr + C::O_COL + q * 32, o);
@@ -573,7 +603,7 @@ extern "C" pkv_status paged_attention_prefill(const void *q, const pkv_cache *ca
   if (st != PKV_OK) return st;
   if (cache->dtype != PKV_BF16) return PKV_ERR_DTYPE;
   if (batch < 0 || num_heads <= 0 || max_blocks <= 0 || num_tokens < 0 || max_query_len < 0 ||
-      !std::isfinite(scale))
+      !std::isfinite(scale) || !(scale > 0.f))
     return PKV_ERR_ARG;
   if (num_heads % cache->num_kv_heads) return PKV_ERR_SHAPE;
   const int g = num_heads / cache->num_kv_heads;
