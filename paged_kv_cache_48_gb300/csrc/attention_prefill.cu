@@ -10,24 +10,29 @@
 // sequence's block table, with scores scale * q.k, a softmax and a weighted
 // sum of V.
 //
-// One CTA owns one (query tile, kv head, sequence).  Its 128 M-rows are the
-// (token, q head) pairs of TQ = floor(128 / g) consecutive chunk tokens times
-// the g q heads of the kv head's group (grouped-query attention packed along
-// M), so every K/V tile the CTA loads serves all of them.  Per key tile of
-// 128 positions (8 cache blocks):
-//   S  = Q K^T     tcgen05.mma, M 128 x N 128 x K head_dim, fp32 in TMEM
-//   P  = exp2(S * scale * log2 e - m)   four softmax warps, one TMEM lane
-//                  (one M-row) per thread, bf16 P written to shared memory
-//   O += P V       tcgen05.mma, M 128 x N head_dim x K 128, fp32 in TMEM
+// One CTA owns two query tiles of one (kv head, sequence).  A tile's 128
+// M-rows are the (token, q head) pairs of TQ = floor(128 / g) consecutive
+// chunk tokens times the g q heads of the kv head's group (grouped-query
+// attention packed along M); the two tiles cover 2 TQ consecutive tokens
+// and share every K/V tile the CTA loads.  Per key tile of 128 positions
+// (8 cache blocks) and query tile t:
+//   S_t  = Q_t K^T   tcgen05.mma, M 128 x N 128 x K head_dim, fp32 in TMEM
+//   P_t  = exp2(S_t * scale * log2 e - m)   four softmax warps per tile,
+//                    one TMEM lane (one M-row) per thread; bf16 P written
+//                    back over the first 64 columns of S_t
+//   O_t += P_t V     tcgen05.mma with A read from TMEM, M 128 x N head_dim
+//                    x K 128, fp32 in TMEM
 // Warp roles: warp 0 issues the TMA loads (Q once; K and V one 16-token
 // block and 64-element head_dim slice per copy, at the block id the table
 // names), warp 1 owns TMEM and issues the MMAs from one thread, warps 2-5
-// run the online softmax and the epilogue.  S(i+1) is issued as soon as the
-// softmax warps have read S(i) into registers, so the tensor core computes
-// the next scores while the current probabilities are formed; O is rescaled
-// in TMEM only when a row's running maximum grows by more than 2^8 (the
-// probabilities stay below 256, exact in fp32 and safe in bf16; the final
-// division by l uses the same maximum, so the result is unchanged).
+// and 6-9 run the online softmax and the epilogue of tiles 0 and 1.  The
+// MMA order PV_0(i), S_0(i+1), PV_1(i), S_1(i+1) keeps the tensor core on
+// one tile while the other tile's probabilities are formed, and since
+// MMAs of one thread run in issue order, S_t(i+1) completing also means
+// PV_t(i) has read P_t(i) and finished updating O_t.  O is rescaled in TMEM
+// only when a row's running maximum grows by more than 2^8 (probabilities
+// stay below 256, exact in fp32 and safe in bf16; the final division by l
+// uses the same maximum, so the result is unchanged).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -63,31 +68,30 @@ struct PrefillCfg {
   static constexpr int SLICES = D / 64;          // 64-element head_dim slices
   static constexpr int SLICE_BYTES = 128 * 128;  // 128 rows x 128 bytes
   static constexpr int TILE_BYTES = SLICES * SLICE_BYTES;
-  // K is released as soon as Q K^T has read it, V only after P V: K runs
-  // one tile ahead of V and gets the deeper ring.
+  // K is released as soon as both Q K^T products have read it, V only after
+  // both P V products: K runs one tile ahead of V and gets the deeper ring.
   static constexpr int KSTAGES = 3;
   static constexpr int VSTAGES = 2;
   static constexpr int KEYS = 128;               // keys per tile (8 blocks)
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + TILE_BYTES;
+  static constexpr int Q_OFF = 0;                // two query tiles
+  static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + KSTAGES * TILE_BYTES;
-  static constexpr int P_OFF = V_OFF + VSTAGES * TILE_BYTES;
-  static constexpr int BAR_OFF = P_OFF + 2 * SLICE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + VSTAGES * TILE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + alignment slack
-  static constexpr uint32_t TMEM_COLS = 256;               // S: 0..127, O: 128..
-  static constexpr uint32_t S_COL = 0, O_COL = 128;
-  static constexpr int THREADS = 192;
+  // TMEM: tile t uses columns 256 t .. 256 t + 127 for S_t (P_t in the
+  // first 64) and 256 t + 128 .. for O_t.
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr int THREADS = 320;
 };
 
 struct PrefillBars {
   uint64_t q_full;
   uint64_t k_full[3], k_empty[3];
   uint64_t v_full[2], v_empty[2];
-  uint64_t v_fix;   // last tile: stale V rows past the keys zeroed
-  uint64_t s_full;  // S(i) in TMEM
-  uint64_t s_free;  // S(i) read by the softmax warps
-  uint64_t p_full;  // P(i) in shared memory, O rescaled
-  uint64_t o_done;  // O += P(i) V(i) complete
+  uint64_t v_fix;      // last tile: stale V rows past the keys zeroed
+  uint64_t s_full[2];  // S_t(i) in TMEM (and PV_t(i-1) complete)
+  uint64_t p_full[2];  // P_t(i) in TMEM, O_t rescaled
+  uint64_t o_done[2];  // O_t += P_t(i) V(i) complete
   uint32_t tmem_slot;
   int abort_flag;
 };
@@ -96,6 +100,20 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// O_t += P_t V with A = P_t read from TMEM (packed bf16 pairs, the even
+// element in the low half; 16 keys = 8 columns per MMA).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
@@ -108,7 +126,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                          const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
@@ -121,7 +139,7 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int b = blockIdx.z, kvh = blockIdx.y;
-  const int qt = gridDim.x - 1 - blockIdx.x;  // longest tiles first
+  const int qp = gridDim.x - 1 - blockIdx.x;  // longest tile pairs first
   const int g = p.group, TQ = p.tile_tokens;
 
   grid_dependency_wait();
@@ -131,16 +149,17 @@ __global__ void __launch_bounds__(192, 1)
   const int n_b = p.query_start_loc[b + 1] - q0;
   const int L = p.seq_lens[b];
   const int c = L - n_b;  // tokens before this chunk
-  const int j0 = qt * TQ;
-  if (j0 >= n_b && n_b >= 0) return;  // this tile has no query token
+  const int j0 = qp * 2 * TQ;
+  if (j0 >= n_b && n_b >= 0) return;  // this pair has no query token
   const bool bad_seq = n_b < 0 || c < 0 || L > p.max_blocks * 16 || q0 < 0 ||
                        (long long)q0 + n_b > p.num_tokens;
-  const int j_last = min(j0 + TQ, n_b) - 1;
-  const int kv_len = c + j_last + 1;  // keys any row of this tile sees
+  const bool has_b = j0 + TQ < n_b;   // the second tile holds a query token
+  const int j_last = min(j0 + 2 * TQ, n_b) - 1;
+  const int kv_len = c + j_last + 1;  // keys any row of the pair sees
   const int n_tiles = (kv_len + C::KEYS - 1) / C::KEYS;
   const int nblk = (kv_len + 15) / 16;
 
-  // every block id this tile reads must be inside the pool
+  // every block id the pair reads must be inside the pool
   int bad = bad_seq ? 1 : 0;
   if (!bad) {
     const int32_t *row = p.block_tables + (size_t)b * p.max_blocks;
@@ -155,7 +174,7 @@ __global__ void __launch_bounds__(192, 1)
     record_error(&g_err_prefill, PKV_ERR_RANGE, b);
   }
   if (__syncthreads_or(bad)) {
-    // zero this tile's output rows of a valid token range, then leave
+    // zero the pair's output rows of a valid token range, then leave
     if (!bad_seq) {
       const int rows = (j_last - j0 + 1) * g;
       for (int idx = threadIdx.x; idx < rows * (D / 8); idx += blockDim.x) {
@@ -180,10 +199,11 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&bars.v_empty[s], 1);
     }
     mbar_init(&bars.v_fix, 1);
-    mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.s_free, 4);
-    mbar_init(&bars.p_full, 4);
-    mbar_init(&bars.o_done, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.p_full[t], 4);
+      mbar_init(&bars.o_done[t], 1);
+    }
     bars.abort_flag = 0;
     fence_barrier_init();
   }
@@ -199,8 +219,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t sQ = smem_u32(smem + C::Q_OFF);
   const uint32_t sK = smem_u32(smem + C::K_OFF);
   const uint32_t sV = smem_u32(smem + C::V_OFF);
-  const uint32_t sP = smem_u32(smem + C::P_OFF);
-  constexpr uint32_t STAGE_BYTES = C::TILE_BYTES;
+  constexpr uint32_t TB = C::TILE_BYTES;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -209,10 +228,12 @@ __global__ void __launch_bounds__(192, 1)
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
-      mbar_arrive_expect_tx(&bars.q_full, C::SLICES * 128 * g * TQ);
-      for (int s = 0; s < C::SLICES; ++s)
-        tc::tma_load_4d(sQ + s * C::SLICE_BYTES, &qmap, smem_u32(&bars.q_full), 0, kvh * g, s,
-                        q0 + j0);
+      const int ntq = has_b ? 2 : 1;
+      mbar_arrive_expect_tx(&bars.q_full, ntq * C::SLICES * 128 * g * TQ);
+      for (int t = 0; t < ntq; ++t)
+        for (int s = 0; s < C::SLICES; ++s)
+          tc::tma_load_4d(sQ + t * TB + s * C::SLICE_BYTES, &qmap, smem_u32(&bars.q_full), 0,
+                          kvh * g, s, q0 + j0 + t * TQ);
       const uint64_t pol = l2_policy_evict_normal();
       // K(i + 1) is issued before V(i): Q K^T of the next tile needs its
       // keys while the current tile's probabilities are still being formed.
@@ -225,7 +246,7 @@ __global__ void __launch_bounds__(192, 1)
           return false;
         const int nv = min(8, nblk - 8 * i);
         mbar_arrive_expect_tx(full, nv * C::SLICES * 2048);
-        uint8_t *dst = smem + (is_k ? C::K_OFF : C::V_OFF) + st * STAGE_BYTES;
+        uint8_t *dst = smem + (is_k ? C::K_OFF : C::V_OFF) + st * TB;
         for (int j = 0; j < nv; ++j) {
           const int blk = row[8 * i + j];
           for (int s = 0; s < C::SLICES; ++s)
@@ -247,7 +268,7 @@ __global__ void __launch_bounds__(192, 1)
     const int last = n_tiles - 1, st = last % C::VSTAGES;
     if (wait_or_abort(&bars.v_full[st], (last / C::VSTAGES) & 1, p, abort_flag)) {
       const int first = kv_len - last * C::KEYS;
-      uint8_t *vbase = smem + C::V_OFF + st * STAGE_BYTES;
+      uint8_t *vbase = smem + C::V_OFF + st * TB;
       for (int idx = first * 8 + lane; idx < C::KEYS * 8; idx += 32)
         for (int s = 0; s < C::SLICES; ++s)
           *reinterpret_cast<uint4 *>(vbase + s * C::SLICE_BYTES + idx * 16) =
@@ -261,75 +282,74 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16_f32(128, C::KEYS, false, false);
       constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
-      auto issue_s = [&](int i) {
-        const int st = i % C::KSTAGES;
-        const uint32_t kb = sK + st * STAGE_BYTES;
+      const int ntq = has_b ? 2 : 1;
+      auto issue_s = [&](int t, int i) {
+        const uint32_t kb = sK + (i % C::KSTAGES) * TB;
+        const uint32_t qb = sQ + t * TB;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k / 4) * C::SLICE_BYTES + (k % 4) * 32;
-          tc::mma_bf16_ss(tmem + C::S_COL,
-                          tc::smem_desc(sQ + off, 16, 1024, tc::kSwizzle128B),
+          tc::mma_bf16_ss(tmem + 256 * t, tc::smem_desc(qb + off, 16, 1024, tc::kSwizzle128B),
                           tc::smem_desc(kb + off, 16, 1024, tc::kSwizzle128B), idS, k > 0);
         }
-        tc::mma_commit(smem_u32(&bars.s_full));
-        tc::mma_commit(smem_u32(&bars.k_empty[st]));
+        tc::mma_commit(smem_u32(&bars.s_full[t]));
+        if (t == ntq - 1) tc::mma_commit(smem_u32(&bars.k_empty[i % C::KSTAGES]));
+      };
+      auto issue_pv = [&](int t, int i) {
+        const uint32_t vb = sV + (i % C::VSTAGES) * TB;
+#pragma unroll
+        for (int k = 0; k < C::KEYS / 16; ++k)
+          mma_bf16_ts(tmem + 256 * t + 128, tmem + 256 * t + 8 * k,
+                      tc::smem_desc(vb + k * 2048, C::SLICE_BYTES, 1024, tc::kSwizzle128B), idO,
+                      (i > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(smem_u32(&bars.o_done[t]));
+        if (t == ntq - 1) tc::mma_commit(smem_u32(&bars.v_empty[i % C::VSTAGES]));
       };
       bool ok = wait_or_abort(&bars.q_full, 0, p, abort_flag) &&
                 wait_or_abort(&bars.k_full[0], 0, p, abort_flag);
       if (ok) {
         tc::fence_after_sync();
-        issue_s(0);
+        for (int t = 0; t < ntq; ++t) issue_s(t, 0);
       }
       for (int i = 0; ok && i < n_tiles; ++i) {
-        const int st = i % C::VSTAGES;
-        if (i + 1 < n_tiles) {
-          const int st1 = (i + 1) % C::KSTAGES;
-          ok = wait_or_abort(&bars.k_full[st1], ((i + 1) / C::KSTAGES) & 1, p, abort_flag) &&
-               wait_or_abort(&bars.s_free, i & 1, p, abort_flag);
-          if (!ok) break;
-          tc::fence_after_sync();
-          issue_s(i + 1);
-        }
-        ok = wait_or_abort(&bars.p_full, i & 1, p, abort_flag) &&
-             wait_or_abort(&bars.v_full[st], (i / C::VSTAGES) & 1, p, abort_flag) &&
+        const int vst = i % C::VSTAGES;
+        ok = wait_or_abort(&bars.v_full[vst], (i / C::VSTAGES) & 1, p, abort_flag) &&
              (i + 1 < n_tiles || wait_or_abort(&bars.v_fix, 0, p, abort_flag));
-        if (!ok) break;
-        tc::fence_after_sync();
-        const uint32_t vb = sV + st * STAGE_BYTES;
-#pragma unroll
-        for (int k = 0; k < C::KEYS / 16; ++k) {
-          tc::mma_bf16_ss(
-              tmem + C::O_COL,
-              tc::smem_desc(sP + (k / 4) * C::SLICE_BYTES + (k % 4) * 32, 16, 1024,
-                            tc::kSwizzle128B),
-              tc::smem_desc(vb + k * 2048, C::SLICE_BYTES, 1024, tc::kSwizzle128B), idO,
-              (i > 0 || k > 0) ? 1u : 0u);
+        const bool next = i + 1 < n_tiles;
+        for (int t = 0; ok && t < ntq; ++t) {
+          if (!(ok = wait_or_abort(&bars.p_full[t], i & 1, p, abort_flag))) break;
+          tc::fence_after_sync();
+          issue_pv(t, i);
+          if (next) {
+            if (t == 0 && !(ok = wait_or_abort(&bars.k_full[(i + 1) % C::KSTAGES],
+                                              ((i + 1) / C::KSTAGES) & 1, p, abort_flag)))
+              break;
+            tc::fence_after_sync();
+            issue_s(t, i + 1);
+          }
         }
-        tc::mma_commit(smem_u32(&bars.v_empty[st]));
-        tc::mma_commit(smem_u32(&bars.o_done));
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
+    const int t = (warp - 2) / 4;  // query tile of this warp
     const int quarter = warp % 4;
     const int r = quarter * 32 + lane;  // M-row = TMEM lane
-    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int jr = j0 + r / g;
+    const uint32_t lane_addr = tmem + 256 * t + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t s_addr = lane_addr, o_addr = lane_addr + 128;
+    const int jr = j0 + t * TQ + r / g;
     const bool row_valid = r < TQ * g && jr < n_b;
     const int lim = row_valid ? c + jr : kv_len - 1;  // last key this row sees
     float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      if (!(ok = wait_or_abort(&bars.s_full, i & 1, p, abort_flag))) break;
+    bool ok = t == 0 || has_b;
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      if (!(ok = wait_or_abort(&bars.s_full[t], i & 1, p, abort_flag))) break;
       tc::fence_after_sync();
       uint32_t sr[4][32];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tc::tmem_ld_32x32b_x32(lane_addr + C::S_COL + q * 32, sr[q]);
+      for (int q = 0; q < 4; ++q) tc::tmem_ld_32x32b_x32(s_addr + q * 32, sr[q]);
       tc::tmem_wait_ld();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(smem_u32(&bars.s_free));
 
       const int key0 = i * C::KEYS;
       if (key0 + C::KEYS - 1 > lim) {
@@ -359,64 +379,48 @@ __global__ void __launch_bounds__(192, 1)
       float ls[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+      // P as packed bf16 pairs, written in place over the consumed scores
 #pragma unroll
       for (int q = 0; q < 4; ++q)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float pe = fast_exp2(fmaf(__uint_as_float(sr[q][e]), p.scale_log2, -m_new));
-          sr[q][e] = __float_as_uint(pe);
-          ls[e % 8] += pe;
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[q][e]), p.scale_log2, -m_new));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[q][e + 1]), p.scale_log2, -m_new));
+          ls[e % 8] += p0;
+          ls[(e + 1) % 8] += p1;
+          sr[q][e / 2] = pack_bf16x2(p0, p1);
         }
       l = l * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
       m_used = m_new;
-      // P(i-1) V(i-1) must be done before P is overwritten and O rescaled
-      if (i > 0) {
-        if (!(ok = wait_or_abort(&bars.o_done, (i - 1) & 1, p, abort_flag))) break;
-        tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, rescale)) {
+      // s_full(i) also means PV_t(i-1) is complete: O_t may be rescaled
+      if (i > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t o[32];
-            tc::tmem_ld_32x32b_x32(lane_addr + C::O_COL + q * 32, o);
-            tc::tmem_wait_ld();
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t o[32];
+          tc::tmem_ld_32x32b_x32(o_addr + q * 32, o);
+          tc::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tc::tmem_st_32x32b_x32(lane_addr + C::O_COL + q * 32, o);
-          }
-          tc::tmem_wait_st();
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tc::tmem_st_32x32b_x32(o_addr + q * 32, o);
         }
       }
-      // P row r, bf16, 128-byte swizzled K-major: keys 64 s .. 64 s + 63 in
-      // slice s, 16-byte chunk ch of the row at chunk (ch ^ (r % 8)).
+      // P_t over the first 64 columns of S_t
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int ch16 = q * 4 + h;  // 16-byte chunk index over 128 keys
-          const int s = ch16 / 8, ch = ch16 % 8;
-          uint4 v;
-          v.x = pack_bf16x2(__uint_as_float(sr[q][8 * h + 0]), __uint_as_float(sr[q][8 * h + 1]));
-          v.y = pack_bf16x2(__uint_as_float(sr[q][8 * h + 2]), __uint_as_float(sr[q][8 * h + 3]));
-          v.z = pack_bf16x2(__uint_as_float(sr[q][8 * h + 4]), __uint_as_float(sr[q][8 * h + 5]));
-          v.w = pack_bf16x2(__uint_as_float(sr[q][8 * h + 6]), __uint_as_float(sr[q][8 * h + 7]));
-          *reinterpret_cast<uint4 *>(smem + C::P_OFF + s * C::SLICE_BYTES + r * 128 +
-                                     ((ch ^ (r & 7)) * 16)) = v;
-        }
-      tc::fence_proxy_async_smem();
+      for (int q = 0; q < 4; ++q) tc::tmem_st_32x32b_x16(s_addr + 16 * q, sr[q]);
+      tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(smem_u32(&bars.p_full));
+      if (lane == 0) tc::mbar_arrive(smem_u32(&bars.p_full[t]));
     }
-    // epilogue: O / l -> bf16 rows of out
-    if (ok && wait_or_abort(&bars.o_done, (n_tiles - 1) & 1, p, abort_flag)) {
+    // epilogue: O_t / l -> bf16 rows of out
+    if (ok && wait_or_abort(&bars.o_done[t], (n_tiles - 1) & 1, p, abort_flag)) {
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16 *orow =
-          p.out + ((size_t)(q0 + jr) * p.num_heads + kvh * g + r % g) * D;
+      __nv_bfloat16 *orow = p.out + ((size_t)(q0 + jr) * p.num_heads + kvh * g + r % g) * D;
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         uint32_t o[32];
-        tc::tmem_ld_32x32b_x32(lane_addr + C::O_COL + q * 32, o);
+        tc::tmem_ld_32x32b_x32(o_addr + q * 32, o);
         tc::tmem_wait_ld();
         if (row_valid) {
 #pragma unroll
@@ -434,12 +438,14 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   // Before TMEM is released every MMA this CTA issued must have completed:
-  // the last o_done phase covers all of them (commits track every earlier
-  // MMA of the issuing thread).  On an abort, wait for it with a bound.
+  // the softmax warps waited for the last P V of their tile, and the
+  // commits behind it track every earlier MMA.  On an abort, wait for the
+  // last commit with a bound.
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 1) {
-    if (*abort_flag && lane == 0) mbar_wait_bounded(&bars.o_done, (n_tiles - 1) & 1, p.timeout_ns);
+    if (*abort_flag && lane == 0)
+      mbar_wait_bounded(&bars.o_done[has_b ? 1 : 0], (n_tiles - 1) & 1, p.timeout_ns);
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, C::TMEM_COLS);
@@ -614,7 +620,7 @@ extern "C" pkv_status paged_attention_prefill(const void *q, const pkv_cache *ca
     return PKV_ERR_ARG;
   if (batch > 65535 || cache->num_kv_heads > 65535 || num_tokens > INT32_MAX) return PKV_ERR_ARG;
   const int tq = 128 / g;
-  const int64_t q_tiles = ((int64_t)max_query_len + tq - 1) / tq;
+  const int64_t q_tiles = ((int64_t)max_query_len + 2 * tq - 1) / (2 * tq);  // tile pairs
   if (q_tiles > INT32_MAX) return PKV_ERR_ARG;
 
   CUtensorMap mq, mk, mv;
