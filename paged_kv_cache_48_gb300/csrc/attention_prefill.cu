@@ -118,6 +118,7 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
                                               const PrefillParams &p, volatile int *abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
   if (*abort_flag) return false;
   if (mbar_wait_bounded(bar, parity, p.timeout_ns)) return true;
   record_error(&g_err_prefill, PKV_ERR_TIMEOUT, -1);
@@ -283,25 +284,29 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idS = tc::idesc_bf16_f32(128, C::KEYS, false, false);
       constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
       const int ntq = has_b ? 2 : 1;
+      // Descriptors are built once; stepping K adds the byte offset / 16 to
+      // the start-address field (bits 0-13), which never carries out.
+      const uint64_t q_desc0 = tc::smem_desc(sQ, 16, 1024, tc::kSwizzle128B);
+      const uint64_t k_desc0 = tc::smem_desc(sK, 16, 1024, tc::kSwizzle128B);
+      const uint64_t v_desc0 = tc::smem_desc(sV, C::SLICE_BYTES, 1024, tc::kSwizzle128B);
       auto issue_s = [&](int t, int i) {
-        const uint32_t kb = sK + (i % C::KSTAGES) * TB;
-        const uint32_t qb = sQ + t * TB;
+        const uint64_t qd = q_desc0 + ((t * TB) >> 4);
+        const uint64_t kd = k_desc0 + (((i % C::KSTAGES) * TB) >> 4);
+        const uint32_t d = tmem + 256 * t;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k / 4) * C::SLICE_BYTES + (k % 4) * 32;
-          tc::mma_bf16_ss(tmem + 256 * t, tc::smem_desc(qb + off, 16, 1024, tc::kSwizzle128B),
-                          tc::smem_desc(kb + off, 16, 1024, tc::kSwizzle128B), idS, k > 0);
+          const uint32_t off = ((k / 4) * C::SLICE_BYTES + (k % 4) * 32) >> 4;
+          tc::mma_bf16_ss(d, qd + off, kd + off, idS, k > 0);
         }
         tc::mma_commit(smem_u32(&bars.s_full[t]));
         if (t == ntq - 1) tc::mma_commit(smem_u32(&bars.k_empty[i % C::KSTAGES]));
       };
       auto issue_pv = [&](int t, int i) {
-        const uint32_t vb = sV + (i % C::VSTAGES) * TB;
+        const uint64_t vd = v_desc0 + (((i % C::VSTAGES) * TB) >> 4);
+        const uint32_t d = tmem + 256 * t + 128, a = tmem + 256 * t;
 #pragma unroll
         for (int k = 0; k < C::KEYS / 16; ++k)
-          mma_bf16_ts(tmem + 256 * t + 128, tmem + 256 * t + 8 * k,
-                      tc::smem_desc(vb + k * 2048, C::SLICE_BYTES, 1024, tc::kSwizzle128B), idO,
-                      (i > 0 || k > 0) ? 1u : 0u);
+          mma_bf16_ts(d, a + 8 * k, vd + ((k * 2048) >> 4), idO, (i > 0 || k > 0) ? 1u : 0u);
         tc::mma_commit(smem_u32(&bars.o_done[t]));
         if (t == ntq - 1) tc::mma_commit(smem_u32(&bars.v_empty[i % C::VSTAGES]));
       };
