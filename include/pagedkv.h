@@ -233,6 +233,49 @@ pkv_status paged_attention_prefill(const void *q, const pkv_cache *cache,
                                    int64_t num_tokens, float scale, void *out,
                                    int32_t max_query_len, void *stream);
 
+/* Cascade (shared-prefix) decode: the same result as
+ * paged_attention_decode, computed with each group's shared prefix read
+ * once for all of the group's sequences.  Source: vLLM internals
+ * (naphjohn.github.io), §1.1-1.2 and Figure 1 (sequences whose prompts
+ * share a prefix point at the same physical blocks, refcounted) and the
+ * vLLM concept page's PagedAttention pseudocode; the two-pass evaluation is
+ * this library's (the pages describe the sharing, not a kernel for it).
+ *   group_start   int32 [num_groups + 1] (device): group G is sequences
+ *                 group_start[G] .. group_start[G+1] - 1 (consecutive rows
+ *                 of q, block_tables, seq_lens); groups must not overlap;
+ *                 sequences outside every group are attended in full.
+ *   prefix_len    int32 [num_groups] (device): tokens of G's shared prefix,
+ *                 a multiple of 16, at most max_prefix_len; every member's
+ *                 table must start with the same prefix_len / 16 block ids
+ *                 and every member must be at least that long.
+ *   max_group_size, max_prefix_len  host bounds (size the prefix grid).
+ *   workspace     at least paged_attention_cascade_workspace_bytes(...),
+ *                 256-byte aligned.
+ *   Other arguments as for paged_attention_decode; scale must be positive
+ *   and the cache bf16 (PKV_ERR_DTYPE otherwise).
+ * Pass 1 (tensor cores) attends each group's member queries to its prefix,
+ * 512 tokens per partition; pass 2 attends each sequence to its own
+ * tokens; a log-sum-exp merge combines the partials.  A group whose
+ * members' tables or lengths break the contract is reported by pkv_check()
+ * and its members are attended in full, so the output stays correct. */
+pkv_status paged_attention_decode_cascade(
+    const void *q, const pkv_cache *cache, const int32_t *block_tables,
+    int32_t max_blocks, const int32_t *seq_lens, int32_t batch,
+    int32_t num_heads, const int32_t *group_start, const int32_t *prefix_len,
+    int32_t num_groups, int32_t max_group_size, int32_t max_prefix_len,
+    float scale, void *out, int32_t max_seq_len, int32_t partition_tokens,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of workspace paged_attention_decode_cascade needs (0 on invalid
+ * arguments).  Host-only. */
+size_t paged_attention_cascade_workspace_bytes(int32_t batch,
+                                               int32_t num_heads,
+                                               int32_t num_kv_heads,
+                                               int32_t head_dim,
+                                               int32_t max_seq_len,
+                                               int32_t max_prefix_len,
+                                               int32_t partition_tokens);
+
 /* Bytes of workspace paged_attention_decode needs for these arguments
  * (0 when no sequence can be split).  Host-only; never fails. */
 size_t paged_attention_workspace_bytes(int32_t batch, int32_t num_heads,

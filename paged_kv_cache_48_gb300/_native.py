@@ -62,6 +62,14 @@ _SIGNATURES = {
         _P, ctypes.POINTER(PkvCache), _P, ctypes.c_int32, _P, _P,
         ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, _P,
         ctypes.c_int32, _P]),
+    "paged_attention_decode_cascade": (ctypes.c_int, [
+        _P, ctypes.POINTER(PkvCache), _P, ctypes.c_int32, _P, ctypes.c_int32,
+        ctypes.c_int32, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_float, _P, ctypes.c_int32, ctypes.c_int32, _P, ctypes.c_size_t,
+        _P]),
+    "paged_attention_cascade_workspace_bytes": (ctypes.c_size_t, [
+        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32]),
     "paged_attention_decode_noalloc": (ctypes.c_int, [
         _P, ctypes.POINTER(PkvCache), _P, ctypes.c_int32, _P, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_float, _P, ctypes.c_int32, ctypes.c_int32,

@@ -57,7 +57,25 @@ struct DecodeParams {
   float scale_log2;  // scale * log2(e) (* k_scale for fp8)
   float v_scale;     // 1 for bf16
   unsigned long long timeout_ns;
+  int32_t grid_parts;  // partition CTAs per (kv head group, sequence)
+  // Shared-prefix (cascade) decode: sequence b starts at token seq_start[b]
+  // (its group's prefix, already reduced into merge slots
+  // 0 .. ceil(seq_start[b] / prefix_part_tokens) - 1); its own partitions
+  // follow in the next slots.  nullptr = every sequence starts at 0.
+  const int32_t *seq_start;
+  int32_t prefix_part_tokens;
 };
+
+// First token this launch attends to in sequence b (a multiple of 16 inside
+// [0, L]; anything else reads as 0) and the merge slots before its first
+// partition.
+__device__ __forceinline__ void suffix_range(const DecodeParams &p, int b, int L, int *start,
+                                             int *slot_base) {
+  int st = p.seq_start ? __ldg(p.seq_start + b) : 0;
+  if (st < 0 || st > L || (st & 15)) st = 0;
+  *start = st;
+  *slot_base = st > 0 ? (st + p.prefix_part_tokens - 1) / p.prefix_part_tokens : 0;
+}
 
 template <bool FP8, int D>
 struct Cfg {
@@ -361,9 +379,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
       L = clamp_len(L, cap);
     }
   }
-  const int nparts = L <= p.part_tokens ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+  int start, slot_base;
+  suffix_range(p, b, L, &start, &slot_base);
+  const int Ls = L - start;
+  const int nparts = Ls <= p.part_tokens ? 1 : (Ls + p.part_tokens - 1) / p.part_tokens;
   if (part >= nparts) return;
-  const int tok0 = part * p.part_tokens;  // multiple of 16
+  const int tok0 = start + part * p.part_tokens;  // multiple of 16
   const int tok1 = min(L, tok0 + p.part_tokens);
   const int blk0 = tok0 >> 4;
   const int nblk = (tok1 - tok0 + 15) >> 4;
@@ -467,11 +488,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     }
     const float res = lsum > 0.f ? acc / lsum * p.v_scale : 0.f;
     const size_t r = row0 + h;
-    if (nparts == 1) {
+    if (nparts == 1 && slot_base == 0) {
       p.out[r * D + d] = __float2bfloat16_rn(res);
     } else {
-      p.part_o[(r * p.max_parts + part) * D + d] = res;
-      if (d == 0) p.part_ml[r * p.max_parts + part] = make_float2(M, lsum);
+      const size_t slot = r * p.max_parts + slot_base + part;
+      p.part_o[slot * D + d] = res;
+      if (d == 0) p.part_ml[slot] = make_float2(M, lsum);
     }
   }
 }
@@ -493,7 +515,11 @@ __global__ void __launch_bounds__(256) paged_decode_merge_kernel(const DecodePar
   const int b = (int)(row / p.num_heads);
   const int cap = min(p.max_blocks * 16, p.max_seq_len);
   const int L = clamp_len(__ldg(p.seq_lens + b), cap);
-  const int nparts = L <= p.part_tokens ? 1 : (L + p.part_tokens - 1) / p.part_tokens;
+  int start, slot_base;
+  suffix_range(p, b, L, &start, &slot_base);
+  const int Ls = L - start;
+  const int nparts =
+      slot_base + (Ls <= p.part_tokens ? 1 : (Ls + p.part_tokens - 1) / p.part_tokens);
   if (nparts <= 1) return;  // the decode kernel wrote this row
   const float2 *ml = p.part_ml + (size_t)row * p.max_parts;
   const float *po = p.part_o + (size_t)row * p.max_parts * D + lane;
@@ -701,7 +727,7 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
       configured[dev] = 1;
     }
   }
-  dim3 grid(p.num_kv_heads * p.q_groups, p.max_parts, p.batch);
+  dim3 grid(p.num_kv_heads * p.q_groups, p.grid_parts, p.batch);
   if (launch_pdl(paged_decode_kernel<FP8, D>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s, mk, mv,
                  p) != cudaSuccess)
     return PKV_ERR_CUDA;
@@ -789,6 +815,7 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
   DecodeParams p;
   std::memset(&p, 0, sizeof p);
   p.max_parts = (int)parts64;
+  p.grid_parts = (int)parts64;
   p.part_tokens = pt;
   const size_t need = paged_attention_workspace_bytes(batch, num_heads, cache->num_kv_heads,
                                                       cache->head_dim, max_seq_len,
@@ -826,6 +853,131 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
   if (fp8)
     return cache->head_dim == 128 ? launch_decode<true, 128>(mk, mv, p, s)
                                   : launch_decode<true, 64>(mk, mv, p, s);
+  return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, s)
+                                : launch_decode<false, 64>(mk, mv, p, s);
+}
+
+// ---------------------------------------------------------------------------
+// Cascade (shared-prefix) decode
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kCascadePrefixPartTokens = 512;  // 4 key tiles of the prefix pass
+
+struct CascadeLayout {
+  int32_t pt, prefix_parts, suffix_parts, stride;
+  size_t ml_off, start_off, bytes;
+};
+
+bool cascade_layout(int32_t batch, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t max_seq_len, int32_t max_prefix_len, int32_t partition_tokens,
+                    CascadeLayout *l) {
+  if (batch <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_seq_len < 0 ||
+      max_prefix_len < 0 || max_prefix_len > max_seq_len)
+    return false;
+  const int32_t pt = paged_attention_partition_tokens(batch, num_heads, num_kv_heads,
+                                                      max_seq_len, partition_tokens);
+  if (pt <= 0) return false;
+  l->pt = pt;
+  l->prefix_parts =
+      std::max(1, (max_prefix_len + kCascadePrefixPartTokens - 1) / kCascadePrefixPartTokens);
+  l->suffix_parts = std::max<int32_t>(1, (int32_t)(((int64_t)max_seq_len + pt - 1) / pt));
+  if ((int64_t)l->prefix_parts + l->suffix_parts > 65535) return false;
+  l->stride = l->prefix_parts + l->suffix_parts;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = (size_t)batch * num_heads * l->stride;
+  l->ml_off = up(rows * head_dim * sizeof(float));
+  l->start_off = l->ml_off + up(rows * sizeof(float2));
+  l->bytes = l->start_off + up((size_t)batch * sizeof(int32_t));
+  return true;
+}
+
+}  // namespace
+
+extern "C" size_t paged_attention_cascade_workspace_bytes(int32_t batch, int32_t num_heads,
+                                                          int32_t num_kv_heads, int32_t head_dim,
+                                                          int32_t max_seq_len,
+                                                          int32_t max_prefix_len,
+                                                          int32_t partition_tokens) {
+  CascadeLayout l;
+  if (!cascade_layout(batch, num_heads, num_kv_heads, head_dim, max_seq_len, max_prefix_len,
+                      partition_tokens, &l))
+    return 0;
+  return l.bytes;
+}
+
+extern "C" pkv_status paged_attention_decode_cascade(
+    const void *q, const pkv_cache *cache, const int32_t *block_tables, int32_t max_blocks,
+    const int32_t *seq_lens, int32_t batch, int32_t num_heads, const int32_t *group_start,
+    const int32_t *prefix_len, int32_t num_groups, int32_t max_group_size, int32_t max_prefix_len,
+    float scale, void *out, int32_t max_seq_len, int32_t partition_tokens, void *workspace,
+    size_t workspace_bytes, void *stream) {
+  pkv_status st = validate_cache(cache);
+  if (st != PKV_OK) return st;
+  if (cache->dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (batch < 0 || num_heads <= 0 || max_blocks <= 0 || max_seq_len < 0 || num_groups < 0 ||
+      max_group_size < 0 || max_prefix_len < 0 || (max_prefix_len & 15) ||
+      partition_tokens < 0 || (partition_tokens & 15) || !std::isfinite(scale) ||
+      !(scale > 0.f))
+    return PKV_ERR_ARG;
+  if (num_heads % cache->num_kv_heads) return PKV_ERR_SHAPE;
+  const int group = num_heads / cache->num_kv_heads;
+  if (group > 128) return PKV_ERR_SHAPE;
+  if (batch == 0) return PKV_OK;
+  if (!q || !out || !block_tables || !seq_lens || (num_groups > 0 && (!group_start || !prefix_len)))
+    return PKV_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 15) return PKV_ERR_ARG;
+  if (batch > 65535 || num_groups > 65535) return PKV_ERR_ARG;
+  CascadeLayout l;
+  if (!cascade_layout(batch, num_heads, cache->num_kv_heads, cache->head_dim, max_seq_len,
+                      max_prefix_len, partition_tokens, &l))
+    return PKV_ERR_ARG;
+  if (!workspace || workspace_bytes < l.bytes || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return PKV_ERR_WORKSPACE;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  float *part_o = reinterpret_cast<float *>(ws);
+  float2 *part_ml = reinterpret_cast<float2 *>(ws + l.ml_off);
+  int32_t *seq_start = reinterpret_cast<int32_t *>(ws + l.start_off);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  // 1. every sequence starts at token 0 unless its group's pass says otherwise
+  if (cudaMemsetAsync(seq_start, 0, (size_t)batch * sizeof(int32_t), s) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  // 2. each group's prefix, once for all its members (tensor cores)
+  if (num_groups > 0) {
+    st = launch_prefix_partials(q, cache, block_tables, max_blocks, seq_lens, group_start,
+                                prefix_len, num_groups, max_group_size, max_prefix_len, batch,
+                                num_heads, scale, part_o, part_ml, l.stride, seq_start,
+                                kCascadePrefixPartTokens, s);
+    if (st != PKV_OK) return st;
+  }
+  // 3. each sequence's own tokens, then the log-sum-exp merge of all slots
+  CUtensorMap mk, mv;
+  if (!get_maps(cache, &mk, &mv)) return PKV_ERR_CUDA;
+  DecodeParams p;
+  std::memset(&p, 0, sizeof p);
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.part_o = part_o;
+  p.part_ml = part_ml;
+  p.batch = batch;
+  p.num_heads = num_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.group = group;
+  p.q_groups = (group + 7) / 8;
+  p.num_blocks = cache->num_blocks;
+  p.max_blocks = max_blocks;
+  p.max_seq_len = max_seq_len;
+  p.max_parts = l.stride;
+  p.grid_parts = l.suffix_parts;
+  p.part_tokens = l.pt;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.v_scale = 1.f;
+  p.timeout_ns = 2000000000ull;
+  p.seq_start = seq_start;
+  p.prefix_part_tokens = kCascadePrefixPartTokens;
   return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, s)
                                 : launch_decode<false, 64>(mk, mv, p, s);
 }

@@ -61,6 +61,20 @@ struct PrefillParams {
   int num_blocks, max_blocks;
   float scale_log2;
   unsigned long long timeout_ns;
+  // Shared-prefix mode (part_o != nullptr): grid.z runs over groups; the
+  // members of group z are rows group_start[z] .. group_start[z+1] - 1 of q
+  // ([batch, num_heads, head_dim]), all reading the prefix_len[z] tokens
+  // named by the first member's table.  Every member row sees every key of
+  // its prefix partition (prefix_part_tokens keys, grid.x / pairs_per_part
+  // of them), and the CTA writes the partition's (m, l, o / l) to merge
+  // slot `partition` of the row instead of a bf16 output.
+  float *part_o;       // [batch * num_heads, part_stride, head_dim]
+  float2 *part_ml;     // [batch * num_heads, part_stride]
+  int part_stride;
+  const int32_t *group_start;  // [num_groups + 1]
+  const int32_t *prefix_len;   // [num_groups], multiples of 16
+  int32_t *seq_start;          // [batch] out: first token after the prefix
+  int prefix_part_tokens, pairs_per_part;
 };
 
 template <int D>
@@ -140,50 +154,107 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int b = blockIdx.z, kvh = blockIdx.y;
-  const int qp = gridDim.x - 1 - blockIdx.x;  // longest tile pairs first
+  const bool prefix_mode = p.part_o != nullptr;
+  const int order = gridDim.x - 1 - blockIdx.x;  // longest tile pairs first
+  const int qp = prefix_mode ? order % p.pairs_per_part : order;
+  const int pp = prefix_mode ? order / p.pairs_per_part : 0;  // prefix partition
   const int g = p.group, TQ = p.tile_tokens;
 
   grid_dependency_wait();
   allow_dependent_launch();
 
-  const int q0 = p.query_start_loc[b];
-  const int n_b = p.query_start_loc[b + 1] - q0;
-  const int L = p.seq_lens[b];
-  const int c = L - n_b;  // tokens before this chunk
+  // Query rows q0 .. q0 + n_b - 1 of the pair's "sequence"; the pair sees
+  // keys kv_begin .. kv_len - 1 through block-table row table_row.
+  int q0, n_b, c = 0, kv_begin = 0, kv_len = 0, table_row = b;
+  bool bad_seq;
   const int j0 = qp * 2 * TQ;
-  if (j0 >= n_b && n_b >= 0) return;  // this pair has no query token
-  const bool bad_seq = n_b < 0 || c < 0 || L > p.max_blocks * 16 || q0 < 0 ||
-                       (long long)q0 + n_b > p.num_tokens;
+  if (prefix_mode) {
+    q0 = p.group_start[b];
+    n_b = p.group_start[b + 1] - q0;
+    const int P = p.prefix_len[b];
+    bad_seq = n_b < 0 || q0 < 0 || (long long)q0 + n_b > p.num_tokens || P < 0 || (P & 15) ||
+              P > p.max_blocks * 16 ||
+              P > (int)(gridDim.x / p.pairs_per_part) * p.prefix_part_tokens ||
+              n_b > p.pairs_per_part * 2 * TQ;
+    if (!bad_seq && pp == 0 && qp == 0 && kvh == 0) {
+      // one CTA per group publishes each member's suffix start and checks
+      // that every member's table begins with the first member's prefix
+      // blocks and that no member is shorter than the prefix
+      const int pb = P / 16;
+      const int32_t *lead = p.block_tables + (size_t)q0 * p.max_blocks;
+      for (int m = threadIdx.x; m < n_b; m += blockDim.x) {
+        const bool ok = p.seq_lens[q0 + m] >= P;
+        if (!ok) record_error(&g_err_prefill, PKV_ERR_RANGE, q0 + m);
+        p.seq_start[q0 + m] = ok ? P : 0;
+      }
+      __syncthreads();  // a mismatch below overrides the start written above
+      for (int idx = threadIdx.x; idx < (n_b - 1) * pb; idx += blockDim.x) {
+        const int m = 1 + idx / pb, j = idx % pb;
+        if (p.block_tables[(size_t)(q0 + m) * p.max_blocks + j] != lead[j]) {
+          record_error(&g_err_prefill, PKV_ERR_RANGE, (long long)(q0 + m) * p.max_blocks + j);
+          p.seq_start[q0 + m] = 0;  // that member is attended in full
+        }
+      }
+    }
+    if (bad_seq) {
+      if (pp == 0 && qp == 0 && kvh == 0) {
+        if (threadIdx.x == 0) record_error(&g_err_prefill, PKV_ERR_RANGE, b);
+        if (q0 >= 0 && n_b > 0 && (long long)q0 + n_b <= p.num_tokens)
+          for (int m = threadIdx.x; m < n_b; m += blockDim.x) p.seq_start[q0 + m] = 0;
+      }
+      return;  // members fall back to whole-sequence attention
+    }
+    kv_begin = pp * p.prefix_part_tokens;
+    kv_len = min(P, kv_begin + p.prefix_part_tokens);
+    if (j0 >= n_b || kv_begin >= kv_len) return;
+    table_row = q0;
+  } else {
+    q0 = p.query_start_loc[b];
+    n_b = p.query_start_loc[b + 1] - q0;
+    const int L = p.seq_lens[b];
+    c = L - n_b;  // tokens before this chunk
+    if (j0 >= n_b && n_b >= 0) return;  // this pair has no query token
+    bad_seq = n_b < 0 || c < 0 || L > p.max_blocks * 16 || q0 < 0 ||
+              (long long)q0 + n_b > p.num_tokens;
+  }
   const bool has_b = j0 + TQ < n_b;   // the second tile holds a query token
   const int j_last = min(j0 + 2 * TQ, n_b) - 1;
-  const int kv_len = c + j_last + 1;  // keys any row of the pair sees
-  const int n_tiles = (kv_len + C::KEYS - 1) / C::KEYS;
-  const int nblk = (kv_len + 15) / 16;
+  if (!prefix_mode) kv_len = c + j_last + 1;  // keys any row of the pair sees
+  const int n_tiles = (kv_len - kv_begin + C::KEYS - 1) / C::KEYS;
+  const int blk_begin = kv_begin / 16;          // kv_begin is a multiple of 128
+  const int nblk = (kv_len + 15) / 16;          // end of the block range
 
   // every block id the pair reads must be inside the pool
   int bad = bad_seq ? 1 : 0;
   if (!bad) {
-    const int32_t *row = p.block_tables + (size_t)b * p.max_blocks;
-    for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+    const int32_t *row = p.block_tables + (size_t)table_row * p.max_blocks;
+    for (int j = blk_begin + threadIdx.x; j < nblk; j += blockDim.x) {
       const int32_t id = row[j];
       if (id < 0 || id >= p.num_blocks) {
         bad = 1;
-        record_error(&g_err_prefill, PKV_ERR_RANGE, (long long)b * p.max_blocks + j);
+        record_error(&g_err_prefill, PKV_ERR_RANGE, (long long)table_row * p.max_blocks + j);
       }
     }
   } else if (threadIdx.x == 0) {
     record_error(&g_err_prefill, PKV_ERR_RANGE, b);
   }
   if (__syncthreads_or(bad)) {
-    // zero the pair's output rows of a valid token range, then leave
+    // zero the pair's output rows of a valid token range (in shared-prefix
+    // mode: an empty partial, weight zero in the merge), then leave
     if (!bad_seq) {
       const int rows = (j_last - j0 + 1) * g;
       for (int idx = threadIdx.x; idx < rows * (D / 8); idx += blockDim.x) {
         const int r = idx / (D / 8), ch = idx % (D / 8);
         const long long tok = (long long)q0 + j0 + r / g;
-        const int h = kvh * g + r % g;
-        *reinterpret_cast<uint4 *>(p.out + ((size_t)tok * p.num_heads + h) * D + ch * 8) =
-            make_uint4(0, 0, 0, 0);
+        const size_t row = (size_t)tok * p.num_heads + kvh * g + r % g;
+        if (prefix_mode) {
+          float *po = p.part_o + (row * p.part_stride + pp) * D + ch * 8;
+          *reinterpret_cast<float4 *>(po) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4 *>(po + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (ch == 0) p.part_ml[row * p.part_stride + pp] = make_float2(-INFINITY, 0.f);
+        } else {
+          *reinterpret_cast<uint4 *>(p.out + row * D + ch * 8) = make_uint4(0, 0, 0, 0);
+        }
       }
     }
     return;
@@ -224,7 +295,7 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    const int32_t *row = p.block_tables + (size_t)b * p.max_blocks;
+    const int32_t *row = p.block_tables + (size_t)table_row * p.max_blocks + blk_begin;
     if (lane == 0) {
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
@@ -245,7 +316,7 @@ __global__ void __launch_bounds__(320, 1)
         uint64_t *full = is_k ? &bars.k_full[st] : &bars.v_full[st];
         if (i >= stages && !wait_or_abort(empty, ((i / stages) - 1) & 1, p, abort_flag))
           return false;
-        const int nv = min(8, nblk - 8 * i);
+        const int nv = min(8, nblk - blk_begin - 8 * i);
         mbar_arrive_expect_tx(full, nv * C::SLICES * 2048);
         uint8_t *dst = smem + (is_k ? C::K_OFF : C::V_OFF) + st * TB;
         for (int j = 0; j < nv; ++j) {
@@ -268,7 +339,7 @@ __global__ void __launch_bounds__(320, 1)
     // that a zero probability never meets a NaN.
     const int last = n_tiles - 1, st = last % C::VSTAGES;
     if (wait_or_abort(&bars.v_full[st], (last / C::VSTAGES) & 1, p, abort_flag)) {
-      const int first = kv_len - last * C::KEYS;
+      const int first = kv_len - kv_begin - last * C::KEYS;
       uint8_t *vbase = smem + C::V_OFF + st * TB;
       for (int idx = first * 8 + lane; idx < C::KEYS * 8; idx += 32)
         for (int s = 0; s < C::SLICES; ++s)
@@ -345,7 +416,8 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t s_addr = lane_addr, o_addr = lane_addr + 128;
     const int jr = j0 + t * TQ + r / g;
     const bool row_valid = r < TQ * g && jr < n_b;
-    const int lim = row_valid ? c + jr : kv_len - 1;  // last key this row sees
+    // last key this row sees (every prefix key in shared-prefix mode)
+    const int lim = row_valid && !prefix_mode ? c + jr : kv_len - 1;
     float m_used = -INFINITY, l = 0.f;
     bool ok = t == 0 || has_b;
     for (int i = 0; ok && i < n_tiles; ++i) {
@@ -356,7 +428,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int q = 0; q < 4; ++q) tc::tmem_ld_32x32b_x32(s_addr + q * 32, sr[q]);
       tc::tmem_wait_ld();
 
-      const int key0 = i * C::KEYS;
+      const int key0 = kv_begin + i * C::KEYS;
       if (key0 + C::KEYS - 1 > lim) {
         // keys past this row's last visible position are excluded by
         // selection (a stale NaN in the cache becomes -inf, never a factor)
@@ -417,17 +489,26 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(smem_u32(&bars.p_full[t]));
     }
-    // epilogue: O_t / l -> bf16 rows of out
+    // epilogue: O_t / l -> bf16 rows of out, or the partition's partial
     if (ok && wait_or_abort(&bars.o_done[t], (n_tiles - 1) & 1, p, abort_flag)) {
       tc::fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16 *orow = p.out + ((size_t)(q0 + jr) * p.num_heads + kvh * g + r % g) * D;
+      const size_t orow_i = (size_t)(q0 + jr) * p.num_heads + kvh * g + r % g;
+      if (prefix_mode && row_valid) p.part_ml[orow_i * p.part_stride + pp] = make_float2(m_used, l);
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         uint32_t o[32];
         tc::tmem_ld_32x32b_x32(o_addr + q * 32, o);
         tc::tmem_wait_ld();
-        if (row_valid) {
+        if (row_valid && prefix_mode) {
+          float *po = p.part_o + (orow_i * p.part_stride + pp) * D + q * 32;
+#pragma unroll
+          for (int h = 0; h < 8; ++h)
+            *reinterpret_cast<float4 *>(po + 4 * h) =
+                make_float4(__uint_as_float(o[4 * h + 0]) * inv, __uint_as_float(o[4 * h + 1]) * inv,
+                            __uint_as_float(o[4 * h + 2]) * inv, __uint_as_float(o[4 * h + 3]) * inv);
+        } else if (row_valid) {
+          __nv_bfloat16 *orow = p.out + orow_i * D;
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             uint4 v;
@@ -584,6 +665,48 @@ pkv_status launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CU
 }
 
 }  // namespace
+
+pkv_status launch_prefix_partials(const void *q, const pkv_cache *cache,
+                                  const int32_t *block_tables, int32_t max_blocks,
+                                  const int32_t *seq_lens, const int32_t *group_start,
+                                  const int32_t *prefix_len, int32_t num_groups,
+                                  int32_t max_group_size, int32_t max_prefix_len, int32_t batch,
+                                  int32_t num_heads, float scale, float *part_o, float2 *part_ml,
+                                  int part_stride, int32_t *seq_start, int prefix_part_tokens,
+                                  cudaStream_t s) {
+  const int g = num_heads / cache->num_kv_heads;
+  const int tq = 128 / g;
+  const int pairs = std::max(1, (max_group_size + 2 * tq - 1) / (2 * tq));
+  const int parts = std::max(1, (max_prefix_len + prefix_part_tokens - 1) / prefix_part_tokens);
+  if ((int64_t)pairs * parts > INT32_MAX || num_groups > 65535) return PKV_ERR_ARG;
+  CUtensorMap mq, mk, mv;
+  if (!encode_query_map(&mq, q, batch, num_heads, cache->head_dim, g, tq)) return PKV_ERR_CUDA;
+  if (!get_prefill_maps(cache, &mk, &mv)) return PKV_ERR_CUDA;
+  PrefillParams p;
+  std::memset(&p, 0, sizeof p);
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.num_tokens = batch;
+  p.batch = num_groups;
+  p.num_heads = num_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.group = g;
+  p.tile_tokens = tq;
+  p.num_blocks = cache->num_blocks;
+  p.max_blocks = max_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = 2000000000ull;
+  p.part_o = part_o;
+  p.part_ml = part_ml;
+  p.part_stride = part_stride;
+  p.group_start = group_start;
+  p.prefix_len = prefix_len;
+  p.seq_start = seq_start;
+  p.prefix_part_tokens = prefix_part_tokens;
+  p.pairs_per_part = pairs;
+  return cache->head_dim == 128 ? launch_prefill<128>(mq, mk, mv, p, pairs * parts, s)
+                                : launch_prefill<64>(mq, mk, mv, p, pairs * parts, s);
+}
 
 unsigned long long read_and_clear_error_prefill(cudaStream_t s, cudaError_t *err) {
   unsigned long long v = 0ull;

@@ -319,6 +319,67 @@ def paged_attention_decode(q: torch.Tensor, cache: PagedKVCache,
     return out
 
 
+def paged_attention_cascade_workspace_bytes(batch: int, num_heads: int,
+                                            num_kv_heads: int, head_dim: int,
+                                            max_seq_len: int, max_prefix_len: int,
+                                            partition_tokens: int = 0) -> int:
+    """Device workspace bytes paged_attention_decode_cascade needs."""
+    return int(_native.lib().paged_attention_cascade_workspace_bytes(
+        batch, num_heads, num_kv_heads, head_dim, max_seq_len, max_prefix_len,
+        partition_tokens))
+
+
+def paged_attention_decode_cascade(q: torch.Tensor, cache: PagedKVCache,
+                                   block_tables: torch.Tensor,
+                                   seq_lens: torch.Tensor,
+                                   group_start: torch.Tensor,
+                                   prefix_len: torch.Tensor, scale: float,
+                                   max_seq_len: int, max_group_size: int,
+                                   max_prefix_len: int,
+                                   out: Optional[torch.Tensor] = None,
+                                   partition_tokens: int = 0,
+                                   workspace: Optional[torch.Tensor] = None,
+                                   stream: Optional[torch.cuda.Stream] = None
+                                   ) -> torch.Tensor:
+    """Decode attention with each group's shared prefix attended once for
+    all its members: group_start int32 [G+1] (members are consecutive
+    sequences), prefix_len int32 [G] (multiples of 16).  Same arguments and
+    result as paged_attention_decode otherwise."""
+    dev = cache.device
+    _require(q, "q", torch.bfloat16, dev, 3)
+    _require(block_tables, "block_tables", torch.int32, dev, 2)
+    _require(seq_lens, "seq_lens", torch.int32, dev, 1)
+    _require(group_start, "group_start", torch.int32, dev, 1)
+    _require(prefix_len, "prefix_len", torch.int32, dev, 1)
+    B, Hq, d = q.shape
+    G = prefix_len.shape[0]
+    if d != cache.head_dim or block_tables.shape[0] != B or \
+            seq_lens.shape[0] != B or group_start.shape[0] != G + 1:
+        raise ValueError("q, block_tables, seq_lens, group_start, prefix_len "
+                         "shapes do not match")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _require(out, "out", torch.bfloat16, dev, 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    need = paged_attention_cascade_workspace_bytes(
+        B, Hq, cache.num_kv_heads, d, max_seq_len, max_prefix_len,
+        partition_tokens)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _require(workspace, "workspace", torch.uint8, dev, 1)
+    st = _native.lib().paged_attention_decode_cascade(
+        q.data_ptr(), ctypes.byref(cache.c_struct()), block_tables.data_ptr(),
+        block_tables.shape[1], seq_lens.data_ptr(), B, Hq,
+        group_start.data_ptr(), prefix_len.data_ptr(), G, int(max_group_size),
+        int(max_prefix_len), float(scale), out.data_ptr(), int(max_seq_len),
+        int(partition_tokens), workspace.data_ptr(), workspace.numel(),
+        _stream_handle(stream, dev))
+    _native.check("paged_attention_decode_cascade", st)
+    return out
+
+
 def paged_attention_prefill(q: torch.Tensor, cache: PagedKVCache,
                             block_tables: torch.Tensor, seq_lens: torch.Tensor,
                             query_start_loc: torch.Tensor, scale: float,

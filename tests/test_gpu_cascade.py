@@ -1,0 +1,130 @@
+"""Cascade (shared-prefix) decode against the fp64 decode oracle.
+
+Cascade decode must return what plain decode returns: the oracle is the
+decode oracle on the same seeded inputs (|gpu - ref| <= 1e-2 + 1e-2 |ref|).
+Cases: the prefix-sharing workload (small and full size), groups with
+different prefix lengths next to ungrouped sequences and single-member
+groups, a member whose table breaks the sharing contract (reported, still
+correct), and the split of long suffixes into several partitions.
+"""
+import numpy as np
+import pytest
+import torch
+
+import harness
+from paged_kv_cache_48_gb300 import (PagedKVCache, PagedKVError,
+                                     paged_attention_decode,
+                                     paged_attention_decode_cascade, pkv_check)
+from paged_kv_cache_48_gb300 import workload as wl
+
+pytestmark = pytest.mark.gpu
+PKV_OK, PKV_ERR_DTYPE, PKV_ERR_RANGE = 0, 2, 5
+
+
+def _i32(a):
+    return torch.tensor(np.asarray(a, np.int32), device="cuda")
+
+
+def _cascade(W, G, group_start, prefix_len, tables=None, partition_tokens=0):
+    sizes = np.diff(group_start)
+    return paged_attention_decode_cascade(
+        G.q, G.cache, G.tables if tables is None else tables, G.seq_lens,
+        _i32(group_start), _i32(prefix_len), W.scale, max_seq_len=W.max_seq_len,
+        max_group_size=int(sizes.max()) if sizes.size else 0,
+        max_prefix_len=int(max(prefix_len)) if len(prefix_len) else 0,
+        partition_tokens=partition_tokens)
+
+
+def _groups_of(W):
+    per = len(W.groups[0]["members"])
+    gs = [grp["members"][0] for grp in W.groups] + [W.groups[-1]["members"][-1] + 1]
+    assert all(grp["members"] == list(range(grp["members"][0], grp["members"][0] + per))
+               for grp in W.groups)
+    plen = [16 * len(grp["prefix_blocks"]) for grp in W.groups]
+    return np.array(gs, np.int32), np.array(plen, np.int32)
+
+
+@pytest.mark.parametrize("pt", [0, 32])
+def test_cascade_prefix_shared_small(pt):
+    W = wl.prefix_shared(small=True)
+    G = harness.upload(W)
+    harness.gpu_step(W, G)
+    gs, plen = _groups_of(W)
+    out = _cascade(W, G, gs, plen, partition_tokens=pt)
+    assert pkv_check()[0] == PKV_OK
+    kc, vc = harness.oracle_cache(W)
+    harness.assert_close(out.float().cpu().numpy(), harness.oracle_out(W, kc, vc), "bf16")
+
+
+def test_cascade_mixed_groups_and_ungrouped_sequences():
+    """Groups of 3, 2 and 1 members with prefixes of 64, 128 and 16 tokens,
+    two sequences in no group, on the Llama-8B shape (g = 4)."""
+    W = wl.llama8b_gqa(small=True)          # 8 sequences, lengths 20..700
+    order = np.argsort(-W.seq_lens)          # longest first: prefixes fit
+    for name in ("seq_lens", "block_tables", "q", "step_k", "step_v", "step_slots"):
+        setattr(W, name, getattr(W, name)[order].copy())
+    tables = W.block_tables.copy()
+    gs = np.array([0, 3, 5, 6], np.int32)   # sequences 6, 7 in no group
+    plen = np.array([64, 128, 16], np.int32)
+    plen = np.minimum(plen, [int(W.seq_lens[gs[i]:gs[i + 1]].min()) // 16 * 16
+                             for i in range(3)]).astype(np.int32)
+    for gi in range(3):
+        lead = gs[gi]
+        for m in range(gs[gi] + 1, gs[gi + 1]):
+            tables[m, :plen[gi] // 16] = tables[lead, :plen[gi] // 16]
+    W.block_tables = tables
+    G = harness.upload(W)
+    harness.gpu_step(W, G)
+    out = _cascade(W, G, gs, plen)
+    assert pkv_check()[0] == PKV_OK
+    kc, vc = harness.oracle_cache(W)
+    harness.assert_close(out.float().cpu().numpy(), harness.oracle_out(W, kc, vc), "bf16")
+
+
+def test_cascade_contract_violation_is_reported_and_still_correct():
+    W = wl.prefix_shared(small=True)
+    G = harness.upload(W)
+    harness.gpu_step(W, G)
+    gs, plen = _groups_of(W)
+    # member 2 of group 0 points its first prefix block elsewhere: its own
+    # table is the truth for the oracle, the group prefix no longer applies
+    bad = W.block_tables.copy()
+    bad[2, 0] = W.groups[1]["prefix_blocks"][0]  # written data, another group's
+    out = _cascade(W, G, gs, plen, tables=torch.from_numpy(bad).cuda())
+    st, detail = pkv_check()
+    assert st == PKV_ERR_RANGE and detail == 2 * W.max_blocks + 0
+    W2 = wl.Workload(**{**W.__dict__})
+    W2.block_tables = bad
+    kc, vc = harness.oracle_cache(W)
+    harness.assert_close(out.float().cpu().numpy(), harness.oracle_out(W2, kc, vc), "bf16")
+
+
+def test_cascade_full_size_matches_decode_and_oracle_samples():
+    """The full prefix-sharing workload (256 sequences in 16 groups sharing
+    1024 tokens): cascade and plain decode agree within the tolerance
+    everywhere, and sampled rows match the oracle."""
+    W = wl.prefix_shared()
+    G = harness.upload(W)
+    harness.gpu_step(W, G)
+    gs, plen = _groups_of(W)
+    out = _cascade(W, G, gs, plen).float().cpu().numpy()
+    dec = paged_attention_decode(G.q, G.cache, G.tables, G.seq_lens, W.scale,
+                                 max_seq_len=W.max_seq_len).float().cpu().numpy()
+    assert pkv_check()[0] == PKV_OK
+    harness.assert_close(out, dec.astype(np.float64), "bf16")
+    rng = np.random.default_rng(1)
+    seqs = sorted(set(rng.choice(W.batch, 10, replace=False).tolist()) | {0, 15, 255})
+    pairs = np.array([(b, h) for b in seqs for h in range(W.num_heads)], np.int32)
+    kc, vc = harness.oracle_cache(W)
+    ref = harness.oracle_out(W, kc, vc, pairs=pairs)
+    harness.assert_close(out[seqs], ref[seqs], "bf16")
+
+
+def test_cascade_rejects_fp8_cache():
+    kc = torch.zeros((4, 16, 1, 64), dtype=torch.uint8, device="cuda")
+    cache = PagedKVCache(kc, kc.clone(), "fp8_e4m3", 1.0, 1.0)
+    q = torch.zeros((2, 1, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(PagedKVError) as e:
+        paged_attention_decode_cascade(q, cache, _i32([[0], [0]]), _i32([4, 4]),
+                                       _i32([0, 2]), _i32([0]), 0.1, 4, 2, 0)
+    assert e.value.status == PKV_ERR_DTYPE
