@@ -53,7 +53,7 @@ def parse_args():
     ap.add_argument("--cpu-sample-seqs", type=int, default=16)
     ap.add_argument("--kernel", default="decode",
                     choices=["decode", "zero_blocks", "copy_blocks", "swap",
-                             "input_prep", "prefill"],
+                             "input_prep", "prefill", "cascade"],
                     help="decode: the decode step (headline); the others time "
                          "the block-movement entry points on the workload's "
                          "pool")
@@ -820,12 +820,120 @@ def run_prefill(args):
     return 0
 
 
+def run_cascade(args):
+    """Shared-prefix decode on the prefix-sharing workload (256 sequences,
+    16 groups sharing 1024 tokens): the cascade path against plain decode on
+    the same cache, as unique and logical KV bytes per second."""
+    import torch
+    import oracle
+    from paged_kv_cache_48_gb300 import (PagedKVCache, paged_attention_decode,
+                                         paged_attention_decode_cascade,
+                                         paged_kv_write, paged_kv_zero_blocks,
+                                         pkv_check)
+    from paged_kv_cache_48_gb300 import workload as wl
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    W = wl.prefix_shared()
+    shape = (W.num_blocks, 16, W.num_kv_heads, W.head_dim)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16)
+    cache = PagedKVCache(
+        torch.from_numpy(W.init_key).view(torch.bfloat16).reshape(shape).to(dev),
+        torch.from_numpy(W.init_value).view(torch.bfloat16).reshape(shape).to(dev),
+        "bf16")
+    paged_kv_write(bf(W.hist_k).to(dev), bf(W.hist_v).to(dev),
+                   torch.from_numpy(W.hist_slots).to(dev), cache)
+    if W.fresh_blocks.size:
+        paged_kv_zero_blocks(cache, W.fresh_blocks)
+    paged_kv_write(bf(W.step_k).to(dev), bf(W.step_v).to(dev),
+                   torch.from_numpy(W.step_slots).to(dev), cache)
+    q = bf(W.q).to(dev)
+    tables = torch.from_numpy(W.block_tables).to(dev)
+    lens = torch.from_numpy(W.seq_lens).to(dev)
+    per = len(W.groups[0]["members"])
+    gs = torch.tensor([g["members"][0] for g in W.groups] + [W.batch],
+                      dtype=torch.int32, device=dev)
+    plen_h = [16 * len(g["prefix_blocks"]) for g in W.groups]
+    plen = torch.tensor(plen_h, dtype=torch.int32, device=dev)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+
+    def cascade():
+        paged_attention_decode_cascade(q, cache, tables, lens, gs, plen, W.scale,
+                                       W.max_seq_len, per, max(plen_h), out=out)
+
+    def plain():
+        paged_attention_decode(q, cache, tables, lens, W.scale, W.max_seq_len,
+                               out=out)
+
+    def time_ms(fn, reps):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    reps = max(10, min(args.steps, 2000))
+    with ClockSampler(0) as clk:
+        c_ms = time_ms(cascade, reps)
+        p_ms = time_ms(plain, reps)
+    st, detail = pkv_check()
+    if st != 0:
+        raise RuntimeError(f"device error {st} at {detail}")
+    unique, logical = W.unique_kv_read_bytes(), W.kv_read_bytes()
+    peak, peak_kind = measured_peak()
+    gbs = unique / (c_ms * 1e-3) / 1e9
+    line = {
+        "kernel": "cascade",
+        "metric": "shared-prefix decode, unique KV-read GB/s (prefix_shared)",
+        "value": round(gbs, 1), "unit": "GB/s", "higher_is_better": True,
+        "ms_per_call": round(c_ms, 4), "steps": reps,
+        "logical_GB_per_s": round(logical / (c_ms * 1e-3) / 1e9, 1),
+        "plain_decode_ms": round(p_ms, 4),
+        "plain_decode_logical_GB_per_s": round(logical / (p_ms * 1e-3) / 1e9, 1),
+        "speedup_vs_plain_decode": round(p_ms / c_ms, 3),
+        "unique_kv_bytes": unique, "logical_kv_bytes": logical,
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": None,
+                     "peak_kind": peak_kind},
+        "gpu_launches_per_call": 4, "clocks": clk.summary(), "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "prefix_shared", "batch": W.batch, "groups": len(W.groups),
+                   "prefix_tokens": max(plen_h), "num_heads": W.num_heads,
+                   "num_kv_heads": W.num_kv_heads, "head_dim": W.head_dim,
+                   "l2": "unique KV bytes larger than L2"},
+    }
+    if not args.no_cpu_baseline:
+        kc, vc = W.init_key.copy(), W.init_value.copy()
+        o = oracle.load()
+        o.kv_write(kc, vc, oracle.DTYPE_BF16, 16, W.num_kv_heads, W.head_dim,
+                   1.0, 1.0, W.hist_k, W.hist_v, W.hist_slots)
+        seqs = list(range(0, W.batch, max(1, W.batch // args.cpu_sample_seqs)))
+        t0 = time.perf_counter()
+        cpu_oracle_step(W, kc, vc, seqs)
+        dt = time.perf_counter() - t0
+        sample = int(W.seq_lens[seqs].astype(np.int64).sum()) * W.num_kv_heads * \
+            W.head_dim * 4
+        line["cpu_baseline"] = {"value": round(sample / dt / 1e9, 3), "unit": "GB/s",
+                                "cores": o.num_threads(0), "kind": "oracle",
+                                "sample": f"{len(seqs)} sequences, logical bytes, {dt:.1f} s"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.kernel == "input_prep":
         return run_input_prep(args)
     if args.kernel == "prefill":
         return run_prefill(args)
+    if args.kernel == "cascade":
+        return run_cascade(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.kernel != "decode":

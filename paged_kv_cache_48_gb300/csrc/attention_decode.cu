@@ -58,23 +58,66 @@ struct DecodeParams {
   float v_scale;     // 1 for bf16
   unsigned long long timeout_ns;
   int32_t grid_parts;  // partition CTAs per (kv head group, sequence)
-  // Shared-prefix (cascade) decode: sequence b starts at token seq_start[b]
-  // (its group's prefix, already reduced into merge slots
-  // 0 .. ceil(seq_start[b] / prefix_part_tokens) - 1); its own partitions
-  // follow in the next slots.  nullptr = every sequence starts at 0.
-  const int32_t *seq_start;
-  int32_t prefix_part_tokens;
+  // Shared-prefix (cascade) decode, when group_start != nullptr: group G is
+  // sequences group_start[G] .. group_start[G+1] - 1 sharing the first
+  // prefix_len[G] tokens.  A member that passes the checks of
+  // cascade_start() starts at token prefix_len[G]: its prefix was reduced
+  // into merge slots 0 .. ceil(prefix_len / prefix_part_tokens) - 1 by the
+  // tensor-core pass, and its own partitions follow.  The decode kernel
+  // records each sequence's start in seq_start[b] for the merge kernel.
+  const int32_t *group_start, *prefix_len;
+  int32_t num_groups, max_group_size, max_prefix_len, prefix_part_tokens;
+  int32_t *seq_start;
 };
 
-// First token this launch attends to in sequence b (a multiple of 16 inside
-// [0, L]; anything else reads as 0) and the merge slots before its first
-// partition.
-__device__ __forceinline__ void suffix_range(const DecodeParams &p, int b, int L, int *start,
-                                             int *slot_base) {
-  int st = p.seq_start ? __ldg(p.seq_start + b) : 0;
-  if (st < 0 || st > L || (st & 15)) st = 0;
-  *start = st;
-  *slot_base = st > 0 ? (st + p.prefix_part_tokens - 1) / p.prefix_part_tokens : 0;
+// First token of sequence b this launch attends to (0, or its group's
+// prefix length when the group and the member pass every check); the same
+// value in every lane of the calling warp.  Checks: the group lies inside
+// the batch and within the host bounds that sized the prefix pass, the
+// prefix is a positive multiple of 16 no longer than the sequence, and the
+// member's first prefix_len / 16 block ids equal the first member's and lie
+// in the pool.  A failed check is recorded (when `report`) and the member
+// is attended in full, which is still the right result.
+__device__ int cascade_start(const DecodeParams &p, int b, int L, int lane, bool report) {
+  if (!p.group_start || p.num_groups <= 0) return 0;
+  int lo = 0, hi = p.num_groups - 1, G = -1;  // last group starting at or before b
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.group_start + mid) <= b) {
+      G = mid;
+      lo = mid + 1;
+    } else {
+      hi = mid - 1;
+    }
+  }
+  if (G < 0) return 0;
+  const int q0 = __ldg(p.group_start + G), n = __ldg(p.group_start + G + 1) - q0;
+  const int P = __ldg(p.prefix_len + G);
+  if (b >= q0 + n || P == 0) return 0;  // in no group / nothing shared
+  if (n < 1 || q0 < 0 || q0 + n > p.batch || P < 0 || (P & 15) || P > p.max_blocks * 16 ||
+      P > p.max_prefix_len || n > p.max_group_size || L < P) {
+    if (report && lane == 0) record_error(&g_err_attention, PKV_ERR_RANGE, b);
+    return 0;
+  }
+  const int32_t *mine = p.block_tables + (size_t)b * p.max_blocks;
+  const int32_t *lead = p.block_tables + (size_t)q0 * p.max_blocks;
+  int bad_j = INT_MAX;
+  for (int j = lane; j < (P >> 4); j += 32) {
+    const int32_t id = __ldg(mine + j);
+    if (id != __ldg(lead + j) || id < 0 || id >= p.num_blocks) bad_j = min(bad_j, j);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) bad_j = min(bad_j, __shfl_xor_sync(0xffffffffu, bad_j, off));
+  if (bad_j != INT_MAX) {
+    if (report && lane == 0)
+      record_error(&g_err_attention, PKV_ERR_RANGE, (long long)b * p.max_blocks + bad_j);
+    return 0;
+  }
+  return P;
+}
+
+__device__ __forceinline__ int prefix_slots(const DecodeParams &p, int start) {
+  return start > 0 ? (start + p.prefix_part_tokens - 1) / p.prefix_part_tokens : 0;
 }
 
 template <bool FP8, int D>
@@ -379,8 +422,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
       L = clamp_len(L, cap);
     }
   }
-  int start, slot_base;
-  suffix_range(p, b, L, &start, &slot_base);
+  const int start =
+      cascade_start(p, b, L, lane, blockIdx.x == 0 && part == 0 && warp == 0);
+  const int slot_base = prefix_slots(p, start);
+  if (p.seq_start && blockIdx.x == 0 && part == 0 && threadIdx.x == 0) p.seq_start[b] = start;
   const int Ls = L - start;
   const int nparts = Ls <= p.part_tokens ? 1 : (Ls + p.part_tokens - 1) / p.part_tokens;
   if (part >= nparts) return;
@@ -515,8 +560,9 @@ __global__ void __launch_bounds__(256) paged_decode_merge_kernel(const DecodePar
   const int b = (int)(row / p.num_heads);
   const int cap = min(p.max_blocks * 16, p.max_seq_len);
   const int L = clamp_len(__ldg(p.seq_lens + b), cap);
-  int start, slot_base;
-  suffix_range(p, b, L, &start, &slot_base);
+  int start = p.seq_start ? __ldg(p.seq_start + b) : 0;  // decided by the decode kernel
+  if (start < 0 || start > L || (start & 15)) start = 0;
+  const int slot_base = prefix_slots(p, start);
   const int Ls = L - start;
   const int nparts =
       slot_base + (Ls <= p.part_tokens ? 1 : (Ls + p.part_tokens - 1) / p.part_tokens);
@@ -709,9 +755,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// join (optional): an event the merge kernel must wait for (the shared-
+// prefix pass running on another stream).
 template <bool FP8, int D>
 pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                         cudaStream_t s) {
+                         cudaStream_t s, cudaEvent_t join = nullptr) {
   using C = Cfg<FP8, D>;
   static int configured[64] = {0};
   static std::mutex mu;
@@ -731,6 +779,7 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
   if (launch_pdl(paged_decode_kernel<FP8, D>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s, mk, mv,
                  p) != cudaSuccess)
     return PKV_ERR_CUDA;
+  if (join && cudaStreamWaitEvent(s, join, 0) != cudaSuccess) return PKV_ERR_CUDA;
   if (p.max_parts > 1) {
     const long long rows = (long long)p.batch * p.num_heads;
     if (launch_pdl(paged_decode_merge_kernel<D>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0,
@@ -864,6 +913,42 @@ namespace {
 
 constexpr int kCascadePrefixPartTokens = 512;  // 4 key tiles of the prefix pass
 
+// A non-blocking side stream per device with its fork / join events; the
+// mutex keeps one call's fork-join sequence together.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+
+SideStream &side_stream() {
+  static SideStream streams[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    static SideStream none;
+    return none;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  SideStream &sd = streams[dev];
+  if (!sd.stream) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    // highest priority: the prefix pass's CTAs (one per SM) take SMs as
+    // they free up instead of queueing behind the whole decode grid
+    int lo = 0, hi = 0;
+    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) hi = 0;
+    if (cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, hi) == cudaSuccess &&
+        cudaEventCreateWithFlags(&f, cudaEventDisableTiming) == cudaSuccess &&
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) == cudaSuccess) {
+      sd.fork = f;
+      sd.join = j;
+      sd.stream = st;
+    }
+  }
+  return sd;
+}
+
 struct CascadeLayout {
   int32_t pt, prefix_parts, suffix_parts, stride;
   size_t ml_off, start_off, bytes;
@@ -940,18 +1025,25 @@ extern "C" pkv_status paged_attention_decode_cascade(
   int32_t *seq_start = reinterpret_cast<int32_t *>(ws + l.start_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // 1. every sequence starts at token 0 unless its group's pass says otherwise
-  if (cudaMemsetAsync(seq_start, 0, (size_t)batch * sizeof(int32_t), s) != cudaSuccess)
-    return PKV_ERR_CUDA;
-  // 2. each group's prefix, once for all its members (tensor cores)
-  if (num_groups > 0) {
+  // 1. each group's prefix, once for all its members (tensor cores), on a
+  //    side stream so that it runs beside pass 2
+  SideStream &side = side_stream();
+  if (!side.stream) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(side.mu);
+  const bool fork = num_groups > 0 && max_prefix_len > 0;
+  if (fork) {
+    if (cudaEventRecord(side.fork, s) != cudaSuccess ||
+        cudaStreamWaitEvent(side.stream, side.fork, 0) != cudaSuccess)
+      return PKV_ERR_CUDA;
     st = launch_prefix_partials(q, cache, block_tables, max_blocks, seq_lens, group_start,
                                 prefix_len, num_groups, max_group_size, max_prefix_len, batch,
-                                num_heads, scale, part_o, part_ml, l.stride, seq_start,
-                                kCascadePrefixPartTokens, s);
+                                num_heads, scale, part_o, part_ml, l.stride,
+                                kCascadePrefixPartTokens, side.stream);
     if (st != PKV_OK) return st;
+    if (cudaEventRecord(side.join, side.stream) != cudaSuccess) return PKV_ERR_CUDA;
   }
-  // 3. each sequence's own tokens, then the log-sum-exp merge of all slots
+  // 2. each sequence's own tokens (and its start), then, after the join, the
+  //    log-sum-exp merge of all slots
   CUtensorMap mk, mv;
   if (!get_maps(cache, &mk, &mv)) return PKV_ERR_CUDA;
   DecodeParams p;
@@ -976,8 +1068,14 @@ extern "C" pkv_status paged_attention_decode_cascade(
   p.scale_log2 = scale * 1.4426950408889634f;
   p.v_scale = 1.f;
   p.timeout_ns = 2000000000ull;
-  p.seq_start = seq_start;
+  p.group_start = fork ? group_start : nullptr;
+  p.prefix_len = prefix_len;
+  p.num_groups = num_groups;
+  p.max_group_size = max_group_size;
+  p.max_prefix_len = max_prefix_len;
   p.prefix_part_tokens = kCascadePrefixPartTokens;
-  return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, s)
-                                : launch_decode<false, 64>(mk, mv, p, s);
+  p.seq_start = seq_start;
+  cudaEvent_t join = fork ? side.join : nullptr;
+  return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, s, join)
+                                : launch_decode<false, 64>(mk, mv, p, s, join);
 }

@@ -67,14 +67,15 @@ struct PrefillParams {
   // named by the first member's table.  Every member row sees every key of
   // its prefix partition (prefix_part_tokens keys, grid.x / pairs_per_part
   // of them), and the CTA writes the partition's (m, l, o / l) to merge
-  // slot `partition` of the row instead of a bf16 output.
+  // slot `partition` of the row instead of a bf16 output.  Which members
+  // use these partials (their table and length checks) is decided by the
+  // decode pass.
   float *part_o;       // [batch * num_heads, part_stride, head_dim]
   float2 *part_ml;     // [batch * num_heads, part_stride]
   int part_stride;
   const int32_t *group_start;  // [num_groups + 1]
   const int32_t *prefix_len;   // [num_groups], multiples of 16
-  int32_t *seq_start;          // [batch] out: first token after the prefix
-  int prefix_part_tokens, pairs_per_part;
+  int prefix_part_tokens, pairs_per_part, max_prefix_len, max_group_size;
 };
 
 template <int D>
@@ -172,38 +173,11 @@ __global__ void __launch_bounds__(320, 1)
     q0 = p.group_start[b];
     n_b = p.group_start[b + 1] - q0;
     const int P = p.prefix_len[b];
-    bad_seq = n_b < 0 || q0 < 0 || (long long)q0 + n_b > p.num_tokens || P < 0 || (P & 15) ||
-              P > p.max_blocks * 16 ||
-              P > (int)(gridDim.x / p.pairs_per_part) * p.prefix_part_tokens ||
-              n_b > p.pairs_per_part * 2 * TQ;
-    if (!bad_seq && pp == 0 && qp == 0 && kvh == 0) {
-      // one CTA per group publishes each member's suffix start and checks
-      // that every member's table begins with the first member's prefix
-      // blocks and that no member is shorter than the prefix
-      const int pb = P / 16;
-      const int32_t *lead = p.block_tables + (size_t)q0 * p.max_blocks;
-      for (int m = threadIdx.x; m < n_b; m += blockDim.x) {
-        const bool ok = p.seq_lens[q0 + m] >= P;
-        if (!ok) record_error(&g_err_prefill, PKV_ERR_RANGE, q0 + m);
-        p.seq_start[q0 + m] = ok ? P : 0;
-      }
-      __syncthreads();  // a mismatch below overrides the start written above
-      for (int idx = threadIdx.x; idx < (n_b - 1) * pb; idx += blockDim.x) {
-        const int m = 1 + idx / pb, j = idx % pb;
-        if (p.block_tables[(size_t)(q0 + m) * p.max_blocks + j] != lead[j]) {
-          record_error(&g_err_prefill, PKV_ERR_RANGE, (long long)(q0 + m) * p.max_blocks + j);
-          p.seq_start[q0 + m] = 0;  // that member is attended in full
-        }
-      }
-    }
-    if (bad_seq) {
-      if (pp == 0 && qp == 0 && kvh == 0) {
-        if (threadIdx.x == 0) record_error(&g_err_prefill, PKV_ERR_RANGE, b);
-        if (q0 >= 0 && n_b > 0 && (long long)q0 + n_b <= p.num_tokens)
-          for (int m = threadIdx.x; m < n_b; m += blockDim.x) p.seq_start[q0 + m] = 0;
-      }
-      return;  // members fall back to whole-sequence attention
-    }
+    // the same structural test the decode pass applies: a group that fails
+    // it is attended in full there, so no partial is needed
+    bad_seq = n_b < 1 || q0 < 0 || (long long)q0 + n_b > p.num_tokens || P <= 0 || (P & 15) ||
+              P > p.max_blocks * 16 || P > p.max_prefix_len || n_b > p.max_group_size;
+    if (bad_seq) return;
     kv_begin = pp * p.prefix_part_tokens;
     kv_len = min(P, kv_begin + p.prefix_part_tokens);
     if (j0 >= n_b || kv_begin >= kv_len) return;
@@ -672,8 +646,7 @@ pkv_status launch_prefix_partials(const void *q, const pkv_cache *cache,
                                   const int32_t *prefix_len, int32_t num_groups,
                                   int32_t max_group_size, int32_t max_prefix_len, int32_t batch,
                                   int32_t num_heads, float scale, float *part_o, float2 *part_ml,
-                                  int part_stride, int32_t *seq_start, int prefix_part_tokens,
-                                  cudaStream_t s) {
+                                  int part_stride, int prefix_part_tokens, cudaStream_t s) {
   const int g = num_heads / cache->num_kv_heads;
   const int tq = 128 / g;
   const int pairs = std::max(1, (max_group_size + 2 * tq - 1) / (2 * tq));
@@ -701,9 +674,10 @@ pkv_status launch_prefix_partials(const void *q, const pkv_cache *cache,
   p.part_stride = part_stride;
   p.group_start = group_start;
   p.prefix_len = prefix_len;
-  p.seq_start = seq_start;
   p.prefix_part_tokens = prefix_part_tokens;
   p.pairs_per_part = pairs;
+  p.max_prefix_len = max_prefix_len;
+  p.max_group_size = max_group_size;
   return cache->head_dim == 128 ? launch_prefill<128>(mq, mk, mv, p, pairs * parts, s)
                                 : launch_prefill<64>(mq, mk, mv, p, pairs * parts, s);
 }

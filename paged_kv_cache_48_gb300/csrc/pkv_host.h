@@ -30,14 +30,13 @@ unsigned long long read_and_clear_error_prefill(cudaStream_t s, cudaError_t *err
 // Shared-prefix pass of cascade decode (attention_prefill.cu): for every
 // group, the members' queries against the group's prefix on the tensor
 // cores, one (m, l, o / l) partial per prefix partition in merge slots
-// 0 .. of each member row; also writes each member's suffix start.
+// 0 .. of each member row.
 pkv_status launch_prefix_partials(const void *q, const pkv_cache *cache,
                                   const int32_t *block_tables, int32_t max_blocks,
                                   const int32_t *seq_lens, const int32_t *group_start,
                                   const int32_t *prefix_len, int32_t num_groups,
                                   int32_t max_group_size, int32_t max_prefix_len, int32_t batch,
                                   int32_t num_heads, float scale, float *part_o, float2 *part_ml,
-                                  int part_stride, int32_t *seq_start, int prefix_part_tokens,
-                                  cudaStream_t s);
+                                  int part_stride, int prefix_part_tokens, cudaStream_t s);
 
 }  // namespace pkv
