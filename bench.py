@@ -40,6 +40,10 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILE = ROOT / "profiles" / "paged_decode_kernel_llama8b_gqa.md"
 KERNEL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_decode.cu",
                   "paged_kv_cache_48_gb300/csrc/pkv_device.cuh"]
+PREFILL_PROFILE = ROOT / "profiles" / "paged_prefill_kernel_chunked_prefill_8k.md"
+PREFILL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_prefill.cu",
+                   "paged_kv_cache_48_gb300/csrc/tcgen05.cuh",
+                   "paged_kv_cache_48_gb300/csrc/pkv_device.cuh"]
 
 
 def parse_args():
@@ -97,9 +101,9 @@ def whole_job_gbs(world: int, bytes_per_rank: int, ms_per_step: float) -> float:
     return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
-def kernel_sha() -> str:
+def kernel_sha(sources=None) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources or KERNEL_SOURCES:
         h.update((ROOT / rel).read_bytes())
     return h.hexdigest()[:16]
 
@@ -126,15 +130,17 @@ def measured_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
-    if not PROFILE.exists():
+def profiled_traffic(profile=None, sources=None):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, if
+    the summary was taken on the current kernel source (the decode kernel by
+    default)."""
+    profile = profile or PROFILE
+    if not profile.exists():
         return None
-    text = PROFILE.read_text()
+    text = profile.read_text()
     sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
     val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not sha or not val or sha.group(1) != kernel_sha():
+    if not sha or not val or sha.group(1) != kernel_sha(sources):
         return None
     return float(val.group(1))
 
@@ -782,7 +788,9 @@ def run_prefill(args):
         "attention_flops": flops,
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2),
                      "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(attn_tflops / peak, 4), "traffic": None,
+                     "frac": round(attn_tflops / peak, 4),
+                     "traffic": profiled_traffic(PREFILL_PROFILE, PREFILL_SOURCES)
+                     if name == "chunked_prefill_8k" else None,
                      "peak_kind": peak_kind + " bf16 burst",
                      "kernel_ms": round(attn_ms, 4)},
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2),
