@@ -66,11 +66,11 @@ def parse_args():
     ap.add_argument("--workload", default="llama8b_gqa",
                     choices=["llama8b_gqa", "prefix_shared", "long_context",
                              "fp8_recycle", "tiny_mha", "prefill_8k",
-                             "chunked_prefill_8k"],
+                             "chunked_prefill_8k", "chunked_prefill_8k_fp8"],
                     help="decode workload (the headline metric is quoted on "
                          "llama8b_gqa, the others are reported for context); "
-                         "with --kernel prefill, prefill_8k or "
-                         "chunked_prefill_8k")
+                         "with --kernel prefill, prefill_8k, "
+                         "chunked_prefill_8k or chunked_prefill_8k_fp8")
     return ap.parse_args()
 
 
@@ -706,10 +706,11 @@ def run_prefill(args):
     W = wl.PREFILL_CONFIGS[name]()
     shape = (W.num_blocks, 16, W.num_kv_heads, W.head_dim)
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16)
+    elt = torch.bfloat16 if W.kv_dtype == "bf16" else torch.uint8
     cache = PagedKVCache(
-        torch.from_numpy(W.init_key).view(torch.bfloat16).reshape(shape).to(dev),
-        torch.from_numpy(W.init_value).view(torch.bfloat16).reshape(shape).to(dev),
-        "bf16")
+        torch.from_numpy(W.init_key).view(elt).reshape(shape).to(dev),
+        torch.from_numpy(W.init_value).view(elt).reshape(shape).to(dev),
+        W.kv_dtype, W.k_scale, W.v_scale)
     if W.hist_slots.size:
         paged_kv_write(bf(W.hist_k).to(dev), bf(W.hist_v).to(dev),
                        torch.from_numpy(W.hist_slots).to(dev), cache)
@@ -777,9 +778,11 @@ def run_prefill(args):
         "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": 1,
         "steps": reps, "warmup": max(3, args.warmup),
         "ms_per_step": round(step_ms, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if W.kv_dtype == "bf16" else "f16 MMA on e4m3 KV",
         "data": "synthetic",
         "config": {"workload": name, "batch": W.batch, "num_tokens": W.num_tokens,
+                   "kv_dtype": W.kv_dtype,
                    "history": [int(x) for x in W.history],
                    "chunk": [int(x) for x in W.chunk],
                    "num_heads": W.num_heads, "num_kv_heads": W.num_kv_heads,
@@ -802,10 +805,11 @@ def run_prefill(args):
     if not args.no_cpu_baseline:
         kc, vc = W.init_key.copy(), W.init_value.copy()
         o = oracle.load()
+        odt = oracle.DTYPE_BF16 if W.kv_dtype == "bf16" else oracle.DTYPE_FP8_E4M3
         for kk, vv, sl in ((W.hist_k, W.hist_v, W.hist_slots),
                            (W.step_k, W.step_v, W.step_slots)):
-            o.kv_write(kc, vc, oracle.DTYPE_BF16, 16, W.num_kv_heads,
-                       W.head_dim, 1.0, 1.0, kk, vv, sl)
+            o.kv_write(kc, vc, odt, 16, W.num_kv_heads, W.head_dim, W.k_scale,
+                       W.v_scale, kk, vv, sl)
         rng = np.random.default_rng(1)
         toks = rng.choice(W.num_tokens, size=128, replace=False)
         rows = np.array([[t, h] for t in toks for h in range(W.num_heads)],
@@ -815,7 +819,7 @@ def run_prefill(args):
         keys = (W.history[seq] + (toks - qsl_h[seq]) + 1).astype(np.int64)
         sample_flops = int(keys.sum()) * W.num_heads * 4 * W.head_dim
         t0 = time.perf_counter()
-        o.attention_prefill(W.q, kc, vc, oracle.DTYPE_BF16, 1.0, 1.0, 16,
+        o.attention_prefill(W.q, kc, vc, odt, W.k_scale, W.v_scale, 16,
                             W.num_kv_heads, W.head_dim, W.block_tables,
                             W.seq_lens, qsl_h, W.scale, rows=rows)
         dt = time.perf_counter() - t0

@@ -999,7 +999,8 @@ extern "C" pkv_status paged_attention_decode_cascade(
     size_t workspace_bytes, void *stream) {
   pkv_status st = validate_cache(cache);
   if (st != PKV_OK) return st;
-  if (cache->dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
+  if (fp8 && !(cache->k_scale > 0.f && cache->v_scale > 0.f)) return PKV_ERR_ARG;
   if (batch < 0 || num_heads <= 0 || max_blocks <= 0 || max_seq_len < 0 || num_groups < 0 ||
       max_group_size < 0 || max_prefix_len < 0 || (max_prefix_len & 15) ||
       partition_tokens < 0 || (partition_tokens & 15) || !std::isfinite(scale) ||
@@ -1065,8 +1066,8 @@ extern "C" pkv_status paged_attention_decode_cascade(
   p.max_parts = l.stride;
   p.grid_parts = l.suffix_parts;
   p.part_tokens = l.pt;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.v_scale = 1.f;
+  p.scale_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
+  p.v_scale = fp8 ? cache->v_scale : 1.f;
   p.timeout_ns = 2000000000ull;
   p.group_start = fork ? group_start : nullptr;
   p.prefix_len = prefix_len;
@@ -1076,6 +1077,9 @@ extern "C" pkv_status paged_attention_decode_cascade(
   p.prefix_part_tokens = kCascadePrefixPartTokens;
   p.seq_start = seq_start;
   cudaEvent_t join = fork ? side.join : nullptr;
+  if (fp8)
+    return cache->head_dim == 128 ? launch_decode<true, 128>(mk, mv, p, s, join)
+                                  : launch_decode<true, 64>(mk, mv, p, s, join);
   return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, s, join)
                                 : launch_decode<false, 64>(mk, mv, p, s, join);
 }

@@ -59,7 +59,8 @@ struct PrefillParams {
   long long num_tokens;
   int batch, num_heads, num_kv_heads, group, tile_tokens;
   int num_blocks, max_blocks;
-  float scale_log2;
+  float scale_log2;   // scale * log2(e) (* k_scale for an fp8 cache)
+  float v_scale;      // 1 for bf16
   unsigned long long timeout_ns;
   // Shared-prefix mode (part_o != nullptr): grid.z runs over groups; the
   // members of group z are rows group_start[z] .. group_start[z+1] - 1 of q
@@ -78,31 +79,47 @@ struct PrefillParams {
   int prefix_part_tokens, pairs_per_part, max_prefix_len, max_group_size;
 };
 
-template <int D>
+// bf16 cache: K and V tiles arrive by TMA directly in the MMA operand
+// layout.  fp8 cache: the MMAs run on f16 operands (every E4M3 value is
+// exact in f16; q is converted from bf16 once), and the producer warp
+// converts each fp8 tile from a TMA staging ring into f16 operand tiles.
+template <bool FP8, int D>
 struct PrefillCfg {
   static constexpr int SLICES = D / 64;          // 64-element head_dim slices
   static constexpr int SLICE_BYTES = 128 * 128;  // 128 rows x 128 bytes
   static constexpr int TILE_BYTES = SLICES * SLICE_BYTES;
   // K is released as soon as both Q K^T products have read it, V only after
   // both P V products: K runs one tile ahead of V and gets the deeper ring.
-  static constexpr int KSTAGES = 3;
+  // fp8 cache: V converted a tile ahead (2 stages), K just in time for the
+  // next Q K^T (1 stage, refilled once both Q K^T of a tile are done).
+  static constexpr int KSTAGES = FP8 ? 1 : 3;
   static constexpr int VSTAGES = 2;
   static constexpr int KEYS = 128;               // keys per tile (8 blocks)
+  static constexpr int STG_HALF = KEYS * D;      // fp8 K (or V) of one tile
+  static constexpr int STG_STAGES = FP8 ? 2 : 0;
   static constexpr int Q_OFF = 0;                // two query tiles
   static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + KSTAGES * TILE_BYTES;
-  static constexpr int BAR_OFF = V_OFF + VSTAGES * TILE_BYTES;
+  static constexpr int STG_OFF = V_OFF + VSTAGES * TILE_BYTES;
+  static constexpr int BAR_OFF = STG_OFF + STG_STAGES * 2 * STG_HALF;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + alignment slack
   // TMEM: tile t uses columns 256 t .. 256 t + 127 for S_t (P_t in the
   // first 64) and 256 t + 128 .. for O_t.
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr int THREADS = 320;
+  // warp 0: TMA producer (and fp8 converter); warp 1: TMEM owner and MMA
+  // issuer; warps 2-5 / 6-9: softmax of tiles 0 / 1; fp8 cache: warps 10
+  // and 11 convert tiles too (12 warps still fit 168 registers a thread).
+  static constexpr int CONVERTERS = FP8 ? 3 : 1;
+  static constexpr int THREADS = FP8 ? 384 : 320;
 };
 
 struct PrefillBars {
   uint64_t q_full;
+  uint64_t q_ready;    // fp8 cache: q converted to f16 in place
   uint64_t k_full[3], k_empty[3];
   uint64_t v_full[2], v_empty[2];
+  uint64_t stg_full[2];  // fp8 cache: a tile's K and V bytes staged
+  uint64_t stg_empty[2]; // fp8 cache: both halves of a stage converted
   uint64_t v_fix;      // last tile: stale V rows past the keys zeroed
   uint64_t s_full[2];  // S_t(i) in TMEM (and PV_t(i-1) complete)
   uint64_t p_full[2];  // P_t(i) in TMEM, O_t rescaled
@@ -117,8 +134,8 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// O_t += P_t V with A = P_t read from TMEM (packed bf16 pairs, the even
-// element in the low half; 16 keys = 8 columns per MMA).
+// O_t += P_t V with A = P_t read from TMEM (packed bf16 / f16 pairs, the
+// even element in the low half; 16 keys = 8 columns per MMA).
 __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -141,12 +158,40 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
   return false;
 }
 
-template <int D>
-__global__ void __launch_bounds__(320, 1)
+// The same for code that the whole warp runs together (TMEM loads and
+// stores, warp barriers): every lane gets the same answer, so a timeout
+// never splits the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const PrefillParams &p,
+                                          volatile int *abort_flag) {
+  return __all_sync(0xffffffffu, wait_or_abort(bar, parity, p, abort_flag));
+}
+
+// 16 E4M3 bytes -> 16 f16 values (two 16-byte chunks, element order kept).
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4 v, uint4 &lo, uint4 &hi) {
+  e4m3x4_to_f16x2x2(v.x, lo.x, lo.y);
+  e4m3x4_to_f16x2x2(v.y, lo.z, lo.w);
+  e4m3x4_to_f16x2x2(v.z, hi.x, hi.y);
+  e4m3x4_to_f16x2x2(v.w, hi.z, hi.w);
+}
+
+// 8 bf16 -> 8 f16 (exact for values inside the f16 range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v));
+  const __half2 h = __float22half2_rn(f);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+template <bool FP8>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+  return FP8 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
+template <bool FP8, int D>
+__global__ void __launch_bounds__(PrefillCfg<FP8, D>::THREADS, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                          const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-  using C = PrefillCfg<D>;
+  using C = PrefillCfg<FP8, D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -234,17 +279,23 @@ __global__ void __launch_bounds__(320, 1)
     return;
   }
 
+  const int ntq = has_b ? 2 : 1;  // query tiles in use
   if (threadIdx.x == 0) {
     mbar_init(&bars.q_full, 1);
+    mbar_init(&bars.q_ready, 4 * ntq);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars.stg_full[s], 1);
+      mbar_init(&bars.stg_empty[s], C::CONVERTERS);
+    }
     for (int s = 0; s < C::KSTAGES; ++s) {
-      mbar_init(&bars.k_full[s], 1);
+      mbar_init(&bars.k_full[s], C::CONVERTERS);
       mbar_init(&bars.k_empty[s], 1);
     }
     for (int s = 0; s < C::VSTAGES; ++s) {
-      mbar_init(&bars.v_full[s], 1);
+      mbar_init(&bars.v_full[s], C::CONVERTERS);
       mbar_init(&bars.v_empty[s], 1);
     }
-    mbar_init(&bars.v_fix, 1);
+    mbar_init(&bars.v_fix, C::CONVERTERS);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.s_full[t], 1);
       mbar_init(&bars.p_full[t], 4);
@@ -267,68 +318,155 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t sV = smem_u32(smem + C::V_OFF);
   constexpr uint32_t TB = C::TILE_BYTES;
 
-  if (warp == 0) {
+  if (warp == 0 || warp >= 10) {
     // ------------------------------------------------------------ producer
     const int32_t *row = p.block_tables + (size_t)table_row * p.max_blocks + blk_begin;
-    if (lane == 0) {
+    const uint64_t pol = l2_policy_evict_normal();
+    if (warp == 0 && lane == 0) {
       prefetch_tensormap(&qmap);
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
-      const int ntq = has_b ? 2 : 1;
       mbar_arrive_expect_tx(&bars.q_full, ntq * C::SLICES * 128 * g * TQ);
       for (int t = 0; t < ntq; ++t)
         for (int s = 0; s < C::SLICES; ++s)
           tc::tma_load_4d(sQ + t * TB + s * C::SLICE_BYTES, &qmap, smem_u32(&bars.q_full), 0,
                           kvh * g, s, q0 + j0 + t * TQ);
-      const uint64_t pol = l2_policy_evict_normal();
-      // K(i + 1) is issued before V(i): Q K^T of the next tile needs its
-      // keys while the current tile's probabilities are still being formed.
-      auto issue = [&](bool is_k, int i) -> bool {
+    }
+    if constexpr (!FP8) {
+      if (lane == 0) {
+        // K(i + 1) is issued before V(i): Q K^T of the next tile needs its
+        // keys while the current tile's probabilities are still formed.
+        auto issue = [&](bool is_k, int i) -> bool {
+          const int stages = is_k ? C::KSTAGES : C::VSTAGES;
+          const int st = i % stages;
+          uint64_t *empty = is_k ? &bars.k_empty[st] : &bars.v_empty[st];
+          uint64_t *full = is_k ? &bars.k_full[st] : &bars.v_full[st];
+          if (i >= stages && !wait_or_abort(empty, ((i / stages) - 1) & 1, p, abort_flag))
+            return false;
+          const int nv = min(8, nblk - blk_begin - 8 * i);
+          mbar_arrive_expect_tx(full, nv * C::SLICES * 2048);
+          uint8_t *dst = smem + (is_k ? C::K_OFF : C::V_OFF) + st * TB;
+          for (int j = 0; j < nv; ++j) {
+            const int blk = row[8 * i + j];
+            for (int s = 0; s < C::SLICES; ++s)
+              tma_load_5d(dst + s * C::SLICE_BYTES + j * 2048, is_k ? &kmap : &vmap, full, 0, 0,
+                          kvh, s, blk, pol);
+          }
+          return true;
+        };
+        bool go = issue(true, 0);
+        for (int i = 0; go && i < n_tiles; ++i) {
+          if (i + 1 < n_tiles) go = issue(true, i + 1);
+          go = go && issue(false, i);
+        }
+      }
+      __syncwarp();
+      // The last tile's V rows past kv_len hold bytes that are not part of
+      // the sequence (stale cache contents or an older stage): zero them so
+      // that a zero probability never meets a NaN.
+      const int last = n_tiles - 1, st = last % C::VSTAGES;
+      if (warp_wait(&bars.v_full[st], (last / C::VSTAGES) & 1, p, abort_flag)) {
+        const int first = kv_len - kv_begin - last * C::KEYS;
+        uint8_t *vbase = smem + C::V_OFF + st * TB;
+        for (int idx = first * 8 + lane; idx < C::KEYS * 8; idx += 32)
+          for (int s = 0; s < C::SLICES; ++s)
+            *reinterpret_cast<uint4 *>(vbase + s * C::SLICE_BYTES + idx * 16) =
+                make_uint4(0, 0, 0, 0);
+        tc::fence_proxy_async_smem();
+      }
+    } else {
+      // fp8 cache: TMA stages each tile's K and V bytes (one box of 16 rows
+      // per block, rows of head_dim bytes, unswizzled) two tiles ahead; the
+      // whole warp converts them into the f16 operand tiles.
+      auto stage_load = [&](int i) {
+        const int sst = i % 2;
+        const int nv = min(8, nblk - blk_begin - 8 * i);
+        mbar_arrive_expect_tx(&bars.stg_full[sst], 2 * nv * 16 * D);
+        uint8_t *dst = smem + C::STG_OFF + sst * 2 * C::STG_HALF;
+        for (int j = 0; j < nv; ++j) {
+          const int blk = row[8 * i + j];
+          tma_load_5d(dst + j * 16 * D, &kmap, &bars.stg_full[sst], 0, 0, kvh, 0, blk, pol);
+          tma_load_5d(dst + C::STG_HALF + j * 16 * D, &vmap, &bars.stg_full[sst], 0, 0, kvh, 0, blk,
+                      pol);
+        }
+      };
+      const int ci = warp == 0 ? 0 : warp - 9;  // converter index
+      constexpr int STRIDE = 32 * C::CONVERTERS;
+      if (warp == 0 && lane == 0) {
+        stage_load(0);
+        if (n_tiles > 1) stage_load(1);
+      }
+      __syncwarp();
+      // Convert tile i's K or V; V rows past the sequence's keys become 0.
+      auto convert = [&](bool is_k, int i) -> bool {
+        const int sst = i % 2;
         const int stages = is_k ? C::KSTAGES : C::VSTAGES;
         const int st = i % stages;
         uint64_t *empty = is_k ? &bars.k_empty[st] : &bars.v_empty[st];
-        uint64_t *full = is_k ? &bars.k_full[st] : &bars.v_full[st];
-        if (i >= stages && !wait_or_abort(empty, ((i / stages) - 1) & 1, p, abort_flag))
+        if (!warp_wait(&bars.stg_full[sst], (i / 2) & 1, p, abort_flag) ||
+            (i >= stages && !warp_wait(empty, ((i / stages) - 1) & 1, p, abort_flag)))
           return false;
-        const int nv = min(8, nblk - blk_begin - 8 * i);
-        mbar_arrive_expect_tx(full, nv * C::SLICES * 2048);
+        const uint8_t *src = smem + C::STG_OFF + sst * 2 * C::STG_HALF + (is_k ? 0 : C::STG_HALF);
         uint8_t *dst = smem + (is_k ? C::K_OFF : C::V_OFF) + st * TB;
-        for (int j = 0; j < nv; ++j) {
-          const int blk = row[8 * i + j];
-          for (int s = 0; s < C::SLICES; ++s)
-            tma_load_5d(dst + s * C::SLICE_BYTES + j * 2048, is_k ? &kmap : &vmap, full, 0, 0,
-                        kvh, s, blk, pol);
+        const int loaded = min(8, nblk - blk_begin - 8 * i) * 16;
+        const int rows = is_k ? loaded : min(C::KEYS, kv_len - kv_begin - i * C::KEYS);
+        const int last_row = is_k ? loaded : C::KEYS;  // K rows past `loaded` stay stale (masked)
+        constexpr int CH = D / 16;                     // 16-byte fp8 chunks per row
+        const int total = last_row * CH;
+        // four chunks per lane in flight: loads first, then convert + store
+        for (int q0c = ci * 32; q0c < total; q0c += 4 * STRIDE) {
+          uint4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int q = q0c + u * STRIDE + lane, r = q / CH;
+            v[u] = (q < total && r < rows)
+                       ? *reinterpret_cast<const uint4 *>(src + r * D + (q % CH) * 16)
+                       : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int q = q0c + u * STRIDE + lane;
+            if (q >= total) break;
+            const int r = q / CH, cb = (q % CH) * 16;  // row, first element
+            uint4 lo, hi;
+            e4m3x16_to_f16(v[u], lo, hi);  // zero bytes give +0
+            const int c16 = (cb % 64) / 8;
+            uint8_t *base = dst + (cb / 64) * C::SLICE_BYTES + r * 128;
+            *reinterpret_cast<uint4 *>(base + ((c16 ^ (r & 7)) * 16)) = lo;
+            *reinterpret_cast<uint4 *>(base + (((c16 + 1) ^ (r & 7)) * 16)) = hi;
+          }
         }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(smem_u32(is_k ? &bars.k_full[st] : &bars.v_full[st]));
         return true;
       };
-      bool go = issue(true, 0);
+      bool go = convert(true, 0);
       for (int i = 0; go && i < n_tiles; ++i) {
-        if (i + 1 < n_tiles) go = issue(true, i + 1);
-        go = go && issue(false, i);
+        go = convert(false, i);
+        if (go && i + 1 < n_tiles) go = convert(true, i + 1);
+        __syncwarp();
+        // both halves of stage i % 2 (K(i) in the previous round, V(i) in
+        // this one) are converted by every converter: warp 0 refills it
+        if (go && lane == 0) tc::mbar_arrive(smem_u32(&bars.stg_empty[i % 2]));
+        if (go && warp == 0 && lane == 0 && i + 2 < n_tiles) {
+          if (!wait_or_abort(&bars.stg_empty[i % 2], (i / 2) & 1, p, abort_flag))
+            go = false;
+          else
+            stage_load(i + 2);
+        }
+        go = __all_sync(0xffffffffu, go);
       }
-    }
-    __syncwarp();
-    // The last tile's V rows past kv_len hold bytes that are not part of
-    // the sequence (stale cache contents or an older stage): zero them so
-    // that a zero probability never meets a NaN.
-    const int last = n_tiles - 1, st = last % C::VSTAGES;
-    if (wait_or_abort(&bars.v_full[st], (last / C::VSTAGES) & 1, p, abort_flag)) {
-      const int first = kv_len - kv_begin - last * C::KEYS;
-      uint8_t *vbase = smem + C::V_OFF + st * TB;
-      for (int idx = first * 8 + lane; idx < C::KEYS * 8; idx += 32)
-        for (int s = 0; s < C::SLICES; ++s)
-          *reinterpret_cast<uint4 *>(vbase + s * C::SLICE_BYTES + idx * 16) =
-              make_uint4(0, 0, 0, 0);
-      tc::fence_proxy_async_smem();
     }
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(smem_u32(&bars.v_fix));
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idS = tc::idesc_bf16_f32(128, C::KEYS, false, false);
-      constexpr uint32_t idO = tc::idesc_bf16_f32(128, D, false, true);
-      const int ntq = has_b ? 2 : 1;
+      constexpr uint32_t idS = FP8 ? tc::idesc_f16_f32(128, C::KEYS, false, false)
+                                   : tc::idesc_bf16_f32(128, C::KEYS, false, false);
+      constexpr uint32_t idO = FP8 ? tc::idesc_f16_f32(128, D, false, true)
+                                   : tc::idesc_bf16_f32(128, D, false, true);
       // Descriptors are built once; stepping K adds the byte offset / 16 to
       // the start-address field (bits 0-13), which never carries out.
       const uint64_t q_desc0 = tc::smem_desc(sQ, 16, 1024, tc::kSwizzle128B);
@@ -355,7 +493,7 @@ __global__ void __launch_bounds__(320, 1)
         tc::mma_commit(smem_u32(&bars.o_done[t]));
         if (t == ntq - 1) tc::mma_commit(smem_u32(&bars.v_empty[i % C::VSTAGES]));
       };
-      bool ok = wait_or_abort(&bars.q_full, 0, p, abort_flag) &&
+      bool ok = wait_or_abort(FP8 ? &bars.q_ready : &bars.q_full, 0, p, abort_flag) &&
                 wait_or_abort(&bars.k_full[0], 0, p, abort_flag);
       if (ok) {
         tc::fence_after_sync();
@@ -381,7 +519,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 10) {
     // ------------------------------------------------------------ softmax
     const int t = (warp - 2) / 4;  // query tile of this warp
     const int quarter = warp % 4;
@@ -394,8 +532,25 @@ __global__ void __launch_bounds__(320, 1)
     const int lim = row_valid && !prefix_mode ? c + jr : kv_len - 1;
     float m_used = -INFINITY, l = 0.f;
     bool ok = t == 0 || has_b;
+    if (FP8 && ok) {
+      // q of this tile from bf16 to f16, in place (same swizzled layout)
+      if ((ok = warp_wait(&bars.q_full, 0, p, abort_flag))) {
+        uint8_t *qt = smem + C::Q_OFF + t * TB;
+        for (int idx = quarter * 32 + lane; idx < TB / 16; idx += 128) {
+          uint4 v = *reinterpret_cast<uint4 *>(qt + idx * 16);
+          v.x = bf16x2_to_f16x2(v.x);
+          v.y = bf16x2_to_f16x2(v.y);
+          v.z = bf16x2_to_f16x2(v.z);
+          v.w = bf16x2_to_f16x2(v.w);
+          *reinterpret_cast<uint4 *>(qt + idx * 16) = v;
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(smem_u32(&bars.q_ready));
+      }
+    }
     for (int i = 0; ok && i < n_tiles; ++i) {
-      if (!(ok = wait_or_abort(&bars.s_full[t], i & 1, p, abort_flag))) break;
+      if (!(ok = warp_wait(&bars.s_full[t], i & 1, p, abort_flag))) break;
       tc::fence_after_sync();
       uint32_t sr[4][32];
 #pragma unroll
@@ -439,7 +594,7 @@ __global__ void __launch_bounds__(320, 1)
           const float p1 = fast_exp2(fmaf(__uint_as_float(sr[q][e + 1]), p.scale_log2, -m_new));
           ls[e % 8] += p0;
           ls[(e + 1) % 8] += p1;
-          sr[q][e / 2] = pack_bf16x2(p0, p1);
+          sr[q][e / 2] = pack_p<FP8>(p0, p1);
         }
       l = l * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
       m_used = m_new;
@@ -464,9 +619,9 @@ __global__ void __launch_bounds__(320, 1)
       if (lane == 0) tc::mbar_arrive(smem_u32(&bars.p_full[t]));
     }
     // epilogue: O_t / l -> bf16 rows of out, or the partition's partial
-    if (ok && wait_or_abort(&bars.o_done[t], (n_tiles - 1) & 1, p, abort_flag)) {
+    if (ok && warp_wait(&bars.o_done[t], (n_tiles - 1) & 1, p, abort_flag)) {
       tc::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = l > 0.f ? p.v_scale / l : 0.f;
       const size_t orow_i = (size_t)(q0 + jr) * p.num_heads + kvh * g + r % g;
       if (prefix_mode && row_valid) p.part_ml[orow_i * p.part_stride + pp] = make_float2(m_used, l);
 #pragma unroll
@@ -534,9 +689,22 @@ PFN_cuTensorMapEncodeTiled_v12000 prefill_encode_fn() {
 // K or V cache: dims {64, 16 tokens, num_kv_heads, head_dim / 64, num_blocks},
 // box {64, 16, 1, 1, 1}: one 64-element head_dim slice of one kv head of
 // one block lands as 16 consecutive 128-byte swizzled rows.
+// fp8 cache: dims {head_dim, 16 tokens, num_kv_heads, 1, num_blocks}, box
+// {head_dim, 16, 1, 1, 1}, unswizzled: a block-head lands as 16 rows of
+// head_dim bytes for the conversion into f16 operand tiles.
 bool encode_prefill_cache_map(CUtensorMap *map, void *base, const pkv_cache *c) {
   auto fn = prefill_encode_fn();
   if (!fn) return false;
+  if (c->dtype == PKV_FP8_E4M3) {
+    const cuuint64_t row = (cuuint64_t)c->head_dim;
+    cuuint64_t dims[5] = {row, 16, (cuuint64_t)c->num_kv_heads, 1, (cuuint64_t)c->num_blocks};
+    cuuint64_t strides[4] = {row * c->num_kv_heads, row, row, row * c->num_kv_heads * 16};
+    cuuint32_t box[5] = {(cuuint32_t)row, 16, 1, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, base, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   const cuuint64_t row = (cuuint64_t)c->head_dim * 2;
   cuuint64_t dims[5] = {64, 16, (cuuint64_t)c->num_kv_heads, (cuuint64_t)c->head_dim / 64,
                         (cuuint64_t)c->num_blocks};
@@ -569,7 +737,7 @@ bool encode_query_map(CUtensorMap *map, const void *q, long long num_tokens, int
 
 struct PrefillMapEntry {
   void *key_cache, *value_cache;
-  int32_t num_blocks, num_kv_heads, head_dim;
+  int32_t num_blocks, num_kv_heads, head_dim, dtype;
   CUtensorMap k, v;
 };
 
@@ -582,7 +750,7 @@ bool get_prefill_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
     const PrefillMapEntry &e = entries[i];
     if (e.key_cache == c->key_cache && e.value_cache == c->value_cache &&
         e.num_blocks == c->num_blocks && e.num_kv_heads == c->num_kv_heads &&
-        e.head_dim == c->head_dim) {
+        e.head_dim == c->head_dim && e.dtype == c->dtype) {
       *k = e.k;
       *v = e.v;
       return true;
@@ -594,6 +762,7 @@ bool get_prefill_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
   e.num_blocks = c->num_blocks;
   e.num_kv_heads = c->num_kv_heads;
   e.head_dim = c->head_dim;
+  e.dtype = c->dtype;
   if (!encode_prefill_cache_map(&e.k, c->key_cache, c) ||
       !encode_prefill_cache_map(&e.v, c->value_cache, c))
     return false;
@@ -605,10 +774,10 @@ bool get_prefill_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
   return true;
 }
 
-template <int D>
+template <bool FP8, int D>
 pkv_status launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                           const PrefillParams &p, int q_tiles, cudaStream_t s) {
-  using C = PrefillCfg<D>;
+  using C = PrefillCfg<FP8, D>;
   static int configured[64] = {0};
   static std::mutex mu;
   int dev = 0;
@@ -616,7 +785,7 @@ pkv_status launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CU
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!configured[dev]) {
-      if (cudaFuncSetAttribute(paged_prefill_kernel<D>,
+      if (cudaFuncSetAttribute(paged_prefill_kernel<FP8, D>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::SMEM_BYTES) != cudaSuccess)
         return PKV_ERR_CUDA;
@@ -633,9 +802,28 @@ pkv_status launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CU
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, paged_prefill_kernel<D>, mq, mk, mv, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, paged_prefill_kernel<FP8, D>, mq, mk, mv, p) != cudaSuccess)
     return PKV_ERR_CUDA;
   return PKV_OK;
+}
+
+pkv_status dispatch_prefill(const pkv_cache *cache, const CUtensorMap &mq, const CUtensorMap &mk,
+                            const CUtensorMap &mv, const PrefillParams &p, int q_tiles,
+                            cudaStream_t s) {
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
+  if (cache->head_dim == 128)
+    return fp8 ? launch_prefill<true, 128>(mq, mk, mv, p, q_tiles, s)
+               : launch_prefill<false, 128>(mq, mk, mv, p, q_tiles, s);
+  return fp8 ? launch_prefill<true, 64>(mq, mk, mv, p, q_tiles, s)
+             : launch_prefill<false, 64>(mq, mk, mv, p, q_tiles, s);
+}
+
+// Score and output scales: fp8 folds k_scale into the score scale and
+// v_scale into the output.
+void set_scales(PrefillParams *p, const pkv_cache *cache, float scale) {
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
+  p->scale_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
+  p->v_scale = fp8 ? cache->v_scale : 1.f;
 }
 
 }  // namespace
@@ -667,7 +855,7 @@ pkv_status launch_prefix_partials(const void *q, const pkv_cache *cache,
   p.tile_tokens = tq;
   p.num_blocks = cache->num_blocks;
   p.max_blocks = max_blocks;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  set_scales(&p, cache, scale);
   p.timeout_ns = 2000000000ull;
   p.part_o = part_o;
   p.part_ml = part_ml;
@@ -678,8 +866,7 @@ pkv_status launch_prefix_partials(const void *q, const pkv_cache *cache,
   p.pairs_per_part = pairs;
   p.max_prefix_len = max_prefix_len;
   p.max_group_size = max_group_size;
-  return cache->head_dim == 128 ? launch_prefill<128>(mq, mk, mv, p, pairs * parts, s)
-                                : launch_prefill<64>(mq, mk, mv, p, pairs * parts, s);
+  return dispatch_prefill(cache, mq, mk, mv, p, pairs * parts, s);
 }
 
 unsigned long long read_and_clear_error_prefill(cudaStream_t s, cudaError_t *err) {
@@ -709,7 +896,8 @@ extern "C" pkv_status paged_attention_prefill(const void *q, const pkv_cache *ca
                                               void *out, int32_t max_query_len, void *stream) {
   pkv_status st = validate_cache(cache);
   if (st != PKV_OK) return st;
-  if (cache->dtype != PKV_BF16) return PKV_ERR_DTYPE;
+  if (cache->dtype == PKV_FP8_E4M3 && !(cache->k_scale > 0.f && cache->v_scale > 0.f))
+    return PKV_ERR_ARG;
   if (batch < 0 || num_heads <= 0 || max_blocks <= 0 || num_tokens < 0 || max_query_len < 0 ||
       !std::isfinite(scale) || !(scale > 0.f))
     return PKV_ERR_ARG;
@@ -744,9 +932,8 @@ extern "C" pkv_status paged_attention_prefill(const void *q, const pkv_cache *ca
   p.tile_tokens = tq;
   p.num_blocks = cache->num_blocks;
   p.max_blocks = max_blocks;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  set_scales(&p, cache, scale);
   p.timeout_ns = 2000000000ull;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return cache->head_dim == 128 ? launch_prefill<128>(mq, mk, mv, p, (int)q_tiles, s)
-                                : launch_prefill<64>(mq, mk, mv, p, (int)q_tiles, s);
+  return dispatch_prefill(cache, mq, mk, mv, p, (int)q_tiles, s);
 }

@@ -403,6 +403,8 @@ class PrefillWorkload:
     init_value: np.ndarray
     scale: float = 0.0
     kv_dtype: str = "bf16"
+    k_scale: float = 1.0
+    v_scale: float = 1.0
     block_size: int = BLOCK_SIZE
     seed: int = 0
 
@@ -427,8 +429,12 @@ class PrefillWorkload:
         return int(self.chunk.max()) if self.batch else 0
 
     @property
+    def elem_bytes(self) -> int:
+        return 2 if self.kv_dtype == "bf16" else 1
+
+    @property
     def block_bytes(self) -> int:
-        return self.block_size * self.num_kv_heads * self.head_dim * 2
+        return self.block_size * self.num_kv_heads * self.head_dim * self.elem_bytes
 
     def attention_flops(self) -> int:
         """Algorithmic multiply-add flops of the step's attention: every
@@ -441,11 +447,14 @@ class PrefillWorkload:
 
 def make_prefill_workload(name: str, history, chunk, num_heads: int,
                           num_kv_heads: int, head_dim: int, seed: int,
-                          pool_factor: float = 1.2) -> PrefillWorkload:
+                          pool_factor: float = 1.2,
+                          kv_dtype: str = "bf16") -> PrefillWorkload:
     """Draw a chunked-prefill step: blocks for every sequence taken from a
     shuffled pool 20% larger than needed, the whole pool first filled with
-    0xFF bytes (bf16 NaN) so that any read of an unwritten slot shows,
-    history K/V drawn N(0,1) in place, the chunk's K/V and q drawn N(0,1)."""
+    0xFF bytes (NaN in bf16 and in E4M3) so that any read of an unwritten
+    slot shows, history K/V drawn N(0,1) in place, the chunk's K/V and q
+    drawn N(0,1).  For an E4M3 cache each tensor's scale maps its largest
+    magnitude to 448 (the values are quantised by the write step)."""
     rng = np.random.default_rng(seed)
     history = np.asarray(history, dtype=np.int32)
     chunk = np.asarray(chunk, dtype=np.int32)
@@ -469,46 +478,64 @@ def make_prefill_workload(name: str, history, chunk, num_heads: int,
     step_slots = np.concatenate([slots_of(b, int(history[b]), int(lens[b]))
                                  for b in range(len(lens))] or [np.zeros(0, np.int64)])
     Th, T = hist_slots.size, step_slots.size
-    pool_bytes = num_blocks * BLOCK_SIZE * Hkv * d * 2
+    elt = 2 if kv_dtype == "bf16" else 1
+    pool_bytes = num_blocks * BLOCK_SIZE * Hkv * d * elt
+    q = _draw_bf16(rng, (T, num_heads, d))
+    hist_k, hist_v = _draw_bf16(rng, (Th, Hkv, d)), _draw_bf16(rng, (Th, Hkv, d))
+    step_k, step_v = _draw_bf16(rng, (T, Hkv, d)), _draw_bf16(rng, (T, Hkv, d))
+    k_scale = v_scale = 1.0
+    if kv_dtype != "bf16":
+        amax = lambda *a: max(float(np.abs(bf16_values(x)).max()) if x.size else 0.0
+                              for x in a)
+        k_scale = float(np.float32(amax(hist_k, step_k) / 448.0))
+        v_scale = float(np.float32(amax(hist_v, step_v) / 448.0))
     return PrefillWorkload(
         name=name, num_heads=num_heads, num_kv_heads=Hkv, head_dim=d,
         num_blocks=num_blocks, max_blocks=max_blocks, history=history,
-        chunk=chunk, block_tables=tables,
-        q=_draw_bf16(rng, (T, num_heads, d)),
-        hist_k=_draw_bf16(rng, (Th, Hkv, d)), hist_v=_draw_bf16(rng, (Th, Hkv, d)),
-        hist_slots=hist_slots,
-        step_k=_draw_bf16(rng, (T, Hkv, d)), step_v=_draw_bf16(rng, (T, Hkv, d)),
-        step_slots=step_slots,
+        chunk=chunk, block_tables=tables, q=q,
+        hist_k=hist_k, hist_v=hist_v, hist_slots=hist_slots,
+        step_k=step_k, step_v=step_v, step_slots=step_slots,
         init_key=np.full(pool_bytes, 0xFF, dtype=np.uint8),
         init_value=np.full(pool_bytes, 0xFF, dtype=np.uint8),
-        scale=1.0 / float(np.sqrt(d)), seed=seed)
+        scale=1.0 / float(np.sqrt(d)), kv_dtype=kv_dtype, k_scale=k_scale,
+        v_scale=v_scale, seed=seed)
 
 
-def prefill_8k(seed: int = 6, small: bool = False) -> PrefillWorkload:
+def prefill_8k(seed: int = 6, small: bool = False,
+               kv_dtype: str = "bf16") -> PrefillWorkload:
     """Prefill step of about 8K tokens (the vLLM v0.17.1 notes' prefill
     batch size): 8 fresh prompts of 1024 tokens, Llama-8B shape (32 q /
     8 kv heads, head_dim 128)."""
     if small:
         return make_prefill_workload("prefill_8k_small", [0, 0, 0],
-                                     [300, 129, 17], 32, 8, 128, seed)
+                                     [300, 129, 17], 32, 8, 128, seed,
+                                     kv_dtype=kv_dtype)
     return make_prefill_workload("prefill_8k", [0] * 8, [1024] * 8, 32, 8, 128,
-                                 seed)
+                                 seed, kv_dtype=kv_dtype)
 
 
-def chunked_prefill_8k(seed: int = 7, small: bool = False) -> PrefillWorkload:
+def chunked_prefill_8k(seed: int = 7, small: bool = False,
+                       kv_dtype: str = "bf16") -> PrefillWorkload:
     """Chunked prefill of about 8K tokens: 8 chunks of 1024 tokens, each
     after a history uniform in [1024, 7168] tokens, Llama-8B shape."""
     rng = np.random.default_rng(seed)
     if small:
         hist = [int(x) for x in rng.integers(50, 600, 4)]
         return make_prefill_workload("chunked_prefill_8k_small", hist,
-                                     [200, 37, 1, 130], 32, 8, 128, seed)
+                                     [200, 37, 1, 130], 32, 8, 128, seed,
+                                     kv_dtype=kv_dtype)
     hist = [int(x) for x in rng.integers(1024, 7169, 8)]
     return make_prefill_workload("chunked_prefill_8k", hist, [1024] * 8, 32, 8,
-                                 128, seed)
+                                 128, seed, kv_dtype=kv_dtype)
+
+
+def chunked_prefill_8k_fp8(seed: int = 7, small: bool = False) -> PrefillWorkload:
+    """The chunked-prefill step on an E4M3 cache with per-tensor scales."""
+    return chunked_prefill_8k(seed, small, kv_dtype="fp8_e4m3")
 
 
 PREFILL_CONFIGS = {
     "prefill_8k": prefill_8k,
     "chunked_prefill_8k": chunked_prefill_8k,
+    "chunked_prefill_8k_fp8": chunked_prefill_8k_fp8,
 }

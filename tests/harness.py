@@ -155,9 +155,10 @@ def upload_prefill(W: PrefillWorkload, device="cuda") -> PrefillGpuState:
     """Pool bytes to the device and the history written through
     paged_kv_write; the chunk's K/V stay pending for the step."""
     shape = (W.num_blocks, W.block_size, W.num_kv_heads, W.head_dim)
-    kc = torch.from_numpy(W.init_key).view(torch.bfloat16).reshape(shape).to(device)
-    vc = torch.from_numpy(W.init_value).view(torch.bfloat16).reshape(shape).to(device)
-    cache = PagedKVCache(kc, vc, "bf16")
+    dt = torch.bfloat16 if W.kv_dtype == "bf16" else torch.uint8
+    kc = torch.from_numpy(W.init_key).view(dt).reshape(shape).to(device)
+    vc = torch.from_numpy(W.init_value).view(dt).reshape(shape).to(device)
+    cache = PagedKVCache(kc, vc, W.kv_dtype, W.k_scale, W.v_scale)
     if W.hist_slots.size:
         chunk = 1 << 18
         for s in range(0, W.hist_slots.size, chunk):
@@ -184,20 +185,25 @@ def gpu_prefill_step(W: PrefillWorkload, G: PrefillGpuState, out=None):
                                    out=out)
 
 
+def _oracle_dtype(W):
+    return oracle.DTYPE_BF16 if W.kv_dtype == "bf16" else oracle.DTYPE_FP8_E4M3
+
+
 def oracle_prefill_cache(W: PrefillWorkload):
     o = oracle.load()
     kc = W.init_key.copy()
     vc = W.init_value.copy()
     for k, v, sl in ((W.hist_k, W.hist_v, W.hist_slots),
                      (W.step_k, W.step_v, W.step_slots)):
-        assert o.kv_write(kc, vc, oracle.DTYPE_BF16, W.block_size,
-                          W.num_kv_heads, W.head_dim, 1.0, 1.0, k, v, sl) == 0
+        assert o.kv_write(kc, vc, _oracle_dtype(W), W.block_size,
+                          W.num_kv_heads, W.head_dim, W.k_scale, W.v_scale,
+                          k, v, sl) == 0
     return kc, vc
 
 
 def oracle_prefill_out(W: PrefillWorkload, kc, vc, rows=None, n_threads=0):
     out, err = oracle.load().attention_prefill(
-        W.q, kc, vc, oracle.DTYPE_BF16, 1.0, 1.0, W.block_size,
+        W.q, kc, vc, _oracle_dtype(W), W.k_scale, W.v_scale, W.block_size,
         W.num_kv_heads, W.head_dim, W.block_tables, W.seq_lens,
         W.query_start_loc, W.scale, rows=rows, n_threads=n_threads)
     assert err == 0

@@ -12,13 +12,12 @@ import pytest
 import torch
 
 import harness
-from paged_kv_cache_48_gb300 import (PagedKVCache, PagedKVError,
-                                     paged_attention_decode,
+from paged_kv_cache_48_gb300 import (paged_attention_decode,
                                      paged_attention_decode_cascade, pkv_check)
 from paged_kv_cache_48_gb300 import workload as wl
 
 pytestmark = pytest.mark.gpu
-PKV_OK, PKV_ERR_DTYPE, PKV_ERR_RANGE = 0, 2, 5
+PKV_OK, PKV_ERR_RANGE = 0, 5
 
 
 def _i32(a):
@@ -120,11 +119,16 @@ def test_cascade_full_size_matches_decode_and_oracle_samples():
     harness.assert_close(out[seqs], ref[seqs], "bf16")
 
 
-def test_cascade_rejects_fp8_cache():
-    kc = torch.zeros((4, 16, 1, 64), dtype=torch.uint8, device="cuda")
-    cache = PagedKVCache(kc, kc.clone(), "fp8_e4m3", 1.0, 1.0)
-    q = torch.zeros((2, 1, 64), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(PagedKVError) as e:
-        paged_attention_decode_cascade(q, cache, _i32([[0], [0]]), _i32([4, 4]),
-                                       _i32([0, 2]), _i32([0]), 0.1, 4, 2, 0)
-    assert e.value.status == PKV_ERR_DTYPE
+def test_cascade_fp8_cache_matches_oracle():
+    """E4M3 cache with per-tensor scales: the prefix pass runs on f16
+    operands, the suffix pass in the fp8 decode kernel."""
+    W = wl.make_workload("prefix_fp8", 8, 40, 8, 128, 5, 60, 21,
+                         kv_dtype="fp8_e4m3", prefix_groups=2, prefix_len=64)
+    G = harness.upload(W)
+    harness.gpu_step(W, G)
+    gs, plen = _groups_of(W)
+    out = _cascade(W, G, gs, plen)
+    assert pkv_check()[0] == PKV_OK
+    kc, vc = harness.oracle_cache(W)
+    harness.assert_close(out.float().cpu().numpy(), harness.oracle_out(W, kc, vc),
+                         "fp8_e4m3")

@@ -5,7 +5,8 @@ paged_kv_write into a pool whose unwritten bytes are 0xFF (bf16 NaN), runs
 paged_attention_prefill and compares every row with the oracle on the same
 seeded inputs (|gpu - ref| <= 1e-2 + 1e-2 |ref|).  Shapes span several
 128-key tiles, several query tiles, ragged tails, one-token chunks, empty
-chunks and group sizes 1, 4, 5 and 8.
+chunks and group sizes 1, 4, 5 and 8, for bf16 and E4M3 caches (fp8 bound
+3e-2 + 3e-2 |ref|).
 """
 import numpy as np
 import pytest
@@ -13,13 +14,12 @@ import torch
 
 import harness
 import oracle
-from paged_kv_cache_48_gb300 import (PagedKVCache, PagedKVError,
-                                     paged_attention_decode,
+from paged_kv_cache_48_gb300 import (paged_attention_decode,
                                      paged_attention_prefill, pkv_check)
 from paged_kv_cache_48_gb300 import workload as wl
 
 pytestmark = pytest.mark.gpu
-PKV_OK, PKV_ERR_DTYPE, PKV_ERR_RANGE = 0, 2, 5
+PKV_OK, PKV_ERR_RANGE = 0, 5
 
 CASES = {
     # name: (history, chunk, Hq, Hkv, d)
@@ -41,14 +41,16 @@ def _run_case(W):
     return out.float().cpu().numpy(), G
 
 
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_prefill_matches_oracle(name):
+def test_prefill_matches_oracle(name, kv_dtype):
     hist, chunk, Hq, Hkv, d = CASES[name]
-    W = wl.make_prefill_workload(name, hist, chunk, Hq, Hkv, d, seed=len(name))
+    W = wl.make_prefill_workload(name, hist, chunk, Hq, Hkv, d, seed=len(name),
+                                 kv_dtype=kv_dtype)
     gpu, _ = _run_case(W)
     kc, vc = harness.oracle_prefill_cache(W)
     ref = harness.oracle_prefill_out(W, kc, vc)
-    harness.assert_close(gpu, ref, "bf16")
+    harness.assert_close(gpu, ref, kv_dtype)
 
 
 @pytest.mark.parametrize("cfg", ["prefill_8k", "chunked_prefill_8k"])
@@ -115,22 +117,26 @@ def test_prefill_bad_block_id_is_reported_and_rows_zeroed():
     harness.assert_close(o[:20], ref[:20], "bf16")
 
 
-def test_prefill_rejects_fp8_cache():
-    kc = torch.zeros((4, 16, 1, 64), dtype=torch.uint8, device="cuda")
-    cache = PagedKVCache(kc, kc.clone(), "fp8_e4m3", 1.0, 1.0)
-    q = torch.zeros((2, 1, 64), dtype=torch.bfloat16, device="cuda")
-    i32 = lambda v: torch.tensor(v, dtype=torch.int32, device="cuda")
-    with pytest.raises(PagedKVError) as e:
-        paged_attention_prefill(q, cache, i32([[0]]), i32([2]), i32([0, 2]),
-                                0.1, 2)
-    assert e.value.status == PKV_ERR_DTYPE
+def test_prefill_fp8_is_deterministic_and_matches_oracle():
+    """fp8 KV (g = 5): two runs are bitwise equal, and the f16 tensor-core
+    path (E4M3 tiles converted to f16 in shared memory) agrees with the
+    oracle on the same cache bytes (|err| <= 3e-2 + 3e-2 |ref|)."""
+    W = wl.make_prefill_workload("f8", [300, 0], [200, 150], 40, 8, 128, seed=12,
+                                 kv_dtype="fp8_e4m3")
+    a, G = _run_case(W)
+    b = paged_attention_prefill(G.q, G.cache, G.tables, G.seq_lens, G.qsl,
+                                W.scale, W.max_query_len).float().cpu().numpy()
+    assert np.array_equal(a, b)
+    kc, vc = harness.oracle_prefill_cache(W)
+    harness.assert_close(a, harness.oracle_prefill_out(W, kc, vc), "fp8_e4m3")
 
 
-def test_prefill_full_size_sampled_rows():
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_prefill_full_size_sampled_rows(kv_dtype):
     """The full 8K-token chunked-prefill step in the bench's launch
     configuration; rows sampled across every sequence (first, last and
     seeded random tokens, all heads of a group) against the oracle."""
-    W = wl.chunked_prefill_8k()
+    W = wl.chunked_prefill_8k(kv_dtype=kv_dtype)
     gpu, _ = _run_case(W)
     rng = np.random.default_rng(0)
     qsl = W.query_start_loc
@@ -143,4 +149,4 @@ def test_prefill_full_size_sampled_rows():
     kc, vc = harness.oracle_prefill_cache(W)
     ref = harness.oracle_prefill_out(W, kc, vc, rows=rows)
     harness.assert_close(gpu[rows[:, 0], rows[:, 1]], ref[rows[:, 0], rows[:, 1]],
-                         "bf16")
+                         kv_dtype)
