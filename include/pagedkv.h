@@ -220,9 +220,11 @@ pkv_status paged_attention_decode(const void *q, const pkv_cache *cache,
  *   max_query_len host upper bound of every n_b (sizes the grid); rows of
  *                 tokens past it are not computed.
  * Query row i of sequence b is at position c_b + i and attends to the key
- * positions 0 .. c_b + i; a one-token chunk is a decode step.  The cache
- * must be bf16 (PKV_ERR_DTYPE otherwise) and num_heads / num_kv_heads at
- * most 128.  Device-detected errors (n_b < 0, c_b < 0, a needed block id
+ * positions 0 .. c_b + i; a one-token chunk is a decode step.  With an
+ * E4M3 cache the products run in f16 (the cache values are exact there; q
+ * is rounded from bf16 to f16, so it must lie inside the f16 range) with
+ * k_scale and v_scale applied as in paged_attention_decode.
+ * num_heads / num_kv_heads must be at most 128.  Device-detected errors (n_b < 0, c_b < 0, a needed block id
  * outside the pool, seq_lens[b] > 16 * max_blocks) are reported by
  * pkv_check(); the affected rows are zeroed where they lie inside q. */
 pkv_status paged_attention_prefill(const void *q, const pkv_cache *cache,
@@ -251,8 +253,9 @@ pkv_status paged_attention_prefill(const void *q, const pkv_cache *cache,
  *   max_group_size, max_prefix_len  host bounds (size the prefix grid).
  *   workspace     at least paged_attention_cascade_workspace_bytes(...),
  *                 256-byte aligned.
- *   Other arguments as for paged_attention_decode; scale must be positive
- *   and the cache bf16 (PKV_ERR_DTYPE otherwise).
+ *   Other arguments as for paged_attention_decode; scale must be positive.
+ *   Both bf16 and E4M3 caches are accepted (the prefix pass of an E4M3
+ *   cache runs on f16 operands, as in paged_attention_prefill).
  * Pass 1 (tensor cores) attends each group's member queries to its prefix,
  * 512 tokens per partition; pass 2 attends each sequence to its own
  * tokens; a log-sum-exp merge combines the partials.  A group whose
