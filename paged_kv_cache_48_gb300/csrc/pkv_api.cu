@@ -73,4 +73,4 @@ extern "C" const char *pkv_status_str(pkv_status status) {
   return "unknown status";
 }
 
-extern "C" int32_t pkv_version(void) { return 100; }
+extern "C" int32_t pkv_version(void) { return 200; }
