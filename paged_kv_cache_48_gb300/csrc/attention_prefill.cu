@@ -83,34 +83,41 @@ struct PrefillParams {
 // layout.  fp8 cache: the MMAs run on f16 operands (every E4M3 value is
 // exact in f16; q is converted from bf16 once), and the producer warp
 // converts each fp8 tile from a TMA staging ring into f16 operand tiles.
-template <bool FP8, int D>
+// PREFIX: the shared-prefix pass of cascade decode.  Its groups hold few
+// query rows, so one query tile, single-stage rings and 6 warps (about
+// 96 KB of shared memory, 256 TMEM columns) let two of its CTAs, or one
+// beside decode CTAs, share an SM.
+template <bool FP8, int D, bool PREFIX = false>
 struct PrefillCfg {
   static constexpr int SLICES = D / 64;          // 64-element head_dim slices
   static constexpr int SLICE_BYTES = 128 * 128;  // 128 rows x 128 bytes
   static constexpr int TILE_BYTES = SLICES * SLICE_BYTES;
+  static constexpr int NQT = PREFIX ? 1 : 2;     // query tiles per CTA
   // K is released as soon as both Q K^T products have read it, V only after
   // both P V products: K runs one tile ahead of V and gets the deeper ring.
   // fp8 cache: V converted a tile ahead (2 stages), K just in time for the
   // next Q K^T (1 stage, refilled once both Q K^T of a tile are done).
-  static constexpr int KSTAGES = FP8 ? 1 : 3;
-  static constexpr int VSTAGES = 2;
+  static constexpr int KSTAGES = PREFIX ? 1 : (FP8 ? 1 : 3);
+  static constexpr int VSTAGES = PREFIX ? 1 : 2;
   static constexpr int KEYS = 128;               // keys per tile (8 blocks)
   static constexpr int STG_HALF = KEYS * D;      // fp8 K (or V) of one tile
   static constexpr int STG_STAGES = FP8 ? 2 : 0;
-  static constexpr int Q_OFF = 0;                // two query tiles
-  static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + NQT * TILE_BYTES;
   static constexpr int V_OFF = K_OFF + KSTAGES * TILE_BYTES;
   static constexpr int STG_OFF = V_OFF + VSTAGES * TILE_BYTES;
   static constexpr int BAR_OFF = STG_OFF + STG_STAGES * 2 * STG_HALF;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + alignment slack
   // TMEM: tile t uses columns 256 t .. 256 t + 127 for S_t (P_t in the
   // first 64) and 256 t + 128 .. for O_t.
-  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TMEM_COLS = 256 * NQT;
   // warp 0: TMA producer (and fp8 converter); warp 1: TMEM owner and MMA
-  // issuer; warps 2-5 / 6-9: softmax of tiles 0 / 1; fp8 cache: warps 10
-  // and 11 convert tiles too (12 warps still fit 168 registers a thread).
-  static constexpr int CONVERTERS = FP8 ? 3 : 1;
-  static constexpr int THREADS = FP8 ? 384 : 320;
+  // issuer; warps 2-5 / 6-9: softmax of tiles 0 / 1; fp8 cache with two
+  // tiles: warps 10 and 11 convert tiles too (12 warps still fit 168
+  // registers a thread).
+  static constexpr int CONVERTERS = (FP8 && !PREFIX) ? 3 : 1;
+  static constexpr int THREADS = PREFIX ? 192 : (FP8 ? 384 : 320);
+  static constexpr int MIN_BLOCKS = PREFIX ? 2 : 1;
 };
 
 struct PrefillBars {
@@ -186,12 +193,13 @@ __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
   return FP8 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
 
-template <bool FP8, int D>
-__global__ void __launch_bounds__(PrefillCfg<FP8, D>::THREADS, 1)
+template <bool FP8, int D, bool PREFIX>
+__global__ void __launch_bounds__(PrefillCfg<FP8, D, PREFIX>::THREADS,
+                                  PrefillCfg<FP8, D, PREFIX>::MIN_BLOCKS)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                          const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
-  using C = PrefillCfg<FP8, D>;
+  using C = PrefillCfg<FP8, D, PREFIX>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -200,7 +208,7 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D>::THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int b = blockIdx.z, kvh = blockIdx.y;
-  const bool prefix_mode = p.part_o != nullptr;
+  constexpr bool prefix_mode = PREFIX;
   const int order = gridDim.x - 1 - blockIdx.x;  // longest tile pairs first
   const int qp = prefix_mode ? order % p.pairs_per_part : order;
   const int pp = prefix_mode ? order / p.pairs_per_part : 0;  // prefix partition
@@ -213,7 +221,7 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D>::THREADS, 1)
   // keys kv_begin .. kv_len - 1 through block-table row table_row.
   int q0, n_b, c = 0, kv_begin = 0, kv_len = 0, table_row = b;
   bool bad_seq;
-  const int j0 = qp * 2 * TQ;
+  const int j0 = qp * C::NQT * TQ;
   if (prefix_mode) {
     q0 = p.group_start[b];
     n_b = p.group_start[b + 1] - q0;
@@ -221,7 +229,8 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D>::THREADS, 1)
     // the same structural test the decode pass applies: a group that fails
     // it is attended in full there, so no partial is needed
     bad_seq = n_b < 1 || q0 < 0 || (long long)q0 + n_b > p.num_tokens || P <= 0 || (P & 15) ||
-              P > p.max_blocks * 16 || P > p.max_prefix_len || n_b > p.max_group_size;
+              P > p.max_blocks * 16 || P > p.max_prefix_len || n_b > p.max_group_size ||
+              n_b > p.pairs_per_part * C::NQT * TQ;
     if (bad_seq) return;
     kv_begin = pp * p.prefix_part_tokens;
     kv_len = min(P, kv_begin + p.prefix_part_tokens);
@@ -236,8 +245,8 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D>::THREADS, 1)
     bad_seq = n_b < 0 || c < 0 || L > p.max_blocks * 16 || q0 < 0 ||
               (long long)q0 + n_b > p.num_tokens;
   }
-  const bool has_b = j0 + TQ < n_b;   // the second tile holds a query token
-  const int j_last = min(j0 + 2 * TQ, n_b) - 1;
+  const bool has_b = C::NQT == 2 && j0 + TQ < n_b;  // a second tile with a query token
+  const int j_last = min(j0 + C::NQT * TQ, n_b) - 1;
   if (!prefix_mode) kv_len = c + j_last + 1;  // keys any row of the pair sees
   const int n_tiles = (kv_len - kv_begin + C::KEYS - 1) / C::KEYS;
   const int blk_begin = kv_begin / 16;          // kv_begin is a multiple of 128
@@ -519,7 +528,7 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D>::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 10) {
+  } else if (warp < 2 + 4 * C::NQT) {
     // ------------------------------------------------------------ softmax
     const int t = (warp - 2) / 4;  // query tile of this warp
     const int quarter = warp % 4;
@@ -774,10 +783,10 @@ bool get_prefill_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
   return true;
 }
 
-template <bool FP8, int D>
+template <bool FP8, int D, bool PREFIX>
 pkv_status launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                           const PrefillParams &p, int q_tiles, cudaStream_t s) {
-  using C = PrefillCfg<FP8, D>;
+  using C = PrefillCfg<FP8, D, PREFIX>;
   static int configured[64] = {0};
   static std::mutex mu;
   int dev = 0;
@@ -785,7 +794,7 @@ pkv_status launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CU
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!configured[dev]) {
-      if (cudaFuncSetAttribute(paged_prefill_kernel<FP8, D>,
+      if (cudaFuncSetAttribute(paged_prefill_kernel<FP8, D, PREFIX>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::SMEM_BYTES) != cudaSuccess)
         return PKV_ERR_CUDA;
@@ -802,20 +811,22 @@ pkv_status launch_prefill(const CUtensorMap &mq, const CUtensorMap &mk, const CU
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, paged_prefill_kernel<FP8, D>, mq, mk, mv, p) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, paged_prefill_kernel<FP8, D, PREFIX>, mq, mk, mv, p) !=
+      cudaSuccess)
     return PKV_ERR_CUDA;
   return PKV_OK;
 }
 
+template <bool PREFIX>
 pkv_status dispatch_prefill(const pkv_cache *cache, const CUtensorMap &mq, const CUtensorMap &mk,
                             const CUtensorMap &mv, const PrefillParams &p, int q_tiles,
                             cudaStream_t s) {
   const bool fp8 = cache->dtype == PKV_FP8_E4M3;
   if (cache->head_dim == 128)
-    return fp8 ? launch_prefill<true, 128>(mq, mk, mv, p, q_tiles, s)
-               : launch_prefill<false, 128>(mq, mk, mv, p, q_tiles, s);
-  return fp8 ? launch_prefill<true, 64>(mq, mk, mv, p, q_tiles, s)
-             : launch_prefill<false, 64>(mq, mk, mv, p, q_tiles, s);
+    return fp8 ? launch_prefill<true, 128, PREFIX>(mq, mk, mv, p, q_tiles, s)
+               : launch_prefill<false, 128, PREFIX>(mq, mk, mv, p, q_tiles, s);
+  return fp8 ? launch_prefill<true, 64, PREFIX>(mq, mk, mv, p, q_tiles, s)
+             : launch_prefill<false, 64, PREFIX>(mq, mk, mv, p, q_tiles, s);
 }
 
 // Score and output scales: fp8 folds k_scale into the score scale and
@@ -837,7 +848,7 @@ pkv_status launch_prefix_partials(const void *q, const pkv_cache *cache,
                                   int part_stride, int prefix_part_tokens, cudaStream_t s) {
   const int g = num_heads / cache->num_kv_heads;
   const int tq = 128 / g;
-  const int pairs = std::max(1, (max_group_size + 2 * tq - 1) / (2 * tq));
+  const int pairs = std::max(1, (max_group_size + tq - 1) / tq);  // one query tile per CTA
   const int parts = std::max(1, (max_prefix_len + prefix_part_tokens - 1) / prefix_part_tokens);
   if ((int64_t)pairs * parts > INT32_MAX || num_groups > 65535) return PKV_ERR_ARG;
   CUtensorMap mq, mk, mv;
@@ -866,7 +877,7 @@ pkv_status launch_prefix_partials(const void *q, const pkv_cache *cache,
   p.pairs_per_part = pairs;
   p.max_prefix_len = max_prefix_len;
   p.max_group_size = max_group_size;
-  return dispatch_prefill(cache, mq, mk, mv, p, pairs * parts, s);
+  return dispatch_prefill<true>(cache, mq, mk, mv, p, pairs * parts, s);
 }
 
 unsigned long long read_and_clear_error_prefill(cudaStream_t s, cudaError_t *err) {
@@ -935,5 +946,5 @@ extern "C" pkv_status paged_attention_prefill(const void *q, const pkv_cache *ca
   set_scales(&p, cache, scale);
   p.timeout_ns = 2000000000ull;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return dispatch_prefill(cache, mq, mk, mv, p, (int)q_tiles, s);
+  return dispatch_prefill<false>(cache, mq, mk, mv, p, (int)q_tiles, s);
 }
