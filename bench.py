@@ -347,15 +347,16 @@ def run_ours(args):
     flush = kv_bytes < 2 * L2_BYTES
     scrub = torch.empty(512 * 2**20, dtype=torch.uint8, device=dev) if flush else None
 
-    def step(ev=None):
+    def step(ev=None, bufs=None):
+        qq, tt, ll, kk, vv, ss, oo = bufs or (q, tables, lens, sk, sv, slots, out)
         if fresh.size:
             paged_kv_zero_blocks(cache, fresh)
-        if slots.numel():
-            paged_kv_write(sk, sv, slots, cache)
+        if ss.numel():
+            paged_kv_write(kk, vv, ss, cache)
         if ev is not None:
             ev[0].record(stream)
-        paged_attention_decode(q, cache, tables, lens, W.scale, max_len,
-                               out=out, partition_tokens=args.partition_tokens,
+        paged_attention_decode(qq, cache, tt, ll, W.scale, max_len,
+                               out=oo, partition_tokens=args.partition_tokens,
                                workspace=ws)
         if ev is not None:
             ev[1].record(stream)
@@ -416,29 +417,68 @@ def run_ours(args):
     with ClockSampler(dev.index) as clocks:
         barrier()
         torch.cuda.synchronize()
-        elapsed_ms = timed_loop(K, lambda i: run_step(evs[i]))
+        # the headline: K steps with events only around the loop (an event
+        # between two kernels would cut their programmatic launch overlap)
+        elapsed_ms = timed_loop(K, lambda i: run_step())
+        barrier()
+        # the dominant launch's duration for the roofline: the same K steps
+        # again with an event pair around each decode call (+ merge)
+        torch.cuda.synchronize()
+        timed_loop(K, lambda i: run_step(evs[i]))
         barrier()
 
-        # end to end: pinned host inputs -> device, step, output -> host
+        # End to end: every step uploads all of its inputs from pinned host
+        # memory and reads its output back.  As a serving loop does, the
+        # copies run on their own streams into two alternating device
+        # buffer sets, so step i's upload overlaps step i-1's compute and
+        # step i's download overlaps step i+1's compute.
         pin = lambda t: t.cpu().pin_memory()
-        h_q, h_tables, h_lens = pin(q), pin(tables), pin(lens)
-        h_sk, h_sv, h_slots = pin(sk), pin(sv), pin(slots)
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        copies = [(h_q, q), (h_tables, tables), (h_lens, lens), (h_sk, sk),
-                  (h_sv, sv), (h_slots, slots)]
-        h2d = sum(h.numel() * h.element_size() for h, _ in copies) + fresh.nbytes
-        d2h = h_out.numel() * h_out.element_size()
-        K2 = max(1, K // 2)
+        h_in = [pin(t) for t in (q, tables, lens, sk, sv, slots)]
+        h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        sets = [[torch.empty_like(t) for t in (q, tables, lens, sk, sv, slots, out)]
+                for _ in range(2)]
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_back = [torch.cuda.Event() for _ in range(2)]
+        h2d = sum(h.numel() * h.element_size() for h in h_in) + fresh.nbytes
+        d2h = h_out[0].numel() * h_out[0].element_size()
+        K2 = max(2, K // 2)
 
         def e2e_step(i):
-            for h, d in copies:
-                d.copy_(h, non_blocking=True)
-            run_step()
-            h_out.copy_(out, non_blocking=True)
+            b = i % 2
+            if i >= 2:
+                up.wait_event(ev_back[b])      # set b free: step i-2 read back
+            with torch.cuda.stream(up):
+                for h, d in zip(h_in, sets[b][:6]):
+                    d.copy_(h, non_blocking=True)
+                ev_in[b].record(up)
+            stream.wait_event(ev_in[b])
+            if args.graph:
+                # the captured graph reads and writes the fixed buffers
+                for d, x in zip((q, tables, lens, sk, sv, slots), sets[b][:6]):
+                    d.copy_(x, non_blocking=True)
+                run_step()
+                sets[b][6].copy_(out, non_blocking=True)
+            else:
+                run_step(bufs=sets[b])
+            ev_done[b].record(stream)
+            down.wait_event(ev_done[b])
+            with torch.cuda.stream(down):
+                h_out[b].copy_(sets[b][6], non_blocking=True)
+                ev_back[b].record(down)
 
         barrier()
         torch.cuda.synchronize()
-        e2e_ms = timed_loop(K2, e2e_step)
+        e_a = torch.cuda.Event(enable_timing=True)
+        e_b = torch.cuda.Event(enable_timing=True)
+        e_a.record(stream)
+        for i in range(K2):
+            e2e_step(i)
+        stream.wait_stream(down)               # the last read-back is inside
+        e_b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e_a.elapsed_time(e_b)
         barrier()
     st, detail = pkv_check()
     if st != 0:
@@ -485,7 +525,9 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": peak_kind,
                      "kernel": "paged_decode_kernel + paged_decode_merge_kernel",
-                     "launch_ms": round(attn_ms, 5)},
+                     "launch_ms": round(attn_ms, 5),
+                     "timed_in": "a second K-step loop, one event pair around "
+                                 "each decode call and its merge"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * K,
