@@ -132,3 +132,20 @@ def test_cascade_fp8_cache_matches_oracle():
     kc, vc = harness.oracle_cache(W)
     harness.assert_close(out.float().cpu().numpy(), harness.oracle_out(W, kc, vc),
                          "fp8_e4m3")
+
+
+def test_cascade_bad_group_falls_back_to_full_attention():
+    """A group whose prefix is not a multiple of 16 breaks the contract: it
+    is reported, and its members are attended in full (still the oracle's
+    result); the other group still uses its shared prefix."""
+    W = wl.prefix_shared(small=True)
+    G = harness.upload(W)
+    harness.gpu_step(W, G)
+    gs, plen = _groups_of(W)
+    plen = plen.copy()
+    plen[1] = 40
+    out = _cascade(W, G, gs, np.array(plen, np.int32))
+    st, detail = pkv_check()
+    assert st == PKV_ERR_RANGE and detail in range(int(gs[1]), int(gs[2]))
+    kc, vc = harness.oracle_cache(W)
+    harness.assert_close(out.float().cpu().numpy(), harness.oracle_out(W, kc, vc), "bf16")

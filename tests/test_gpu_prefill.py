@@ -150,3 +150,52 @@ def test_prefill_full_size_sampled_rows(kv_dtype):
     ref = harness.oracle_prefill_out(W, kc, vc, rows=rows)
     harness.assert_close(gpu[rows[:, 0], rows[:, 1]], ref[rows[:, 0], rows[:, 1]],
                          kv_dtype)
+
+
+def _sweep_cases(n=12, seed=2026):
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        g = int(rng.choice([1, 2, 4, 5, 8]))
+        Hkv = int(rng.choice([1, 2, 8])) if g < 8 else int(rng.choice([1, 4]))
+        d = int(rng.choice([64, 128]))
+        B = int(rng.integers(1, 6))
+        hist = [int(x) for x in rng.integers(0, 700, B) * (rng.random(B) < 0.7)]
+        chunk = [int(x) for x in rng.integers(0, 260, B)]
+        if sum(chunk) == 0:
+            chunk[0] = 1
+        kv = str(rng.choice(["bf16", "fp8_e4m3"]))
+        cases.append((i, hist, chunk, g * Hkv, Hkv, d, kv))
+    return cases
+
+
+@pytest.mark.parametrize("case", _sweep_cases(), ids=lambda c: f"sweep{c[0]}")
+def test_prefill_random_sweep(case):
+    """Seeded random shapes: group sizes 1-8, 1-8 kv heads, head_dim 64 and
+    128, both cache dtypes, zero to several hundred tokens of history and
+    chunk per sequence."""
+    i, hist, chunk, Hq, Hkv, d, kv = case
+    W = wl.make_prefill_workload(f"sweep{i}", hist, chunk, Hq, Hkv, d,
+                                 seed=100 + i, kv_dtype=kv)
+    gpu, _ = _run_case(W)
+    kc, vc = harness.oracle_prefill_cache(W)
+    harness.assert_close(gpu, harness.oracle_prefill_out(W, kc, vc), kv)
+
+
+def test_prefill_bad_query_start_loc_is_reported():
+    """A chunk longer than its sequence (query_start_loc past seq_len) is a
+    device range error; the other sequence is still right."""
+    W = wl.make_prefill_workload("badq", [30, 10], [20, 8], 32, 8, 128, seed=5)
+    G = harness.upload_prefill(W)
+    harness.gpu_prefill_step(W, G)
+    assert pkv_check()[0] == PKV_OK
+    lens = G.seq_lens.clone()
+    lens[1] = 4                                   # shorter than its 8-token chunk
+    out = torch.full_like(G.q, 3.0)
+    paged_attention_prefill(G.q, G.cache, G.tables, lens, G.qsl, W.scale,
+                            W.max_query_len, out=out)
+    st, detail = pkv_check()
+    assert st == PKV_ERR_RANGE and detail == 1
+    kc, vc = harness.oracle_prefill_cache(W)
+    ref = harness.oracle_prefill_out(W, kc, vc)
+    harness.assert_close(out.float().cpu().numpy()[:20], ref[:20], "bf16")
