@@ -955,7 +955,7 @@ def run_cascade(args):
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": None,
                      "peak_kind": peak_kind},
-        "gpu_launches_per_call": 4, "clocks": clk.summary(), "dtype": "bf16",
+        "gpu_launches_per_call": 3, "clocks": clk.summary(), "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": "prefix_shared", "batch": W.batch, "groups": len(W.groups),
                    "prefix_tokens": max(plen_h), "num_heads": W.num_heads,
