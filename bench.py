@@ -15,6 +15,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import platform
 import os
 import re
 import statistics
@@ -38,6 +39,11 @@ SEQ_LENS = {"llama8b_gqa": "uniform [512, 4096]",
             "tiny_mha": "{1, 17, 33, 64}"}
 FALLBACK_HBM_GBS = 6800.0
 PROFILE = ROOT / "profiles" / "paged_decode_kernel_llama8b_gqa.md"
+# decode workloads with a committed ncu summary of the decode kernel
+DECODE_PROFILES = {
+    "llama8b_gqa": PROFILE,
+    "long_context": ROOT / "profiles" / "paged_decode_kernel_long_context.md",
+}
 KERNEL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_decode.cu",
                   "paged_kv_cache_48_gb300/csrc/pkv_device.cuh"]
 PREFILL_PROFILE = ROOT / "profiles" / "paged_prefill_kernel_chunked_prefill_8k.md"
@@ -229,20 +235,58 @@ def oracle_setup(W):
     return kc, vc, o.num_threads()
 
 
-def time_cpu_oracle(W, n_seqs, steps, warmup=0):
+def time_cpu_oracle(W, n_seqs, steps, warmup=0, n_threads=0):
     """Seconds per oracle step on the first n_seqs sequences; returns
-    (value GB/s, seq-steps/s, seconds per step, threads, bytes)."""
-    kc, vc, threads = oracle_setup(W)
+    (value GB/s, seq-steps/s, seconds per step, threads, bytes).
+    n_threads = 0 uses every host core."""
+    import oracle
+    kc, vc, _ = oracle_setup(W)
+    threads = oracle.load().num_threads(n_threads)
     seqs = list(range(min(n_seqs, W.batch)))
     kv_bytes = int(W.seq_lens[seqs].astype(np.int64).sum()) * \
         W.num_kv_heads * W.head_dim * 2 * W.elem_bytes
     for _ in range(warmup):
-        cpu_oracle_step(W, kc, vc, seqs)
+        cpu_oracle_step(W, kc, vc, seqs, n_threads)
     t0 = time.perf_counter()
     for _ in range(steps):
-        cpu_oracle_step(W, kc, vc, seqs)
+        cpu_oracle_step(W, kc, vc, seqs, n_threads)
     dt = (time.perf_counter() - t0) / max(1, steps)
     return kv_bytes / dt / 1e9, len(seqs) / dt, dt, threads, kv_bytes
+
+
+def host_cpu_model():
+    """The host CPU as /proc/cpuinfo names it (x86 'model name', or the Arm
+    implementer / part codes), with the number of online cores."""
+    name = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for line in info.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() == "model name":
+                name = v.strip()
+                break
+        if name is None:
+            fields = {}
+            for line in info.splitlines():
+                k, _, v = line.partition(":")
+                fields.setdefault(k.strip(), v.strip())
+            if "CPU part" in fields:
+                name = (f"arm implementer {fields.get('CPU implementer', '?')} "
+                        f"part {fields['CPU part']}")
+    except OSError:
+        pass
+    return f"{name or platform.machine()}, {os.cpu_count()} cores"
+
+
+def one_core_baseline(W, n_seqs):
+    """The same oracle step on one host core (a single step of a smaller
+    sample: a quarter of the sequences, at least one)."""
+    gbs, _, dt, _, kvb = time_cpu_oracle(W, max(1, n_seqs // 4), steps=1,
+                                         warmup=0, n_threads=1)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1,
+            "sample": f"first {max(1, min(n_seqs // 4, W.batch))} sequences, "
+                      f"1 step ({kvb / 1e6:.1f} MB of KV)"}
 
 
 def run_reference(args):
@@ -271,7 +315,8 @@ def run_reference(args):
                    "l2": "host oracle (no L2 flush)"},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s",
                          "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "cpu": host_cpu_model(),
+                         "one_core": one_core_baseline(W, args.cpu_sample_seqs)},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -495,7 +540,8 @@ def run_ours(args):
     e2e_value = whole_job_gbs(world, kv_bytes, e2e_ms / K2)
     peak, peak_kind = measured_peak()
     achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
-    traffic = profiled_traffic() if args.workload == "llama8b_gqa" else None
+    traffic = (profiled_traffic(DECODE_PROFILES[args.workload])
+               if args.workload in DECODE_PROFILES else None)
     l2 = (f"L2 flushed between steps ({kv_bytes / 1e6:.1f} MB of KV per step)"
           if flush else
           f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV read per step, "
@@ -541,7 +587,9 @@ def run_ours(args):
             "kind": "oracle",
             "sample": (f"first {min(args.cpu_sample_seqs, W.batch)} of "
                        f"{W.batch} sequences, all heads, 2 steps "
-                       f"({kvb / 1e6:.1f} MB of KV per step)")}
+                       f"({kvb / 1e6:.1f} MB of KV per step)"),
+            "cpu": host_cpu_model(),
+            "one_core": one_core_baseline(W, args.cpu_sample_seqs)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -155,11 +155,37 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Slow path of a wait: mbarrier.try_wait with a suspend-time hint, so that
+// the waiting thread sleeps until the phase completes (or the hint runs
+// out) instead of polling and taking issue slots from the warps that share
+// its SM sub-partition; bounded by `limit_ns` of wall time.  Out of line:
+// the callers' hot loops keep only the first, non-suspending test.
+constexpr uint32_t kWaitHintNs = 10000;
+
+__device__ __noinline__ bool wait_suspended(uint64_t *bar, uint32_t parity,
+                                            unsigned long long limit_ns) {
+  const uint64_t start = global_timer_ns();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitHintNs)
+        : "memory");
+    if (done) return true;
+    if (global_timer_ns() - start > limit_ns) return false;
+  }
+}
+
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity,
                                               const PrefillParams &p, volatile int *abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   if (*abort_flag) return false;
-  if (mbar_wait_bounded(bar, parity, p.timeout_ns)) return true;
+  if (wait_suspended(bar, parity, p.timeout_ns)) return true;
   record_error(&g_err_prefill, PKV_ERR_TIMEOUT, -1);
   *abort_flag = 1;
   return false;
