@@ -214,6 +214,47 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// Two-lane fp32 arithmetic (sm_100 family): one instruction for a pair of
+// elements, each lane rounded as the scalar fma / add would be.  The
+// softmax uses them to halve its FMA-pipe instructions; those instructions
+// compete for issue slots with the one thread that issues the MMAs, and
+// fewer of them shorten the MMA chain of every tile.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n"
+      ".reg .b64 ra, rb, rc, rd;\n"
+      "mov.b64 ra, {%2, %3};\n"
+      "mov.b64 rb, {%4, %5};\n"
+      "mov.b64 rc, {%6, %7};\n"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n"
+      "mov.b64 {%0, %1}, rd;\n"
+      "}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n"
+      ".reg .b64 ra, rb, rd;\n"
+      "mov.b64 ra, {%2, %3};\n"
+      "mov.b64 rb, {%4, %5};\n"
+      "add.rn.f32x2 rd, ra, rb;\n"
+      "mov.b64 {%0, %1}, rd;\n"
+      "}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <bool FP8>
 __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
   return FP8 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
@@ -602,36 +643,45 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D, PREFIX>::THREADS,
           for (int e = 0; e < 32; ++e)
             if (key0 + q * 32 + e > lim) sr[q][e] = __float_as_uint(-INFINITY);
       }
-      // Row maximum of the raw scores in eight independent chains (the
-      // scale is positive, so it commutes with the maximum).
+      // Row maximum of the raw scores in eight independent chains, two new
+      // scores per step (the scale is positive, so it commutes with the
+      // maximum).
       float mx[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx[e % 8] = fmaxf(mx[e % 8], __uint_as_float(sr[q][e]));
+        for (int e = 0; e < 32; e += 2)
+          mx[(e / 2) % 8] = max3(mx[(e / 2) % 8], __uint_as_float(sr[q][e]),
+                                 __uint_as_float(sr[q][e + 1]));
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
                        p.scale_log2;
       const bool rescale = mt > m_used + 8.f;
       const float m_new = rescale ? mt : m_used;
       const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;  // 0 on the first tile
-      float ls[8];
+      // Eight partial sums of p kept as four lane pairs: pair j holds the
+      // sums of columns 2j and 2j + 1 (mod 8).
+      float2 ls[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) ls[k] = 0.f;
+      for (int k = 0; k < 4; ++k) ls[k] = make_float2(0.f, 0.f);
+      const float2 scale2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 neg_m2 = make_float2(-m_new, -m_new);
       // P as packed bf16 pairs, written in place over the consumed scores
 #pragma unroll
       for (int q = 0; q < 4; ++q)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[q][e]), p.scale_log2, -m_new));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[q][e + 1]), p.scale_log2, -m_new));
-          ls[e % 8] += p0;
-          ls[(e + 1) % 8] += p1;
+          const float2 x = fma2(
+              make_float2(__uint_as_float(sr[q][e]), __uint_as_float(sr[q][e + 1])), scale2,
+              neg_m2);
+          const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+          ls[(e / 2) % 4] = add2(ls[(e / 2) % 4], make_float2(p0, p1));
           sr[q][e / 2] = pack_p<FP8>(p0, p1);
         }
-      l = l * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+      l = l * alpha + (((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) +
+                       ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y)));
       m_used = m_new;
       // s_full(i) also means PV_t(i-1) is complete: O_t may be rescaled
       if (i > 0 && __any_sync(0xffffffffu, rescale)) {
