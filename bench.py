@@ -466,6 +466,24 @@ def run_ours(args):
         # between two kernels would cut their programmatic launch overlap)
         elapsed_ms = timed_loop(K, lambda i: run_step())
         barrier()
+        warm_ms = None
+        if flush:
+            # The same steps without the flush (KV left in L2 by the
+            # previous step), reported beside the cold headline.  Each step
+            # is timed on its own as in the cold loop; a GPU sleep that
+            # touches no memory takes the flush's place, so the host has
+            # queued the step before the GPU reaches it.
+            torch.cuda.synchronize()
+            wpairs = [(torch.cuda.Event(enable_timing=True),
+                       torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+            for i in range(K):
+                torch.cuda._sleep(100000)
+                wpairs[i][0].record(stream)
+                run_step()
+                wpairs[i][1].record(stream)
+            torch.cuda.synchronize()
+            warm_ms = sum(x.elapsed_time(y) for x, y in wpairs)
+            barrier()
         # the dominant launch's duration for the roofline: the same K steps
         # again with an event pair around each decode call (+ merge)
         torch.cuda.synchronize()
@@ -534,6 +552,8 @@ def run_ours(args):
     attn_ms = statistics.fmean(a.elapsed_time(b) for a, b in evs)
     elapsed_ms, e2e_ms, attn_ms = max_over_ranks([elapsed_ms, e2e_ms, attn_ms],
                                                  device=dev)
+    if warm_ms is not None:
+        warm_ms = max_over_ranks([warm_ms], device=dev)[0]
 
     ms_per_step = elapsed_ms / K
     value = whole_job_gbs(world, kv_bytes, ms_per_step)
@@ -556,6 +576,7 @@ def run_ours(args):
         "data": "synthetic",
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "seq_steps_per_s": round(world * W.batch / (ms_per_step * 1e-3), 1),
+        "attention_seq_steps_per_s": round(world * W.batch / (attn_ms * 1e-3), 1),
         "config": {"workload": W.name, "batch": W.batch,
                    "num_heads": W.num_heads, "num_kv_heads": W.num_kv_heads,
                    "head_dim": W.head_dim, "block_size": 16,
@@ -579,6 +600,10 @@ def run_ours(args):
         "gpu_launches": launches_per_step * K,
         "clocks": clocks.summary(),
     }
+    if warm_ms is not None:
+        line["warm"] = {"value": round(whole_job_gbs(world, kv_bytes, warm_ms / K), 2),
+                        "unit": "GB/s", "ms_per_step": round(warm_ms / K, 5),
+                        "note": "the same steps, each timed alone, without the L2 flush"}
     if rank == 0 and not args.no_cpu_baseline:
         gbs, sps, dt, threads, kvb = time_cpu_oracle(W, args.cpu_sample_seqs,
                                                      steps=2, warmup=0)
