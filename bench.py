@@ -347,7 +347,7 @@ def run_ours(args):
     from paged_kv_cache_48_gb300 import (PagedKVCache, paged_attention_decode,
                                          paged_attention_partition_tokens,
                                          paged_attention_workspace_bytes,
-                                         paged_kv_write, paged_kv_zero_blocks,
+                                         paged_kv_write, paged_kv_zero_and_write,
                                          pkv_check)
     from paged_kv_cache_48_gb300 import workload as wl
 
@@ -381,10 +381,10 @@ def run_ours(args):
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
-    # zeroing (when the step opens blocks), the write, the decode kernel and
-    # the merge of split sequences (when a sequence can be split)
+    # zeroing + write (one launch), the decode kernel and the merge of
+    # split sequences (when a sequence can be split)
     split = -(-max_len // pt) > 1
-    launches_per_step = (1 if fresh.size else 0) + (1 if slots.numel() else 0) \
+    launches_per_step = (1 if fresh.size or slots.numel() else 0) \
         + 1 + (1 if split else 0)
     kv_bytes = W.kv_read_bytes()
     # Workloads whose KV fits in twice the L2 are timed step by step with an
@@ -394,10 +394,10 @@ def run_ours(args):
 
     def step(ev=None, bufs=None):
         qq, tt, ll, kk, vv, ss, oo = bufs or (q, tables, lens, sk, sv, slots, out)
-        if fresh.size:
-            paged_kv_zero_blocks(cache, fresh)
-        if ss.numel():
-            paged_kv_write(kk, vv, ss, cache)
+        if fresh.size or ss.numel():
+            # zeroing of the step's fresh blocks and the write of its
+            # tokens, in one launch
+            paged_kv_zero_and_write(kk, vv, ss, cache, fresh)
         if ev is not None:
             ev[0].record(stream)
         paged_attention_decode(qq, cache, tt, ll, W.scale, max_len,

@@ -98,6 +98,21 @@ pkv_status paged_kv_zero_blocks(const pkv_cache *cache,
                                 const int32_t *block_ids, int64_t n,
                                 int ids_on_host, void *stream);
 
+/* Zeroing of freshly allocated blocks and the slot-mapped write of new
+ * tokens in one launch: the result is that of paged_kv_zero_blocks(cache,
+ * block_ids, n, ids_on_host) followed by paged_kv_write(k, v, slot_mapping,
+ * num_tokens, cache).  Sources: those of the two calls (vLLM v0.17.1 notes,
+ * "修复方案"; vLLM concept page, "15 分钟专家深入" item 2).  Arguments and
+ * device range errors are those of the two calls; either count may be 0.
+ * A zeroing CTA clears only the rows of its block that no token of this
+ * call writes, and the writing CTAs write every token, so the two never
+ * touch the same bytes.  More than 4096 host ids take several launches, the
+ * first of which also writes the tokens. */
+pkv_status paged_kv_zero_and_write(const void *k, const void *v,
+                                   const int64_t *slot_mapping, int64_t num_tokens,
+                                   const pkv_cache *cache, const int32_t *block_ids,
+                                   int64_t n, int ids_on_host, void *stream);
+
 /* Copy whole blocks: for each i, every byte of key_cache[dst_ids[i]] and
  * value_cache[dst_ids[i]] becomes the byte of block src_ids[i].  Source:
  * vLLM internals (naphjohn.github.io), §1.1 (copy-on-write of a shared

@@ -14,7 +14,8 @@ from .ops import (PagedKVCache, PagedKVError, paged_attention_decode,
                   paged_attention_partition_tokens,
                   paged_attention_workspace_bytes, paged_kv_copy_blocks,
                   paged_kv_swap_in, paged_kv_swap_out, paged_kv_write,
-                  paged_kv_zero_blocks, paged_prepare_inputs, pkv_check,
+                  paged_kv_zero_and_write, paged_kv_zero_blocks,
+                  paged_prepare_inputs, pkv_check,
                   raise_on_device_error)
 
 __all__ = [
@@ -23,7 +24,8 @@ __all__ = [
     "paged_attention_prefill",
     "paged_attention_partition_tokens", "paged_attention_workspace_bytes",
     "paged_kv_copy_blocks", "paged_kv_swap_in", "paged_kv_swap_out",
-    "paged_kv_write", "paged_kv_zero_blocks", "paged_prepare_inputs",
+    "paged_kv_write", "paged_kv_zero_and_write", "paged_kv_zero_blocks",
+    "paged_prepare_inputs",
     "pkv_check",
     "raise_on_device_error",
 ]

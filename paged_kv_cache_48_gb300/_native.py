@@ -43,6 +43,9 @@ _SIGNATURES = {
                                       ctypes.POINTER(PkvCache), _P]),
     "paged_kv_zero_blocks": (ctypes.c_int, [ctypes.POINTER(PkvCache), _P,
                                             ctypes.c_int64, ctypes.c_int, _P]),
+    "paged_kv_zero_and_write": (ctypes.c_int, [_P, _P, _P, ctypes.c_int64,
+                                               ctypes.POINTER(PkvCache), _P,
+                                               ctypes.c_int64, ctypes.c_int, _P]),
     "paged_kv_copy_blocks": (ctypes.c_int, [ctypes.POINTER(PkvCache), _P, _P,
                                             ctypes.c_int64, ctypes.c_int, _P]),
     "paged_kv_swap_out": (ctypes.c_int, [ctypes.POINTER(PkvCache), _P,

@@ -21,6 +21,28 @@ namespace pkv {
 
 static __device__ unsigned long long g_err_write_zero = 0ull;
 
+// Eight bf16 values to eight E4M3 bytes: the IEEE binary32 quotient
+// x / scale, rounded to nearest even and saturated to +-448.
+__device__ __forceinline__ uint2 quant8_e4m3(const uint4 &src, float scale) {
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&src);
+  uint32_t out[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float2 f = __bfloat1622float2(h[2 * i + j]);
+      float2 qv;
+      qv.x = __fdiv_rn(f.x, scale);
+      qv.y = __fdiv_rn(f.y, scale);
+      const __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(qv, __NV_SATFINITE, __NV_E4M3);
+      word |= (uint32_t)two << (16 * j);
+    }
+    out[i] = word;
+  }
+  return make_uint2(out[0], out[1]);
+}
+
 // ---------------------------------------------------------------------------
 // Slot-mapped write.  Work item = one 16-byte vector of one token's K row
 // (8 bf16) plus the matching V vector.  A token row is num_kv_heads *
@@ -54,30 +76,8 @@ kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
       reinterpret_cast<uint4 *>(key_cache)[dst_vec] = kv;
       reinterpret_cast<uint4 *>(value_cache)[dst_vec] = vv;
     } else {
-      // E4M3 of the IEEE binary32 quotient x / scale, round to nearest
-      // even, saturating to +-448.
-      auto quant8 = [](const uint4 &src, float scale) {
-        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&src);
-        uint32_t out[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          uint32_t word = 0;
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            const float2 f = __bfloat1622float2(h[2 * i + j]);
-            float2 qv;
-            qv.x = __fdiv_rn(f.x, scale);
-            qv.y = __fdiv_rn(f.y, scale);
-            const __nv_fp8x2_storage_t two =
-                __nv_cvt_float2_to_fp8x2(qv, __NV_SATFINITE, __NV_E4M3);
-            word |= (uint32_t)two << (16 * j);
-          }
-          out[i] = word;
-        }
-        return make_uint2(out[0], out[1]);
-      };
-      reinterpret_cast<uint2 *>(key_cache)[dst_vec] = quant8(kv, k_scale);
-      reinterpret_cast<uint2 *>(value_cache)[dst_vec] = quant8(vv, v_scale);
+      reinterpret_cast<uint2 *>(key_cache)[dst_vec] = quant8_e4m3(kv, k_scale);
+      reinterpret_cast<uint2 *>(value_cache)[dst_vec] = quant8_e4m3(vv, v_scale);
     }
   }
 }
@@ -140,6 +140,87 @@ zero_blocks_param_kernel(uint4 *__restrict__ key_cache,
       continue;
     }
     zero_one_block(key_cache, value_cache, vecs_per_block, id);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Zeroing and write in one launch (the same result as zeroing the blocks
+// and then writing the tokens).  CTAs 0 .. zero_ctas - 1 take fresh blocks:
+// each first collects which of its block's 16 slots this step writes
+// (a scan of slot_mapping) and zeroes only the other rows; the remaining
+// CTAs write every token.  The two sets of addresses are disjoint, so no
+// CTA waits for another.  Ids come in the launch parameters (ids.n > 0) or
+// through a device pointer.
+// ---------------------------------------------------------------------------
+template <bool FP8>
+__global__ void __launch_bounds__(256)
+kv_zero_write_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                     const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
+                     int vecs_per_row, uint8_t *__restrict__ key_cache,
+                     uint8_t *__restrict__ value_cache, int32_t num_blocks, float k_scale,
+                     float v_scale, const int32_t *__restrict__ dev_ids, int64_t n_dev_ids,
+                     const __grid_constant__ ZeroIds ids, int64_t id_base, int zero_ctas,
+                     int write_tokens) {
+  grid_dependency_wait();
+  allow_dependent_launch();
+  const int64_t num_slots = (int64_t)num_blocks * 16;
+  if ((int)blockIdx.x < zero_ctas) {
+    __shared__ uint32_t written;  // bit r: slot r of the block is written this step
+    const int64_t n = ids.n > 0 ? ids.n : n_dev_ids;
+    // a row of the block in 16-byte units of the cache element type
+    const int row_vecs = FP8 ? vecs_per_row / 2 : vecs_per_row;
+    for (int64_t i = blockIdx.x; i < n; i += zero_ctas) {
+      const int32_t id = ids.n > 0 ? ids.ids[i] : __ldg(dev_ids + i);
+      if (id < 0 || id >= num_blocks) {
+        if (threadIdx.x == 0) record_error(&g_err_write_zero, PKV_ERR_RANGE, id_base + i);
+        continue;
+      }
+      if (threadIdx.x == 0) written = 0u;
+      __syncthreads();
+      const int64_t lo = (int64_t)id * 16;
+      uint32_t mine = 0u;
+      for (int64_t t = threadIdx.x; t < num_tokens; t += blockDim.x) {
+        const int64_t slot = __ldg(slot_mapping + t);
+        if (slot >= lo && slot < lo + 16) mine |= 1u << (int)(slot - lo);
+      }
+      if (mine) atomicOr(&written, mine);
+      __syncthreads();
+      const uint32_t keep = written;
+      uint4 *kb = reinterpret_cast<uint4 *>(key_cache) + lo * row_vecs;
+      uint4 *vb = reinterpret_cast<uint4 *>(value_cache) + lo * row_vecs;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int j = threadIdx.x; j < 16 * row_vecs; j += blockDim.x) {
+        if ((keep >> (j / row_vecs)) & 1u) continue;
+        kb[j] = z;
+        vb[j] = z;
+      }
+      __syncthreads();  // `written` is reused for the next block
+    }
+    return;
+  }
+  if (!write_tokens) return;
+  const int64_t total = num_tokens * vecs_per_row;
+  const int64_t stride = (int64_t)(gridDim.x - zero_ctas) * blockDim.x;
+  for (int64_t idx = (blockIdx.x - zero_ctas) * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += stride) {
+    const int64_t tok = idx / vecs_per_row;
+    const int vec = (int)(idx - tok * vecs_per_row);
+    const int64_t slot = __ldg(slot_mapping + tok);
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (vec == 0) record_error(&g_err_write_zero, PKV_ERR_RANGE, tok);
+      continue;
+    }
+    const uint4 kv = __ldg(k + idx);
+    const uint4 vv = __ldg(v + idx);
+    const int64_t dst_vec = slot * vecs_per_row + vec;  // in 8-element units
+    if (!FP8) {
+      reinterpret_cast<uint4 *>(key_cache)[dst_vec] = kv;
+      reinterpret_cast<uint4 *>(value_cache)[dst_vec] = vv;
+    } else {
+      reinterpret_cast<uint2 *>(key_cache)[dst_vec] = quant8_e4m3(kv, k_scale);
+      reinterpret_cast<uint2 *>(value_cache)[dst_vec] = quant8_e4m3(vv, v_scale);
+    }
   }
 }
 
@@ -258,6 +339,60 @@ extern "C" pkv_status paged_kv_zero_blocks(const pkv_cache *cache,
     const int grid = std::min(m, sms * 16);
     if (launch_pdl(zero_blocks_param_kernel, dim3(grid), dim3(threads), s, kc, vc,
                    vecs_per_block, cache->num_blocks, chunk, base) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+extern "C" pkv_status paged_kv_zero_and_write(const void *k, const void *v,
+                                              const int64_t *slot_mapping, int64_t num_tokens,
+                                              const pkv_cache *cache, const int32_t *block_ids,
+                                              int64_t n, int ids_on_host, void *stream) {
+  pkv_status st = validate_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0 || n < 0) return PKV_ERR_ARG;
+  if (num_tokens == 0 && n == 0) return PKV_OK;
+  if (num_tokens > 0) {
+    if (!k || !v || !slot_mapping) return PKV_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15)
+      return PKV_ERR_ARG;  // 16-byte vector loads
+  }
+  if (n > 0 && !block_ids) return PKV_ERR_ARG;
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
+  if (fp8 && !(cache->k_scale > 0.f && cache->v_scale > 0.f)) return PKV_ERR_ARG;
+  const int sms = device_sm_count();
+  if (sms <= 0) return PKV_ERR_CUDA;
+  const int vecs_per_row = cache->num_kv_heads * cache->head_dim / 8;
+  const int threads = 256;
+  const int64_t want = (num_tokens * vecs_per_row + threads - 1) / threads;
+  const int write_ctas = (int)std::min<int64_t>(want, (int64_t)sms * 8);
+  const float ks = fp8 ? cache->k_scale : 1.f, vs = fp8 ? cache->v_scale : 1.f;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto launch = [&](const int32_t *dev_ids, int64_t n_dev, const ZeroIds &ids, int64_t base,
+                    int zero_ctas, int with_write) -> bool {
+    const int grid = zero_ctas + (with_write ? write_ctas : 0);
+    if (grid == 0) return true;
+    auto kern = fp8 ? kv_zero_write_kernel<true> : kv_zero_write_kernel<false>;
+    return launch_pdl(kern, dim3(grid), dim3(threads), s, static_cast<const uint4 *>(k),
+                      static_cast<const uint4 *>(v), slot_mapping, num_tokens, vecs_per_row,
+                      static_cast<uint8_t *>(cache->key_cache),
+                      static_cast<uint8_t *>(cache->value_cache), cache->num_blocks, ks, vs,
+                      dev_ids, n_dev, ids, base, zero_ctas, with_write) == cudaSuccess;
+  };
+  static thread_local ZeroIds chunk;
+  if (n == 0 || !ids_on_host) {
+    chunk.n = 0;
+    const int zero_ctas = (int)std::min<int64_t>(n, (int64_t)sms * 16);
+    return launch(block_ids, n, chunk, 0, zero_ctas, num_tokens > 0) ? PKV_OK : PKV_ERR_CUDA;
+  }
+  // Host ids ride in the launch parameters, kZeroIdsPerLaunch at a time;
+  // the first launch also writes the tokens, the later ones only zero (each
+  // zeroing CTA still skips the rows this step writes).
+  for (int64_t base = 0; base < n; base += kZeroIdsPerLaunch) {
+    const int m = (int)std::min<int64_t>(kZeroIdsPerLaunch, n - base);
+    chunk.n = m;
+    std::memcpy(chunk.ids, block_ids + base, sizeof(int32_t) * m);
+    if (!launch(nullptr, 0, chunk, base, std::min(m, sms * 16), base == 0 && num_tokens > 0))
       return PKV_ERR_CUDA;
   }
   return PKV_OK;

@@ -145,6 +145,30 @@ def paged_kv_zero_blocks(cache: PagedKVCache, block_ids,
     _native.check("paged_kv_zero_blocks", st)
 
 
+def paged_kv_zero_and_write(k: torch.Tensor, v: torch.Tensor,
+                            slot_mapping: torch.Tensor, cache: PagedKVCache,
+                            block_ids,
+                            stream: Optional[torch.cuda.Stream] = None) -> None:
+    """paged_kv_zero_blocks(cache, block_ids) then paged_kv_write(k, v,
+    slot_mapping, cache), in one launch (more than 4096 host ids take
+    several)."""
+    dev = cache.device
+    _require(k, "k", torch.bfloat16, dev, 3)
+    _require(v, "v", torch.bfloat16, dev, 3)
+    _require(slot_mapping, "slot_mapping", torch.int64, dev, 1)
+    T = k.shape[0]
+    if v.shape != k.shape or slot_mapping.shape[0] != T or \
+            k.shape[1:] != (cache.num_kv_heads, cache.head_dim):
+        raise ValueError("k, v, slot_mapping shapes do not match the cache")
+    ptr, n, on_host, keep = _block_ids(block_ids, dev)
+    st = _native.lib().paged_kv_zero_and_write(
+        k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+        ctypes.byref(cache.c_struct()), ptr, n, on_host,
+        _stream_handle(stream, dev))
+    del keep
+    _native.check("paged_kv_zero_and_write", st)
+
+
 def _block_ids(ids, dev):
     """(pointer, count, ids_on_host, keep-alive) for a block-id list."""
     if isinstance(ids, torch.Tensor) and ids.is_cuda:
