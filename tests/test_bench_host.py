@@ -1,0 +1,73 @@
+"""Host-side pieces of bench.py, on CPU: the reference arm's JSON line (the
+oracle timed on the host cores), the buffer packing of a step's inputs, the
+profile lookup that supplies roofline traffic, and the host CPU name."""
+import json
+import subprocess
+import sys
+from pathlib import Path
+
+import numpy as np
+import pytest
+import torch
+
+ROOT = Path(__file__).resolve().parents[1]
+sys.path.insert(0, str(ROOT))
+import bench  # noqa: E402
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_mha", "--steps", "1", "--warmup", "0",
+                        "--cpu-sample-seqs", "4"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["config"]["workload"] == "tiny_mha"
+    assert d["higher_is_better"] is True and d["value"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["one_core"]["cores"] == 1 and cb["one_core"]["value"] > 0
+    assert cb["cpu"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_packed_views_hold_the_tensors_at_aligned_offsets():
+    ts = [torch.arange(7, dtype=torch.int32), torch.randn(3, 5).to(torch.bfloat16),
+          torch.arange(11, dtype=torch.int64), torch.zeros(0, dtype=torch.int32)]
+    buf, views = bench.packed(ts)
+    assert buf.dtype == torch.uint8
+    for v, t in zip(views, ts):
+        assert v.dtype == t.dtype and v.shape == t.shape and torch.equal(v, t)
+        assert (v.data_ptr() - buf.data_ptr()) % 256 == 0
+    # the views alias the buffer: a write through one is seen in the other
+    views[0][0] = 99
+    assert int(buf[:4].view(torch.int32)[0]) == 99
+
+
+def test_profile_traffic_follows_the_kernel_source_hash(tmp_path):
+    sha = bench.kernel_sha(bench.KERNEL_SOURCES)
+    good = tmp_path / "good.md"
+    good.write_text(f"kernel_source_sha256: {sha}\ndram_bytes_per_launch: 123456\n")
+    assert bench.profiled_traffic(good, bench.KERNEL_SOURCES) == 123456.0
+    stale = tmp_path / "stale.md"
+    stale.write_text("kernel_source_sha256: 0000000000000000\ndram_bytes_per_launch: 1\n")
+    assert bench.profiled_traffic(stale, bench.KERNEL_SOURCES) is None
+    assert bench.profiled_traffic(tmp_path / "missing.md", bench.KERNEL_SOURCES) is None
+    # every committed profile that names a source hash parses
+    for p in (ROOT / "profiles").glob("*.md"):
+        text = p.read_text()
+        if "kernel_source_sha256:" in text:
+            assert "dram_bytes_per_launch:" in text, p.name
+
+
+def test_host_cpu_model_names_the_cores():
+    s = bench.host_cpu_model()
+    assert isinstance(s, str) and s.endswith("cores")
