@@ -15,7 +15,8 @@ import torch
 import oracle
 from paged_kv_cache_48_gb300 import (PagedKVCache, paged_attention_decode,
                                      paged_attention_prefill, paged_kv_write,
-                                     paged_kv_zero_blocks, pkv_check)
+                                     paged_kv_zero_and_write, paged_kv_zero_blocks,
+                                     pkv_check)
 from paged_kv_cache_48_gb300.workload import PrefillWorkload, Workload
 
 # Tolerances of the parity bar: |gpu - ref| <= ATOL + RTOL * |ref| per
@@ -69,21 +70,25 @@ def upload(W: Workload, device="cuda", write_history=True) -> GpuState:
 
 
 def gpu_step(W: Workload, G: GpuState, partition_tokens=0, skip_zero=False,
-             out=None):
-    """One decode step: zero fresh blocks, write the step's tokens, attend."""
-    if not skip_zero and G.fresh.size:
-        paged_kv_zero_blocks(G.cache, G.fresh)
-    if G.step_slots.numel():
-        paged_kv_write(G.step_k, G.step_v, G.step_slots, G.cache)
+             out=None, fused=False):
+    """One decode step: zero fresh blocks, write the step's tokens, attend.
+    fused: the zeroing and the write as one paged_kv_zero_and_write call."""
+    if fused and not skip_zero:
+        paged_kv_zero_and_write(G.step_k, G.step_v, G.step_slots, G.cache, G.fresh)
+    else:
+        if not skip_zero and G.fresh.size:
+            paged_kv_zero_blocks(G.cache, G.fresh)
+        if G.step_slots.numel():
+            paged_kv_write(G.step_k, G.step_v, G.step_slots, G.cache)
     return paged_attention_decode(G.q, G.cache, G.tables, G.seq_lens, W.scale,
                                   max_seq_len=W.max_seq_len, out=out,
                                   partition_tokens=partition_tokens)
 
 
 def run_gpu(W: Workload, partition_tokens=0, skip_zero=False, device="cuda",
-            want_cache=True):
+            want_cache=True, fused=False):
     G = upload(W, device)
-    out = gpu_step(W, G, partition_tokens, skip_zero)
+    out = gpu_step(W, G, partition_tokens, skip_zero, fused=fused)
     status, detail = pkv_check()
     res = {"out": out.float().cpu().numpy(), "status": status,
            "detail": detail, "state": G}
