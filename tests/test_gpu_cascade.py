@@ -149,3 +149,19 @@ def test_cascade_bad_group_falls_back_to_full_attention():
     assert st == PKV_ERR_RANGE and detail in range(int(gs[1]), int(gs[2]))
     kc, vc = harness.oracle_cache(W)
     harness.assert_close(out.float().cpu().numpy(), harness.oracle_out(W, kc, vc), "bf16")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_cascade_long_prefix_in_several_partitions(kv_dtype):
+    """Two groups of 4 sharing a 2304-token prefix: 16 (group, kv head)
+    units leave most SMs free, so the prefix is cut into several partitions
+    (the last one short) whose slots the merge combines."""
+    W = wl.make_workload("prefix_long", 8, 32, 8, 128, 5, 200, 23, kv_dtype=kv_dtype,
+                         prefix_groups=2, prefix_len=2304)
+    G = harness.upload(W)
+    harness.gpu_step(W, G)
+    gs, plen = _groups_of(W)
+    out = _cascade(W, G, gs, plen)
+    assert pkv_check()[0] == PKV_OK
+    kc, vc = harness.oracle_cache(W)
+    harness.assert_close(out.float().cpu().numpy(), harness.oracle_out(W, kc, vc), kv_dtype)
