@@ -548,15 +548,29 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
 // m_j (log2 domain), l_j and its normalised output o_j; the result is
 // sum_j 2^(m_j - M) l_j o_j / sum_j 2^(m_j - M) l_j with M = max_j m_j.  The
 // (m, l) pairs of up to 32 partitions are loaded at once (one per lane) and
-// reduced with shuffles; outputs accumulate partition by partition.
+// reduced with shuffles; outputs accumulate partition by partition, in
+// partition order.
 template <int D>
 __global__ void __launch_bounds__(256) paged_decode_merge_kernel(const DecodeParams p) {
   constexpr int KD = D / 32;
+  constexpr int PRE = 4;  // partitions loaded before the row's count is known
   grid_dependency_wait();
   allow_dependent_launch();
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= (long long)p.batch * p.num_heads) return;
+  const float2 *ml = p.part_ml + (size_t)row * p.max_parts;
+  const float *po = p.part_o + (size_t)row * p.max_parts * D + lane;
+  // Every slot below max_parts lies inside this row's workspace, so the
+  // first partitions' (m, l) and outputs are loaded alongside the sequence
+  // length rather than after it: one memory round trip instead of three.
+  // Slots past the row's partition count are never used.
+  const float2 v0 = lane < p.max_parts ? ml[lane] : make_float2(-INFINITY, 0.f);
+  float pre[PRE][KD];
+#pragma unroll
+  for (int r = 0; r < PRE; ++r)
+#pragma unroll
+    for (int k = 0; k < KD; ++k) pre[r][k] = r < p.max_parts ? po[(size_t)r * D + 32 * k] : 0.f;
   const int b = (int)(row / p.num_heads);
   const int cap = min(p.max_blocks * 16, p.max_seq_len);
   const int L = clamp_len(__ldg(p.seq_lens + b), cap);
@@ -567,14 +581,12 @@ __global__ void __launch_bounds__(256) paged_decode_merge_kernel(const DecodePar
   const int nparts =
       slot_base + (Ls <= p.part_tokens ? 1 : (Ls + p.part_tokens - 1) / p.part_tokens);
   if (nparts <= 1) return;  // the decode kernel wrote this row
-  const float2 *ml = p.part_ml + (size_t)row * p.max_parts;
-  const float *po = p.part_o + (size_t)row * p.max_parts * D + lane;
   float wsum = 0.f, acc[KD];
 #pragma unroll
   for (int k = 0; k < KD; ++k) acc[k] = 0.f;
   if (nparts <= 32) {
-    // common case: lane j holds partition j's (m, l); one load round trip
-    const float2 v = lane < nparts ? ml[lane] : make_float2(-INFINITY, 0.f);
+    // common case: lane j holds partition j's (m, l); shuffles reduce them
+    const float2 v = lane < nparts ? v0 : make_float2(-INFINITY, 0.f);
     float M = v.x;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -583,8 +595,16 @@ __global__ void __launch_bounds__(256) paged_decode_merge_kernel(const DecodePar
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
     wsum = t;
+#pragma unroll
+    for (int r = 0; r < PRE; ++r) {
+      const float wr = __shfl_sync(0xffffffffu, w, r);
+      if (r < nparts) {
+#pragma unroll
+        for (int k = 0; k < KD; ++k) acc[k] += wr * pre[r][k];
+      }
+    }
 #pragma unroll 4
-    for (int r = 0; r < nparts; ++r) {
+    for (int r = PRE; r < nparts; ++r) {
       const float wr = __shfl_sync(0xffffffffu, w, r);
       const float *pj = po + (size_t)r * D;
 #pragma unroll
