@@ -43,6 +43,7 @@ PROFILE = ROOT / "profiles" / "paged_decode_kernel_llama8b_gqa.md"
 DECODE_PROFILES = {
     "llama8b_gqa": PROFILE,
     "long_context": ROOT / "profiles" / "paged_decode_kernel_long_context.md",
+    "fp8_recycle": ROOT / "profiles" / "paged_decode_kernel_fp8_recycle.md",
 }
 KERNEL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_decode.cu",
                   "paged_kv_cache_48_gb300/csrc/pkv_device.cuh"]
