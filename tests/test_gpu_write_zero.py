@@ -6,8 +6,8 @@ import torch
 import harness
 import oracle
 from paged_kv_cache_48_gb300 import (PagedKVCache, PagedKVError,
-                                     paged_kv_write, paged_kv_zero_blocks,
-                                     pkv_check)
+                                     paged_kv_write, paged_kv_zero_and_write,
+                                     paged_kv_zero_blocks, pkv_check)
 from paged_kv_cache_48_gb300 import workload as wl
 
 pytestmark = pytest.mark.gpu
@@ -60,6 +60,51 @@ def test_fp8_write_extremes_bit_exact():
                            float(scale), float(scale), bits, bits, slots)
     assert np.array_equal(kc.cpu().numpy().reshape(-1), ok)
     assert np.array_equal(vc.cpu().numpy().reshape(-1), ov)
+
+
+_E4M3_SCALES = [1.0, 0.5, 3.0, 0.0123, 4.7 / 448, 1e30, 3e-38, 1e-39]
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["write", "zero_and_write"])
+@pytest.mark.parametrize("scale", _E4M3_SCALES)
+def test_fp8_encode_every_bf16_value(scale, fused):
+    """Every bf16 bit pattern through the E4M3 encode, for scales that make
+    the quotient exact (1, 0.5), put ties within an ulp of x * RN(1/scale)
+    (3), are awkward (0.0123, 4.7/448), large, tiny, or subnormal (the
+    reciprocal overflows).  Bytes equal the oracle's IEEE quotient rounded
+    to E4M3 for every value that is not a NaN; NaN inputs give a NaN code
+    (0x7F or 0xFF) on both sides."""
+    Hkv, d = 1, 128
+    allbits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    T = allbits.size // (Hkv * d)
+    NB = T // 16
+    kbits = allbits.reshape(T, Hkv, d)
+    vbits = allbits[::-1].copy().reshape(T, Hkv, d)
+    slots = np.random.default_rng(9).permutation(NB * 16).astype(np.int64)
+    s32 = float(np.float32(scale))
+    shape = (NB, 16, Hkv, d)
+    kc = torch.full(shape, 0xAB, dtype=torch.uint8, device="cuda")
+    vc = torch.full(shape, 0xCD, dtype=torch.uint8, device="cuda")
+    cache = PagedKVCache(kc, vc, "fp8_e4m3", s32, s32)
+    kt = torch.from_numpy(kbits).view(torch.bfloat16).cuda()
+    vt = torch.from_numpy(vbits).view(torch.bfloat16).cuda()
+    st = torch.from_numpy(slots).cuda()
+    if fused:
+        paged_kv_zero_and_write(kt, vt, st, cache, np.zeros(0, np.int32))
+    else:
+        paged_kv_write(kt, vt, st, cache)
+    assert pkv_check()[0] == PKV_OK
+    ok = np.full(NB * 16 * Hkv * d, 0xAB, np.uint8)
+    ov = np.full(NB * 16 * Hkv * d, 0xCD, np.uint8)
+    assert oracle.load().kv_write(ok, ov, oracle.DTYPE_FP8_E4M3, 16, Hkv, d, s32, s32,
+                                  kbits, vbits, slots) == 0
+    for gpu, ref, bits in ((kc, ok, kbits), (vc, ov, vbits)):
+        g = gpu.cpu().numpy().reshape(NB * 16, d)[slots]
+        r = ref.reshape(NB * 16, d)[slots]
+        b = bits.reshape(T, d)
+        nan_in = (b & 0x7FFF) > 0x7F80
+        assert np.array_equal(g[~nan_in], r[~nan_in])
+        assert np.all((g[nan_in] & 0x7F) == 0x7F) and np.all((r[nan_in] & 0x7F) == 0x7F)
 
 
 def test_write_skips_negative_and_reports_out_of_range():
