@@ -70,3 +70,25 @@ def test_argument_validation(lib):
     assert lib.paged_attention_decode(16, ctypes.byref(c), 16, 4, 16, 0, 4,
                                       0.1, 16, 64, 0, None, 0, None) == 0
     assert lib.paged_attention_partition_tokens(8, 64, 8, 1000, 17) == -1
+
+
+def test_missing_library_fails_loudly():
+    """Without the built library every call raises: the package has no CPU
+    or PyTorch fallback to take over."""
+    import subprocess
+    import sys
+    code = (
+        "from pathlib import Path\n"
+        "from paged_kv_cache_48_gb300 import _native\n"
+        "_native.LIBRARY = Path('/nonexistent/libpagedkv.so')\n"
+        "_native._LIB = None\n"
+        "import paged_kv_cache_48_gb300 as pk\n"
+        "try:\n"
+        "    pk.pkv_check()\n"
+        "except RuntimeError as e:\n"
+        "    print('raised:', 'missing' in str(e))\n"
+    )
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                       timeout=300, cwd=str(_native.PKG.parent))
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "raised: True" in r.stdout
