@@ -21,9 +21,47 @@ namespace pkv {
 
 static __device__ unsigned long long g_err_write_zero = 0ull;
 
-// Eight bf16 values to eight E4M3 bytes: the IEEE binary32 quotient
+// Reciprocal bounds for the E4M3 encode: lo and hi bracket 1 / scale
+// tightly enough that x * lo and x * hi (each rounded once) enclose the
+// rounded quotient RN(x / scale) for every finite x whose quotient is a
+// normal binary32 number: lo = RN(RN(1/s)(1 - 2^-20)) is below
+// (1/s)(1 - 2^-21), so x * lo, rounded, stays below x/s (1 - 2^-21), which
+// is below RN(x/s) (relative error at most 2^-24); hi likewise above.  E4M3
+// rounding is monotonic, so when both products round to the same E4M3 code
+// the quotient does too.  Where they differ (the quotient is near an E4M3
+// midpoint) the quotient is computed by IEEE division; tiny quotients, in
+// binary32's subnormal range, are far below the smallest E4M3 step and give
+// +-0 either way.  ok = 0 (a scale below 1e-38 or above 2^126, where the
+// reciprocal or its bounds leave the normal range) sends every value to
+// division.
+struct E4m3Recip {
+  float lo, hi;
+  int ok;
+};
+
+__device__ __forceinline__ E4m3Recip e4m3_recip(float scale) {
+  const float r = __frcp_rn(scale);
+  E4m3Recip e;
+  e.ok = r >= 1.17549435e-38f && r < 1e38f;
+  e.lo = __fmul_rn(r, 1.f - 0x1p-20f);
+  e.hi = __fmul_rn(r, 1.f + 0x1p-20f);
+  return e;
+}
+
+// Two values to two E4M3 bytes (low byte = a): the IEEE binary32 quotient
 // x / scale, rounded to nearest even and saturated to +-448.
-__device__ __forceinline__ uint2 quant8_e4m3(const uint4 &src, float scale) {
+__device__ __forceinline__ uint32_t quant2_e4m3(float a, float b, float scale, E4m3Recip r) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a * r.lo, b * r.lo), __NV_SATFINITE,
+                                               __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(a * r.hi, b * r.hi), __NV_SATFINITE,
+                                               __NV_E4M3);
+  if (r.ok && lo == hi) return lo;
+  return __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a, scale), __fdiv_rn(b, scale)),
+                                  __NV_SATFINITE, __NV_E4M3);
+}
+
+// Eight bf16 values to eight E4M3 bytes.
+__device__ __forceinline__ uint2 quant8_e4m3(const uint4 &src, float scale, E4m3Recip r) {
   const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&src);
   uint32_t out[2];
 #pragma unroll
@@ -32,15 +70,67 @@ __device__ __forceinline__ uint2 quant8_e4m3(const uint4 &src, float scale) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const float2 f = __bfloat1622float2(h[2 * i + j]);
-      float2 qv;
-      qv.x = __fdiv_rn(f.x, scale);
-      qv.y = __fdiv_rn(f.y, scale);
-      const __nv_fp8x2_storage_t two = __nv_cvt_float2_to_fp8x2(qv, __NV_SATFINITE, __NV_E4M3);
-      word |= (uint32_t)two << (16 * j);
+      word |= quant2_e4m3(f.x, f.y, scale, r) << (16 * j);
     }
     out[i] = word;
   }
   return make_uint2(out[0], out[1]);
+}
+
+// The slot-mapped write of work items first, first + stride, ... < total
+// (see kv_write_kernel).  I is the index type: 32-bit whenever the items
+// fit, so that the per-item token index is a 32-bit shift (a power-of-two
+// row, vpr_shift >= 0) or a 32-bit division instead of a 64-bit division.
+template <bool FP8, typename I>
+__device__ __forceinline__ void write_items(const uint4 *__restrict__ k,
+                                            const uint4 *__restrict__ v,
+                                            const int64_t *__restrict__ slot_mapping, I total,
+                                            I first, I stride, int vecs_per_row, int vpr_shift,
+                                            uint8_t *__restrict__ key_cache,
+                                            uint8_t *__restrict__ value_cache, int64_t num_slots,
+                                            float k_scale, float v_scale) {
+  const E4m3Recip kr = e4m3_recip(k_scale), vr = e4m3_recip(v_scale);
+  const I vpr = (I)vecs_per_row;
+  for (I idx = first; idx < total; idx += stride) {
+    const I tok = vpr_shift >= 0 ? idx >> vpr_shift : idx / vpr;
+    const int vec = (int)(idx - tok * vpr);
+    const int64_t slot = __ldg(slot_mapping + tok);
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      if (vec == 0) record_error(&g_err_write_zero, PKV_ERR_RANGE, (long long)tok);
+      continue;
+    }
+    const uint4 kv = __ldg(k + idx);
+    const uint4 vv = __ldg(v + idx);
+    const int64_t dst_vec = slot * vecs_per_row + vec;  // in 8-element units
+    if (!FP8) {
+      reinterpret_cast<uint4 *>(key_cache)[dst_vec] = kv;
+      reinterpret_cast<uint4 *>(value_cache)[dst_vec] = vv;
+    } else {
+      reinterpret_cast<uint2 *>(key_cache)[dst_vec] = quant8_e4m3(kv, k_scale, kr);
+      reinterpret_cast<uint2 *>(value_cache)[dst_vec] = quant8_e4m3(vv, v_scale, vr);
+    }
+  }
+}
+
+template <bool FP8>
+__device__ __forceinline__ void write_all_items(const uint4 *__restrict__ k,
+                                                const uint4 *__restrict__ v,
+                                                const int64_t *__restrict__ slot_mapping,
+                                                int64_t num_tokens, int vecs_per_row,
+                                                uint8_t *__restrict__ key_cache,
+                                                uint8_t *__restrict__ value_cache,
+                                                int64_t num_slots, float k_scale, float v_scale,
+                                                int64_t first, int64_t stride) {
+  const int64_t total = num_tokens * vecs_per_row;
+  const int vpr_shift = (vecs_per_row & (vecs_per_row - 1)) ? -1 : __ffs(vecs_per_row) - 1;
+  if (total + stride <= (int64_t)UINT32_MAX)
+    write_items<FP8, uint32_t>(k, v, slot_mapping, (uint32_t)total, (uint32_t)first,
+                               (uint32_t)stride, vecs_per_row, vpr_shift, key_cache, value_cache,
+                               num_slots, k_scale, v_scale);
+  else
+    write_items<FP8, int64_t>(k, v, slot_mapping, total, first, stride, vecs_per_row, vpr_shift,
+                              key_cache, value_cache, num_slots, k_scale, v_scale);
 }
 
 // ---------------------------------------------------------------------------
@@ -58,28 +148,9 @@ kv_write_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                 float k_scale, float v_scale) {
   grid_dependency_wait();
   allow_dependent_launch();
-  const int64_t total = num_tokens * vecs_per_row;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-       idx < total; idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t tok = idx / vecs_per_row;
-    const int vec = (int)(idx - tok * vecs_per_row);
-    const int64_t slot = __ldg(slot_mapping + tok);
-    if (slot < 0) continue;  // padding token
-    if (slot >= num_slots) {
-      if (vec == 0) record_error(&g_err_write_zero, PKV_ERR_RANGE, tok);
-      continue;
-    }
-    const uint4 kv = __ldg(k + idx);
-    const uint4 vv = __ldg(v + idx);
-    const int64_t dst_vec = slot * vecs_per_row + vec;  // in 8-element units
-    if (!FP8) {
-      reinterpret_cast<uint4 *>(key_cache)[dst_vec] = kv;
-      reinterpret_cast<uint4 *>(value_cache)[dst_vec] = vv;
-    } else {
-      reinterpret_cast<uint2 *>(key_cache)[dst_vec] = quant8_e4m3(kv, k_scale);
-      reinterpret_cast<uint2 *>(value_cache)[dst_vec] = quant8_e4m3(vv, v_scale);
-    }
-  }
+  write_all_items<FP8>(k, v, slot_mapping, num_tokens, vecs_per_row, key_cache, value_cache,
+                       num_slots, k_scale, v_scale, blockIdx.x * (int64_t)blockDim.x + threadIdx.x,
+                       (int64_t)gridDim.x * blockDim.x);
 }
 
 // ---------------------------------------------------------------------------
@@ -199,29 +270,10 @@ kv_zero_write_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
     return;
   }
   if (!write_tokens) return;
-  const int64_t total = num_tokens * vecs_per_row;
-  const int64_t stride = (int64_t)(gridDim.x - zero_ctas) * blockDim.x;
-  for (int64_t idx = (blockIdx.x - zero_ctas) * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += stride) {
-    const int64_t tok = idx / vecs_per_row;
-    const int vec = (int)(idx - tok * vecs_per_row);
-    const int64_t slot = __ldg(slot_mapping + tok);
-    if (slot < 0) continue;  // padding token
-    if (slot >= num_slots) {
-      if (vec == 0) record_error(&g_err_write_zero, PKV_ERR_RANGE, tok);
-      continue;
-    }
-    const uint4 kv = __ldg(k + idx);
-    const uint4 vv = __ldg(v + idx);
-    const int64_t dst_vec = slot * vecs_per_row + vec;  // in 8-element units
-    if (!FP8) {
-      reinterpret_cast<uint4 *>(key_cache)[dst_vec] = kv;
-      reinterpret_cast<uint4 *>(value_cache)[dst_vec] = vv;
-    } else {
-      reinterpret_cast<uint2 *>(key_cache)[dst_vec] = quant8_e4m3(kv, k_scale);
-      reinterpret_cast<uint2 *>(value_cache)[dst_vec] = quant8_e4m3(vv, v_scale);
-    }
-  }
+  write_all_items<FP8>(k, v, slot_mapping, num_tokens, vecs_per_row, key_cache, value_cache,
+                       num_slots, k_scale, v_scale,
+                       (blockIdx.x - zero_ctas) * (int64_t)blockDim.x + threadIdx.x,
+                       (int64_t)(gridDim.x - zero_ctas) * blockDim.x);
 }
 
 // ---------------------------------------------------------------------------
