@@ -363,6 +363,110 @@ __device__ __forceinline__ void attend_block(uint32_t sk, uint32_t sv, int nv,
     block_update<FP8, D, false>(sv, nv, sc, scale_log2, st, lane);
 }
 
+// fp8 caches: two 16-token blocks per online-softmax step.  Their scores
+// come from independent mma chains, one shuffle reduction and one rescale
+// serve both, and both P.V products accumulate into O.  The result is the
+// same softmax, with the running maximum advanced once per pair.
+template <int D, bool FULL>
+__device__ __forceinline__ void pair_update(uint32_t sva, int nva, const float (&sa)[4],
+                                            uint32_t svb, int nvb, const float (&sb)[4],
+                                            float scale_log2, WarpState<true, D> &st, int lane) {
+  using C = Cfg<true, D>;
+  const int g = lane >> 2, c = lane & 3;
+  const int v_row = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int v_chk = lane >> 4;
+  const bool a_lo = FULL || g < nva, a_hi = FULL || g + 8 < nva;
+  const bool b_lo = FULL || g < nvb, b_hi = FULL || g + 8 < nvb;
+  const float s0 = a_lo ? sa[0] * scale_log2 : -INFINITY;
+  const float s1 = a_lo ? sa[1] * scale_log2 : -INFINITY;
+  const float s2 = a_hi ? sa[2] * scale_log2 : -INFINITY;
+  const float s3 = a_hi ? sa[3] * scale_log2 : -INFINITY;
+  const float t0 = b_lo ? sb[0] * scale_log2 : -INFINITY;
+  const float t1 = b_lo ? sb[1] * scale_log2 : -INFINITY;
+  const float t2 = b_hi ? sb[2] * scale_log2 : -INFINITY;
+  const float t3 = b_hi ? sb[3] * scale_log2 : -INFINITY;
+  float bm0 = fmaxf(fmaxf(s0, s2), fmaxf(t0, t2)), bm1 = fmaxf(fmaxf(s1, s3), fmaxf(t1, t3));
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+  }
+  const float mn0 = fmaxf(st.m0, bm0), mn1 = fmaxf(st.m1, bm1);
+  const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
+  const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float al0 = exp2f(st.m0 - mu0), al1 = exp2f(st.m1 - mu1);
+  const float p0 = exp2f(s0 - mu0), p2 = exp2f(s2 - mu0);
+  const float p1 = exp2f(s1 - mu1), p3 = exp2f(s3 - mu1);
+  const float q0 = exp2f(t0 - mu0), q2 = exp2f(t2 - mu0);
+  const float q1 = exp2f(t1 - mu1), q3 = exp2f(t3 - mu1);
+  st.l0 = st.l0 * al0 + ((p0 + p2) + (q0 + q2));
+  st.l1 = st.l1 * al1 + ((p1 + p3) + (q1 + q3));
+  st.m0 = mn0;
+  st.m1 = mn1;
+  if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+    for (int mt = 0; mt < C::MT; ++mt) {
+      st.o[mt][0] *= al0;
+      st.o[mt][1] *= al1;
+      st.o[mt][2] *= al0;
+      st.o[mt][3] *= al1;
+    }
+  }
+  const uint32_t pa0 = movmatrix_trans(pack_f16x2(p0, p1));
+  const uint32_t pa1 = movmatrix_trans(pack_f16x2(p2, p3));
+  const uint32_t pb0 = movmatrix_trans(pack_f16x2(q0, q1));
+  const uint32_t pb1 = movmatrix_trans(pack_f16x2(q2, q3));
+  // stale V rows (past the sequence) are zeroed in the A fragments, as in
+  // block_update
+  uint32_t ma_lo = 0xffffffffu, ma_hi = 0xffffffffu, mb_lo = 0xffffffffu, mb_hi = 0xffffffffu;
+  if (!FULL) {
+    ma_lo = (2 * c < nva ? 0x0000ffffu : 0u) | (2 * c + 1 < nva ? 0xffff0000u : 0u);
+    ma_hi = (2 * c + 8 < nva ? 0x0000ffffu : 0u) | (2 * c + 9 < nva ? 0xffff0000u : 0u);
+    mb_lo = (2 * c < nvb ? 0x0000ffffu : 0u) | (2 * c + 1 < nvb ? 0xffff0000u : 0u);
+    mb_hi = (2 * c + 8 < nvb ? 0x0000ffffu : 0u) | (2 * c + 9 < nvb ? 0xffff0000u : 0u);
+  }
+  auto mask = [&](uint32_t x, uint32_t m) { return FULL ? x : (x & m); };
+#pragma unroll
+  for (int qq = 0; qq < C::MT / 2; ++qq) {
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {
+      const uint32_t sv = blk ? svb : sva;
+      const uint32_t m_lo = blk ? mb_lo : ma_lo, m_hi = blk ? mb_hi : ma_hi;
+      const uint32_t f0 = blk ? pb0 : pa0, f1 = blk ? pb1 : pa1;
+      uint32_t r0, r1, r2, r3;
+      ldmatrix_x4_trans(sv + tile_offset<C::BOX_BYTES>(v_row, 2 * qq + v_chk), r0, r1, r2, r3);
+      const uint32_t x0 = prmt(r0, 0u, 0x3120u), x1 = prmt(r1, 0u, 0x3120u);
+      const uint32_t x2 = prmt(r2, 0u, 0x3120u), x3 = prmt(r3, 0u, 0x3120u);
+      uint32_t c0l, c0h, c1l, c1h, c2l, c2h, c3l, c3h;
+      e4m3x4_to_f16x2x2(x0, c0l, c0h);
+      e4m3x4_to_f16x2x2(x1, c1l, c1h);
+      e4m3x4_to_f16x2x2(x2, c2l, c2h);
+      e4m3x4_to_f16x2x2(x3, c3l, c3h);
+      mma_kv<true>(st.o[2 * qq], mask(c0l, m_lo), mask(c0h, m_lo), mask(c1l, m_hi),
+                   mask(c1h, m_hi), f0, f1);
+      mma_kv<true>(st.o[2 * qq + 1], mask(c2l, m_lo), mask(c2h, m_lo), mask(c3l, m_hi),
+                   mask(c3h, m_hi), f0, f1);
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void attend_pair(uint32_t ska, int nva, uint32_t skb, int nvb,
+                                            const uint32_t (&qf)[Cfg<true, D>::MT][2],
+                                            float scale_log2, WarpState<true, D> &st,
+                                            int lane) {
+  using C = Cfg<true, D>;
+  float sa[4], sb[4];
+  block_scores<true, D>(ska, qf, sa, lane);
+  block_scores<true, D>(skb, qf, sb, lane);
+  if (nva == 16 && nvb == 16)
+    pair_update<D, true>(ska + C::TILE_BYTES, nva, sa, skb + C::TILE_BYTES, nvb, sb, scale_log2,
+                         st, lane);
+  else
+    pair_update<D, false>(ska + C::TILE_BYTES, nva, sa, skb + C::TILE_BYTES, nvb, sb,
+                          scale_log2, st, lane);
+}
+
 // Lane 0 issues the TMA loads of one block-head (K and V tiles) into a
 // stage: one box per tile, [head_dim slice][token][BOX_BYTES].
 template <bool FP8, int D>
@@ -468,7 +572,27 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   for (; issued < pre; ++issued) issue(issued);
 
   bool failed = false;
-  for (int i = 0; i < my_n; ++i) {
+  int i = 0;
+  if constexpr (FP8 && C::STAGES >= 4) {
+    // two blocks per step while two more are in flight
+    for (; i + 1 < my_n; i += 2) {
+      const int sa = i % C::STAGES, sb = (i + 1) % C::STAGES;
+      if (!mbar_wait_bounded(&bars[warp][sa], (i / C::STAGES) & 1, p.timeout_ns) ||
+          !mbar_wait_bounded(&bars[warp][sb], ((i + 1) / C::STAGES) & 1, p.timeout_ns)) {
+        failed = true;
+        break;
+      }
+      const int ja = blk0 + warp + i * C::NW, jb = ja + C::NW;
+      const int nva = stage_ok[warp][sa] ? min(16, tok1 - ja * 16) : 0;
+      const int nvb = stage_ok[warp][sb] ? min(16, tok1 - jb * 16) : 0;
+      attend_pair<D>(smem_u32(ring + sa * C::STAGE_BYTES), nva,
+                     smem_u32(ring + sb * C::STAGE_BYTES), nvb, qf, p.scale_log2, st, lane);
+      __syncwarp();
+      if (issued < my_n) issue(issued++);
+      if (issued < my_n) issue(issued++);
+    }
+  }
+  for (; !failed && i < my_n; ++i) {
     const int stage = i % C::STAGES;
     if (!mbar_wait_bounded(&bars[warp][stage], (i / C::STAGES) & 1, p.timeout_ns)) {
       failed = true;
