@@ -272,7 +272,8 @@ pkv_status paged_attention_prefill(const void *q, const pkv_cache *cache,
  *   Both bf16 and E4M3 caches are accepted (the prefix pass of an E4M3
  *   cache runs on f16 operands, as in paged_attention_prefill).
  * Pass 1 (tensor cores) attends each group's member queries to its prefix,
- * 512 tokens per partition; pass 2 attends each sequence to its own
+ * in partitions of at least 512 tokens (longer when that still fills one
+ * wave of CTAs); pass 2 attends each sequence to its own
  * tokens; a log-sum-exp merge combines the partials.  A group whose
  * members' tables or lengths break the contract is reported by pkv_check()
  * and its members are attended in full, so the output stays correct. */
