@@ -259,7 +259,8 @@ pkv_status paged_attention_prefill(const void *q, const pkv_cache *cache,
  * this library's (the pages describe the sharing, not a kernel for it).
  *   group_start   int32 [num_groups + 1] (device): group G is sequences
  *                 group_start[G] .. group_start[G+1] - 1 (consecutive rows
- *                 of q, block_tables, seq_lens); groups must not overlap;
+ *                 of q, block_tables, seq_lens); groups must not overlap
+ *                 (group_start never decreases);
  *                 sequences outside every group are attended in full.
  *   prefix_len    int32 [num_groups] (device): tokens of G's shared prefix,
  *                 a multiple of 16, at most max_prefix_len; every member's

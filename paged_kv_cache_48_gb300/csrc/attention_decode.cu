@@ -80,29 +80,51 @@ struct DecodeParams {
 // is attended in full, which is still the right result.
 __device__ int cascade_start(const DecodeParams &p, int b, int L, int lane, bool report) {
   if (!p.group_start || p.num_groups <= 0) return 0;
-  int lo = 0, hi = p.num_groups - 1, G = -1;  // last group starting at or before b
-  while (lo <= hi) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(p.group_start + mid) <= b) {
-      G = mid;
-      lo = mid + 1;
-    } else {
-      hi = mid - 1;
+  // Two dependent memory round trips.  First, what does not depend on the
+  // group: this sequence's first table entries and the group starts, 32 a
+  // time; starts ascend, so a ballot finds the last one at or before b.
+  constexpr int PRE = 2;  // table entries per lane loaded ahead (prefixes <= 1024 tokens)
+  const int nchk = min(p.max_prefix_len >> 4, p.max_blocks);  // entries a prefix can cover
+  const int32_t *mine = p.block_tables + (size_t)b * p.max_blocks;
+  int32_t mine_pre[PRE], lead_pre[PRE];
+#pragma unroll
+  for (int k = 0; k < PRE; ++k) mine_pre[k] = lane + 32 * k < nchk ? __ldg(mine + lane + 32 * k) : 0;
+  int G = -1, q0 = 0;
+  for (int base = 0; base < p.num_groups; base += 32) {
+    const int gi = base + lane;
+    const int st = gi < p.num_groups ? __ldg(p.group_start + gi) : INT_MAX;
+    const unsigned m = __ballot_sync(0xffffffffu, st <= b);
+    if (m) {
+      const int last = 31 - __clz(m);
+      G = base + last;
+      q0 = __shfl_sync(0xffffffffu, st, last);
     }
+    if (m != 0xffffffffu) break;
   }
   if (G < 0) return 0;
-  const int q0 = __ldg(p.group_start + G), n = __ldg(p.group_start + G + 1) - q0;
-  const int P = __ldg(p.prefix_len + G);
+  // Second: the group's end and prefix length, and the first member's
+  // table entries.
+  const int q1 = __ldg(p.group_start + G + 1), P = __ldg(p.prefix_len + G);
+  const int32_t *lead = p.block_tables + (size_t)max(q0, 0) * p.max_blocks;
+  const bool lead_ok = q0 >= 0 && q0 < p.batch;
+#pragma unroll
+  for (int k = 0; k < PRE; ++k)
+    lead_pre[k] = lead_ok && lane + 32 * k < nchk ? __ldg(lead + lane + 32 * k) : 0;
+  const int n = q1 - q0;
   if (b >= q0 + n || P == 0) return 0;  // in no group / nothing shared
   if (n < 1 || q0 < 0 || q0 + n > p.batch || P < 0 || (P & 15) || P > p.max_blocks * 16 ||
       P > p.max_prefix_len || n > p.max_group_size || L < P) {
     if (report && lane == 0) record_error(&g_err_attention, PKV_ERR_RANGE, b);
     return 0;
   }
-  const int32_t *mine = p.block_tables + (size_t)b * p.max_blocks;
-  const int32_t *lead = p.block_tables + (size_t)q0 * p.max_blocks;
   int bad_j = INT_MAX;
-  for (int j = lane; j < (P >> 4); j += 32) {
+#pragma unroll
+  for (int k = 0; k < PRE; ++k) {
+    const int j = lane + 32 * k;
+    const int32_t id = mine_pre[k];
+    if (j < (P >> 4) && (id != lead_pre[k] || id < 0 || id >= p.num_blocks)) bad_j = min(bad_j, j);
+  }
+  for (int j = lane + 32 * PRE; j < (P >> 4); j += 32) {
     const int32_t id = __ldg(mine + j);
     if (id != __ldg(lead + j) || id < 0 || id >= p.num_blocks) bad_j = min(bad_j, j);
   }
