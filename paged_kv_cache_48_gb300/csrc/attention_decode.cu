@@ -538,6 +538,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   grid_dependency_wait();
   allow_dependent_launch();
 
+  // q does not depend on the sequence's extent: its loads go out first
+  const int heads_here = min(8, p.group - qg * 8);
+  const size_t row0 = (size_t)b * p.num_heads + (size_t)kvh * p.group + qg * 8;
+  uint32_t qf[C::MT][2];
+  load_q<FP8, D>(qf, p.q + row0 * D, heads_here, lane);
+
   // ---- sequence extent and this CTA's partition --------------------------
   int L = __ldg(p.seq_lens + b);
   {
@@ -560,11 +566,6 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int blk0 = tok0 >> 4;
   const int nblk = (tok1 - tok0 + 15) >> 4;
   const int my_n = nblk > warp ? (nblk - warp + C::NW - 1) / C::NW : 0;
-  const int heads_here = min(8, p.group - qg * 8);
-  const size_t row0 = (size_t)b * p.num_heads + (size_t)kvh * p.group + qg * 8;
-
-  uint32_t qf[C::MT][2];
-  load_q<FP8, D>(qf, p.q + row0 * D, heads_here, lane);
 
   // ---- block ids of this warp, 32 at a time in registers -----------------
   const int32_t *table = p.block_tables + (size_t)b * p.max_blocks + blk0 + warp;
