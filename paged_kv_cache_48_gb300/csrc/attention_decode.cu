@@ -543,6 +543,15 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const size_t row0 = (size_t)b * p.num_heads + (size_t)kvh * p.group + qg * 8;
   uint32_t qf[C::MT][2];
   load_q<FP8, D>(qf, p.q + row0 * D, heads_here, lane);
+  // Without shared prefixes the partition's first block is part * part_tokens
+  // / 16 whatever the length: this warp's first 32 block ids go out now too
+  // (masked to the partition's blocks once the length is known).
+  const bool ids_early = !p.group_start;
+  int ids_pre = -1;
+  if (ids_early) {
+    const long long j = (long long)part * (p.part_tokens >> 4) + warp + (long long)lane * C::NW;
+    if (j < p.max_blocks) ids_pre = __ldg(p.block_tables + (size_t)b * p.max_blocks + j);
+  }
 
   // ---- sequence extent and this CTA's partition --------------------------
   int L = __ldg(p.seq_lens + b);
@@ -572,7 +581,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   int ids_reg = -1;
   const uint64_t policy = l2_policy_evict_normal();
   auto issue = [&](int i) {
-    if ((i & 31) == 0) ids_reg = (i + lane < my_n) ? __ldg(table + (i + lane) * C::NW) : -1;
+    if ((i & 31) == 0)
+      ids_reg = (i + lane < my_n) ? (i == 0 && ids_early ? ids_pre : __ldg(table + (i + lane) * C::NW))
+                                  : -1;
     int phys = __shfl_sync(0xffffffffu, ids_reg, i & 31);
     if (lane == 0) {
       const int stage = i % C::STAGES;
