@@ -71,3 +71,13 @@ def test_profile_traffic_follows_the_kernel_source_hash(tmp_path):
 def test_host_cpu_model_names_the_cores():
     s = bench.host_cpu_model()
     assert isinstance(s, str) and s.endswith("cores")
+
+
+def test_profile_summaries_name_only_committed_commands():
+    """Every ncu summary gives the command that made it, and that command
+    runs files of the repository (bench.py), never a scratch script."""
+    for p in (ROOT / "profiles").glob("*.md"):
+        text = p.read_text()
+        assert "ncu " in text and "--clock-control none" in text, p.name
+        assert "python bench.py" in text, p.name
+        assert "_work" not in text, p.name
