@@ -46,7 +46,8 @@ def test_packed_views_hold_the_tensors_at_aligned_offsets():
     assert buf.dtype == torch.uint8
     for v, t in zip(views, ts):
         assert v.dtype == t.dtype and v.shape == t.shape and torch.equal(v, t)
-        assert (v.data_ptr() - buf.data_ptr()) % 256 == 0
+        if v.numel():  # an empty view may report a null data pointer
+            assert (v.data_ptr() - buf.data_ptr()) % 256 == 0
     # the views alias the buffer: a write through one is seen in the other
     views[0][0] = 99
     assert int(buf[:4].view(torch.int32)[0]) == 99
