@@ -1,7 +1,7 @@
 // pkv_api.cu -- shared host entry points of the paged KV-cache library:
 // argument validation, device properties, the error-word check, status
 // strings and the version.
-#include <mutex>
+#include <atomic>
 
 #include "pkv_host.h"
 
@@ -20,19 +20,19 @@ pkv_status validate_cache(const pkv_cache *c) {
 }
 
 int device_sm_count() {
-  static std::mutex mu;
-  static int cached[64] = {0};
+  // one entry per device, written once with the same value by any thread
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
-  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  if (dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
       cudaSuccess)
     return -1;
-  if (dev < 64) {
-    std::lock_guard<std::mutex> lock(mu);
-    cached[dev] = sms;
-  }
+  if (dev < 64) cached[dev].store(sms, std::memory_order_relaxed);
   return sms;
 }
 
