@@ -146,6 +146,29 @@ def test_bad_block_id_is_reported_not_faulted():
     assert pkv_check()[0] == PKV_OK
 
 
+@pytest.mark.parametrize("partition_tokens", [0, 64])
+def test_fp8_bad_block_inside_a_pair_is_masked(partition_tokens):
+    """E4M3 decode takes blocks two at a time: a bad block id inside a pair
+    is reported, contributes nothing, and leaves every other sequence equal
+    to the oracle."""
+    W, ref = _case("fp8_small")
+    b = int(np.argmax(W.seq_lens))
+    assert W.seq_lens[b] > 6 * 16
+    G = harness.upload(W)
+    harness.gpu_step(W, G)
+    tables = G.tables.clone()
+    tables[b, 5] = W.num_blocks + 7
+    out = paged_attention_decode(G.q, G.cache, tables, G.seq_lens, W.scale,
+                                 max_seq_len=W.max_seq_len,
+                                 partition_tokens=partition_tokens)
+    st, detail = pkv_check()
+    assert st == PKV_ERR_RANGE and detail == b
+    got = out.float().cpu().numpy()
+    keep = [i for i in range(W.batch) if i != b]
+    harness.assert_close(got[keep], ref[keep], "fp8_e4m3")
+    assert np.isfinite(got[b]).all()
+
+
 def test_seq_len_beyond_bound_is_reported():
     W, _ = _case("tiny")
     G = harness.upload(W)
