@@ -70,6 +70,12 @@ def test_argument_validation(lib):
     assert lib.paged_attention_decode(16, ctypes.byref(c), 16, 4, 16, 0, 4,
                                       0.1, 16, 64, 0, None, 0, None) == 0
     assert lib.paged_attention_partition_tokens(8, 64, 8, 1000, 17) == -1
+    # grid limits are checked on the host: batch (grid z) and partitions
+    # (grid y) at most 65535
+    assert lib.paged_attention_decode(16, ctypes.byref(c), 16, 4, 16, 65536, 4,
+                                      0.1, 16, 64, 0, None, 0, None) == 1
+    assert lib.paged_attention_decode(16, ctypes.byref(c), 16, 1 << 16, 16, 2, 4,
+                                      0.1, 16, 16 * 65536, 16, None, 0, None) == 1
 
 
 def test_missing_library_fails_loudly():
