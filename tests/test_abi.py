@@ -98,3 +98,28 @@ def test_missing_library_fails_loudly():
                        timeout=300, cwd=str(_native.PKG.parent))
     assert r.returncode == 0, r.stderr[-2000:]
     assert "raised: True" in r.stdout
+
+
+def test_cascade_argument_validation(lib):
+    """Shared-prefix decode rejects bad arguments on the host, before any
+    CUDA call: unaligned prefix bound, non-positive scale, groups wider than
+    128 query heads per kv head, too many groups, missing workspace."""
+    c = _cache()
+
+    def call(batch=2, num_heads=4, num_groups=1, max_prefix_len=32, scale=0.1,
+             workspace=None, workspace_bytes=0, partition_tokens=16):
+        return lib.paged_attention_decode_cascade(
+            16, ctypes.byref(c), 16, 8, 16, batch, num_heads, 16, 16, num_groups, 2,
+            max_prefix_len, scale, 16, 128, partition_tokens, workspace,
+            workspace_bytes, None)
+
+    assert call(max_prefix_len=24) == 1
+    assert call(scale=0.0) == 1
+    assert call(scale=-1.0) == 1
+    assert call(num_heads=2 * 130) == 3
+    assert call(num_groups=65536) == 1
+    assert call() == 7                       # no workspace
+    need = lib.paged_attention_cascade_workspace_bytes(2, 4, 2, 128, 128, 32, 16)
+    assert need > 0
+    assert call(workspace=256, workspace_bytes=need - 1) == 7
+    assert call(batch=0) == 0                # empty batch: nothing to do
