@@ -123,3 +123,27 @@ def test_cascade_argument_validation(lib):
     assert need > 0
     assert call(workspace=256, workspace_bytes=need - 1) == 7
     assert call(batch=0) == 0                # empty batch: nothing to do
+
+
+def test_prefill_argument_validation(lib):
+    """Chunked prefill rejects bad arguments on the host, before any CUDA
+    call, and treats an empty step as a no-op."""
+    c = _cache()
+
+    def call(batch=2, num_heads=4, num_tokens=10, scale=0.1, max_query_len=8, q=16,
+             cache=c):
+        return lib.paged_attention_prefill(q, ctypes.byref(cache), 16, 8, 16, 16, batch,
+                                           num_heads, num_tokens, scale, 16, max_query_len,
+                                           None)
+
+    assert call(scale=0.0) == 1
+    assert call(scale=float("nan")) == 1
+    assert call(num_tokens=-1) == 1
+    assert call(num_heads=3) == 3            # not a multiple of the kv heads
+    assert call(num_heads=2 * 130) == 3      # more than 128 query heads per kv head
+    assert call(q=8) == 1                    # q not 16-byte aligned
+    assert call(batch=65536) == 1
+    assert call(num_tokens=1 << 31) == 1
+    assert call(batch=0) == 0 and call(num_tokens=0) == 0 and call(max_query_len=0) == 0
+    fp8_no_scale = _cache(dtype=1, k_scale=0.0)
+    assert call(cache=fp8_no_scale) == 1
