@@ -147,3 +147,35 @@ def test_prefill_argument_validation(lib):
     assert call(batch=0) == 0 and call(num_tokens=0) == 0 and call(max_query_len=0) == 0
     fp8_no_scale = _cache(dtype=1, k_scale=0.0)
     assert call(cache=fp8_no_scale) == 1
+
+
+def test_blocks_write_and_prep_argument_validation(lib):
+    """Block copy / swap, the fused zeroing + write and step input
+    preparation reject bad arguments on the host, before any CUDA call."""
+    c = _cache()
+    cp = ctypes.byref(c)
+    # copy-on-write and swap: negative counts, missing id lists; empty = no-op
+    assert lib.paged_kv_copy_blocks(cp, 16, 16, -1, 1, None) == 1
+    assert lib.paged_kv_copy_blocks(cp, None, 16, 3, 1, None) == 1
+    assert lib.paged_kv_copy_blocks(cp, 16, 16, 0, 1, None) == 0
+    for fn in (lib.paged_kv_swap_out, lib.paged_kv_swap_in):
+        assert fn(cp, 16, -1, 1, 16, 16, None) == 1
+        assert fn(cp, None, 3, 1, 16, 16, None) == 1
+        assert fn(cp, 16, 0, 1, 16, 16, None) == 0
+    # zeroing + write in one launch
+    zw = lib.paged_kv_zero_and_write
+    assert zw(16, 16, 16, -1, cp, 16, 1, 1, None) == 1
+    assert zw(8, 16, 16, 1, cp, 16, 0, 1, None) == 1     # k not 16-byte aligned
+    assert zw(16, 16, 16, 1, cp, None, 2, 1, None) == 1  # ids missing
+    assert zw(16, 16, 16, 0, cp, None, 0, 1, None) == 0  # nothing to do
+    # step input preparation
+    def prep(batch=2, max_blocks=8, max_model_len=128, num_rows=4, total=5,
+             qsl=16, positions=16):
+        return lib.paged_prepare_inputs(16, 16, batch, 16, max_blocks, 16, 16, max_model_len,
+                                        num_rows, total, 16, 16, qsl, positions, 16, 16, None)
+    assert prep(batch=-1) == 1
+    assert prep(max_blocks=0) == 1
+    assert prep(max_model_len=0) == 1
+    assert prep(qsl=None) == 1
+    assert prep(positions=None) == 1
+    assert prep(max_blocks=1 << 27) == 1     # max_blocks * 16 past int32
