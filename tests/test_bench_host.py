@@ -82,3 +82,14 @@ def test_profile_summaries_name_only_committed_commands():
         assert "ncu " in text and "--clock-control none" in text, p.name
         assert "python bench.py" in text, p.name
         assert "_work" not in text, p.name
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    """Under torchrun only rank 0 runs and prints the reference line; the
+    other ranks exit 0 at once."""
+    env = dict(__import__("os").environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, str(ROOT / "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_mha", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert not [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
