@@ -340,6 +340,38 @@ def pin_prepare_inputs_range_errors(oracle):
     assert sl[9] == sbt[3, 1] * 16 + 15
 
 
+def pin_prepare_inputs_negative_and_overflowing_counts(oracle):
+    """A negative count schedules nothing; an entry whose tokens do not all
+    fit below total_tokens writes nothing, while query_start_loc stays the
+    exclusive prefix sum of the clamped counts.  Expected values written
+    out by hand for this batch (total_tokens 8, counts 2, -3, 4, 5, 1):
+      entry 0 (row 2, c 10): tokens 0, 1 at positions 10, 11;
+      entry 1 (row 0, c 3):  count -3 -> 0 tokens, seq_len 3, an error;
+      entry 2 (row 1, c 0):  tokens 2..5 at positions 0..3;
+      entry 3 (row 3):       starts at 6, needs 6..10 > 7: nothing, an error;
+      entry 4 (row 1):       starts at 11 > 7: nothing, an error."""
+    sbt = np.array([[40, 41], [50, 51], [60, 61], [70, 71]], np.int32)
+    snc = np.array([3, 0, 10, 5], np.int32)
+    tok = np.arange(4 * 40, dtype=np.int32).reshape(4, 40) + 1000
+    idx = np.array([2, 0, 1, 3, 1], np.int32)
+    ns = np.array([2, -3, 4, 5, 1], np.int32)
+    out, err = oracle.prepare_inputs(idx, ns, sbt, snc, tok, 8)
+    assert err == 3
+    assert list(out["query_start_loc"]) == [0, 2, 2, 6, 11, 12]
+    assert list(out["seq_lens"][:3]) == [12, 3, 4]
+    assert np.array_equal(out["block_tables"][:3], sbt[[2, 0, 1]])
+    assert list(out["positions"][:6]) == [10, 11, 0, 1, 2, 3]
+    assert list(out["input_ids"][:6]) == [1090, 1091, 1040, 1041, 1042, 1043]
+    assert list(out["slot_mapping"][:6]) == [60 * 16 + 10, 60 * 16 + 11,
+                                             50 * 16, 50 * 16 + 1, 50 * 16 + 2, 50 * 16 + 3]
+    # entries 3 and 4 wrote nothing (the wrapper's fill value -7 remains),
+    # not even the two slots of entry 3 that would have fitted
+    assert list(out["seq_lens"][3:]) == [-7, -7]
+    assert (out["block_tables"][3:] == -7).all()
+    for k in ("positions", "input_ids", "slot_mapping"):
+        assert list(out[k][6:]) == [-7, -7], k
+
+
 # ---------------------------------------------------------------------------
 # attention: closed forms
 # ---------------------------------------------------------------------------

@@ -28,22 +28,38 @@ def _run(idx, ns, sbt, snc, tok, T):
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
+def _defined(idx, ns, R, T):
+    """Which outputs the oracle header defines for these inputs: entries
+    whose tokens all fit below T (`fits`), of which those with a valid row
+    (`valid`), and the token indices such entries own (`written`)."""
+    n = np.maximum(ns.astype(np.int64), 0)
+    qsl = np.concatenate([[0], np.cumsum(n)])
+    fits = qsl[1:] <= T
+    valid = fits & (idx >= 0) & (idx < R)
+    written = np.zeros(T, bool)
+    for b in range(idx.size):
+        if fits[b]:
+            written[qsl[b]:qsl[b + 1]] = True
+    return fits, valid, written
+
+
 def _compare(gpu, ref, ns, idx, R):
-    valid = (idx >= 0) & (idx < R)
+    """Element-wise equality on every output position the oracle defines."""
+    T = ref["slot_mapping"].size
+    _, valid, written = _defined(idx, ns, R, T)
     assert np.array_equal(gpu["query_start_loc"], ref["query_start_loc"])
     assert np.array_equal(gpu["seq_lens"][valid], ref["seq_lens"][valid])
     assert np.array_equal(gpu["block_tables"][valid], ref["block_tables"][valid])
-    T = ref["slot_mapping"].size
-    written = np.zeros(T, bool)
+    assert np.array_equal(gpu["slot_mapping"][written], ref["slot_mapping"][written])
+    assert (ref["slot_mapping"][~written] == -7).all()   # the oracle left them alone
+    has_row = np.zeros(T, bool)
     qsl = ref["query_start_loc"]
-    for b in range(idx.size):
-        if valid[b]:
-            written[qsl[b]:qsl[b] + max(ns[b], 0)] = True
-    assert np.array_equal(gpu["slot_mapping"], ref["slot_mapping"]) or \
-        np.array_equal(gpu["slot_mapping"][written], ref["slot_mapping"][written])
-    assert np.array_equal(gpu["positions"][written], ref["positions"][written])
+    for b in np.flatnonzero(valid):
+        has_row[qsl[b]:qsl[b] + max(ns[b], 0)] = True
+    assert np.array_equal(gpu["positions"][has_row], ref["positions"][has_row])
     ok = written & (ref["slot_mapping"] >= 0)
     assert np.array_equal(gpu["input_ids"][ok], ref["input_ids"][ok])
+    return written
 
 
 @pytest.mark.parametrize("kind", ["decode", "mixed", "large"])
@@ -65,7 +81,7 @@ def test_prepare_inputs_matches_oracle(kind):
     assert pkv_check()[0] == PKV_OK
     ref, err = oracle.load().prepare_inputs(idx, ns, sbt, snc, tok, T)
     assert err == 0
-    _compare(gpu, ref, ns, idx, R)
+    assert _compare(gpu, ref, ns, idx, R).all()   # every token is an output
 
 
 def test_prepare_inputs_reports_range_errors():
@@ -116,3 +132,39 @@ def test_decode_step_driven_by_prepared_inputs():
     kc, vc = harness.oracle_cache(W)
     ref = harness.oracle_out(W, kc, vc)[order]
     harness.assert_close(out.float().cpu().numpy(), ref, W.kv_dtype)
+
+
+def test_prepare_inputs_negative_and_overflowing_counts():
+    """Negative counts schedule nothing; entries whose tokens do not all fit
+    below total_tokens write nothing while query_start_loc keeps the prefix
+    sum of the clamped counts.  The GPU reports a range error and matches
+    the oracle on every output the oracle defines."""
+    # the hand-checked batch of the oracle's own pin
+    sbt = np.array([[40, 41], [50, 51], [60, 61], [70, 71]], np.int32)
+    snc = np.array([3, 0, 10, 5], np.int32)
+    tok = np.arange(4 * 40, dtype=np.int32).reshape(4, 40) + 1000
+    idx = np.array([2, 0, 1, 3, 1], np.int32)
+    ns = np.array([2, -3, 4, 5, 1], np.int32)
+    gpu = _run(idx, ns, sbt, snc, tok, 8)
+    st, detail = pkv_check()
+    assert st == PKV_ERR_RANGE and detail in (1, 3, 4)
+    ref, err = oracle.load().prepare_inputs(idx, ns, sbt, snc, tok, 8)
+    assert err == 3
+    assert _compare(gpu, ref, ns, idx, 4).sum() == 6
+    # a larger batch spanning several scan chunks: scattered negative counts
+    # and a token buffer that ends inside the batch
+    rng = np.random.default_rng(6)
+    R, MB, ML = 400, 32, 512
+    sbt, snc, tok = _state(rng, R, MB, ML, max_computed=ML - 64)
+    B = 2500
+    idx = rng.integers(0, R, B).astype(np.int32)
+    ns = rng.integers(0, 40, B).astype(np.int32)
+    ns[rng.choice(B, 37, replace=False)] = -rng.integers(1, 100, 37)
+    T = int(np.maximum(ns, 0).sum() * 0.6)
+    gpu = _run(idx, ns, sbt, snc, tok, T)
+    assert pkv_check()[0] == PKV_ERR_RANGE
+    ref, err = oracle.load().prepare_inputs(idx, ns, sbt, snc, tok, T)
+    fits, _, _ = _defined(idx, ns, R, T)
+    assert err == 37 + int((~fits).sum())
+    written = _compare(gpu, ref, ns, idx, R)
+    assert 0 < written.sum() <= T

@@ -86,6 +86,18 @@ MUTANTS = [
      "            seq_lens[b] = c;"),
     ("prepare_start_loc_inclusive", "        query_start_loc[b] = (int32_t)t0;",
      "        query_start_loc[b] = (int32_t)(t0 + n);"),
+    ("prepare_negative_count_kept",
+     "            ++errors;\n            n = 0;\n",
+     "            ++errors;\n"),
+    ("prepare_negative_count_not_reported",
+     "            ++errors;\n            n = 0;\n",
+     "            n = 0;\n"),
+    ("prepare_overflow_offset_not_advanced",
+     "            ++errors;\n            t0 += n;\n            continue;",
+     "            ++errors;\n            continue;"),
+    ("prepare_overflow_not_reported",
+     "            ++errors;\n            t0 += n;\n            continue;",
+     "            t0 += n;\n            continue;"),
 ]
 
 _RUNNER = textwrap.dedent("""
