@@ -326,17 +326,22 @@ int32_t paged_attention_partition_tokens(int32_t batch, int32_t num_heads,
  * callers only.
  *   Arguments are those of paged_attention_decode without the workspace:
  *   the split-KV partials go to a library-owned __device__ array of
- *   PKV_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds
- *   until the process exits.  Calls whose scratch need
- *   (paged_attention_workspace_bytes for the same arguments) exceeds that
- *   size return PKV_ERR_WORKSPACE without launching anything.  The call
- *   allocates nothing.
+ *   PKV_NOALLOC_SCRATCH_BYTES.  Invalid arguments get the answer
+ *   paged_attention_decode would give (PKV_ERR_ARG / PKV_ERR_SHAPE, e.g.
+ *   more than 65535 partitions per sequence); valid calls whose scratch
+ *   need (paged_attention_workspace_bytes for the same arguments) exceeds
+ *   the array return PKV_ERR_WORKSPACE without launching anything.
  *   The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) and caches it: make that first call before any
- *   stream capture.  All calls share the array and it keeps the last
- *   call's contents (nothing in it needs to start at zero); calls whose
- *   kernels overlap on the GPU race on it, so order them on one stream or
- *   with events. */
+ *   stream capture.  That look-up is also when the CUDA driver loads the
+ *   array (lazy module loading, the default) and takes its 16 MiB from the
+ *   device, so a caller that cannot allocate later should make one call at
+ *   set-up, while memory is available; after it, calls allocate nothing and
+ *   the device holds the array until the process exits.  The cached
+ *   address does not survive cudaDeviceReset.  All calls share the array
+ *   and it keeps the last call's contents (nothing in it needs to start at
+ *   zero); calls whose kernels overlap on the GPU race on it, so order them
+ *   on one stream or with events. */
 pkv_status paged_attention_decode_noalloc(const void *q, const pkv_cache *cache,
                                           const int32_t *block_tables,
                                           int32_t max_blocks,
@@ -347,11 +352,13 @@ pkv_status paged_attention_decode_noalloc(const void *q, const pkv_cache *cache,
                                           int32_t partition_tokens,
                                           void *stream);
 
-/* Synchronise `stream`, then read and clear the device error word of the
- * current device.  Returns PKV_OK, PKV_ERR_RANGE or PKV_ERR_TIMEOUT (the
- * first error recorded since the last check), or PKV_ERR_CUDA.  When
- * `detail` is not NULL it receives the offending index (slot, block id or
- * sequence) of that first error, or -1. */
+/* Synchronise `stream`, then read and clear the device error records of
+ * the current device.  Returns PKV_OK, PKV_ERR_RANGE or PKV_ERR_TIMEOUT
+ * (the first error recorded since the last check, by the GPU's global
+ * timer, whichever kernel recorded it), or PKV_ERR_CUDA.  When `detail` is
+ * not NULL it receives the offending index (slot, block id or sequence) of
+ * that first error, or -1.  Every record is cleared, so errors recorded
+ * after the first one are not reported. */
 pkv_status pkv_check(void *stream, int64_t *detail);
 
 /* Static description of a status code. */

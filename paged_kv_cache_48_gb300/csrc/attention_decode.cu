@@ -41,7 +41,7 @@
 
 namespace pkv {
 
-static __device__ unsigned long long g_err_attention = 0ull;
+static __device__ ErrorWord g_err_attention = {0ull, 0ull};
 
 struct DecodeParams {
   const __nv_bfloat16 *q;      // [B, Hq, D]
@@ -969,20 +969,7 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
 
 }  // namespace
 
-unsigned long long read_and_clear_error_attention(cudaStream_t s, cudaError_t *err) {
-  unsigned long long v = 0ull;
-  *err = cudaMemcpyFromSymbolAsync(&v, g_err_attention, sizeof v, 0, cudaMemcpyDeviceToHost, s);
-  if (*err != cudaSuccess) return 0ull;
-  *err = cudaStreamSynchronize(s);
-  if (*err != cudaSuccess) return 0ull;
-  if (v) {
-    const unsigned long long zero = 0ull;
-    *err = cudaMemcpyToSymbolAsync(g_err_attention, &zero, sizeof zero, 0,
-                                   cudaMemcpyHostToDevice, s);
-    if (*err == cudaSuccess) *err = cudaStreamSynchronize(s);
-  }
-  return v;
-}
+const void *error_word_attention() { return &g_err_attention; }
 
 }  // namespace pkv
 

@@ -10,12 +10,18 @@
 // For them this file keeps one fixed scratch area in the library's own
 // device memory and forwards to paged_attention_decode with it.
 //
-// The scratch is a file-scope __device__ array: every GPU that loads the
-// library holds it, PKV_NOALLOC_SCRATCH_BYTES bytes, until the process
-// exits.  Its name is only a host-side stand-in in host code, so the device
-// address is looked up once per device with cudaGetSymbolAddress (with that
-// device current) and cached; the first call on each device does this
-// look-up, so make that first call before capturing any stream.
+// The scratch is a file-scope __device__ array of PKV_NOALLOC_SCRATCH_BYTES.
+// Its name is only a host-side stand-in in host code, so the device address
+// is looked up once per device with cudaGetSymbolAddress (with that device
+// current) and cached; the first call on each device does this look-up, so
+// make that first call before capturing any stream.  That first look-up is
+// also when the CUDA driver loads the module holding the array (with lazy
+// module loading, the default, nothing is loaded earlier) and so when the
+// 16 MiB are taken from the device: a caller that cannot allocate later
+// should make one call at set-up, while memory is still available.  From
+// then on the device holds the array until the process exits, and calls
+// allocate nothing.  The cached address does not survive cudaDeviceReset:
+// do not call this entry point on a device after resetting it.
 //
 // All calls share the one array and it keeps whatever the last call left
 // there.  Nothing in it has to start at zero: a call writes every partial
@@ -60,6 +66,14 @@ extern "C" pkv_status paged_attention_decode_noalloc(
   if (batch < 0 || num_heads <= 0 || max_seq_len < 0 || partition_tokens < 0 ||
       partition_tokens % 16)
     return PKV_ERR_ARG;
+  // Arguments paged_attention_decode rejects as invalid get that answer here
+  // too, before the scratch size is looked at: more than 65535 sequences or
+  // partitions per sequence (grid limits), or an invalid head count.
+  if (num_heads % cache->num_kv_heads) return PKV_ERR_SHAPE;
+  if (batch > 65535) return PKV_ERR_ARG;
+  const int32_t pt = paged_attention_partition_tokens(batch, num_heads, cache->num_kv_heads,
+                                                      max_seq_len, partition_tokens);
+  if (pt <= 0 || ((int64_t)max_seq_len + pt - 1) / pt > 65535) return PKV_ERR_ARG;
   const size_t need = paged_attention_workspace_bytes(
       batch, num_heads, cache->num_kv_heads, cache->head_dim, max_seq_len, partition_tokens);
   if (need > PKV_NOALLOC_SCRATCH_BYTES) return PKV_ERR_WORKSPACE;

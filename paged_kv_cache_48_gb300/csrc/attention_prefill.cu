@@ -49,7 +49,7 @@
 
 namespace pkv {
 
-__device__ unsigned long long g_err_prefill = 0ull;
+__device__ ErrorWord g_err_prefill = {0ull, 0ull};
 
 struct PrefillParams {
   const int32_t *block_tables;     // [batch, max_blocks]
@@ -956,20 +956,7 @@ pkv_status launch_prefix_partials(const void *q, const pkv_cache *cache,
   return dispatch_prefill<true>(cache, mq, mk, mv, p, pairs * parts, s);
 }
 
-unsigned long long read_and_clear_error_prefill(cudaStream_t s, cudaError_t *err) {
-  unsigned long long v = 0ull;
-  *err = cudaMemcpyFromSymbolAsync(&v, g_err_prefill, sizeof v, 0, cudaMemcpyDeviceToHost, s);
-  if (*err != cudaSuccess) return 0ull;
-  *err = cudaStreamSynchronize(s);
-  if (*err != cudaSuccess) return 0ull;
-  if (v) {
-    const unsigned long long zero = 0ull;
-    *err = cudaMemcpyToSymbolAsync(g_err_prefill, &zero, sizeof zero, 0, cudaMemcpyHostToDevice,
-                                   s);
-    if (*err == cudaSuccess) *err = cudaStreamSynchronize(s);
-  }
-  return v;
-}
+const void *error_word_prefill() { return &g_err_prefill; }
 
 }  // namespace pkv
 

@@ -16,7 +16,7 @@
 
 namespace pkv {
 
-static __device__ unsigned long long g_err_prep = 0ull;
+static __device__ ErrorWord g_err_prep = {0ull, 0ull};
 
 struct PrepParams {
   const int32_t *idx_mapping, *num_scheduled;
@@ -134,19 +134,7 @@ static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, c
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-unsigned long long read_and_clear_error_prep(cudaStream_t s, cudaError_t *err) {
-  unsigned long long v = 0ull;
-  *err = cudaMemcpyFromSymbolAsync(&v, g_err_prep, sizeof v, 0, cudaMemcpyDeviceToHost, s);
-  if (*err != cudaSuccess) return 0ull;
-  *err = cudaStreamSynchronize(s);
-  if (*err != cudaSuccess) return 0ull;
-  if (v) {
-    const unsigned long long zero = 0ull;
-    *err = cudaMemcpyToSymbolAsync(g_err_prep, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
-    if (*err == cudaSuccess) *err = cudaStreamSynchronize(s);
-  }
-  return v;
-}
+const void *error_word_prep() { return &g_err_prep; }
 
 }  // namespace pkv
 

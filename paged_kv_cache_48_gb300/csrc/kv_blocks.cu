@@ -21,7 +21,7 @@
 
 namespace pkv {
 
-static __device__ unsigned long long g_err_blocks = 0ull;
+static __device__ ErrorWord g_err_blocks = {0ull, 0ull};
 
 constexpr int kIdsPerLaunch = 2048;
 
@@ -125,19 +125,7 @@ static void *device_view(const void *p) {
   return attr.devicePointer;
 }
 
-unsigned long long read_and_clear_error_blocks(cudaStream_t s, cudaError_t *err) {
-  unsigned long long v = 0ull;
-  *err = cudaMemcpyFromSymbolAsync(&v, g_err_blocks, sizeof v, 0, cudaMemcpyDeviceToHost, s);
-  if (*err != cudaSuccess) return 0ull;
-  *err = cudaStreamSynchronize(s);
-  if (*err != cudaSuccess) return 0ull;
-  if (v) {
-    const unsigned long long zero = 0ull;
-    *err = cudaMemcpyToSymbolAsync(g_err_blocks, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
-    if (*err == cudaSuccess) *err = cudaStreamSynchronize(s);
-  }
-  return v;
-}
+const void *error_word_blocks() { return &g_err_blocks; }
 
 }  // namespace pkv
 

@@ -19,7 +19,7 @@
 
 namespace pkv {
 
-static __device__ unsigned long long g_err_write_zero = 0ull;
+static __device__ ErrorWord g_err_write_zero = {0ull, 0ull};
 
 // Reciprocal bounds for the E4M3 encode: lo and hi bracket 1 / scale
 // tightly enough that x * lo and x * hi (each rounded once) enclose the
@@ -296,22 +296,7 @@ static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block,
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-unsigned long long read_and_clear_error_write_zero(cudaStream_t s,
-                                                   cudaError_t *err) {
-  unsigned long long v = 0ull;
-  *err = cudaMemcpyFromSymbolAsync(&v, g_err_write_zero, sizeof v, 0,
-                                   cudaMemcpyDeviceToHost, s);
-  if (*err != cudaSuccess) return 0ull;
-  *err = cudaStreamSynchronize(s);
-  if (*err != cudaSuccess) return 0ull;
-  if (v) {
-    const unsigned long long zero = 0ull;
-    *err = cudaMemcpyToSymbolAsync(g_err_write_zero, &zero, sizeof zero, 0,
-                                   cudaMemcpyHostToDevice, s);
-    if (*err == cudaSuccess) *err = cudaStreamSynchronize(s);
-  }
-  return v;
-}
+const void *error_word_write_zero() { return &g_err_write_zero; }
 
 }  // namespace pkv
 

@@ -43,17 +43,28 @@ using namespace pkv;
 extern "C" pkv_status pkv_check(void *stream, int64_t *detail) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (detail) *detail = -1;
-  cudaError_t e[5] = {cudaSuccess, cudaSuccess, cudaSuccess, cudaSuccess, cudaSuccess};
-  const unsigned long long words[5] = {
-      read_and_clear_error_write_zero(s, &e[0]), read_and_clear_error_attention(s, &e[1]),
-      read_and_clear_error_blocks(s, &e[2]), read_and_clear_error_prep(s, &e[3]),
-      read_and_clear_error_prefill(s, &e[4])};
-  unsigned long long w = 0ull;
-  for (int i = 0; i < 5; ++i) {
-    if (e[i] != cudaSuccess) return PKV_ERR_CUDA;
-    if (!w) w = words[i];
-  }
-  if (!w) return PKV_OK;
+  constexpr int kUnits = 5;
+  const void *sym[kUnits] = {error_word_write_zero(), error_word_attention(),
+                             error_word_blocks(), error_word_prep(), error_word_prefill()};
+  // one 16-byte record per unit: {code, global-timer stamp}
+  unsigned long long rec[kUnits][2] = {};
+  for (int i = 0; i < kUnits; ++i)
+    if (cudaMemcpyFromSymbolAsync(rec[i], sym[i], sizeof rec[i], 0, cudaMemcpyDeviceToHost, s) !=
+        cudaSuccess)
+      return PKV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+  // the earliest record over all units (ties: the lower unit index) wins
+  int first = -1;
+  for (int i = 0; i < kUnits; ++i)
+    if (rec[i][0] && (first < 0 || rec[i][1] < rec[first][1])) first = i;
+  if (first < 0) return PKV_OK;
+  static const unsigned long long zero[2] = {0ull, 0ull};
+  for (int i = 0; i < kUnits; ++i)
+    if (rec[i][0] && cudaMemcpyToSymbolAsync(sym[i], zero, sizeof zero, 0, cudaMemcpyHostToDevice,
+                                             s) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+  const unsigned long long w = rec[first][0];
   if (detail) *detail = (int64_t)(w & 0x00FFFFFFFFFFFFFFull) - 1;
   return static_cast<pkv_status>(w >> 56);
 }

@@ -17,15 +17,26 @@ namespace pkv {
 
 // ---------------------------------------------------------------------------
 // Device error word.  Each translation unit owns one (no relocatable device
-// code); the first error since the last pkv_check() wins.  Encoding:
-// bits 63..56 = pkv_status, bits 55..0 = offending index + 1 (0 = none).
+// code).  Within a unit the first error since the last pkv_check() wins the
+// compare-and-swap on `code` and stamps `when` with the GPU's global
+// nanosecond timer; pkv_check() reports the earliest stamp over all units.
+// Encoding of `code`: bits 63..56 = pkv_status, bits 55..0 = offending
+// index + 1 (0 = none).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void record_error(unsigned long long *word,
-                                             int status, long long index) {
-  unsigned long long v =
+struct ErrorWord {
+  unsigned long long code;
+  unsigned long long when;
+};
+
+__device__ __forceinline__ void record_error(ErrorWord *word, int status, long long index) {
+  const unsigned long long v =
       ((unsigned long long)(status & 0xFF) << 56) |
       ((unsigned long long)(index + 1) & 0x00FFFFFFFFFFFFFFull);
-  atomicCAS(word, 0ull, v);
+  if (atomicCAS(&word->code, 0ull, v) == 0ull) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    word->when = t;
+  }
 }
 
 // ---------------------------------------------------------------------------

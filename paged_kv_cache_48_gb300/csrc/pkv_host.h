@@ -17,15 +17,15 @@ pkv_status validate_cache(const pkv_cache *cache);
 // SM count of the current device (cached per device); <= 0 on failure.
 int device_sm_count();
 
-// Each translation unit that launches kernels owns a device error word;
-// these read it (after synchronising `s`) and clear it when set.
-unsigned long long read_and_clear_error_write_zero(cudaStream_t s,
-                                                   cudaError_t *err);
-unsigned long long read_and_clear_error_attention(cudaStream_t s,
-                                                  cudaError_t *err);
-unsigned long long read_and_clear_error_blocks(cudaStream_t s, cudaError_t *err);
-unsigned long long read_and_clear_error_prep(cudaStream_t s, cudaError_t *err);
-unsigned long long read_and_clear_error_prefill(cudaStream_t s, cudaError_t *err);
+// Each translation unit that launches kernels owns a device error word
+// (ErrorWord in pkv_device.cuh: a code and the global-timer stamp of the
+// moment it was recorded); these return the host-side handle of each unit's
+// word for cudaMemcpy{From,To}SymbolAsync.
+const void *error_word_write_zero();
+const void *error_word_attention();
+const void *error_word_blocks();
+const void *error_word_prep();
+const void *error_word_prefill();
 
 // Shared-prefix pass of cascade decode (attention_prefill.cu): for every
 // group, the members' queries against the group's prefix on the tensor

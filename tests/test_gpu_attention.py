@@ -12,7 +12,7 @@ import torch
 import harness
 from paged_kv_cache_48_gb300 import (paged_attention_decode,
                                      paged_attention_partition_tokens,
-                                     pkv_check)
+                                     paged_kv_zero_blocks, pkv_check)
 from paged_kv_cache_48_gb300 import workload as wl
 
 pytestmark = pytest.mark.gpu
@@ -185,3 +185,31 @@ def test_auto_partition_choice_is_reported():
     assert auto > 0 and auto % 256 == 0
     assert paged_attention_partition_tokens(8, 64, 8, 131072, 512) == 512
     assert paged_attention_partition_tokens(8, 64, 8, 131072, 17) == -1
+
+
+@pytest.mark.parametrize("decode_first", [True, False])
+def test_check_reports_the_earliest_error_across_kernels(decode_first):
+    """Two range errors recorded by different kernels (decode attention and
+    block zeroing) in a known stream order: pkv_check reports the earlier
+    one, then everything is cleared."""
+    W, _ = _case("tiny")
+    G = harness.upload(W)
+    tables = G.tables.clone()
+    tables[3, 1] = W.num_blocks + 100                    # decode: detail 3
+    bad_ids = np.array([1, 2, 4, 5, W.num_blocks + 7], np.int32)   # zeroing: detail 4
+
+    def decode():
+        paged_attention_decode(G.q, G.cache, tables, G.seq_lens, W.scale,
+                               max_seq_len=W.max_seq_len)
+
+    def zero():
+        paged_kv_zero_blocks(G.cache, bad_ids)
+
+    first, second = (decode, zero) if decode_first else (zero, decode)
+    first()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(20000)   # a gap of GPU time between the two records
+    second()
+    st, detail = pkv_check()
+    assert st == PKV_ERR_RANGE and detail == (3 if decode_first else 4)
+    assert pkv_check()[0] == PKV_OK

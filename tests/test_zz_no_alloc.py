@@ -20,7 +20,7 @@ from paged_kv_cache_48_gb300 import workload as wl
 from paged_kv_cache_48_gb300.ops import paged_attention_workspace_bytes
 
 pytestmark = pytest.mark.gpu
-PKV_OK, PKV_ERR_WORKSPACE = 0, 7
+PKV_OK, PKV_ERR_ARG, PKV_ERR_WORKSPACE = 0, 1, 7
 
 
 def _call_existing(W, G, pt):
@@ -70,21 +70,46 @@ def test_noalloc_matches_workspace_entry_point_twice(make, pt):
     assert harness.pkv_check()[0] == PKV_OK
 
 
+def _call_noalloc_sized(W, G, out, max_seq_len, pt):
+    return _native.lib().paged_attention_decode_noalloc(
+        G.q.data_ptr(), ctypes.byref(G.cache.c_struct()), G.tables.data_ptr(),
+        G.tables.shape[1], G.seq_lens.data_ptr(), W.batch, W.num_heads,
+        W.scale, out.data_ptr(), max_seq_len, pt,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+
+
 def test_noalloc_rejects_needs_beyond_its_scratch():
     W = wl.tiny_mha()
     G = harness.upload(W)
-    # 4 sequences x 8 heads x 2^20 partitions would need far more than the
-    # fixed scratch: rejected on the host, nothing launched.
     out = torch.empty_like(G.q)
-    big = 16 * (1 << 20)
-    need = paged_attention_workspace_bytes(W.batch, W.num_heads,
-                                           W.num_kv_heads, W.head_dim, big, 16)
-    assert need > _native.PKV_NOALLOC_SCRATCH_BYTES
     assert _call_noalloc(W, G, 16, out) == PKV_OK  # small need: fine
-    st = _native.lib().paged_attention_decode_noalloc(
-        G.q.data_ptr(), ctypes.byref(G.cache.c_struct()), G.tables.data_ptr(),
-        G.tables.shape[1], G.seq_lens.data_ptr(), W.batch, W.num_heads,
-        W.scale, out.data_ptr(), big, 16,
-        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
-    assert st == PKV_ERR_WORKSPACE
+    # 65535 partitions of 16 tokens: a valid grid whose partials (4 x 8 x
+    # 65535 rows) need far more than the fixed scratch; rejected on the
+    # host, nothing launched.
+    most = 16 * 65535
+    need = paged_attention_workspace_bytes(W.batch, W.num_heads,
+                                           W.num_kv_heads, W.head_dim, most, 16)
+    assert need > _native.PKV_NOALLOC_SCRATCH_BYTES
+    assert _call_noalloc_sized(W, G, out, most, 16) == PKV_ERR_WORKSPACE
+    # one partition more is an invalid grid: the answer
+    # paged_attention_decode gives, whatever the scratch size
+    assert _call_noalloc_sized(W, G, out, most + 16, 16) == PKV_ERR_ARG
     torch.cuda.synchronize()
+
+
+def test_noalloc_takes_no_device_memory_after_its_first_call():
+    """The first call on a device may load the scratch array (and take its
+    16 MiB then); every later call leaves the device's free memory as it
+    was."""
+    W = wl.llama8b_gqa(small=True)
+    G = harness.upload(W)
+    out = torch.empty_like(G.q)
+    assert _call_noalloc(W, G, 64, out) == PKV_OK   # set-up call
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        assert _call_noalloc(W, G, 64, out) == PKV_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert harness.pkv_check()[0] == PKV_OK
