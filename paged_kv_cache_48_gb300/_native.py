@@ -12,6 +12,7 @@ from pathlib import Path
 PKG = Path(__file__).resolve().parent
 LIBRARY = PKG / "libpagedkv.so"
 HEADER = PKG.parent / "include" / "pagedkv.h"
+HEADERS = sorted((PKG.parent / "include").glob("*.h"))
 
 PKV_OK = 0
 STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_ARG", 2: "PKV_ERR_DTYPE",
@@ -86,6 +87,7 @@ _SIGNATURES = {
     "pkv_check": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_int64)]),
     "pkv_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_version": (ctypes.c_int32, []),
+    "pkv_testing_fail_decode_sequence": (None, [ctypes.c_int32]),
 }
 
 _LIB = None
@@ -105,8 +107,8 @@ class PagedKVError(RuntimeError):
 
 
 def declared_functions() -> list:
-    """Names of the functions include/pagedkv.h declares."""
-    text = HEADER.read_text()
+    """Names of the functions the headers under include/ declare."""
+    text = "\n".join(h.read_text() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
     keywords = {"if", "sizeof", "defined"}

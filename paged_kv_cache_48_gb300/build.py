@@ -48,7 +48,7 @@ def build(verbose: bool = False, force: bool = False,
     BUILD.mkdir(exist_ok=True)
     nvcc = _nvcc()
     header_deps = [CSRC / h for h in HEADERS] + \
-        [PKG.parent / "include" / "pagedkv.h"]
+        sorted((PKG.parent / "include").glob("*.h"))
 
     def compile_one(src: str) -> Path:
         obj = BUILD / (Path(src).stem + ".o")

@@ -33,11 +33,13 @@
 
 #include <algorithm>
 #include <cmath>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
 #include "pkv_device.cuh"
 #include "pkv_host.h"
+#include "../../include/pagedkv_testing.h"
 
 namespace pkv {
 
@@ -57,7 +59,18 @@ struct DecodeParams {
   float scale_log2;  // scale * log2(e) (* k_scale for fp8)
   float v_scale;     // 1 for bf16
   unsigned long long timeout_ns;
-  int32_t grid_parts;  // partition CTAs per (kv head group, sequence)
+  int32_t grid_parts;  // partitions per (kv head group, sequence)
+  // 0: the CTA's warps share one partition (blocks dealt round-robin) and
+  // merge through shared memory.  1: each warp owns one partition (warp w
+  // of grid row y takes partition 4y + w, its blocks in order) and writes
+  // its own partial, with no cross-warp step: short partitions then cost
+  // no CTA-wide merge and a CTA still streams four partitions' worth.
+  int32_t warp_parts;
+  // Test hook (-1 = off): every warp working on this sequence stops after
+  // its first block as if the wait for the next one had timed out.  No wait
+  // is shortened; the copies already issued are drained as on a real
+  // timeout.  Set only through pkv_testing_fail_decode_sequence().
+  int32_t test_fail_seq;
   // Shared-prefix (cascade) decode, when group_start != nullptr: group G is
   // sequences group_start[G] .. group_start[G+1] - 1 sharing the first
   // prefix_len[G] tokens.  A member that passes the checks of
@@ -158,8 +171,8 @@ struct Cfg {
   static constexpr int MT = D / 16;                    // 16-row tiles of head_dim
   static constexpr int OS_STRIDE = D + 4;              // padded row of o_s
   static constexpr int SMEM_BYTES = NW * STAGES * STAGE_BYTES + 1024;
-  static_assert(8 * OS_STRIDE * 4 <= STAGES * STAGE_BYTES,
-                "combine scratch must fit in a warp's ring");
+  static_assert(8 * OS_STRIDE * 4 + 8 * 8 <= STAGES * STAGE_BYTES,
+                "combine scratch (outputs, then max/sum pairs) must fit in a warp's ring");
 };
 
 __device__ __forceinline__ int clamp_len(int L, int cap) {
@@ -522,8 +535,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int c = lane & 3;
   const int kvh = blockIdx.x / p.q_groups;
   const int qg = blockIdx.x - kvh * p.q_groups;
-  const int part = blockIdx.y;
+  const bool wmode = p.warp_parts != 0;  // uniform over the grid
+  const int part = wmode ? blockIdx.y * C::NW + warp : blockIdx.y;
   const int b = blockIdx.z;
+  // this warp's blocks of the partition: j0 + i * jstep
+  const int j_off = wmode ? 0 : warp, jstep = wmode ? 1 : C::NW;
 
   const uint32_t base_u32 = smem_u32(smem_dyn);
   uint8_t *rings = smem_dyn + (((base_u32 + 1023u) & ~1023u) - base_u32);
@@ -549,7 +565,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const bool ids_early = !p.group_start;
   int ids_pre = -1;
   if (ids_early) {
-    const long long j = (long long)part * (p.part_tokens >> 4) + warp + (long long)lane * C::NW;
+    const long long j = (long long)part * (p.part_tokens >> 4) + j_off + (long long)lane * jstep;
     if (j < p.max_blocks) ids_pre = __ldg(p.block_tables + (size_t)b * p.max_blocks + j);
   }
 
@@ -569,20 +585,20 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   if (p.seq_start && blockIdx.x == 0 && part == 0 && threadIdx.x == 0) p.seq_start[b] = start;
   const int Ls = L - start;
   const int nparts = Ls <= p.part_tokens ? 1 : (Ls + p.part_tokens - 1) / p.part_tokens;
-  if (part >= nparts) return;
+  if (part >= nparts) return;  // the whole CTA, or (warp-owned) this warp
   const int tok0 = start + part * p.part_tokens;  // multiple of 16
   const int tok1 = min(L, tok0 + p.part_tokens);
   const int blk0 = tok0 >> 4;
   const int nblk = (tok1 - tok0 + 15) >> 4;
-  const int my_n = nblk > warp ? (nblk - warp + C::NW - 1) / C::NW : 0;
+  const int my_n = wmode ? nblk : (nblk > warp ? (nblk - warp + C::NW - 1) / C::NW : 0);
 
   // ---- block ids of this warp, 32 at a time in registers -----------------
-  const int32_t *table = p.block_tables + (size_t)b * p.max_blocks + blk0 + warp;
+  const int32_t *table = p.block_tables + (size_t)b * p.max_blocks + blk0 + j_off;
   int ids_reg = -1;
   const uint64_t policy = l2_policy_evict_normal();
   auto issue = [&](int i) {
     if ((i & 31) == 0)
-      ids_reg = (i + lane < my_n) ? (i == 0 && ids_early ? ids_pre : __ldg(table + (i + lane) * C::NW))
+      ids_reg = (i + lane < my_n) ? (i == 0 && ids_early ? ids_pre : __ldg(table + (i + lane) * jstep))
                                   : -1;
     int phys = __shfl_sync(0xffffffffu, ids_reg, i & 31);
     if (lane == 0) {
@@ -607,16 +623,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   bool failed = false;
   int i = 0;
+  const int stop_at = b == p.test_fail_seq ? min(my_n, 1) : my_n;  // test hook
   if constexpr (FP8 && C::STAGES >= 4) {
     // two blocks per step while two more are in flight
-    for (; i + 1 < my_n; i += 2) {
+    for (; i + 1 < stop_at; i += 2) {
       const int sa = i % C::STAGES, sb = (i + 1) % C::STAGES;
       if (!mbar_wait_bounded(&bars[warp][sa], (i / C::STAGES) & 1, p.timeout_ns) ||
           !mbar_wait_bounded(&bars[warp][sb], ((i + 1) / C::STAGES) & 1, p.timeout_ns)) {
         failed = true;
         break;
       }
-      const int ja = blk0 + warp + i * C::NW, jb = ja + C::NW;
+      const int ja = blk0 + j_off + i * jstep, jb = ja + jstep;
       const int nva = stage_ok[warp][sa] ? min(16, tok1 - ja * 16) : 0;
       const int nvb = stage_ok[warp][sb] ? min(16, tok1 - jb * 16) : 0;
       attend_pair<D>(smem_u32(ring + sa * C::STAGE_BYTES), nva,
@@ -626,19 +643,20 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
       if (issued < my_n) issue(issued++);
     }
   }
-  for (; !failed && i < my_n; ++i) {
+  for (; !failed && i < stop_at; ++i) {
     const int stage = i % C::STAGES;
     if (!mbar_wait_bounded(&bars[warp][stage], (i / C::STAGES) & 1, p.timeout_ns)) {
       failed = true;
       break;
     }
-    const int j = blk0 + warp + i * C::NW;
+    const int j = blk0 + j_off + i * jstep;
     const int nv = stage_ok[warp][stage] ? min(16, tok1 - j * 16) : 0;
     const uint32_t sk = smem_u32(ring + stage * C::STAGE_BYTES);
     attend_block<FP8, D>(sk, sk + C::TILE_BYTES, nv, qf, p.scale_log2, st, lane);
     __syncwarp();
     if (issued < my_n) issue(issued++);
   }
+  if (i < my_n) failed = true;  // only under the test hook, or after a timeout
 
   if (failed) {
     if (lane == 0) record_error(&g_err_attention, PKV_ERR_TIMEOUT, b);
@@ -649,9 +667,47 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     st.m0 = st.m1 = -INFINITY;
   }
 
-  // ---- merge the warps' states -------------------------------------------
+  // ---- warp-owned partition: this warp's result, staged through its ring --
   st.reduce_l();
   float *o_s = reinterpret_cast<float *>(ring);  // this warp's ring, now idle
+  if (wmode) {
+    float2 *ml_w = reinterpret_cast<float2 *>(o_s + 8 * C::OS_STRIDE);
+    if (!failed) {
+#pragma unroll
+      for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+        for (int hi = 0; hi < 2; ++hi) {
+          const int d = o_row<FP8>(mt, hi, g);
+          o_s[(2 * c) * C::OS_STRIDE + d] = st.o[mt][2 * hi];
+          o_s[(2 * c + 1) * C::OS_STRIDE + d] = st.o[mt][2 * hi + 1];
+        }
+      }
+    }
+    if (g == 0) {
+      ml_w[2 * c] = make_float2(st.m0, st.l0);
+      ml_w[2 * c + 1] = make_float2(st.m1, st.l1);
+    }
+    __syncwarp();
+    const bool direct = nparts == 1 && slot_base == 0;
+    for (int idx = lane; idx < heads_here * D; idx += 32) {
+      const int h = idx / D;
+      const int d = idx - h * D;
+      const float2 ml = ml_w[h];
+      const bool live = !failed && ml.x != -INFINITY && ml.y > 0.f;
+      const float res = live ? o_s[h * C::OS_STRIDE + d] / ml.y * p.v_scale : 0.f;
+      const size_t r = row0 + h;
+      if (direct) {
+        p.out[r * D + d] = __float2bfloat16_rn(res);
+      } else {
+        const size_t slot = r * p.max_parts + slot_base + part;
+        p.part_o[slot * D + d] = res;
+        if (d == 0) p.part_ml[slot] = live ? ml : make_float2(-INFINITY, 0.f);
+      }
+    }
+    return;
+  }
+
+  // ---- merge the warps' states -------------------------------------------
   if (!failed && my_n > 0) {
 #pragma unroll
     for (int mt = 0; mt < C::MT; ++mt) {
@@ -799,6 +855,107 @@ __global__ void __launch_bounds__(256) paged_decode_merge_kernel(const DecodePar
   for (int k = 0; k < KD; ++k) orow[32 * k] = __float2bfloat16_rn(acc[k] * inv);
 }
 
+// The same merge for sequences split into many partitions: one CTA of 8
+// warps per (sequence, query head) row.  The row's maximum M comes from a
+// block-wide reduction over its (m, l) pairs; the weights 2^(m_j - M) l_j go
+// to shared memory (kMergeChunk at a time); partition j is accumulated by
+// slot j mod 8*PPW (a warp covers PPW partitions per step, each lane four
+// consecutive head_dim elements with one 16-byte load), and the slots are
+// summed in a fixed order at the end, so the result is deterministic.
+constexpr int kMergeWideThreads = 256;
+constexpr int kMergeChunk = 2048;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeWideThreads)
+paged_decode_merge_wide_kernel(const DecodeParams p) {
+  constexpr int NWM = kMergeWideThreads / 32;
+  constexpr int LPP = D / 4;      // lanes per partition (float4 each)
+  constexpr int PPW = 32 / LPP;   // partitions per warp step
+  constexpr int SLOTS = NWM * PPW;
+  __shared__ float w_s[kMergeChunk];
+  __shared__ float red_s[NWM];
+  __shared__ float4 acc_s[SLOTS][LPP];
+  grid_dependency_wait();
+  allow_dependent_launch();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long row = blockIdx.x;
+  const int b = (int)(row / p.num_heads);
+  const int cap = min(p.max_blocks * 16, p.max_seq_len);
+  const int L = clamp_len(__ldg(p.seq_lens + b), cap);
+  int start = p.seq_start ? __ldg(p.seq_start + b) : 0;  // decided by the decode kernel
+  if (start < 0 || start > L || (start & 15)) start = 0;
+  const int slot_base = prefix_slots(p, start);
+  const int Ls = L - start;
+  const int nparts =
+      slot_base + (Ls <= p.part_tokens ? 1 : (Ls + p.part_tokens - 1) / p.part_tokens);
+  if (nparts <= 1) return;  // the decode kernel wrote this row (uniform over the CTA)
+  const float2 *ml = p.part_ml + (size_t)row * p.max_parts;
+  // 1. the row maximum
+  float M = -INFINITY;
+  for (int j = tid; j < nparts; j += kMergeWideThreads) M = fmaxf(M, ml[j].x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) red_s[warp] = M;
+  __syncthreads();
+  M = red_s[0];
+#pragma unroll
+  for (int w = 1; w < NWM; ++w) M = fmaxf(M, red_s[w]);
+  // 2. weights and the weighted sum of outputs, a chunk of partitions at a time
+  const int sub = lane / LPP, l4 = lane - sub * LPP;
+  const int slot = warp * PPW + sub;
+  float wsum = 0.f;  // this thread's weights, in j order
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < nparts; c0 += kMergeChunk) {
+    const int cnt = min(kMergeChunk, nparts - c0);
+    __syncthreads();  // the previous chunk's weights are consumed (and red_s read)
+    for (int j = tid; j < cnt; j += kMergeWideThreads) {
+      const float2 v = ml[c0 + j];
+      const float w = v.x == -INFINITY ? 0.f : exp2f(v.x - M) * v.y;
+      w_s[j] = w;
+      wsum += w;
+    }
+    __syncthreads();
+    const float4 *po =
+        reinterpret_cast<const float4 *>(p.part_o + ((size_t)row * p.max_parts + c0) * D) + l4;
+#pragma unroll 4
+    for (int j = slot; j < cnt; j += SLOTS) {
+      const float w = w_s[j];
+      const float4 o = po[(size_t)j * LPP];
+      acc.x += w * o.x;
+      acc.y += w * o.y;
+      acc.z += w * o.z;
+      acc.w += w * o.w;
+    }
+  }
+  acc_s[slot][l4] = acc;
+  // 3. the total weight: fixed-order warp and block sums
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+  __syncthreads();  // acc_s written; everyone is past the reads of red_s
+  if (lane == 0) red_s[warp] = wsum;
+  __syncthreads();
+  if (tid < LPP) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWM; ++w) t += red_s[w];
+    float4 a = acc_s[0][tid];
+#pragma unroll
+    for (int k = 1; k < SLOTS; ++k) {
+      const float4 v = acc_s[k][tid];
+      a.x += v.x;
+      a.y += v.y;
+      a.z += v.z;
+      a.w += v.w;
+    }
+    const float inv = t > 0.f ? 1.f / t : 0.f;
+    __nv_bfloat16 *orow = p.out + (size_t)row * D + 4 * tid;  // out is only 2-byte aligned
+    orow[0] = __float2bfloat16_rn(a.x * inv);
+    orow[1] = __float2bfloat16_rn(a.y * inv);
+    orow[2] = __float2bfloat16_rn(a.z * inv);
+    orow[3] = __float2bfloat16_rn(a.w * inv);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -886,6 +1043,16 @@ bool get_maps(const pkv_cache *c, CUtensorMap *k, CUtensorMap *v) {
 
 constexpr int kCtasPerSm = 3;  // 64 KiB rings
 
+// Sequence index for DecodeParams::test_fail_seq (-1 = off).
+std::atomic<int32_t> g_test_fail_seq{-1};
+
+// Rows of sequences split into more partitions than this are merged by one
+// CTA each (paged_decode_merge_wide_kernel), fewer by one warp each.
+constexpr int kMergeWarpMaxParts = 8;
+
+// Partitions this short are owned by single warps (DecodeParams::warp_parts).
+constexpr int kWarpPartMaxTokens = 512;
+
 // Automatic partition length: the longest of 256 * 2^k tokens that still
 // gives about three waves of CTAs for the worst case (every sequence at
 // max_seq_len); no split at all when the sequences alone fill them.
@@ -953,16 +1120,21 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
       configured[dev] = 1;
     }
   }
-  dim3 grid(p.num_kv_heads * p.q_groups, p.grid_parts, p.batch);
+  const int grid_y = p.warp_parts ? (p.grid_parts + C::NW - 1) / C::NW : p.grid_parts;
+  dim3 grid(p.num_kv_heads * p.q_groups, grid_y, p.batch);
   if (launch_pdl(paged_decode_kernel<FP8, D>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s, mk, mv,
                  p) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (join && cudaStreamWaitEvent(s, join, 0) != cudaSuccess) return PKV_ERR_CUDA;
   if (p.max_parts > 1) {
     const long long rows = (long long)p.batch * p.num_heads;
-    if (launch_pdl(paged_decode_merge_kernel<D>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0,
-                   s, p) != cudaSuccess)
-      return PKV_ERR_CUDA;
+    const cudaError_t e =
+        p.max_parts > kMergeWarpMaxParts
+            ? launch_pdl(paged_decode_merge_wide_kernel<D>, dim3((unsigned)rows),
+                         dim3(kMergeWideThreads), 0, s, p)
+            : launch_pdl(paged_decode_merge_kernel<D>, dim3((unsigned)((rows + 7) / 8)),
+                         dim3(256), 0, s, p);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }
@@ -974,6 +1146,10 @@ const void *error_word_attention() { return &g_err_attention; }
 }  // namespace pkv
 
 using namespace pkv;
+
+extern "C" void pkv_testing_fail_decode_sequence(int32_t sequence) {
+  g_test_fail_seq.store(sequence < 0 ? -1 : sequence, std::memory_order_relaxed);
+}
 
 extern "C" int32_t paged_attention_partition_tokens(int32_t batch, int32_t num_heads,
                                                     int32_t num_kv_heads, int32_t max_seq_len,
@@ -1031,6 +1207,8 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
   p.max_parts = (int)parts64;
   p.grid_parts = (int)parts64;
   p.part_tokens = pt;
+  p.warp_parts = parts64 > 1 && pt <= kWarpPartMaxTokens;
+  p.test_fail_seq = g_test_fail_seq.load(std::memory_order_relaxed);
   const size_t need = paged_attention_workspace_bytes(batch, num_heads, cache->num_kv_heads,
                                                       cache->head_dim, max_seq_len,
                                                       partition_tokens);
@@ -1098,7 +1276,11 @@ int cascade_prefix_part_tokens(int32_t num_groups, int32_t num_heads, int32_t nu
 }
 
 // A non-blocking side stream per device with its fork / join events; the
-// mutex keeps one call's fork-join sequence together.
+// mutex keeps one call's fork-join sequence together.  Every cascade call
+// on a device shares them: calls from different streams are serialised
+// behind each other's prefix pass, and while one thread captures a cascade
+// call into a CUDA graph the side stream belongs to that capture, so no
+// other cascade call may run on the device until the capture ends.
 struct SideStream {
   cudaStream_t stream = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
@@ -1218,21 +1400,29 @@ extern "C" pkv_status paged_attention_decode_cascade(
   const bool fork = num_groups > 0 && max_prefix_len > 0;
   const int part_tokens = cascade_prefix_part_tokens(num_groups, num_heads, cache->num_kv_heads,
                                                      max_group_size, max_prefix_len);
+  // After the fork, every return joins the side stream back into `s`, so
+  // that a capture of `s` never ends with the side stream still forked.
+  auto join_back = [&](pkv_status ret) {
+    if (cudaEventRecord(side.join, side.stream) != cudaSuccess ||
+        cudaStreamWaitEvent(s, side.join, 0) != cudaSuccess)
+      return ret == PKV_OK ? PKV_ERR_CUDA : ret;
+    return ret;
+  };
   if (fork) {
-    if (cudaEventRecord(side.fork, s) != cudaSuccess ||
-        cudaStreamWaitEvent(side.stream, side.fork, 0) != cudaSuccess)
-      return PKV_ERR_CUDA;
+    if (cudaEventRecord(side.fork, s) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaStreamWaitEvent(side.stream, side.fork, 0) != cudaSuccess)
+      return join_back(PKV_ERR_CUDA);
     st = launch_prefix_partials(q, cache, block_tables, max_blocks, seq_lens, group_start,
                                 prefix_len, num_groups, max_group_size, max_prefix_len, batch,
                                 num_heads, scale, part_o, part_ml, l.stride, part_tokens,
                                 side.stream);
-    if (st != PKV_OK) return st;
-    if (cudaEventRecord(side.join, side.stream) != cudaSuccess) return PKV_ERR_CUDA;
+    if (st != PKV_OK) return join_back(st);
+    if (cudaEventRecord(side.join, side.stream) != cudaSuccess) return join_back(PKV_ERR_CUDA);
   }
   // 2. each sequence's own tokens (and its start), then, after the join, the
   //    log-sum-exp merge of all slots
   CUtensorMap mk, mv;
-  if (!get_maps(cache, &mk, &mv)) return PKV_ERR_CUDA;
+  if (!get_maps(cache, &mk, &mv)) return fork ? join_back(PKV_ERR_CUDA) : PKV_ERR_CUDA;
   DecodeParams p;
   std::memset(&p, 0, sizeof p);
   p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -1252,6 +1442,8 @@ extern "C" pkv_status paged_attention_decode_cascade(
   p.max_parts = l.stride;
   p.grid_parts = l.suffix_parts;
   p.part_tokens = l.pt;
+  p.warp_parts = l.pt <= kWarpPartMaxTokens;
+  p.test_fail_seq = g_test_fail_seq.load(std::memory_order_relaxed);
   p.scale_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
   p.v_scale = fp8 ? cache->v_scale : 1.f;
   p.timeout_ns = 2000000000ull;
@@ -1263,9 +1455,14 @@ extern "C" pkv_status paged_attention_decode_cascade(
   p.prefix_part_tokens = part_tokens;
   p.seq_start = seq_start;
   cudaEvent_t join = fork ? side.join : nullptr;
-  if (fp8)
-    return cache->head_dim == 128 ? launch_decode<true, 128>(mk, mv, p, s, join)
-                                  : launch_decode<true, 64>(mk, mv, p, s, join);
-  return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, s, join)
-                                : launch_decode<false, 64>(mk, mv, p, s, join);
+  const pkv_status ret =
+      fp8 ? (cache->head_dim == 128 ? launch_decode<true, 128>(mk, mv, p, s, join)
+                                    : launch_decode<true, 64>(mk, mv, p, s, join))
+          : (cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, s, join)
+                                    : launch_decode<false, 64>(mk, mv, p, s, join));
+  // launch_decode makes `s` wait for the join before the merge; if it failed
+  // before that point, wait here (the join event already marks the prefix
+  // pass's end)
+  if (ret != PKV_OK && fork) (void)cudaStreamWaitEvent(s, side.join, 0);
+  return ret;
 }
