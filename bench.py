@@ -528,7 +528,8 @@ def run_ours(args):
         ev_back = [torch.cuda.Event() for _ in range(2)]
         h2d = sum(h.numel() * h.element_size() for h in h_in) + fresh.nbytes
         d2h = h_out[0].numel() * h_out[0].element_size()
-        K2 = max(2, K // 2)
+        K2 = max(10, K // 2)   # timed end-to-end steps
+        E2E_WARM = 4           # untimed: both buffer sets used twice
 
         def e2e_step(i):
             b = i % 2
@@ -551,12 +552,15 @@ def run_ours(args):
                 h_out[b].copy_(sets[b][6], non_blocking=True)
                 ev_back[b].record(down)
 
+        for i in range(E2E_WARM):
+            e2e_step(i)
+        stream.wait_stream(down)
         barrier()
         torch.cuda.synchronize()
         e_a = torch.cuda.Event(enable_timing=True)
         e_b = torch.cuda.Event(enable_timing=True)
         e_a.record(stream)
-        for i in range(K2):
+        for i in range(E2E_WARM, E2E_WARM + K2):
             e2e_step(i)
         stream.wait_stream(down)               # the last read-back is inside
         e_b.record(stream)
@@ -616,6 +620,8 @@ def run_ours(args):
                      "timed_in": "a second K-step loop, one event pair around "
                                  "each decode call and its merge"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms / K2, 5), "steps": K2,
+                "untimed_steps_before": E2E_WARM,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * K,
         "clocks": clocks.summary(),

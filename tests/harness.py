@@ -70,9 +70,11 @@ def upload(W: Workload, device="cuda", write_history=True) -> GpuState:
 
 
 def gpu_step(W: Workload, G: GpuState, partition_tokens=0, skip_zero=False,
-             out=None, fused=False):
+             out=None, fused=False, max_seq_len=None):
     """One decode step: zero fresh blocks, write the step's tokens, attend.
-    fused: the zeroing and the write as one paged_kv_zero_and_write call."""
+    fused: the zeroing and the write as one paged_kv_zero_and_write call.
+    max_seq_len: the host bound given to attention (default: the longest
+    sequence; bench.py gives the table width, max_blocks * 16)."""
     if fused and not skip_zero:
         paged_kv_zero_and_write(G.step_k, G.step_v, G.step_slots, G.cache, G.fresh)
     else:
@@ -81,14 +83,16 @@ def gpu_step(W: Workload, G: GpuState, partition_tokens=0, skip_zero=False,
         if G.step_slots.numel():
             paged_kv_write(G.step_k, G.step_v, G.step_slots, G.cache)
     return paged_attention_decode(G.q, G.cache, G.tables, G.seq_lens, W.scale,
-                                  max_seq_len=W.max_seq_len, out=out,
+                                  max_seq_len=W.max_seq_len if max_seq_len is None
+                                  else max_seq_len, out=out,
                                   partition_tokens=partition_tokens)
 
 
 def run_gpu(W: Workload, partition_tokens=0, skip_zero=False, device="cuda",
-            want_cache=True, fused=False):
+            want_cache=True, fused=False, max_seq_len=None):
     G = upload(W, device)
-    out = gpu_step(W, G, partition_tokens, skip_zero, fused=fused)
+    out = gpu_step(W, G, partition_tokens, skip_zero, fused=fused,
+                   max_seq_len=max_seq_len)
     status, detail = pkv_check()
     res = {"out": out.float().cpu().numpy(), "status": status,
            "detail": detail, "state": G}

@@ -16,7 +16,7 @@ from paged_kv_cache_48_gb300 import (paged_attention_decode,
 from paged_kv_cache_48_gb300 import workload as wl
 
 pytestmark = pytest.mark.gpu
-PKV_OK, PKV_ERR_RANGE = 0, 5
+PKV_OK, PKV_ERR_RANGE, PKV_ERR_TIMEOUT = 0, 5, 6
 
 SMALL = {
     "tiny": wl.tiny_mha,
@@ -213,3 +213,30 @@ def test_check_reports_the_earliest_error_across_kernels(decode_first):
     st, detail = pkv_check()
     assert st == PKV_ERR_RANGE and detail == (3 if decode_first else 4)
     assert pkv_check()[0] == PKV_OK
+
+
+@pytest.mark.parametrize("name,partition_tokens", [
+    ("llama_small", 0), ("llama_small", 64), ("fp8_small", 0), ("fp8_small", 32)])
+def test_timeout_path_reports_and_spares_other_sequences(name, partition_tokens):
+    """The bounded-wait failure path, reached through the test hook (every
+    warp on one sequence gives up after its first block as if its wait had
+    run out; no wait is shortened): pkv_check reports PKV_ERR_TIMEOUT with
+    that sequence, its row stays finite, every other sequence still matches
+    the oracle, and with the hook off the next call is clean again."""
+    from paged_kv_cache_48_gb300 import _native
+    W, ref = _case(name)
+    victim = int(np.argmax(W.seq_lens))          # long enough to have a second block
+    assert W.seq_lens[victim] > 16 * 8
+    _native.lib().pkv_testing_fail_decode_sequence(victim)
+    try:
+        res = harness.run_gpu(W, partition_tokens=partition_tokens, want_cache=False)
+    finally:
+        _native.lib().pkv_testing_fail_decode_sequence(-1)
+    assert res["status"] == PKV_ERR_TIMEOUT and res["detail"] == victim
+    assert np.all(np.isfinite(res["out"]))
+    others = np.ones(W.batch, bool)
+    others[victim] = False
+    harness.assert_close(res["out"][others], ref[others], W.kv_dtype)
+    again = harness.run_gpu(W, partition_tokens=partition_tokens, want_cache=False)
+    assert again["status"] == PKV_OK
+    harness.assert_close(again["out"], ref, W.kv_dtype)

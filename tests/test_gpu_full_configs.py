@@ -1,8 +1,12 @@
-"""The five workloads at full size, in the launch configuration bench.py
-times (automatic partitioning) and, for the long-context workload, with the
-512-token partitions it specifies.
+"""The five workloads at full size, each in exactly the step bench.py times:
+the zeroing of fresh blocks and the write of the step's tokens in one
+paged_kv_zero_and_write launch, then decode attention with the table width
+(max_blocks * 16) as the host bound and automatic partitioning; the
+long-context workload also with the 512-token partitions it specifies.  One
+more case runs the fp8 workload with the zeroing and the write as separate
+calls and the longest sequence as the bound.
 
-Per workload:
+Per case:
  - both caches after zeroing and writing equal the oracle's byte for byte;
  - sampled output rows (every query head of two sequences, four heads of
    every other sequence) match the fp64 oracle within the tolerance;
@@ -18,13 +22,15 @@ from paged_kv_cache_48_gb300 import workload as wl
 
 pytestmark = pytest.mark.gpu
 
+# (id, workload, partition_tokens, fused zeroing + write, host bound)
 CASES = [
-    ("llama8b_gqa", wl.llama8b_gqa, 0),
-    ("prefix_shared", wl.prefix_shared, 0),
-    ("long_context", wl.long_context, 0),
-    ("long_context_p512", wl.long_context, 512),
-    ("fp8_recycle", wl.fp8_recycle, 0),
-    ("tiny_mha", wl.tiny_mha, 0),
+    ("llama8b_gqa", wl.llama8b_gqa, 0, True, "table"),
+    ("prefix_shared", wl.prefix_shared, 0, True, "table"),
+    ("long_context", wl.long_context, 0, True, "table"),
+    ("long_context_p512", wl.long_context, 512, True, "table"),
+    ("fp8_recycle", wl.fp8_recycle, 0, True, "table"),
+    ("fp8_recycle_separate_calls", wl.fp8_recycle, 0, False, "longest"),
+    ("tiny_mha", wl.tiny_mha, 0, True, "table"),
 ]
 
 
@@ -39,10 +45,13 @@ def _pairs(W, rng):
     return np.asarray(pairs, dtype=np.int32)
 
 
-@pytest.mark.parametrize("name,make,pt", CASES, ids=[c[0] for c in CASES])
-def test_full_size_parity(name, make, pt):
+@pytest.mark.parametrize("name,make,pt,fused,bound", CASES, ids=[c[0] for c in CASES])
+def test_full_size_parity(name, make, pt, fused, bound):
     W = make()
-    res = harness.run_gpu(W, partition_tokens=pt, want_cache=True)
+    if name == "fp8_recycle":
+        assert W.fresh_blocks.size == 515   # the recycled blocks, zeroed in the fused launch
+    res = harness.run_gpu(W, partition_tokens=pt, want_cache=True, fused=fused,
+                          max_seq_len=W.max_blocks * 16 if bound == "table" else None)
     assert res["status"] == 0, res["status"]
     kc, vc = harness.oracle_cache(W)
     assert np.array_equal(res["key"], kc), "key cache differs from the oracle"

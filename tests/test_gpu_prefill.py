@@ -131,12 +131,16 @@ def test_prefill_fp8_is_deterministic_and_matches_oracle():
     harness.assert_close(a, harness.oracle_prefill_out(W, kc, vc), "fp8_e4m3")
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
-def test_prefill_full_size_sampled_rows(kv_dtype):
-    """The full 8K-token chunked-prefill step in the bench's launch
+@pytest.mark.parametrize("make,kv_dtype", [
+    (wl.chunked_prefill_8k, "bf16"), (wl.chunked_prefill_8k, "fp8_e4m3"),
+    (wl.prefill_8k, "bf16"), (wl.prefill_8k, "fp8_e4m3")],
+    ids=["chunked_bf16", "chunked_fp8", "prompts_bf16", "prompts_fp8"])
+def test_prefill_full_size_sampled_rows(make, kv_dtype):
+    """The full 8K-token prefill steps (8 chunks of 1024 tokens after a
+    history, and 8 fresh 1024-token prompts) in the bench's launch
     configuration; rows sampled across every sequence (first, last and
-    seeded random tokens, all heads of a group) against the oracle."""
-    W = wl.chunked_prefill_8k(kv_dtype=kv_dtype)
+    seeded random tokens, heads from several groups) against the oracle."""
+    W = make(kv_dtype=kv_dtype)
     gpu, _ = _run_case(W)
     rng = np.random.default_rng(0)
     qsl = W.query_start_loc
