@@ -197,9 +197,10 @@ pkv_status paged_prepare_inputs(const int32_t *idx_mapping,
  *                 sequence is clamped and reported as a range error.
  *   partition_tokens  0 = automatic (see paged_attention_partition_tokens);
  *                 otherwise a multiple of 16: every sequence is split into
- *                 partitions of that many tokens, one CTA each per kv head;
- *                 a second kernel merges the partitions of split sequences
- *                 with a log-sum-exp reduce.
+ *                 partitions of that many tokens, each attended by one CTA
+ *                 per kv head (by one warp when partitions hold at most 512
+ *                 tokens); a second kernel merges the partitions of split
+ *                 sequences with a log-sum-exp reduce.
  *   workspace     device scratch of workspace_bytes, at least
  *                 paged_attention_workspace_bytes(...) for the same
  *                 arguments; may be NULL when that function returns 0.

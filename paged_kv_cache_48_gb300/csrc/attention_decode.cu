@@ -559,13 +559,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const size_t row0 = (size_t)b * p.num_heads + (size_t)kvh * p.group + qg * 8;
   uint32_t qf[C::MT][2];
   load_q<FP8, D>(qf, p.q + row0 * D, heads_here, lane);
-  // Without shared prefixes the partition's first block is part * part_tokens
-  // / 16 whatever the length: this warp's first 32 block ids go out now too
-  // (masked to the partition's blocks once the length is known).
-  const bool ids_early = !p.group_start;
+  // The partition's first block is (start + part * part_tokens) / 16 whatever
+  // the length, where start is 0 without shared prefixes: this warp's first
+  // 32 block ids go out now too (masked to the partition's blocks once the
+  // length is known).  With shared prefixes the start is guessed to be the
+  // longest prefix (every member of a group that shares it) and the ids are
+  // used only if the guess proves right.
+  const int spec_start = p.group_start ? p.max_prefix_len : 0;
   int ids_pre = -1;
-  if (ids_early) {
-    const long long j = (long long)part * (p.part_tokens >> 4) + j_off + (long long)lane * jstep;
+  {
+    const long long j = (long long)(spec_start >> 4) + (long long)part * (p.part_tokens >> 4) +
+                        j_off + (long long)lane * jstep;
     if (j < p.max_blocks) ids_pre = __ldg(p.block_tables + (size_t)b * p.max_blocks + j);
   }
 
@@ -582,6 +586,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int start =
       cascade_start(p, b, L, lane, blockIdx.x == 0 && part == 0 && warp == 0);
   const int slot_base = prefix_slots(p, start);
+  const bool ids_early = start == spec_start;
   if (p.seq_start && blockIdx.x == 0 && part == 0 && threadIdx.x == 0) p.seq_start[b] = start;
   const int Ls = L - start;
   const int nparts = Ls <= p.part_tokens ? 1 : (Ls + p.part_tokens - 1) / p.part_tokens;
@@ -917,8 +922,24 @@ paged_decode_merge_wide_kernel(const DecodeParams p) {
     __syncthreads();
     const float4 *po =
         reinterpret_cast<const float4 *>(p.part_o + ((size_t)row * p.max_parts + c0) * D) + l4;
-#pragma unroll 4
-    for (int j = slot; j < cnt; j += SLOTS) {
+    // batches of 8 partitions: their loads go out together, then the sums
+    // in partition order
+    constexpr int BATCH = 8;
+    int j = slot;
+    for (; j + (BATCH - 1) * SLOTS < cnt; j += BATCH * SLOTS) {
+      float4 o[BATCH];
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) o[k] = po[(size_t)(j + k * SLOTS) * LPP];
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) {
+        const float w = w_s[j + k * SLOTS];
+        acc.x += w * o[k].x;
+        acc.y += w * o[k].y;
+        acc.z += w * o[k].z;
+        acc.w += w * o[k].w;
+      }
+    }
+    for (; j < cnt; j += SLOTS) {
       const float w = w_s[j];
       const float4 o = po[(size_t)j * LPP];
       acc.x += w * o.x;
@@ -1083,10 +1104,11 @@ PartLayout part_layout(int64_t batch, int64_t num_heads, int64_t num_kv_heads,
   return l;
 }
 
-// Launch with programmatic stream serialisation (see grid_dependency_wait).
+// Launch with programmatic stream serialisation (see grid_dependency_wait),
+// or, with pdl false, in plain stream order.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t s, Args &&...args) {
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, bool pdl, Args &&...args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -1096,9 +1118,19 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+  return launch_kernel(kernel, grid, block, smem, s, true, std::forward<Args>(args)...);
+}
+
+// Cascade decode: whether the suffix pass may launch programmatically, while
+// the kernel before it in the stream is still running.
+constexpr bool kCascadeSuffixPdl = true;
 
 // join (optional): an event the merge kernel must wait for (the shared-
 // prefix pass running on another stream).
@@ -1122,8 +1154,8 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
   }
   const int grid_y = p.warp_parts ? (p.grid_parts + C::NW - 1) / C::NW : p.grid_parts;
   dim3 grid(p.num_kv_heads * p.q_groups, grid_y, p.batch);
-  if (launch_pdl(paged_decode_kernel<FP8, D>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s, mk, mv,
-                 p) != cudaSuccess)
+  if (launch_kernel(paged_decode_kernel<FP8, D>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s,
+                    !join || kCascadeSuffixPdl, mk, mv, p) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (join && cudaStreamWaitEvent(s, join, 0) != cudaSuccess) return PKV_ERR_CUDA;
   if (p.max_parts > 1) {

@@ -84,9 +84,9 @@ struct PrefillParams {
 // exact in f16; q is converted from bf16 once), and the producer warp
 // converts each fp8 tile from a TMA staging ring into f16 operand tiles.
 // PREFIX: the shared-prefix pass of cascade decode.  Its groups hold few
-// query rows, so one query tile, single-stage rings and 6 warps (about
-// 96 KB of shared memory, 256 TMEM columns) let two of its CTAs, or one
-// beside decode CTAs, share an SM.
+// query rows, so one query tile, a 2-stage K ring, a 1-stage V ring and 6
+// warps (about 128 KB of shared memory, 256 TMEM columns) let one of its
+// CTAs share an SM with a decode CTA.
 template <bool FP8, int D, bool PREFIX = false>
 struct PrefillCfg {
   static constexpr int SLICES = D / 64;          // 64-element head_dim slices
@@ -97,7 +97,7 @@ struct PrefillCfg {
   // both P V products: K runs one tile ahead of V and gets the deeper ring.
   // fp8 cache: V converted a tile ahead (2 stages), K just in time for the
   // next Q K^T (1 stage, refilled once both Q K^T of a tile are done).
-  static constexpr int KSTAGES = PREFIX ? 1 : (FP8 ? 1 : 3);
+  static constexpr int KSTAGES = PREFIX ? 2 : (FP8 ? 1 : 3);
   static constexpr int VSTAGES = PREFIX ? 1 : 2;
   static constexpr int KEYS = 128;               // keys per tile (8 blocks)
   static constexpr int STG_HALF = KEYS * D;      // fp8 K (or V) of one tile
@@ -117,7 +117,7 @@ struct PrefillCfg {
   // registers a thread).
   static constexpr int CONVERTERS = (FP8 && !PREFIX) ? 3 : 1;
   static constexpr int THREADS = PREFIX ? 192 : (FP8 ? 384 : 320);
-  static constexpr int MIN_BLOCKS = PREFIX ? 2 : 1;
+  static constexpr int MIN_BLOCKS = 1;
 };
 
 struct PrefillBars {
@@ -289,6 +289,12 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D, PREFIX>::THREADS,
   int q0, n_b, c = 0, kv_begin = 0, kv_len = 0, table_row = b;
   bool bad_seq;
   const int j0 = qp * C::NQT * TQ;
+  // Ordinary prefill reads table row b from entry 0 on: each thread loads
+  // one entry alongside the sequence's extent, so that checking the ids
+  // costs no round trip of its own.
+  int32_t spec_id = 0;
+  const bool spec_ok = !prefix_mode && (int)threadIdx.x < p.max_blocks;
+  if (spec_ok) spec_id = __ldg(p.block_tables + (size_t)b * p.max_blocks + threadIdx.x);
   if (prefix_mode) {
     q0 = p.group_start[b];
     n_b = p.group_start[b + 1] - q0;
@@ -318,44 +324,12 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D, PREFIX>::THREADS,
   const int n_tiles = (kv_len - kv_begin + C::KEYS - 1) / C::KEYS;
   const int blk_begin = kv_begin / 16;          // kv_begin is a multiple of 128
   const int nblk = (kv_len + 15) / 16;          // end of the block range
+  const int ntq = has_b ? 2 : 1;                // query tiles in use
+  const int32_t *row = p.block_tables + (size_t)table_row * p.max_blocks + blk_begin;
 
-  // every block id the pair reads must be inside the pool
-  int bad = bad_seq ? 1 : 0;
-  if (!bad) {
-    const int32_t *row = p.block_tables + (size_t)table_row * p.max_blocks;
-    for (int j = blk_begin + threadIdx.x; j < nblk; j += blockDim.x) {
-      const int32_t id = row[j];
-      if (id < 0 || id >= p.num_blocks) {
-        bad = 1;
-        record_error(&g_err_prefill, PKV_ERR_RANGE, (long long)table_row * p.max_blocks + j);
-      }
-    }
-  } else if (threadIdx.x == 0) {
-    record_error(&g_err_prefill, PKV_ERR_RANGE, b);
-  }
-  if (__syncthreads_or(bad)) {
-    // zero the pair's output rows of a valid token range (in shared-prefix
-    // mode: an empty partial, weight zero in the merge), then leave
-    if (!bad_seq) {
-      const int rows = (j_last - j0 + 1) * g;
-      for (int idx = threadIdx.x; idx < rows * (D / 8); idx += blockDim.x) {
-        const int r = idx / (D / 8), ch = idx % (D / 8);
-        const long long tok = (long long)q0 + j0 + r / g;
-        const size_t row = (size_t)tok * p.num_heads + kvh * g + r % g;
-        if (prefix_mode) {
-          float *po = p.part_o + (row * p.part_stride + pp) * D + ch * 8;
-          *reinterpret_cast<float4 *>(po) = make_float4(0.f, 0.f, 0.f, 0.f);
-          *reinterpret_cast<float4 *>(po + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (ch == 0) p.part_ml[row * p.part_stride + pp] = make_float2(-INFINITY, 0.f);
-        } else {
-          *reinterpret_cast<uint4 *>(p.out + row * D + ch * 8) = make_uint4(0, 0, 0, 0);
-        }
-      }
-    }
-    return;
-  }
-
-  const int ntq = has_b ? 2 : 1;  // query tiles in use
+  // ---- barriers, TMEM and (ordinary prefill) the first copies, while the
+  // ---- block ids are checked.  A copy at an id outside the pool reads
+  // ---- zeros (the tensor map's bounds), so nothing faults before the check.
   if (threadIdx.x == 0) {
     mbar_init(&bars.q_full, 1);
     mbar_init(&bars.q_ready, 4 * ntq);
@@ -380,34 +354,119 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D, PREFIX>::THREADS,
     bars.abort_flag = 0;
     fence_barrier_init();
   }
+  const bool early = !prefix_mode && !bad_seq;  // first copies before the check
+  const uint64_t pol = l2_policy_evict_normal();
+  constexpr uint32_t TB = C::TILE_BYTES;
+  // bf16: K(0) and V(0); fp8: the staging of tiles 0 and 1
+  auto first_copies = [&]() {
+    if constexpr (!FP8) {
+      const int nv = min(8, nblk - blk_begin);
+      mbar_arrive_expect_tx(&bars.k_full[0], nv * C::SLICES * 2048);
+      mbar_arrive_expect_tx(&bars.v_full[0], nv * C::SLICES * 2048);
+      for (int j = 0; j < nv; ++j) {
+        const int blk = row[j];
+        for (int s = 0; s < C::SLICES; ++s) {
+          tma_load_5d(smem + C::K_OFF + s * C::SLICE_BYTES + j * 2048, &kmap, &bars.k_full[0], 0,
+                      0, kvh, s, blk, pol);
+          tma_load_5d(smem + C::V_OFF + s * C::SLICE_BYTES + j * 2048, &vmap, &bars.v_full[0], 0,
+                      0, kvh, s, blk, pol);
+        }
+      }
+    } else {
+      for (int i = 0; i < min(2, n_tiles); ++i) {
+        const int nv = min(8, nblk - blk_begin - 8 * i);
+        mbar_arrive_expect_tx(&bars.stg_full[i], 2 * nv * 16 * D);
+        uint8_t *dst = smem + C::STG_OFF + i * 2 * C::STG_HALF;
+        for (int j = 0; j < nv; ++j) {
+          const int blk = row[8 * i + j];
+          tma_load_5d(dst + j * 16 * D, &kmap, &bars.stg_full[i], 0, 0, kvh, 0, blk, pol);
+          tma_load_5d(dst + C::STG_HALF + j * 16 * D, &vmap, &bars.stg_full[i], 0, 0, kvh, 0, blk,
+                      pol);
+        }
+      }
+    }
+  };
+  if (threadIdx.x == 0 && !bad_seq) {
+    prefetch_tensormap(&qmap);
+    prefetch_tensormap(&kmap);
+    prefetch_tensormap(&vmap);
+    mbar_arrive_expect_tx(&bars.q_full, ntq * C::SLICES * 128 * g * TQ);
+    for (int t = 0; t < ntq; ++t)
+      for (int s = 0; s < C::SLICES; ++s)
+        tc::tma_load_4d(smem_u32(smem + C::Q_OFF + t * TB + s * C::SLICE_BYTES), &qmap,
+                        smem_u32(&bars.q_full), 0, kvh * g, s, q0 + j0 + t * TQ);
+    if (early) first_copies();
+  }
   if (warp == 1) {
     tc::tmem_alloc(smem_u32(&bars.tmem_slot), C::TMEM_COLS);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
-  __syncthreads();
+
+  // every block id the pair reads must be inside the pool
+  int bad = bad_seq ? 1 : 0;
+  if (!bad) {
+    const int32_t *trow = p.block_tables + (size_t)table_row * p.max_blocks;
+    for (int j = blk_begin + threadIdx.x; j < nblk; j += blockDim.x) {
+      const int32_t id = (spec_ok && j == (int)threadIdx.x) ? spec_id : trow[j];
+      if (id < 0 || id >= p.num_blocks) {
+        bad = 1;
+        record_error(&g_err_prefill, PKV_ERR_RANGE, (long long)table_row * p.max_blocks + j);
+      }
+    }
+  } else if (threadIdx.x == 0) {
+    record_error(&g_err_prefill, PKV_ERR_RANGE, b);
+  }
+  if (__syncthreads_or(bad)) {
+    // let the copies already issued land, release TMEM, zero the pair's
+    // output rows of a valid token range (in shared-prefix mode: an empty
+    // partial, weight zero in the merge), then leave
+    if (threadIdx.x == 0 && !bad_seq) {
+      mbar_wait_bounded(&bars.q_full, 0, p.timeout_ns);
+      if (early) {
+        if constexpr (!FP8) {
+          mbar_wait_bounded(&bars.k_full[0], 0, p.timeout_ns);
+          mbar_wait_bounded(&bars.v_full[0], 0, p.timeout_ns);
+        } else {
+          for (int i = 0; i < min(2, n_tiles); ++i)
+            mbar_wait_bounded(&bars.stg_full[i], 0, p.timeout_ns);
+        }
+      }
+    }
+    if (warp == 1) {
+      tc::fence_after_sync();
+      tc::tmem_dealloc(bars.tmem_slot, C::TMEM_COLS);
+    }
+    if (!bad_seq) {
+      const int rows = (j_last - j0 + 1) * g;
+      for (int idx = threadIdx.x; idx < rows * (D / 8); idx += blockDim.x) {
+        const int r = idx / (D / 8), ch = idx % (D / 8);
+        const long long tok = (long long)q0 + j0 + r / g;
+        const size_t orow = (size_t)tok * p.num_heads + kvh * g + r % g;
+        if (prefix_mode) {
+          float *po = p.part_o + (orow * p.part_stride + pp) * D + ch * 8;
+          *reinterpret_cast<float4 *>(po) = make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4 *>(po + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (ch == 0) p.part_ml[orow * p.part_stride + pp] = make_float2(-INFINITY, 0.f);
+        } else {
+          *reinterpret_cast<uint4 *>(p.out + orow * D + ch * 8) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    return;
+  }
   tc::fence_after_sync();
   const uint32_t tmem = bars.tmem_slot;
 
   const uint32_t sQ = smem_u32(smem + C::Q_OFF);
   const uint32_t sK = smem_u32(smem + C::K_OFF);
   const uint32_t sV = smem_u32(smem + C::V_OFF);
-  constexpr uint32_t TB = C::TILE_BYTES;
 
   if (warp == 0 || warp >= 10) {
     // ------------------------------------------------------------ producer
-    const int32_t *row = p.block_tables + (size_t)table_row * p.max_blocks + blk_begin;
-    const uint64_t pol = l2_policy_evict_normal();
-    if (warp == 0 && lane == 0) {
-      prefetch_tensormap(&qmap);
-      prefetch_tensormap(&kmap);
-      prefetch_tensormap(&vmap);
-      mbar_arrive_expect_tx(&bars.q_full, ntq * C::SLICES * 128 * g * TQ);
-      for (int t = 0; t < ntq; ++t)
-        for (int s = 0; s < C::SLICES; ++s)
-          tc::tma_load_4d(sQ + t * TB + s * C::SLICE_BYTES, &qmap, smem_u32(&bars.q_full), 0,
-                          kvh * g, s, q0 + j0 + t * TQ);
-    }
+    // (the Q tiles, and for ordinary prefill the first copies, went out
+    // before the block-id check)
+    if (warp == 0 && lane == 0 && !early) first_copies();
     if constexpr (!FP8) {
       if (lane == 0) {
         // K(i + 1) is issued before V(i): Q K^T of the next tile needs its
@@ -430,10 +489,11 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D, PREFIX>::THREADS,
           }
           return true;
         };
-        bool go = issue(true, 0);
+        // K(0) and V(0) are in flight already
+        bool go = true;
         for (int i = 0; go && i < n_tiles; ++i) {
           if (i + 1 < n_tiles) go = issue(true, i + 1);
-          go = go && issue(false, i);
+          if (i > 0) go = go && issue(false, i);
         }
       }
       __syncwarp();
@@ -468,10 +528,7 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D, PREFIX>::THREADS,
       };
       const int ci = warp == 0 ? 0 : warp - 9;  // converter index
       constexpr int STRIDE = 32 * C::CONVERTERS;
-      if (warp == 0 && lane == 0) {
-        stage_load(0);
-        if (n_tiles > 1) stage_load(1);
-      }
+      // (tiles 0 and 1 are staged already)
       __syncwarp();
       // Convert tile i's K or V; V rows past the sequence's keys become 0.
       auto convert = [&](bool is_k, int i) -> bool {
