@@ -40,6 +40,10 @@ SEQ_LENS = {"llama8b_gqa": "uniform [512, 4096]",
 FALLBACK_HBM_GBS = 6800.0
 PROFILE = ROOT / "profiles" / "paged_decode_kernel_llama8b_gqa.md"
 # decode workloads with a committed ncu summary of the decode kernel
+# GPU clock cycles of the sleep that precedes a timed loop (about 2 ms):
+# long enough for the host to queue a few dozen steps.
+PRIME_CYCLES = 4_000_000
+
 DECODE_PROFILES = {
     "llama8b_gqa": PROFILE,
     "long_context": ROOT / "profiles" / "paged_decode_kernel_long_context.md",
@@ -434,10 +438,16 @@ def run_ours(args):
 
     def timed_loop(n, body):
         """Device time of n calls of body(): one event pair around the loop,
-        or per call with an L2 flush in between when flushing."""
+        or per call with an L2 flush in between when flushing.  The GPU
+        first runs a sleep that touches no memory, outside the events, so
+        that the host has queued the first steps when the start event is
+        reached: the device time then holds the steps, not the host's
+        latency to its first launch (which is several steps' worth when K
+        is small)."""
         if not flush:
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(PRIME_CYCLES)
             a.record(stream)
             for i in range(n):
                 body(i)
@@ -682,6 +692,7 @@ def run_blocks(args):
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(PRIME_CYCLES)  # the host queues calls meanwhile
         a.record(stream)
         for _ in range(reps):
             fn()
@@ -878,6 +889,7 @@ def run_prefill(args):
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(PRIME_CYCLES)  # the host queues calls meanwhile
         a.record(stream)
         for _ in range(reps):
             fn()
@@ -1053,6 +1065,7 @@ def run_cascade(args):
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(PRIME_CYCLES)  # the host queues calls meanwhile
         a.record(stream)
         for _ in range(reps):
             fn()

@@ -155,7 +155,8 @@ __device__ __forceinline__ int prefix_slots(const DecodeParams &p, int start) {
   return start > 0 ? (start + p.prefix_part_tokens - 1) / p.prefix_part_tokens : 0;
 }
 
-template <bool FP8, int D>
+// NW warps per CTA share RING_KB KiB of stages (3 CTAs/SM at 4 warps, 64).
+template <bool FP8, int D, int NW_ = 4, int RING_KB = 64>
 struct Cfg {
   static constexpr int ELT = FP8 ? 1 : 2;
   static constexpr int ROW_BYTES = D * ELT;
@@ -164,8 +165,8 @@ struct Cfg {
   static constexpr int BOX_ELEMS = BOX_BYTES / ELT;
   static constexpr int TILE_BYTES = 16 * ROW_BYTES;    // K (or V) of a block-head
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;   // K + V
-  static constexpr int NW = 4;                         // warps per CTA
-  static constexpr int RING_BYTES = 64 * 1024;         // all stages of a CTA (3 CTAs/SM)
+  static constexpr int NW = NW_;                       // warps per CTA
+  static constexpr int RING_BYTES = RING_KB * 1024;    // all stages of a CTA
   static constexpr int S0 = RING_BYTES / (NW * STAGE_BYTES);
   static constexpr int STAGES = S0 < 2 ? 2 : (S0 > 8 ? 8 : S0);
   static constexpr int MT = D / 16;                    // 16-row tiles of head_dim
@@ -517,12 +518,12 @@ __device__ __forceinline__ void issue_block(uint8_t *stage, uint64_t *bar,
 // ===========================================================================
 // Decode kernel
 // ===========================================================================
-template <bool FP8, int D>
-__global__ void __launch_bounds__(Cfg<FP8, D>::NW * 32)
+template <bool FP8, int D, int NW = 4, int RING_KB = 64>
+__global__ void __launch_bounds__(NW * 32)
 paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v,
                     const DecodeParams p) {
-  using C = Cfg<FP8, D>;
+  using C = Cfg<FP8, D, NW, RING_KB>;
   extern __shared__ uint8_t smem_dyn[];
   __shared__ uint64_t bars[C::NW][C::STAGES];
   __shared__ int stage_ok[C::NW][C::STAGES];
@@ -1134,10 +1135,10 @@ constexpr bool kCascadeSuffixPdl = true;
 
 // join (optional): an event the merge kernel must wait for (the shared-
 // prefix pass running on another stream).
-template <bool FP8, int D>
+template <bool FP8, int D, int NW = 4, int RING_KB = 64>
 pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                          cudaStream_t s, cudaEvent_t join = nullptr) {
-  using C = Cfg<FP8, D>;
+  using C = Cfg<FP8, D, NW, RING_KB>;
   static int configured[64] = {0};
   static std::mutex mu;
   int dev = 0;
@@ -1145,7 +1146,7 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!configured[dev]) {
-      if (cudaFuncSetAttribute(paged_decode_kernel<FP8, D>,
+      if (cudaFuncSetAttribute(paged_decode_kernel<FP8, D, NW, RING_KB>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                C::SMEM_BYTES) != cudaSuccess)
         return PKV_ERR_CUDA;
@@ -1154,7 +1155,7 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
   }
   const int grid_y = p.warp_parts ? (p.grid_parts + C::NW - 1) / C::NW : p.grid_parts;
   dim3 grid(p.num_kv_heads * p.q_groups, grid_y, p.batch);
-  if (launch_kernel(paged_decode_kernel<FP8, D>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s,
+  if (launch_kernel(paged_decode_kernel<FP8, D, NW, RING_KB>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s,
                     !join || kCascadeSuffixPdl, mk, mv, p) != cudaSuccess)
     return PKV_ERR_CUDA;
   if (join && cudaStreamWaitEvent(s, join, 0) != cudaSuccess) return PKV_ERR_CUDA;
