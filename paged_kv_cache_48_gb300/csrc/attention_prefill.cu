@@ -546,6 +546,37 @@ __global__ void __launch_bounds__(PrefillCfg<FP8, D, PREFIX>::THREADS,
         const int last_row = is_k ? loaded : C::KEYS;  // K rows past `loaded` stay stale (masked)
         constexpr int CH = D / 16;                     // 16-byte fp8 chunks per row
         const int total = last_row * CH;
+        if (rows >= last_row) {
+          // Every row comes from the staging (full tiles, and K): a lane
+          // keeps one 16-byte column, so its source and destination
+          // columns are fixed and only the row moves (rows row0 + k RSTEP).
+          static_assert(STRIDE % CH == 0, "converter lanes keep their column");
+          constexpr int RSTEP = STRIDE / CH;
+          const int tid = ci * 32 + lane;
+          const int cc = tid % CH;
+          const int c16 = ((cc * 16) % 64) / 8;  // 16-byte column of the low half
+          const uint8_t *s0 = src + cc * 16;
+          uint8_t *d0 = dst + ((cc * 16) / 64) * C::SLICE_BYTES;
+          auto put = [&](int rr, const uint4 &v) {
+            uint4 lo, hi;
+            e4m3x16_to_f16(v, lo, hi);
+            uint8_t *base = d0 + rr * 128;
+            const int sw = rr & 7;
+            *reinterpret_cast<uint4 *>(base + ((c16 ^ sw) << 4)) = lo;
+            *reinterpret_cast<uint4 *>(base + (((c16 + 1) ^ sw) << 4)) = hi;
+          };
+          int r = tid / CH;
+          // four rows per lane in flight: loads first, then convert + store
+          for (; r + 3 * RSTEP < last_row; r += 4 * RSTEP) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              v[u] = *reinterpret_cast<const uint4 *>(s0 + (r + u * RSTEP) * D);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) put(r + u * RSTEP, v[u]);
+          }
+          for (; r < last_row; r += RSTEP) put(r, *reinterpret_cast<const uint4 *>(s0 + r * D));
+        } else
         // four chunks per lane in flight: loads first, then convert + store
         for (int q0c = ci * 32; q0c < total; q0c += 4 * STRIDE) {
           uint4 v[4];
