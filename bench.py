@@ -48,6 +48,8 @@ DECODE_PROFILES = {
     "llama8b_gqa": PROFILE,
     "long_context": ROOT / "profiles" / "paged_decode_kernel_long_context.md",
     "fp8_recycle": ROOT / "profiles" / "paged_decode_kernel_fp8_recycle.md",
+    # (workload, partition tokens) where a partition length has its own capture
+    ("long_context", 512): ROOT / "profiles" / "paged_decode_kernel_long_context_p512.md",
 }
 KERNEL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_decode.cu",
                   "paged_kv_cache_48_gb300/csrc/pkv_device.cuh"]
@@ -594,8 +596,8 @@ def run_ours(args):
     e2e_value = whole_job_gbs(world, kv_bytes, e2e_ms / K2)
     peak, peak_kind = measured_peak()
     achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
-    traffic = (profiled_traffic(DECODE_PROFILES[args.workload])
-               if args.workload in DECODE_PROFILES else None)
+    prof = DECODE_PROFILES.get((args.workload, pt), DECODE_PROFILES.get(args.workload))
+    traffic = profiled_traffic(prof) if prof is not None else None
     l2 = (f"L2 flushed between steps ({kv_bytes / 1e6:.1f} MB of KV per step)"
           if flush else
           f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV read per step, "
