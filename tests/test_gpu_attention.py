@@ -240,3 +240,22 @@ def test_timeout_path_reports_and_spares_other_sequences(name, partition_tokens)
     again = harness.run_gpu(W, partition_tokens=partition_tokens, want_cache=False)
     assert again["status"] == PKV_OK
     harness.assert_close(again["out"], ref, W.kv_dtype)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_thousands_of_partitions_per_row(kv_dtype):
+    """16-token partitions over sequences of up to 40,000 tokens: one warp
+    per 16-token partition and more than 2048 partials in a row, so the
+    one-CTA-per-row merge walks its weights in several chunks.  Matches
+    the oracle on every row; bitwise equal on a second run."""
+    W = wl.make_workload(f"many_parts_{kv_dtype}", 3, 8, 2, 128, 0, 0, 36,
+                         kv_dtype=kv_dtype, seq_lens=[40000, 33000, 17],
+                         fresh_policy="recycle515" if kv_dtype != "bf16" else "new_token")
+    assert (W.seq_lens.max() + 15) // 16 > 2048
+    kc, vc = harness.oracle_cache(W)
+    ref = harness.oracle_out(W, kc, vc)
+    res = harness.run_gpu(W, partition_tokens=16, want_cache=False)
+    assert res["status"] == PKV_OK, res
+    harness.assert_close(res["out"], ref, W.kv_dtype)
+    again = harness.run_gpu(W, partition_tokens=16, want_cache=False)
+    assert np.array_equal(res["out"], again["out"])
