@@ -49,12 +49,30 @@ __device__ __forceinline__ E4m3Recip e4m3_recip(float scale) {
 }
 
 // Two values to two E4M3 bytes (low byte = a): the IEEE binary32 quotient
-// x / scale, rounded to nearest even and saturated to +-448.
+// x / scale, rounded to nearest even and saturated to +-448.  Both
+// bracketing products of the pair come from one two-lane multiply each
+// (each lane rounded as the scalar multiply), and each pair of products
+// converts in one instruction.
 __device__ __forceinline__ uint32_t quant2_e4m3(float a, float b, float scale, E4m3Recip r) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a * r.lo, b * r.lo), __NV_SATFINITE,
-                                               __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(a * r.hi, b * r.hi), __NV_SATFINITE,
-                                               __NV_E4M3);
+  uint32_t lo, hi;
+  asm("{\n"
+      ".reg .b64 x, pl, ph, rl, rh;\n"
+      ".reg .f32 l0, l1, h0, h1;\n"
+      ".reg .b16 cl, ch;\n"
+      "mov.b64 x, {%2, %3};\n"
+      "mov.b64 rl, {%4, %4};\n"
+      "mov.b64 rh, {%5, %5};\n"
+      "mul.rn.f32x2 pl, x, rl;\n"
+      "mul.rn.f32x2 ph, x, rh;\n"
+      "mov.b64 {l0, l1}, pl;\n"
+      "mov.b64 {h0, h1}, ph;\n"
+      "cvt.rn.satfinite.e4m3x2.f32 cl, l1, l0;\n"
+      "cvt.rn.satfinite.e4m3x2.f32 ch, h1, h0;\n"
+      "cvt.u32.u16 %0, cl;\n"
+      "cvt.u32.u16 %1, ch;\n"
+      "}\n"
+      : "=r"(lo), "=r"(hi)
+      : "f"(a), "f"(b), "f"(r.lo), "f"(r.hi));
   if (r.ok && lo == hi) return lo;
   return __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a, scale), __fdiv_rn(b, scale)),
                                   __NV_SATFINITE, __NV_E4M3);
@@ -62,19 +80,12 @@ __device__ __forceinline__ uint32_t quant2_e4m3(float a, float b, float scale, E
 
 // Eight bf16 values to eight E4M3 bytes.
 __device__ __forceinline__ uint2 quant8_e4m3(const uint4 &src, float scale, E4m3Recip r) {
-  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&src);
-  uint32_t out[2];
+  const uint32_t w[4] = {src.x, src.y, src.z, src.w};
+  uint32_t q[4];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float2 f = __bfloat1622float2(h[2 * i + j]);
-      word |= quant2_e4m3(f.x, f.y, scale, r) << (16 * j);
-    }
-    out[i] = word;
-  }
-  return make_uint2(out[0], out[1]);
+  for (int i = 0; i < 4; ++i)  // bf16 pair -> the binary32 values (exact)
+    q[i] = quant2_e4m3(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u), scale, r);
+  return make_uint2(__byte_perm(q[0], q[1], 0x5410), __byte_perm(q[2], q[3], 0x5410));
 }
 
 // The slot-mapped write of work items first, first + stride, ... < total
