@@ -279,12 +279,10 @@ pkv_status paged_attention_prefill(const void *q, const pkv_cache *cache,
  * tokens; a log-sum-exp merge combines the partials.  A group whose
  * members' tables or lengths break the contract is reported by pkv_check()
  * and its members are attended in full, so the output stays correct.
- * Pass 1 runs on a library-owned side stream that forks from `stream` and
- * joins it again before the merge (also on every error return).  All
- * cascade calls on a device share that side stream: calls from different
- * streams wait for each other's pass 1, and while one thread captures a
- * cascade call into a CUDA graph no other cascade call may run on the same
- * device. */
+ * All three launches go on `stream`, in that order, with programmatic
+ * dependent launch: pass 2 starts while pass 1 runs (the passes do not
+ * depend on each other), and the merge waits for both.  The call keeps no
+ * state between calls and shares nothing across streams. */
 pkv_status paged_attention_decode_cascade(
     const void *q, const pkv_cache *cache, const int32_t *block_tables,
     int32_t max_blocks, const int32_t *seq_lens, int32_t batch,

@@ -81,6 +81,14 @@ struct DecodeParams {
   const int32_t *group_start, *prefix_len;
   int32_t num_groups, max_group_size, max_prefix_len, prefix_part_tokens;
   int32_t *seq_start;
+  // 1: the launch just before this one in the stream is the shared-prefix
+  // pass, whose CTAs all waited for the kernels before it before letting
+  // this grid launch.  This grid then skips its own wait at entry (which
+  // would wait for the whole prefix pass) and runs beside the prefix pass;
+  // its last CTA waits for the prefix pass before it exits, so that the
+  // grid does not complete, and the merge after it does not start, before
+  // the prefix partials are written.
+  int32_t defer_dep_wait;
 };
 
 // First token of sequence b this launch attends to (0, or its group's
@@ -552,7 +560,9 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     prefetch_tensormap(&tmap_v);
   }
   __syncwarp();
-  grid_dependency_wait();
+  const bool wait_at_exit = p.defer_dep_wait && blockIdx.x == gridDim.x - 1 &&
+                            blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1;
+  if (!p.defer_dep_wait) grid_dependency_wait();
   allow_dependent_launch();
 
   // q does not depend on the sequence's extent: its loads go out first
@@ -591,7 +601,10 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   if (p.seq_start && blockIdx.x == 0 && part == 0 && threadIdx.x == 0) p.seq_start[b] = start;
   const int Ls = L - start;
   const int nparts = Ls <= p.part_tokens ? 1 : (Ls + p.part_tokens - 1) / p.part_tokens;
-  if (part >= nparts) return;  // the whole CTA, or (warp-owned) this warp
+  if (part >= nparts) {  // the whole CTA, or (warp-owned) this warp
+    if (wait_at_exit) grid_dependency_wait();
+    return;
+  }
   const int tok0 = start + part * p.part_tokens;  // multiple of 16
   const int tok1 = min(L, tok0 + p.part_tokens);
   const int blk0 = tok0 >> 4;
@@ -710,6 +723,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
         if (d == 0) p.part_ml[slot] = live ? ml : make_float2(-INFINITY, 0.f);
       }
     }
+    if (wait_at_exit) grid_dependency_wait();
     return;
   }
 
@@ -761,6 +775,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
       if (d == 0) p.part_ml[slot] = make_float2(M, lsum);
     }
   }
+  if (wait_at_exit) grid_dependency_wait();
 }
 
 // Log-sum-exp merge of split sequences: one warp per (sequence, query head)
@@ -1105,11 +1120,10 @@ PartLayout part_layout(int64_t batch, int64_t num_heads, int64_t num_kv_heads,
   return l;
 }
 
-// Launch with programmatic stream serialisation (see grid_dependency_wait),
-// or, with pdl false, in plain stream order.
+// Launch with programmatic stream serialisation (see grid_dependency_wait).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                          cudaStream_t s, bool pdl, Args &&...args) {
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -1119,25 +1133,13 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t s, Args &&...args) {
-  return launch_kernel(kernel, grid, block, smem, s, true, std::forward<Args>(args)...);
-}
-
-// Cascade decode: whether the suffix pass may launch programmatically, while
-// the kernel before it in the stream is still running.
-constexpr bool kCascadeSuffixPdl = true;
-
-// join (optional): an event the merge kernel must wait for (the shared-
-// prefix pass running on another stream).
 template <bool FP8, int D, int NW = 4, int RING_KB = 64>
 pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                         cudaStream_t s, cudaEvent_t join = nullptr) {
+                         cudaStream_t s) {
   using C = Cfg<FP8, D, NW, RING_KB>;
   static int configured[64] = {0};
   static std::mutex mu;
@@ -1155,10 +1157,9 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
   }
   const int grid_y = p.warp_parts ? (p.grid_parts + C::NW - 1) / C::NW : p.grid_parts;
   dim3 grid(p.num_kv_heads * p.q_groups, grid_y, p.batch);
-  if (launch_kernel(paged_decode_kernel<FP8, D, NW, RING_KB>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s,
-                    !join || kCascadeSuffixPdl, mk, mv, p) != cudaSuccess)
+  if (launch_pdl(paged_decode_kernel<FP8, D, NW, RING_KB>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s,
+                 mk, mv, p) != cudaSuccess)
     return PKV_ERR_CUDA;
-  if (join && cudaStreamWaitEvent(s, join, 0) != cudaSuccess) return PKV_ERR_CUDA;
   if (p.max_parts > 1) {
     const long long rows = (long long)p.batch * p.num_heads;
     const cudaError_t e =
@@ -1308,46 +1309,6 @@ int cascade_prefix_part_tokens(int32_t num_groups, int32_t num_heads, int32_t nu
   return (int)std::max<int64_t>(kCascadePrefixPartTokens, std::min<int64_t>(tokens, INT32_MAX / 2));
 }
 
-// A non-blocking side stream per device with its fork / join events; the
-// mutex keeps one call's fork-join sequence together.  Every cascade call
-// on a device shares them: calls from different streams are serialised
-// behind each other's prefix pass, and while one thread captures a cascade
-// call into a CUDA graph the side stream belongs to that capture, so no
-// other cascade call may run on the device until the capture ends.
-struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  std::mutex mu;
-};
-
-SideStream &side_stream() {
-  static SideStream streams[64];
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    static SideStream none;
-    return none;
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  SideStream &sd = streams[dev];
-  if (!sd.stream) {
-    cudaStream_t st = nullptr;
-    cudaEvent_t f = nullptr, j = nullptr;
-    // highest priority: the prefix pass's CTAs (one per SM) take SMs as
-    // they free up instead of queueing behind the whole decode grid
-    int lo = 0, hi = 0;
-    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) hi = 0;
-    if (cudaStreamCreateWithPriority(&st, cudaStreamNonBlocking, hi) == cudaSuccess &&
-        cudaEventCreateWithFlags(&f, cudaEventDisableTiming) == cudaSuccess &&
-        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) == cudaSuccess) {
-      sd.fork = f;
-      sd.join = j;
-      sd.stream = st;
-    }
-  }
-  return sd;
-}
-
 struct CascadeLayout {
   int32_t pt, prefix_parts, suffix_parts, stride;
   size_t ml_off, start_off, bytes;
@@ -1425,37 +1386,22 @@ extern "C" pkv_status paged_attention_decode_cascade(
   int32_t *seq_start = reinterpret_cast<int32_t *>(ws + l.start_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  // 1. each group's prefix, once for all its members (tensor cores), on a
-  //    side stream so that it runs beside pass 2
-  SideStream &side = side_stream();
-  if (!side.stream) return PKV_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(side.mu);
-  const bool fork = num_groups > 0 && max_prefix_len > 0;
+  CUtensorMap mk, mv;
+  if (!get_maps(cache, &mk, &mv)) return PKV_ERR_CUDA;
+  // 1. each group's prefix, once for all its members (tensor cores).  Its
+  //    CTAs (one wave) start first; the decode pass launches programmatically
+  //    beside them, since the two passes do not depend on each other
+  const bool with_prefix = num_groups > 0 && max_prefix_len > 0;
   const int part_tokens = cascade_prefix_part_tokens(num_groups, num_heads, cache->num_kv_heads,
                                                      max_group_size, max_prefix_len);
-  // After the fork, every return joins the side stream back into `s`, so
-  // that a capture of `s` never ends with the side stream still forked.
-  auto join_back = [&](pkv_status ret) {
-    if (cudaEventRecord(side.join, side.stream) != cudaSuccess ||
-        cudaStreamWaitEvent(s, side.join, 0) != cudaSuccess)
-      return ret == PKV_OK ? PKV_ERR_CUDA : ret;
-    return ret;
-  };
-  if (fork) {
-    if (cudaEventRecord(side.fork, s) != cudaSuccess) return PKV_ERR_CUDA;
-    if (cudaStreamWaitEvent(side.stream, side.fork, 0) != cudaSuccess)
-      return join_back(PKV_ERR_CUDA);
+  if (with_prefix) {
     st = launch_prefix_partials(q, cache, block_tables, max_blocks, seq_lens, group_start,
                                 prefix_len, num_groups, max_group_size, max_prefix_len, batch,
-                                num_heads, scale, part_o, part_ml, l.stride, part_tokens,
-                                side.stream);
-    if (st != PKV_OK) return join_back(st);
-    if (cudaEventRecord(side.join, side.stream) != cudaSuccess) return join_back(PKV_ERR_CUDA);
+                                num_heads, scale, part_o, part_ml, l.stride, part_tokens, s);
+    if (st != PKV_OK) return st;
   }
-  // 2. each sequence's own tokens (and its start), then, after the join, the
-  //    log-sum-exp merge of all slots
-  CUtensorMap mk, mv;
-  if (!get_maps(cache, &mk, &mv)) return fork ? join_back(PKV_ERR_CUDA) : PKV_ERR_CUDA;
+  // 2. each sequence's own tokens (and its start), then the log-sum-exp
+  //    merge of all slots
   DecodeParams p;
   std::memset(&p, 0, sizeof p);
   p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -1480,22 +1426,16 @@ extern "C" pkv_status paged_attention_decode_cascade(
   p.scale_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
   p.v_scale = fp8 ? cache->v_scale : 1.f;
   p.timeout_ns = 2000000000ull;
-  p.group_start = fork ? group_start : nullptr;
+  p.group_start = with_prefix ? group_start : nullptr;
   p.prefix_len = prefix_len;
   p.num_groups = num_groups;
   p.max_group_size = max_group_size;
   p.max_prefix_len = max_prefix_len;
   p.prefix_part_tokens = part_tokens;
   p.seq_start = seq_start;
-  cudaEvent_t join = fork ? side.join : nullptr;
-  const pkv_status ret =
-      fp8 ? (cache->head_dim == 128 ? launch_decode<true, 128>(mk, mv, p, s, join)
-                                    : launch_decode<true, 64>(mk, mv, p, s, join))
-          : (cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, s, join)
-                                    : launch_decode<false, 64>(mk, mv, p, s, join));
-  // launch_decode makes `s` wait for the join before the merge; if it failed
-  // before that point, wait here (the join event already marks the prefix
-  // pass's end)
-  if (ret != PKV_OK && fork) (void)cudaStreamWaitEvent(s, side.join, 0);
-  return ret;
+  p.defer_dep_wait = with_prefix;
+  return fp8 ? (cache->head_dim == 128 ? launch_decode<true, 128>(mk, mv, p, s)
+                                       : launch_decode<true, 64>(mk, mv, p, s))
+             : (cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, s)
+                                       : launch_decode<false, 64>(mk, mv, p, s));
 }

@@ -165,3 +165,23 @@ def test_cascade_long_prefix_in_several_partitions(kv_dtype):
     assert pkv_check()[0] == PKV_OK
     kc, vc = harness.oracle_cache(W)
     harness.assert_close(out.float().cpu().numpy(), harness.oracle_out(W, kc, vc), kv_dtype)
+
+
+def test_cascade_merge_waits_for_a_prefix_pass_longer_than_a_wave():
+    """40 groups of 2 sharing 2048-token prefixes with 1-16 private tokens:
+    the prefix pass (320 CTAs, more than one wave) is the long pole and the
+    decode pass beside it ends first, so a merge that did not wait for the
+    prefix pass would read unwritten slots.  Three calls in a row on one
+    stream give bitwise-equal outputs that match the oracle."""
+    W = wl.make_workload("prefix_wave", 80, 32, 8, 128, 1, 16, 31,
+                         prefix_groups=40, prefix_len=2048)
+    G = harness.upload(W)
+    harness.gpu_step(W, G)
+    gs, plen = _groups_of(W)
+    outs = [_cascade(W, G, gs, plen) for _ in range(3)]
+    assert pkv_check()[0] == PKV_OK
+    first = outs[0].float().cpu().numpy()
+    for o in outs[1:]:
+        assert np.array_equal(o.float().cpu().numpy(), first)
+    kc, vc = harness.oracle_cache(W)
+    harness.assert_close(first, harness.oracle_out(W, kc, vc), "bf16")

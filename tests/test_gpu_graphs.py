@@ -3,8 +3,8 @@ the eager result.
 
 A serving step runner captures its step once and replays it; the library's
 launches (programmatic dependent launch, launch parameters carrying host
-ids, the cascade path's side stream joined by events) must survive
-capture.  Each case runs eagerly, then is captured on a side stream and
+ids, the cascade path's decode pass running beside its prefix pass) must
+survive capture.  Each case runs eagerly, then is captured on a side stream and
 replayed twice; outputs must be bitwise equal and pkv_check clean.
 """
 import numpy as np
