@@ -74,6 +74,11 @@ def parse_args():
                     help="decode: the decode step (headline); the others time "
                          "the block-movement entry points on the workload's "
                          "pool")
+    ap.add_argument("--two-call-step", action="store_true",
+                    help="decode step as paged_kv_zero_and_write + "
+                         "paged_attention_decode even where the step's only "
+                         "writes are the new tokens (default there: one "
+                         "paged_attention_decode_step call)")
     ap.add_argument("--graph", action="store_true",
                     help="replay the decode step as one captured CUDA graph")
     ap.add_argument("--workload", default="llama8b_gqa",
@@ -112,6 +117,30 @@ def whole_job_gbs(world: int, bytes_per_rank: int, ms_per_step: float) -> float:
     """Aggregate throughput: every rank moves bytes_per_rank per step and
     the job's step time is the slowest rank's."""
     return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
+def new_token_rows(W):
+    """Rows of the step's writes holding each sequence's new token (position
+    seq_lens[b] - 1), in sequence order, when those are the step's only
+    writes and the only fresh blocks are blocks the new tokens open; else
+    None."""
+    import numpy as np
+    pos = {int(s): i for i, s in enumerate(W.step_slots)}
+    rows, opened = [], set()
+    for b in range(W.batch):
+        L = int(W.seq_lens[b])
+        if L == 0:
+            return None  # (a sequence without a new token has no row)
+        blk = int(W.block_tables[b, (L - 1) // 16])
+        i = pos.get(blk * 16 + (L - 1) % 16)
+        if i is None:
+            return None
+        rows.append(i)
+        if (L - 1) % 16 == 0:
+            opened.add(blk)
+    if len(rows) != W.step_slots.size or set(int(f) for f in W.fresh_blocks) != opened:
+        return None
+    return np.asarray(rows)
 
 
 def kernel_sha(sources=None) -> str:
@@ -371,6 +400,7 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
 
     from paged_kv_cache_48_gb300 import (PagedKVCache, paged_attention_decode,
+                                         paged_attention_decode_step,
                                          paged_attention_partition_tokens,
                                          paged_attention_workspace_bytes,
                                          paged_kv_write, paged_kv_zero_and_write,
@@ -394,9 +424,19 @@ def run_ours(args):
     q = bf(W.q).to(dev)
     tables = torch.from_numpy(W.block_tables).to(dev)
     lens = torch.from_numpy(W.seq_lens).to(dev)
-    sk, sv = bf(W.step_k).to(dev), bf(W.step_v).to(dev)
-    slots = torch.from_numpy(W.step_slots).to(dev)
-    fresh = W.fresh_blocks
+    new_tokens = None if args.two_call_step else new_token_rows(W)
+    if new_tokens is not None:
+        # every write of the step is a sequence's new token, and the only
+        # fresh blocks are the blocks those tokens open: the step is one
+        # paged_attention_decode_step call (the write inside the decode
+        # kernel)
+        sk, sv = bf(W.step_k[new_tokens]).to(dev), bf(W.step_v[new_tokens]).to(dev)
+        slots = torch.empty(0, dtype=torch.int64, device=dev)
+        fresh = np.zeros(0, dtype=np.int32)
+    else:
+        sk, sv = bf(W.step_k).to(dev), bf(W.step_v).to(dev)
+        slots = torch.from_numpy(W.step_slots).to(dev)
+        fresh = W.fresh_blocks
     # the step's device inputs live in one buffer (one copy moves them)
     d_main, (q, tables, lens, sk, sv, slots) = packed((q, tables, lens, sk, sv, slots), dev)
     max_len = int(W.max_blocks * 16)  # host bound: the table width
@@ -409,8 +449,9 @@ def run_ours(args):
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
-    # zeroing + write (one launch), the decode kernel and the merge of
-    # split sequences (when a sequence can be split)
+    # zeroing + write (one launch, unless the decode kernel writes the new
+    # tokens), the decode kernel and the merge of split sequences (when a
+    # sequence can be split)
     split = -(-max_len // pt) > 1
     launches_per_step = (1 if fresh.size or slots.numel() else 0) \
         + 1 + (1 if split else 0)
@@ -422,6 +463,16 @@ def run_ours(args):
 
     def step(ev=None, bufs=None):
         qq, tt, ll, kk, vv, ss, oo = bufs or (q, tables, lens, sk, sv, slots, out)
+        if new_tokens is not None:
+            # the new tokens' write, then attention, in the decode kernel
+            if ev is not None:
+                ev[0].record(stream)
+            paged_attention_decode_step(qq, kk, vv, cache, tt, ll, W.scale, max_len,
+                                        out=oo, partition_tokens=args.partition_tokens,
+                                        workspace=ws)
+            if ev is not None:
+                ev[1].record(stream)
+            return
         if fresh.size or ss.numel():
             # zeroing of the step's fresh blocks and the write of its
             # tokens, in one launch
@@ -617,8 +668,12 @@ def run_ours(args):
                    "num_heads": W.num_heads, "num_kv_heads": W.num_kv_heads,
                    "head_dim": W.head_dim, "block_size": 16,
                    "seq_lens": SEQ_LENS[W.name], "kv_dtype": W.kv_dtype,
-                   "num_blocks": W.num_blocks, "fresh_blocks": int(fresh.size),
-                   "step_tokens_written": int(slots.numel()),
+                   "num_blocks": W.num_blocks,
+                   "fresh_blocks": int(W.fresh_blocks.size),
+                   "step_tokens_written": int(W.step_slots.size),
+                   "step_calls": ("paged_attention_decode_step (new tokens written "
+                                  "by the decode kernel)" if new_tokens is not None
+                                  else "paged_kv_zero_and_write + paged_attention_decode"),
                    "partition_tokens": pt, "kv_read_bytes": kv_bytes,
                    "cuda_graph": bool(args.graph),
                    "unique_kv_read_bytes": W.unique_kv_read_bytes(),
@@ -630,7 +685,9 @@ def run_ours(args):
                      "kernel": "paged_decode_kernel + paged_decode_merge_kernel",
                      "launch_ms": round(attn_ms, 5),
                      "timed_in": "a second K-step loop, one event pair around "
-                                 "each decode call and its merge"},
+                                 "each decode call and its merge"
+                                 + (" (the call writes the new tokens too)"
+                                    if new_tokens is not None else "")},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms / K2, 5), "steps": K2,
                 "untimed_steps_before": E2E_WARM,

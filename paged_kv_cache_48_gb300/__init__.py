@@ -9,6 +9,7 @@ package binds them for PyTorch tensors.  Build with
 ``python -m paged_kv_cache_48_gb300.build``.
 """
 from .ops import (PagedKVCache, PagedKVError, paged_attention_decode,
+                  paged_attention_decode_step,
                   paged_attention_cascade_workspace_bytes,
                   paged_attention_decode_cascade, paged_attention_prefill,
                   paged_attention_partition_tokens,
@@ -20,6 +21,7 @@ from .ops import (PagedKVCache, PagedKVError, paged_attention_decode,
 
 __all__ = [
     "PagedKVCache", "PagedKVError", "paged_attention_decode",
+    "paged_attention_decode_step",
     "paged_attention_cascade_workspace_bytes", "paged_attention_decode_cascade",
     "paged_attention_prefill",
     "paged_attention_partition_tokens", "paged_attention_workspace_bytes",

@@ -20,7 +20,7 @@ LIBRARY = PKG / "libpagedkv.so"
 SOURCES = ["kv_write_zero.cu", "attention_decode.cu", "pkv_api.cu",
            "attention_noalloc.cu", "kv_blocks.cu", "input_prep.cu",
            "attention_prefill.cu"]
-HEADERS = ["pkv_device.cuh", "pkv_host.h", "tcgen05.cuh"]
+HEADERS = ["e4m3_encode.cuh", "pkv_device.cuh", "pkv_host.h", "tcgen05.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -37,6 +37,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "e4m3_encode.cuh"
 #include "pkv_device.cuh"
 #include "pkv_host.h"
 #include "../../include/pagedkv_testing.h"
@@ -89,6 +90,15 @@ struct DecodeParams {
   // grid does not complete, and the merge after it does not start, before
   // the prefix partials are written.
   int32_t defer_dep_wait;
+  // Decode step (k_new != nullptr): sequence b's new token, at position
+  // seq_lens[b] - 1, is written into the cache before it is attended:
+  // k_new / v_new [B, Hkv, D] bf16, the cache bases and k_scale for the
+  // E4M3 encode (v_scale above).  When the token opens its block (position
+  // a multiple of 16) the block's other rows are zeroed first.  The warp
+  // that reads the token's block writes its kv head's rows of it.
+  const __nv_bfloat16 *k_new, *v_new;
+  uint8_t *k_cache, *v_cache;
+  float k_scale;
 };
 
 // First token of sequence b this launch attends to (0, or its group's
@@ -523,6 +533,50 @@ __device__ __forceinline__ void issue_block(uint8_t *stage, uint64_t *bar,
   tma_load_5d(stage + C::TILE_BYTES, tv, bar, 0, 0, kvh, 0, phys, policy);
 }
 
+// Generic-proxy global stores made visible to the async proxy (TMA) of the
+// warp's later copies.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Decode step: the warp's part of writing sequence b's new token into block
+// `blk`, row `off`, of kv head kvh (see DecodeParams::k_new).  src is this
+// lane's 16 bytes of the token's K row (lanes 0 .. D/8 - 1) or V row (the
+// next D/8 lanes).  When off == 0 the block's rows 1 .. 15 of this head are
+// zeroed too (the other heads' rows by their own warps).  Ends with the
+// proxy fence: a TMA copy of the block issued by this warp afterwards reads
+// the new bytes.
+template <bool FP8, int D>
+__device__ __forceinline__ void write_new_token(const DecodeParams &p, int blk, int off, int kvh,
+                                                const uint4 &src, int lane) {
+  constexpr int ELT = FP8 ? 1 : 2;
+  constexpr int CH = D * ELT / 16;  // 16-byte chunks of one head's row
+  const size_t row_bytes = (size_t)p.num_kv_heads * D * ELT;
+  const size_t head0 = (size_t)blk * 16 * row_bytes + (size_t)kvh * D * ELT;
+  uint8_t *kc = p.k_cache + head0, *vc = p.v_cache + head0;
+  if (off == 0) {
+    for (int idx = lane; idx < 2 * 15 * CH; idx += 32) {
+      const int rem = idx % (15 * CH);
+      uint8_t *base = idx < 15 * CH ? kc : vc;
+      *reinterpret_cast<uint4 *>(base + (size_t)(1 + rem / CH) * row_bytes + (rem % CH) * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  if (lane < 2 * (D / 8)) {
+    const bool is_v = lane >= D / 8;
+    const int vec = is_v ? lane - D / 8 : lane;  // 8 elements
+    uint8_t *dst = (is_v ? vc : kc) + (size_t)off * row_bytes;
+    if constexpr (FP8) {
+      const float scale = is_v ? p.v_scale : p.k_scale;
+      *reinterpret_cast<uint2 *>(dst + vec * 8) = quant8_e4m3(src, scale, e4m3_recip(scale));
+    } else {
+      *reinterpret_cast<uint4 *>(dst + vec * 16) = src;
+    }
+  }
+  fence_proxy_async_global();
+  __syncwarp();
+}
+
 // ===========================================================================
 // Decode kernel
 // ===========================================================================
@@ -545,8 +599,12 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   const int kvh = blockIdx.x / p.q_groups;
   const int qg = blockIdx.x - kvh * p.q_groups;
   const bool wmode = p.warp_parts != 0;  // uniform over the grid
-  const int part = wmode ? blockIdx.y * C::NW + warp : blockIdx.y;
-  const int b = blockIdx.z;
+  // grid (kv head group, partition, sequence); with warp-owned partitions
+  // (kv head group, sequence, row of 4 partitions), so that every
+  // sequence's first rows launch before any sequence's last
+  const int prow = wmode ? blockIdx.z : blockIdx.y;
+  const int part = wmode ? prow * C::NW + warp : prow;
+  const int b = wmode ? blockIdx.y : blockIdx.z;
   // this warp's blocks of the partition: j0 + i * jstep
   const int j_off = wmode ? 0 : warp, jstep = wmode ? 1 : C::NW;
 
@@ -638,6 +696,26 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   st.reset();
   int issued = 0;
   const int pre = min(C::STAGES, my_n);
+  // Decode step: the warp that reads the new token's block (the last block
+  // of the sequence's last partition) writes the token first.  Its copies
+  // of earlier blocks go out before the write, the copy of that block after.
+  const bool writer = p.k_new != nullptr && part == nparts - 1 && my_n > 0 &&
+                      (wmode || warp == (nblk - 1) % C::NW);
+  if (writer) {
+    const int pos = L - 1;
+    const int wblk = __ldg(p.block_tables + (size_t)b * p.max_blocks + (pos >> 4));
+    uint4 src = make_uint4(0u, 0u, 0u, 0u);
+    if (lane < 2 * (D / 8)) {
+      const bool is_v = lane >= D / 8;
+      const size_t row = ((size_t)b * p.num_kv_heads + kvh) * D;
+      src = __ldg(reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) + row) +
+                  (is_v ? lane - D / 8 : lane));
+    }
+    for (; issued < min(pre, my_n - 1); ++issued) issue(issued);
+    if (wblk >= 0 && wblk < p.num_blocks)
+      write_new_token<FP8, D>(p, wblk, pos & 15, kvh, src, lane);
+    // (an id outside the pool is reported when the block is issued)
+  }
   for (; issued < pre; ++issued) issue(issued);
 
   bool failed = false;
@@ -1156,7 +1234,11 @@ pkv_status launch_decode(const CUtensorMap &mk, const CUtensorMap &mv, const Dec
     }
   }
   const int grid_y = p.warp_parts ? (p.grid_parts + C::NW - 1) / C::NW : p.grid_parts;
-  dim3 grid(p.num_kv_heads * p.q_groups, grid_y, p.batch);
+  // partition-row-major launch order for warp-owned partitions: 512-token
+  // partitions on the long-context step 412.6 -> 405.7 us; sequence-major
+  // for CTA-shared partitions (Llama-8B step 95.9 vs 97.9 us part-major)
+  dim3 grid = p.warp_parts ? dim3(p.num_kv_heads * p.q_groups, p.batch, grid_y)
+                           : dim3(p.num_kv_heads * p.q_groups, grid_y, p.batch);
   if (launch_pdl(paged_decode_kernel<FP8, D, NW, RING_KB>, grid, dim3(C::NW * 32), C::SMEM_BYTES, s,
                  mk, mv, p) != cudaSuccess)
     return PKV_ERR_CUDA;
@@ -1208,13 +1290,15 @@ extern "C" size_t paged_attention_workspace_bytes(int32_t batch, int32_t num_hea
   return part_layout(batch, num_heads, num_kv_heads, head_dim, parts).bytes;
 }
 
-extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cache,
-                                             const int32_t *block_tables, int32_t max_blocks,
-                                             const int32_t *seq_lens, int32_t batch,
-                                             int32_t num_heads, float scale, void *out,
-                                             int32_t max_seq_len, int32_t partition_tokens,
-                                             void *workspace, size_t workspace_bytes,
-                                             void *stream) {
+namespace {
+
+// paged_attention_decode, and with k_new / v_new the decode step (see
+// DecodeParams::k_new).
+pkv_status decode_entry(const void *q, const void *k_new, const void *v_new,
+                        const pkv_cache *cache, const int32_t *block_tables, int32_t max_blocks,
+                        const int32_t *seq_lens, int32_t batch, int32_t num_heads, float scale,
+                        void *out, int32_t max_seq_len, int32_t partition_tokens,
+                        void *workspace, size_t workspace_bytes, void *stream) {
   pkv_status st = validate_cache(cache);
   if (st != PKV_OK) return st;
   if (batch < 0 || num_heads <= 0 || max_blocks <= 0 || max_seq_len < 0 ||
@@ -1234,7 +1318,7 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
                                                       max_seq_len, partition_tokens);
   if (pt <= 0) return PKV_ERR_ARG;
   const int64_t parts64 = std::max<int64_t>(1, ((int64_t)max_seq_len + pt - 1) / pt);
-  if (parts64 > 65535) return PKV_ERR_ARG;  // grid.y
+  if (parts64 > 65535) return PKV_ERR_ARG;  // grid.y or grid.z
 
   DecodeParams p;
   std::memset(&p, 0, sizeof p);
@@ -1274,6 +1358,13 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
   p.scale_log2 = scale * 1.4426950408889634f * (fp8 ? cache->k_scale : 1.f);
   p.v_scale = fp8 ? cache->v_scale : 1.f;
   p.timeout_ns = 2000000000ull;
+  if (k_new) {
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    p.k_cache = static_cast<uint8_t *>(cache->key_cache);
+    p.v_cache = static_cast<uint8_t *>(cache->value_cache);
+    p.k_scale = fp8 ? cache->k_scale : 1.f;
+  }
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (fp8)
@@ -1281,6 +1372,34 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
                                   : launch_decode<true, 64>(mk, mv, p, s);
   return cache->head_dim == 128 ? launch_decode<false, 128>(mk, mv, p, s)
                                 : launch_decode<false, 64>(mk, mv, p, s);
+}
+
+}  // namespace
+
+extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cache,
+                                             const int32_t *block_tables, int32_t max_blocks,
+                                             const int32_t *seq_lens, int32_t batch,
+                                             int32_t num_heads, float scale, void *out,
+                                             int32_t max_seq_len, int32_t partition_tokens,
+                                             void *workspace, size_t workspace_bytes,
+                                             void *stream) {
+  return decode_entry(q, nullptr, nullptr, cache, block_tables, max_blocks, seq_lens, batch,
+                      num_heads, scale, out, max_seq_len, partition_tokens, workspace,
+                      workspace_bytes, stream);
+}
+
+extern "C" pkv_status paged_attention_decode_step(
+    const void *q, const void *k_new, const void *v_new, const pkv_cache *cache,
+    const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens, int32_t batch,
+    int32_t num_heads, float scale, void *out, int32_t max_seq_len, int32_t partition_tokens,
+    void *workspace, size_t workspace_bytes, void *stream) {
+  if (batch > 0 && (!k_new || !v_new ||
+                    ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) &
+                     15)))
+    return PKV_ERR_ARG;
+  return decode_entry(q, batch > 0 ? k_new : nullptr, v_new, cache, block_tables, max_blocks,
+                      seq_lens, batch, num_heads, scale, out, max_seq_len, partition_tokens,
+                      workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -312,6 +312,32 @@ def paged_attention_decode(q: torch.Tensor, cache: PagedKVCache,
     """Decode attention: q [B, Hq, d] bf16, block_tables int32 [B,
     max_blocks], seq_lens int32 [B] (device), max_seq_len a host bound of
     seq_lens.  Returns out [B, Hq, d] bf16."""
+    return _decode("paged_attention_decode", q, None, None, cache,
+                   block_tables, seq_lens, scale, max_seq_len, out,
+                   partition_tokens, workspace, stream)
+
+
+def paged_attention_decode_step(q: torch.Tensor, k_new: torch.Tensor,
+                                v_new: torch.Tensor, cache: PagedKVCache,
+                                block_tables: torch.Tensor,
+                                seq_lens: torch.Tensor, scale: float,
+                                max_seq_len: int,
+                                out: Optional[torch.Tensor] = None,
+                                partition_tokens: int = 0,
+                                workspace: Optional[torch.Tensor] = None,
+                                stream: Optional[torch.cuda.Stream] = None
+                                ) -> torch.Tensor:
+    """One decode step: k_new / v_new [B, Hkv, d] bf16, the K and V of
+    each sequence's new token at position seq_lens[b] - 1, are written into
+    the cache (zeroing the rest of a block the token opens), then attention
+    as paged_attention_decode.  Returns out [B, Hq, d] bf16."""
+    return _decode("paged_attention_decode_step", q, k_new, v_new, cache,
+                   block_tables, seq_lens, scale, max_seq_len, out,
+                   partition_tokens, workspace, stream)
+
+
+def _decode(name, q, k_new, v_new, cache, block_tables, seq_lens, scale,
+            max_seq_len, out, partition_tokens, workspace, stream):
     dev = cache.device
     _require(q, "q", torch.bfloat16, dev, 3)
     _require(block_tables, "block_tables", torch.int32, dev, 2)
@@ -334,12 +360,20 @@ def paged_attention_decode(q: torch.Tensor, cache: PagedKVCache,
             workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         _require(workspace, "workspace", torch.uint8, dev, 1)
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
-    st = _native.lib().paged_attention_decode(
-        q.data_ptr(), ctypes.byref(cache.c_struct()), block_tables.data_ptr(),
-        block_tables.shape[1], seq_lens.data_ptr(), B, Hq, float(scale),
-        out.data_ptr(), int(max_seq_len), int(partition_tokens), ws_ptr,
-        ws_bytes, _stream_handle(stream, dev))
-    _native.check("paged_attention_decode", st)
+    common = (ctypes.byref(cache.c_struct()), block_tables.data_ptr(),
+              block_tables.shape[1], seq_lens.data_ptr(), B, Hq, float(scale),
+              out.data_ptr(), int(max_seq_len), int(partition_tokens), ws_ptr,
+              ws_bytes, _stream_handle(stream, dev))
+    if k_new is None:
+        st = _native.lib().paged_attention_decode(q.data_ptr(), *common)
+    else:
+        for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+            _require(t, n, torch.bfloat16, dev, 3)
+            if t.shape != (B, cache.num_kv_heads, d):
+                raise ValueError(f"{n} must be [batch, num_kv_heads, head_dim]")
+        st = _native.lib().paged_attention_decode_step(
+            q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), *common)
+    _native.check(name, st)
     return out
 
 

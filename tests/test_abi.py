@@ -125,6 +125,22 @@ def test_cascade_argument_validation(lib):
     assert call(batch=0) == 0                # empty batch: nothing to do
 
 
+def test_decode_step_argument_validation(lib):
+    """The decode step rejects a missing or unaligned new-token buffer on
+    the host, before any CUDA call, and treats an empty batch as a no-op."""
+    c = _cache()
+
+    def call(k=16, v=16, batch=2):
+        return lib.paged_attention_decode_step(16, k, v, ctypes.byref(c), 16, 8, 16, batch, 4,
+                                               0.1, 16, 128, 0, None, 0, None)
+
+    assert call(k=None) == 1
+    assert call(v=None) == 1
+    assert call(k=24) == 1
+    assert call(v=8) == 1
+    assert call(batch=0) == 0
+
+
 def test_prefill_argument_validation(lib):
     """Chunked prefill rejects bad arguments on the host, before any CUDA
     call, and treats an empty step as a no-op."""

@@ -51,7 +51,7 @@ def test_result_does_not_depend_on_workspace_contents(make, pt):
     assert need > 0
     first = None
     for name, ws in _fills(need, seed=pt):
-        for rep in range(2):  # the second call finds the tickets this call left
+        for rep in range(2):  # the second call finds the partials this call left
             got = _decode(W, G, pt, ws)
             if first is None:
                 first = got.clone()
@@ -63,7 +63,7 @@ def test_result_does_not_depend_on_workspace_contents(make, pt):
 
 def test_workspace_reused_across_layouts():
     """One buffer used by calls of different batch size and partition
-    length: each call's partials and tickets land at other offsets than the
+    length: each call's partials land at other offsets than the
     previous call's, so every call starts on another call's leftovers."""
     W = wl.llama8b_gqa(small=True)
     G = harness.upload(W)
