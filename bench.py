@@ -52,7 +52,8 @@ DECODE_PROFILES = {
     ("long_context", 512): ROOT / "profiles" / "paged_decode_kernel_long_context_p512.md",
 }
 KERNEL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_decode.cu",
-                  "paged_kv_cache_48_gb300/csrc/pkv_device.cuh"]
+                  "paged_kv_cache_48_gb300/csrc/pkv_device.cuh",
+                  "paged_kv_cache_48_gb300/csrc/e4m3_encode.cuh"]
 PREFILL_PROFILE = ROOT / "profiles" / "paged_prefill_kernel_chunked_prefill_8k.md"
 PREFILL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_prefill.cu",
                    "paged_kv_cache_48_gb300/csrc/tcgen05.cuh",
