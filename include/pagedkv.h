@@ -236,7 +236,9 @@ pkv_status paged_attention_decode(const void *q, const pkv_cache *cache,
  * paged_kv_zero_and_write would leave with that block listed as fresh and
  * the token's slot in slot_mapping, and the output equals that of
  * paged_attention_decode on that cache bit for bit.  A table entry outside
- * the pool writes nothing and is reported by pkv_check().  The write is
+ * the pool, or a length above max_seq_len or the table's width (attended
+ * clamped, as by paged_attention_decode), writes nothing and is reported by
+ * pkv_check().  The write is
  * done inside the decode kernel, by the warp that reads the token's block,
  * so no separate write launch precedes the attention.  Only the new
  * token's block and row are written: blocks recycled with stale rows that

@@ -644,12 +644,14 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   // ---- sequence extent and this CTA's partition --------------------------
   int L = __ldg(p.seq_lens + b);
+  bool len_ok = true;  // (a clamped length writes no new token)
   {
     const int cap = min(p.max_blocks * 16, p.max_seq_len);
     if (L < 0 || L > cap) {
       if (part == 0 && blockIdx.x == 0 && threadIdx.x == 0)
         record_error(&g_err_attention, PKV_ERR_RANGE, b);
       L = clamp_len(L, cap);
+      len_ok = false;
     }
   }
   const int start =
@@ -699,7 +701,7 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   // Decode step: the warp that reads the new token's block (the last block
   // of the sequence's last partition) writes the token first.  Its copies
   // of earlier blocks go out before the write, the copy of that block after.
-  const bool writer = p.k_new != nullptr && part == nparts - 1 && my_n > 0 &&
+  const bool writer = p.k_new != nullptr && len_ok && part == nparts - 1 && my_n > 0 &&
                       (wmode || warp == (nblk - 1) % C::NW);
   if (writer) {
     const int pos = L - 1;

@@ -11,7 +11,8 @@ oracle's cache (byte-exact) and attention (|gpu - ref| <= 1e-2 + 1e-2
 |ref|, 3e-2 for an E4M3 cache).  Cases span bf16 and E4M3 caches, head_dim
 64 and 128, group sizes 1, 4, 5 and 8, CTA-shared and warp-owned
 partitions, tokens that open a block and tokens that do not, an empty
-sequence, and a table entry outside the pool.
+sequence, a table entry outside the pool and a length above the host
+bound.
 """
 import numpy as np
 import pytest
@@ -19,7 +20,8 @@ import torch
 
 import harness
 from paged_kv_cache_48_gb300 import (paged_attention_decode,
-                                     paged_attention_decode_step, pkv_check)
+                                     paged_attention_decode_step,
+                                     paged_kv_zero_and_write, pkv_check)
 from paged_kv_cache_48_gb300 import workload as wl
 
 pytestmark = pytest.mark.gpu
@@ -141,7 +143,6 @@ def test_step_bad_block_id_writes_nothing_and_is_reported():
     # the reference: the same step without sequence 1's write
     A = harness.upload(W)
     keep = np.array([s // 16 != int(W.block_tables[1, (L1 - 1) // 16]) for s in W.step_slots])
-    from paged_kv_cache_48_gb300 import paged_kv_zero_and_write
     fresh = np.array([f for f in W.fresh_blocks if f != int(W.block_tables[1, (L1 - 1) // 16])],
                      np.int32)
     idx = torch.from_numpy(np.nonzero(keep)[0]).cuda()
@@ -155,6 +156,27 @@ def test_step_bad_block_id_writes_nothing_and_is_reported():
     rows = [0, 2, 3]
     assert torch.equal(out[rows], ref[rows])
     assert not np.array_equal(before_k, kb)  # the other sequences did write
+
+
+def test_step_length_above_bound_writes_nothing():
+    """A length above max_seq_len is attended clamped and reported, and its
+    new token is not written: nothing lands at the clamped position."""
+    W = wl.make_workload("longer", 2, 32, 8, 128, 0, 0, 29, seq_lens=[40, 100])
+    G = harness.upload(W)
+    _step(W, G, 0, max_seq_len=64)
+    st, detail = pkv_check()
+    assert st == PKV_ERR_RANGE and detail == 1
+    # the reference: sequence 0's token alone (neither token opens a block)
+    A = harness.upload(W)
+    s0 = int(W.block_tables[0, 39 // 16]) * 16 + 39 % 16
+    i0 = W.step_slots.tolist().index(s0)
+    paged_kv_zero_and_write(A.step_k[i0:i0 + 1].contiguous(), A.step_v[i0:i0 + 1].contiguous(),
+                            A.step_slots[i0:i0 + 1].contiguous(), A.cache,
+                            np.zeros(0, np.int32))
+    assert pkv_check()[0] == PKV_OK
+    ka, va = _caches(A)
+    kb, vb = _caches(G)
+    assert np.array_equal(ka, kb) and np.array_equal(va, vb)
 
 
 @pytest.mark.parametrize("pt", [0, 512])

@@ -14,6 +14,7 @@ import torch
 import harness
 from paged_kv_cache_48_gb300 import (paged_attention_decode,
                                      paged_attention_decode_cascade,
+                                     paged_attention_decode_step,
                                      paged_attention_prefill,
                                      paged_prepare_inputs, pkv_check)
 from paged_kv_cache_48_gb300 import workload as wl
@@ -57,6 +58,30 @@ def test_decode_step_in_graph():
     _replay_matches(lambda: paged_attention_decode(
         G.q, G.cache, G.tables, G.seq_lens, W.scale, W.max_seq_len, out=out,
         partition_tokens=64, workspace=ws), out)
+
+
+@pytest.mark.parametrize("pt", [0, 64])
+def test_one_call_decode_step_in_graph(pt):
+    """paged_attention_decode_step (the new tokens written by the decode
+    kernel) replayed from a graph: the same output, and the cache keeps the
+    oracle's bytes (the replays rewrite the same tokens)."""
+    W = wl.llama8b_gqa(small=True)
+    G = harness.upload(W)
+    slots = W.step_slots.tolist()
+    rows = [slots.index(int(W.block_tables[b, (L - 1) // 16]) * 16 + (L - 1) % 16)
+            for b, L in enumerate(W.seq_lens.tolist())]
+    idx = torch.tensor(rows, device="cuda")
+    kn, vn = G.step_k[idx].contiguous(), G.step_v[idx].contiguous()
+    out = torch.empty_like(G.q)
+    ws = torch.empty(1 << 22, dtype=torch.uint8, device="cuda")
+    _replay_matches(lambda: paged_attention_decode_step(
+        G.q, kn, vn, G.cache, G.tables, G.seq_lens, W.scale, W.max_seq_len, out=out,
+        partition_tokens=pt, workspace=ws), out)
+    kc, vc = harness.oracle_cache(W)
+    assert np.array_equal(G.cache.key_cache.view(torch.uint8).cpu().numpy().reshape(-1),
+                          kc.view(np.uint8).reshape(-1))
+    assert np.array_equal(G.cache.value_cache.view(torch.uint8).cpu().numpy().reshape(-1),
+                          vc.view(np.uint8).reshape(-1))
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
