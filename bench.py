@@ -647,7 +647,15 @@ def run_ours(args):
     value = whole_job_gbs(world, kv_bytes, ms_per_step)
     e2e_value = whole_job_gbs(world, kv_bytes, e2e_ms / K2)
     peak, peak_kind = measured_peak()
-    achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
+    # The dominant launches are the decode kernel and its merge.  When a
+    # step is one paged_attention_decode_step call (eager), the headline
+    # loop holds nothing else, so its time per step is their average
+    # duration back to back; otherwise (a separate write launch in the step,
+    # or a replayed graph) the per-call event pairs of the second loop,
+    # which also cut the programmatic overlap between calls.
+    pair_only = new_tokens is not None and not args.graph
+    roof_ms = ms_per_step if pair_only else attn_ms
+    achieved = kv_bytes / (roof_ms * 1e-3) / 1e9
     prof = DECODE_PROFILES.get((args.workload, pt), DECODE_PROFILES.get(args.workload))
     traffic = profiled_traffic(prof) if prof is not None else None
     l2 = (f"L2 flushed between steps ({kv_bytes / 1e6:.1f} MB of KV per step)"
@@ -684,11 +692,14 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": peak_kind,
                      "kernel": "paged_decode_kernel + paged_decode_merge_kernel",
-                     "launch_ms": round(attn_ms, 5),
-                     "timed_in": "a second K-step loop, one event pair around "
-                                 "each decode call and its merge"
-                                 + (" (the call writes the new tokens too)"
-                                    if new_tokens is not None else "")},
+                     "launch_ms": round(roof_ms, 5),
+                     "timed_in": ("the headline K-step loop (events around the "
+                                  "loop); each step is one decode kernel, which "
+                                  "also writes the new tokens, and one merge"
+                                  if pair_only else
+                                  "a second K-step loop, one event pair around "
+                                  "each decode call and its merge"),
+                     "per_call_launch_ms": round(attn_ms, 5)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms / K2, 5), "steps": K2,
                 "untimed_steps_before": E2E_WARM,
