@@ -9,7 +9,7 @@ opened blocks listed as fresh, and give bit for bit the output of
 paged_attention_decode on that cache; both are checked against the
 oracle's cache (byte-exact) and attention (|gpu - ref| <= 1e-2 + 1e-2
 |ref|, 3e-2 for an E4M3 cache).  Cases span bf16 and E4M3 caches, head_dim
-64 and 128, group sizes 1, 4, 5 and 8, CTA-shared and warp-owned
+64 and 128, group sizes 1, 4, 5, 8 and 16, CTA-shared and warp-owned
 partitions, tokens that open a block and tokens that do not, an empty
 sequence, a table entry outside the pool and a length above the host
 bound.
@@ -82,6 +82,12 @@ CASES = {
         seq_lens=[1, 17, 33, 48, 129]), 0),
     "opening_blocks_bf16": (lambda: wl.make_workload(
         "open_bf16", 6, 32, 8, 128, 0, 0, 9, seq_lens=[1, 16, 17, 513, 1024, 1025]), 0),
+    # g = 16: two query sub-groups per kv head, whose warps both write the
+    # token's (identical) bytes
+    "g16_two_writers": (lambda: wl.make_workload(
+        "g16", 4, 32, 2, 128, 0, 0, 10, seq_lens=[1, 33, 200, 700]), 0),
+    "g16_two_writers_pt64": (lambda: wl.make_workload(
+        "g16", 4, 32, 2, 128, 0, 0, 10, seq_lens=[1, 33, 200, 700]), 64),
 }
 
 
