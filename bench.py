@@ -54,7 +54,9 @@ DECODE_PROFILES = {
 KERNEL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_decode.cu",
                   "paged_kv_cache_48_gb300/csrc/pkv_device.cuh",
                   "paged_kv_cache_48_gb300/csrc/e4m3_encode.cuh"]
-PREFILL_PROFILE = ROOT / "profiles" / "paged_prefill_kernel_chunked_prefill_8k.md"
+# prefill workloads with a committed ncu summary of the prefill kernel
+PREFILL_PROFILES = {w: ROOT / "profiles" / f"paged_prefill_kernel_{w}.md"
+                    for w in ("chunked_prefill_8k", "chunked_prefill_8k_fp8", "prefill_8k")}
 PREFILL_SOURCES = ["paged_kv_cache_48_gb300/csrc/attention_prefill.cu",
                    "paged_kv_cache_48_gb300/csrc/tcgen05.cuh",
                    "paged_kv_cache_48_gb300/csrc/pkv_device.cuh"]
@@ -1045,8 +1047,8 @@ def run_prefill(args):
         "roofline": {"bound": "tensor", "achieved": round(attn_tflops, 2),
                      "peak": peak, "unit": "TFLOP/s",
                      "frac": round(attn_tflops / peak, 4),
-                     "traffic": profiled_traffic(PREFILL_PROFILE, PREFILL_SOURCES)
-                     if name == "chunked_prefill_8k" else None,
+                     "traffic": profiled_traffic(PREFILL_PROFILES[name], PREFILL_SOURCES)
+                     if name in PREFILL_PROFILES else None,
                      "peak_kind": peak_kind + " bf16 burst",
                      "kernel_ms": round(attn_ms, 4)},
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 2),

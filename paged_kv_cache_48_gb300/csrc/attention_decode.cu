@@ -26,9 +26,17 @@
 // sequence split into several partitions writes (max, sum, output)
 // partials that a second kernel merges with a log-sum-exp reduce (one warp
 // per output row, launched with programmatic dependent launch so that it is
-// resident before the decode kernel ends).  Every reduction has a fixed
-// order, so results are bitwise deterministic and independent of where
-// blocks sit in the pool.
+// resident before the decode kernel ends; one CTA per row when a row may
+// hold more than 8 partitions).  Every reduction has a fixed order, so
+// results are bitwise deterministic and independent of where blocks sit in
+// the pool.
+//
+// Also here: the decode step in one call (each sequence's new token written
+// into the cache by the warp that reads its block, before that block's
+// copy; vLLM concept page, "15 分钟专家深入" item 2, and the v0.17.1 notes'
+// zeroing of a freshly allocated block), and the host side of shared-prefix
+// (cascade) decode: the tensor-core prefix pass (attention_prefill.cu), this
+// kernel over each sequence's own tokens launched beside it, and the merge.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
