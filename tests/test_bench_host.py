@@ -1,6 +1,7 @@
 """Host-side pieces of bench.py, on CPU: the reference arm's JSON line (the
 oracle timed on the host cores), the buffer packing of a step's inputs, the
-profile lookup that supplies roofline traffic, and the host CPU name."""
+profile lookup that supplies roofline traffic, the host CPU name, and the
+choice of the one-call decode step."""
 import json
 import subprocess
 import sys
@@ -93,3 +94,23 @@ def test_reference_arm_other_ranks_exit_without_work():
                        capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
     assert not [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+
+
+def test_one_call_step_is_chosen_only_for_new_token_steps():
+    """bench.py runs a step as one paged_attention_decode_step call exactly
+    when the step's writes are the sequences' new tokens and its fresh blocks
+    are the blocks those tokens open: the rows it picks are those tokens, in
+    sequence order; the recycled-block workload keeps the two-call step."""
+    from paged_kv_cache_48_gb300 import workload as wl
+    W = wl.llama8b_gqa(small=True)
+    rows = bench.new_token_rows(W)
+    assert rows is not None and len(rows) == W.batch
+    for b, i in enumerate(rows):
+        L = int(W.seq_lens[b])
+        assert W.step_slots[i] == W.block_tables[b, (L - 1) // 16] * 16 + (L - 1) % 16
+    assert bench.new_token_rows(wl.fp8_recycle(small=True)) is None
+    # a sequence without a token, or an extra fresh block, falls back too
+    W0 = wl.make_workload("empty", 3, 8, 8, 64, 0, 0, 1, seq_lens=[0, 5, 9])
+    assert bench.new_token_rows(W0) is None
+    W.fresh_blocks = np.append(W.fresh_blocks, np.int32(W.num_blocks - 1))
+    assert bench.new_token_rows(W) is None
