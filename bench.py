@@ -122,30 +122,6 @@ def whole_job_gbs(world: int, bytes_per_rank: int, ms_per_step: float) -> float:
     return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
-def new_token_rows(W):
-    """Rows of the step's writes holding each sequence's new token (position
-    seq_lens[b] - 1), in sequence order, when those are the step's only
-    writes and the only fresh blocks are blocks the new tokens open; else
-    None."""
-    import numpy as np
-    pos = {int(s): i for i, s in enumerate(W.step_slots)}
-    rows, opened = [], set()
-    for b in range(W.batch):
-        L = int(W.seq_lens[b])
-        if L == 0:
-            return None  # (a sequence without a new token has no row)
-        blk = int(W.block_tables[b, (L - 1) // 16])
-        i = pos.get(blk * 16 + (L - 1) % 16)
-        if i is None:
-            return None
-        rows.append(i)
-        if (L - 1) % 16 == 0:
-            opened.add(blk)
-    if len(rows) != W.step_slots.size or set(int(f) for f in W.fresh_blocks) != opened:
-        return None
-    return np.asarray(rows)
-
-
 def kernel_sha(sources=None) -> str:
     h = hashlib.sha256()
     for rel in sources or KERNEL_SOURCES:
@@ -427,14 +403,21 @@ def run_ours(args):
     q = bf(W.q).to(dev)
     tables = torch.from_numpy(W.block_tables).to(dev)
     lens = torch.from_numpy(W.seq_lens).to(dev)
-    new_tokens = None if args.two_call_step else new_token_rows(W)
+    new_tokens = None if args.two_call_step else W.new_token_tail()
+    if new_tokens is not None and not np.all(np.diff(new_tokens[1]) == 1):
+        # Several new tokens a sequence (the fp8 workload rewrites each
+        # sequence's last four or five blocks): one call was measured about
+        # 1% slower than the separate write launch there, since the decode
+        # warps' encoding sits on their streams' critical path.
+        new_tokens = None
     if new_tokens is not None:
-        # every write of the step is a sequence's new token, and the only
-        # fresh blocks are the blocks those tokens open: the step is one
+        # every sequence's one write is its new token, and the fresh blocks
+        # are the blocks those tokens open: the step is one
         # paged_attention_decode_step call (the write inside the decode
         # kernel)
-        sk, sv = bf(W.step_k[new_tokens]).to(dev), bf(W.step_v[new_tokens]).to(dev)
-        slots = torch.empty(0, dtype=torch.int64, device=dev)
+        rows, _ = new_tokens
+        sk, sv = bf(W.step_k[rows]).to(dev), bf(W.step_v[rows]).to(dev)
+        slots = torch.empty(0, dtype=torch.int32, device=dev)
         fresh = np.zeros(0, dtype=np.int32)
     else:
         sk, sv = bf(W.step_k).to(dev), bf(W.step_v).to(dev)
@@ -456,8 +439,7 @@ def run_ours(args):
     # tokens), the decode kernel and the merge of split sequences (when a
     # sequence can be split)
     split = -(-max_len // pt) > 1
-    launches_per_step = (1 if fresh.size or slots.numel() else 0) \
-        + 1 + (1 if split else 0)
+    launches_per_step = (0 if new_tokens is not None else 1) + 1 + (1 if split else 0)
     kv_bytes = W.kv_read_bytes()
     # Workloads whose KV fits in twice the L2 are timed step by step with an
     # L2 flush (a 512 MiB write) between steps, outside the timed events.

@@ -216,35 +216,41 @@ pkv_status paged_attention_decode(const void *q, const pkv_cache *cache,
                                   int32_t partition_tokens, void *workspace,
                                   size_t workspace_bytes, void *stream);
 
-/* One decode step in one call: each sequence's new token is written into
+/* One decode step in one call: each sequence's new tokens are written into
  * the cache, then every sequence is attended as by paged_attention_decode.
  * Source: vLLM concept page (compassingai.com), "15 分钟专家深入" item 2
  * (a new token's K/V goes to the block its table names, allocated on
  * demand), vLLM v0.17.1 notes (admirer.cn), "修复方案" (a freshly allocated
  * block is zeroed before attention reads it), and the "技术原理" pseudocode
  * for the attention; the fusion is this library's.
- *   k_new, v_new  bf16 [batch, num_kv_heads, head_dim] (device, 16-byte
- *                 aligned): the K and V of each sequence's new token, whose
- *                 position is seq_lens[b] - 1 (seq_lens counts it).
+ *   k_new, v_new  bf16 [num_new_tokens, num_kv_heads, head_dim] (device,
+ *                 16-byte aligned): the new tokens' K and V.
+ *   new_start_loc int32 [batch + 1] (device) or NULL: sequence b's new
+ *                 tokens are rows new_start_loc[b] .. new_start_loc[b+1] - 1,
+ *                 at its last n_b positions L - n_b .. L - 1 (L =
+ *                 seq_lens[b], which counts them).  NULL: one new token per
+ *                 sequence, row b (num_new_tokens must equal batch).
  *   Other arguments, the workspace and the result as for
  *   paged_attention_decode.
- * For every sequence with seq_lens[b] >= 1, the token goes to row
- * (L - 1) % 16 of block block_tables[b][(L - 1) / 16], E4M3-encoded as by
- * paged_kv_write for an fp8 cache.  When the token opens its block
- * ((L - 1) % 16 == 0, a block allocated for this step) the block's other
- * 15 rows of K and V are zeroed first.  The cache then holds the bytes that
- * paged_kv_zero_and_write would leave with that block listed as fresh and
- * the token's slot in slot_mapping, and the output equals that of
- * paged_attention_decode on that cache bit for bit.  A table entry outside
- * the pool, or a length above max_seq_len or the table's width (attended
- * clamped, as by paged_attention_decode), writes nothing and is reported by
- * pkv_check().  The write is
- * done inside the decode kernel, by the warp that reads the token's block,
- * so no separate write launch precedes the attention.  Only the new
- * token's block and row are written: blocks recycled with stale rows that
- * the step does not overwrite need paged_kv_zero_and_write. */
+ * Position t of sequence b goes to row t % 16 of block
+ * block_tables[b][t / 16], E4M3-encoded as by paged_kv_write for an fp8
+ * cache.  A block whose first position is one of the new tokens is a block
+ * allocated for this step: its rows past L are zeroed (rows of earlier
+ * positions in the block holding L - n_b are left as they are).  The cache
+ * then holds the bytes that paged_kv_zero_and_write would leave with those
+ * blocks listed as fresh and the new tokens' slots in slot_mapping, and the
+ * output equals that of paged_attention_decode on that cache bit for bit.
+ * A table entry outside the pool writes nothing for that block; a length
+ * above max_seq_len or the table's width (attended clamped, as by
+ * paged_attention_decode), n_b < 0, n_b > L or rows past num_new_tokens
+ * write nothing for the sequence; each is reported by pkv_check().  The
+ * writes are done inside the decode kernel, by the warps that read the
+ * blocks, so no separate write launch precedes the attention.  Stale rows
+ * of blocks the new tokens do not reach need paged_kv_zero_and_write. */
 pkv_status paged_attention_decode_step(const void *q, const void *k_new,
                                        const void *v_new,
+                                       const int32_t *new_start_loc,
+                                       int64_t num_new_tokens,
                                        const pkv_cache *cache,
                                        const int32_t *block_tables,
                                        int32_t max_blocks,

@@ -63,9 +63,9 @@ _SIGNATURES = {
         ctypes.c_int32, ctypes.c_float, _P, ctypes.c_int32, ctypes.c_int32,
         _P, ctypes.c_size_t, _P]),
     "paged_attention_decode_step": (ctypes.c_int, [
-        _P, _P, _P, ctypes.POINTER(PkvCache), _P, ctypes.c_int32, _P,
-        ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P, ctypes.c_int32,
-        ctypes.c_int32, _P, ctypes.c_size_t, _P]),
+        _P, _P, _P, _P, ctypes.c_int64, ctypes.POINTER(PkvCache), _P,
+        ctypes.c_int32, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _P,
+        ctypes.c_int32, ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "paged_attention_prefill": (ctypes.c_int, [
         _P, ctypes.POINTER(PkvCache), _P, ctypes.c_int32, _P, _P,
         ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, _P,

@@ -98,13 +98,17 @@ struct DecodeParams {
   // grid does not complete, and the merge after it does not start, before
   // the prefix partials are written.
   int32_t defer_dep_wait;
-  // Decode step (k_new != nullptr): sequence b's new token, at position
-  // seq_lens[b] - 1, is written into the cache before it is attended:
-  // k_new / v_new [B, Hkv, D] bf16, the cache bases and k_scale for the
-  // E4M3 encode (v_scale above).  When the token opens its block (position
-  // a multiple of 16) the block's other rows are zeroed first.  The warp
-  // that reads the token's block writes its kv head's rows of it.
+  // Decode step (k_new != nullptr): sequence b's new tokens, the last n_b
+  // of its seq_lens[b] positions, are written into the cache before they
+  // are attended: k_new / v_new [num_new, Hkv, D] bf16 rows
+  // new_start_loc[b] .. new_start_loc[b+1] - 1 (without new_start_loc, one
+  // token per sequence, row b), the cache bases and k_scale for the E4M3
+  // encode (v_scale above).  A block whose first position is a new token
+  // was allocated for this step: its rows past the sequence are zeroed.
+  // Each warp writes its kv head's rows of the blocks it reads.
   const __nv_bfloat16 *k_new, *v_new;
+  const int32_t *new_start_loc;
+  long long num_new;
   uint8_t *k_cache, *v_cache;
   float k_scale;
 };
@@ -541,48 +545,67 @@ __device__ __forceinline__ void issue_block(uint8_t *stage, uint64_t *bar,
   tma_load_5d(stage + C::TILE_BYTES, tv, bar, 0, 0, kvh, 0, phys, policy);
 }
 
-// Generic-proxy global stores made visible to the async proxy (TMA) of the
-// warp's later copies.
+// Generic-proxy global stores of this thread ordered before the async
+// proxy's (TMA) later accesses to them: each writing lane runs this, then the
+// warp synchronises, then lane 0 issues the copy.
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Decode step: the warp's part of writing sequence b's new token into block
-// `blk`, row `off`, of kv head kvh (see DecodeParams::k_new).  src is this
-// lane's 16 bytes of the token's K row (lanes 0 .. D/8 - 1) or V row (the
-// next D/8 lanes).  When off == 0 the block's rows 1 .. 15 of this head are
-// zeroed too (the other heads' rows by their own warps).  Ends with the
-// proxy fence: a TMA copy of the block issued by this warp afterwards reads
-// the new bytes.
+// Decode step: the warp's part of sequence b's new tokens in block j
+// (physical id blk) of kv head kvh: the rows of new positions (w0 .. L - 1)
+// get the tokens' K and V (position t from token row src0 + t - w0), and a
+// block that opens at or after w0 has its rows past L zeroed; rows before
+// w0 are left alone.  Loads go out eight 16-byte vectors a lane at a time
+// before their stores.  The caller fences (fence_proxy_async_global) before
+// the warp's TMA copy of the block.
 template <bool FP8, int D>
-__device__ __forceinline__ void write_new_token(const DecodeParams &p, int blk, int off, int kvh,
-                                                const uint4 &src, int lane) {
+__device__ __forceinline__ void write_new_rows(const DecodeParams &p, int blk, int j, int w0,
+                                               int L, long long src0, int kvh, int lane) {
   constexpr int ELT = FP8 ? 1 : 2;
-  constexpr int CH = D * ELT / 16;  // 16-byte chunks of one head's row
+  constexpr int VPR = D / 8;  // 8-element vectors of one head's row
+  constexpr int ITEMS_PER_ROW = 2 * VPR;  // K and V
+  constexpr int BATCH = 8;
   const size_t row_bytes = (size_t)p.num_kv_heads * D * ELT;
-  const size_t head0 = (size_t)blk * 16 * row_bytes + (size_t)kvh * D * ELT;
-  uint8_t *kc = p.k_cache + head0, *vc = p.v_cache + head0;
-  if (off == 0) {
-    for (int idx = lane; idx < 2 * 15 * CH; idx += 32) {
-      const int rem = idx % (15 * CH);
-      uint8_t *base = idx < 15 * CH ? kc : vc;
-      *reinterpret_cast<uint4 *>(base + (size_t)(1 + rem / CH) * row_bytes + (rem % CH) * 16) =
-          make_uint4(0u, 0u, 0u, 0u);
+  uint8_t *kc = p.k_cache + (size_t)blk * 16 * row_bytes + (size_t)kvh * D * ELT;
+  uint8_t *vc = p.v_cache + (size_t)blk * 16 * row_bytes + (size_t)kvh * D * ELT;
+  const int t0 = 16 * j;
+  const int r_lo = max(0, w0 - t0);        // first row written
+  const int r_hi = min(16, L - t0);        // one past the last row written
+  const int r_end = t0 >= w0 ? 16 : r_hi;  // and then the zeroed rows
+  const int items = (r_end - r_lo) * ITEMS_PER_ROW;
+  const E4m3Recip kr = e4m3_recip(p.k_scale), vr = e4m3_recip(p.v_scale);
+  for (int base = 0; base < items; base += 32 * BATCH) {
+    uint4 src[BATCH];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int idx = base + u * 32 + lane;
+      const int r = r_lo + idx / ITEMS_PER_ROW, rem = idx % ITEMS_PER_ROW;
+      const bool is_v = rem >= VPR;
+      src[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (idx < items && r < r_hi) {
+        const long long tok = src0 + (t0 + r - w0);
+        src[u] = __ldg(reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) +
+                                                       ((size_t)tok * p.num_kv_heads + kvh) * D) +
+                       (is_v ? rem - VPR : rem));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int idx = base + u * 32 + lane;
+      if (idx >= items) break;
+      const int r = r_lo + idx / ITEMS_PER_ROW, rem = idx % ITEMS_PER_ROW;
+      const bool is_v = rem >= VPR;
+      uint8_t *dst = (is_v ? vc : kc) + (size_t)r * row_bytes + (is_v ? rem - VPR : rem) * 8 * ELT;
+      if constexpr (FP8) {
+        *reinterpret_cast<uint2 *>(dst) =
+            r < r_hi ? quant8_e4m3(src[u], is_v ? p.v_scale : p.k_scale, is_v ? vr : kr)
+                     : make_uint2(0u, 0u);
+      } else {
+        *reinterpret_cast<uint4 *>(dst) = src[u];  // zero past r_hi
+      }
     }
   }
-  if (lane < 2 * (D / 8)) {
-    const bool is_v = lane >= D / 8;
-    const int vec = is_v ? lane - D / 8 : lane;  // 8 elements
-    uint8_t *dst = (is_v ? vc : kc) + (size_t)off * row_bytes;
-    if constexpr (FP8) {
-      const float scale = is_v ? p.v_scale : p.k_scale;
-      *reinterpret_cast<uint2 *>(dst + vec * 8) = quant8_e4m3(src, scale, e4m3_recip(scale));
-    } else {
-      *reinterpret_cast<uint4 *>(dst + vec * 16) = src;
-    }
-  }
-  fence_proxy_async_global();
-  __syncwarp();
 }
 
 // ===========================================================================
@@ -652,6 +675,11 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
 
   // ---- sequence extent and this CTA's partition --------------------------
   int L = __ldg(p.seq_lens + b);
+  int nsl0 = 0, nsl1 = 0;  // decode step: the sequence's new-token rows
+  if (p.k_new != nullptr && p.new_start_loc) {
+    nsl0 = __ldg(p.new_start_loc + b);
+    nsl1 = __ldg(p.new_start_loc + b + 1);
+  }
   bool len_ok = true;  // (a clamped length writes no new token)
   {
     const int cap = min(p.max_blocks * 16, p.max_seq_len);
@@ -706,25 +734,33 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
   st.reset();
   int issued = 0;
   const int pre = min(C::STAGES, my_n);
-  // Decode step: the warp that reads the new token's block (the last block
-  // of the sequence's last partition) writes the token first.  Its copies
-  // of earlier blocks go out before the write, the copy of that block after.
-  const bool writer = p.k_new != nullptr && len_ok && part == nparts - 1 && my_n > 0 &&
-                      (wmode || warp == (nblk - 1) % C::NW);
-  if (writer) {
-    const int pos = L - 1;
-    const int wblk = __ldg(p.block_tables + (size_t)b * p.max_blocks + (pos >> 4));
-    uint4 src = make_uint4(0u, 0u, 0u, 0u);
-    if (lane < 2 * (D / 8)) {
-      const bool is_v = lane >= D / 8;
-      const size_t row = ((size_t)b * p.num_kv_heads + kvh) * D;
-      src = __ldg(reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) + row) +
-                  (is_v ? lane - D / 8 : lane));
+  // Decode step: the warp writes the new tokens of the blocks it reads (the
+  // sequence's last blocks, so its last ones) first.  Its copies of earlier
+  // blocks go out before the write, the copies of those blocks after.
+  if (p.k_new != nullptr && len_ok) {
+    // without new_start_loc: one new token per non-empty sequence, row b
+    const int n_new = p.new_start_loc ? nsl1 - nsl0 : (L > 0 ? 1 : 0);
+    const long long src0 = p.new_start_loc ? nsl0 : b;
+    const bool ok_new = n_new >= 0 && n_new <= L && nsl0 >= 0 &&
+                        (!p.new_start_loc || (long long)nsl1 <= p.num_new);
+    if (!ok_new && part == 0 && blockIdx.x == 0 && threadIdx.x == 0)
+      record_error(&g_err_attention, PKV_ERR_RANGE, b);
+    const int w0 = L - n_new;  // first new position
+    // the warp's first block at or after the one holding w0
+    const int jw = (w0 >> 4) - blk0 - j_off;
+    const int i_w = jw <= 0 ? 0 : (jw + jstep - 1) / jstep;
+    if (ok_new && n_new > 0 && my_n > 0 && i_w < my_n) {
+      for (; issued < min(pre, i_w); ++issued) issue(issued);
+      const int32_t *trow = p.block_tables + (size_t)b * p.max_blocks;
+      for (int ii = i_w; ii < my_n; ++ii) {
+        const int j = blk0 + j_off + ii * jstep;
+        const int wblk = __ldg(trow + j);
+        if (wblk >= 0 && wblk < p.num_blocks)  // (else reported when issued)
+          write_new_rows<FP8, D>(p, wblk, j, w0, L, src0, kvh, lane);
+      }
+      fence_proxy_async_global();
+      __syncwarp();
     }
-    for (; issued < min(pre, my_n - 1); ++issued) issue(issued);
-    if (wblk >= 0 && wblk < p.num_blocks)
-      write_new_token<FP8, D>(p, wblk, pos & 15, kvh, src, lane);
-    // (an id outside the pool is reported when the block is issued)
   }
   for (; issued < pre; ++issued) issue(issued);
 
@@ -1305,6 +1341,7 @@ namespace {
 // paged_attention_decode, and with k_new / v_new the decode step (see
 // DecodeParams::k_new).
 pkv_status decode_entry(const void *q, const void *k_new, const void *v_new,
+                        const int32_t *new_start_loc, int64_t num_new,
                         const pkv_cache *cache, const int32_t *block_tables, int32_t max_blocks,
                         const int32_t *seq_lens, int32_t batch, int32_t num_heads, float scale,
                         void *out, int32_t max_seq_len, int32_t partition_tokens,
@@ -1371,6 +1408,8 @@ pkv_status decode_entry(const void *q, const void *k_new, const void *v_new,
   if (k_new) {
     p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
     p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    p.new_start_loc = new_start_loc;
+    p.num_new = num_new;
     p.k_cache = static_cast<uint8_t *>(cache->key_cache);
     p.v_cache = static_cast<uint8_t *>(cache->value_cache);
     p.k_scale = fp8 ? cache->k_scale : 1.f;
@@ -1393,23 +1432,26 @@ extern "C" pkv_status paged_attention_decode(const void *q, const pkv_cache *cac
                                              int32_t max_seq_len, int32_t partition_tokens,
                                              void *workspace, size_t workspace_bytes,
                                              void *stream) {
-  return decode_entry(q, nullptr, nullptr, cache, block_tables, max_blocks, seq_lens, batch,
-                      num_heads, scale, out, max_seq_len, partition_tokens, workspace,
-                      workspace_bytes, stream);
+  return decode_entry(q, nullptr, nullptr, nullptr, 0, cache, block_tables, max_blocks,
+                      seq_lens, batch, num_heads, scale, out, max_seq_len, partition_tokens,
+                      workspace, workspace_bytes, stream);
 }
 
 extern "C" pkv_status paged_attention_decode_step(
-    const void *q, const void *k_new, const void *v_new, const pkv_cache *cache,
-    const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens, int32_t batch,
-    int32_t num_heads, float scale, void *out, int32_t max_seq_len, int32_t partition_tokens,
-    void *workspace, size_t workspace_bytes, void *stream) {
-  if (batch > 0 && (!k_new || !v_new ||
-                    ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) &
-                     15)))
+    const void *q, const void *k_new, const void *v_new, const int32_t *new_start_loc,
+    int64_t num_new_tokens, const pkv_cache *cache, const int32_t *block_tables,
+    int32_t max_blocks, const int32_t *seq_lens, int32_t batch, int32_t num_heads, float scale,
+    void *out, int32_t max_seq_len, int32_t partition_tokens, void *workspace,
+    size_t workspace_bytes, void *stream) {
+  if (num_new_tokens < 0 || (!new_start_loc && num_new_tokens != batch))
     return PKV_ERR_ARG;
-  return decode_entry(q, batch > 0 ? k_new : nullptr, v_new, cache, block_tables, max_blocks,
-                      seq_lens, batch, num_heads, scale, out, max_seq_len, partition_tokens,
-                      workspace, workspace_bytes, stream);
+  const bool any = batch > 0 && num_new_tokens > 0;
+  if (any && (!k_new || !v_new ||
+              ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15)))
+    return PKV_ERR_ARG;
+  return decode_entry(q, any ? k_new : nullptr, v_new, new_start_loc, num_new_tokens, cache,
+                      block_tables, max_blocks, seq_lens, batch, num_heads, scale, out,
+                      max_seq_len, partition_tokens, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

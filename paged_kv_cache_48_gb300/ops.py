@@ -325,19 +325,24 @@ def paged_attention_decode_step(q: torch.Tensor, k_new: torch.Tensor,
                                 out: Optional[torch.Tensor] = None,
                                 partition_tokens: int = 0,
                                 workspace: Optional[torch.Tensor] = None,
-                                stream: Optional[torch.cuda.Stream] = None
+                                stream: Optional[torch.cuda.Stream] = None,
+                                new_start_loc: Optional[torch.Tensor] = None
                                 ) -> torch.Tensor:
-    """One decode step: k_new / v_new [B, Hkv, d] bf16, the K and V of
-    each sequence's new token at position seq_lens[b] - 1, are written into
-    the cache (zeroing the rest of a block the token opens), then attention
-    as paged_attention_decode.  Returns out [B, Hq, d] bf16."""
+    """One decode step: the new tokens' K and V (k_new / v_new [N, Hkv, d]
+    bf16) are written into the cache, then attention as
+    paged_attention_decode.  Without new_start_loc, N = B and row b is
+    sequence b's token at position seq_lens[b] - 1; with it (int32 [B + 1],
+    device), rows new_start_loc[b] .. new_start_loc[b+1] - 1 are sequence
+    b's last positions.  Blocks whose first position is new have their
+    rows past the sequence zeroed.  Returns out [B, Hq, d] bf16."""
     return _decode("paged_attention_decode_step", q, k_new, v_new, cache,
                    block_tables, seq_lens, scale, max_seq_len, out,
-                   partition_tokens, workspace, stream)
+                   partition_tokens, workspace, stream, new_start_loc)
 
 
 def _decode(name, q, k_new, v_new, cache, block_tables, seq_lens, scale,
-            max_seq_len, out, partition_tokens, workspace, stream):
+            max_seq_len, out, partition_tokens, workspace, stream,
+            new_start_loc=None):
     dev = cache.device
     _require(q, "q", torch.bfloat16, dev, 3)
     _require(block_tables, "block_tables", torch.int32, dev, 2)
@@ -367,12 +372,21 @@ def _decode(name, q, k_new, v_new, cache, block_tables, seq_lens, scale,
     if k_new is None:
         st = _native.lib().paged_attention_decode(q.data_ptr(), *common)
     else:
+        n_new = k_new.shape[0] if k_new.dim() == 3 else -1
         for t, n in ((k_new, "k_new"), (v_new, "v_new")):
             _require(t, n, torch.bfloat16, dev, 3)
-            if t.shape != (B, cache.num_kv_heads, d):
-                raise ValueError(f"{n} must be [batch, num_kv_heads, head_dim]")
+            if t.shape != (n_new, cache.num_kv_heads, d):
+                raise ValueError(f"{n} must be [num_new, num_kv_heads, head_dim]")
+        nsl = None
+        if new_start_loc is not None:
+            _require(new_start_loc, "new_start_loc", torch.int32, dev, 1)
+            if new_start_loc.shape[0] != B + 1:
+                raise ValueError("new_start_loc must be [batch + 1]")
+            nsl = new_start_loc.data_ptr()
+        elif n_new != B:
+            raise ValueError("without new_start_loc, k_new holds one row per sequence")
         st = _native.lib().paged_attention_decode_step(
-            q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), *common)
+            q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), nsl, n_new, *common)
     _native.check(name, st)
     return out
 

@@ -114,6 +114,37 @@ class Workload:
     groups: list = field(default_factory=list)   # prefix-sharing groups
     seed: int = 0
 
+    def new_token_tail(self):
+        """(rows, start_loc) when the step's writes are, for every
+        sequence, its last n_b >= 1 positions, and the fresh blocks are
+        exactly the blocks whose first position is among them (the layout of
+        a decode step that appends new tokens): rows orders the step's write
+        rows sequence by sequence, position by position, and start_loc
+        (int32 [batch + 1]) delimits each sequence's rows.  Otherwise None."""
+        bs = self.block_size
+        pos = {int(s): i for i, s in enumerate(self.step_slots)}
+        rows, start, opened = [], [0], set()
+        for b in range(self.batch):
+            L = int(self.seq_lens[b])
+            t, mine = L - 1, []
+            while t >= 0:
+                i = pos.get(int(self.block_tables[b, t // bs]) * bs + t % bs)
+                if i is None:
+                    break
+                mine.append(i)
+                t -= 1
+            if not mine:
+                return None
+            w0 = t + 1
+            rows += mine[::-1]
+            start.append(len(rows))
+            for j in range(-(-w0 // bs), (L - 1) // bs + 1):
+                opened.add(int(self.block_tables[b, j]))
+        if len(rows) != self.step_slots.size or \
+                set(int(f) for f in self.fresh_blocks) != opened:
+            return None
+        return np.asarray(rows, dtype=np.int64), np.asarray(start, dtype=np.int32)
+
     @property
     def elem_bytes(self) -> int:
         return 2 if self.kv_dtype == "bf16" else 1
@@ -303,6 +334,34 @@ def make_workload(name: str, batch: int, num_heads: int, num_kv_heads: int,
         init_key=init_key, init_value=init_value, k_scale=k_scale,
         v_scale=v_scale, scale=1.0 / float(np.sqrt(head_dim)),
         refcount=pool.refcount.copy(), groups=groups, seed=seed)
+
+
+def with_step_tail(W: Workload, tails, seed: int) -> Workload:
+    """W with a different step: sequence b rewrites its last tails[b]
+    positions (at most its length) with fresh seeded values, and the fresh
+    blocks are the blocks whose first position is among them.  W's own step
+    writes that the new tails leave out move to the set-up history, so that
+    every position below seq_lens is written."""
+    from dataclasses import replace
+    bs = W.block_size
+    rng = np.random.default_rng(seed)
+    slots, fresh = [], set()
+    for b in range(W.batch):
+        L = int(W.seq_lens[b])
+        w0 = L - min(int(tails[b]), L)
+        for t in range(w0, L):
+            slots.append(int(W.block_tables[b, t // bs]) * bs + t % bs)
+        for j in range(-(-w0 // bs), (L - 1) // bs + 1 if L else 0):
+            fresh.add(int(W.block_tables[b, j]))
+    hkd = (W.num_kv_heads, W.head_dim)
+    keep = ~np.isin(W.step_slots, np.asarray(slots, dtype=np.int64))
+    return replace(W, step_k=_draw_bf16(rng, (len(slots), *hkd)),
+                   step_v=_draw_bf16(rng, (len(slots), *hkd)),
+                   step_slots=np.asarray(slots, dtype=np.int64),
+                   fresh_blocks=np.asarray(sorted(fresh), dtype=np.int32),
+                   hist_k=np.concatenate([W.hist_k, W.step_k[keep]]),
+                   hist_v=np.concatenate([W.hist_v, W.step_v[keep]]),
+                   hist_slots=np.concatenate([W.hist_slots, W.step_slots[keep]]))
 
 
 # ---------------------------------------------------------------------------

@@ -126,19 +126,23 @@ def test_cascade_argument_validation(lib):
 
 
 def test_decode_step_argument_validation(lib):
-    """The decode step rejects a missing or unaligned new-token buffer on
-    the host, before any CUDA call, and treats an empty batch as a no-op."""
+    """The decode step rejects a missing or unaligned new-token buffer and a
+    row count that does not match on the host, before any CUDA call, and
+    treats an empty batch as a no-op."""
     c = _cache()
 
-    def call(k=16, v=16, batch=2):
-        return lib.paged_attention_decode_step(16, k, v, ctypes.byref(c), 16, 8, 16, batch, 4,
-                                               0.1, 16, 128, 0, None, 0, None)
+    def call(k=16, v=16, batch=2, nsl=None, n_new=2):
+        return lib.paged_attention_decode_step(16, k, v, nsl, n_new, ctypes.byref(c), 16, 8, 16,
+                                               batch, 4, 0.1, 16, 128, 0, None, 0, None)
 
     assert call(k=None) == 1
     assert call(v=None) == 1
     assert call(k=24) == 1
     assert call(v=8) == 1
-    assert call(batch=0) == 0
+    assert call(n_new=3) == 1              # one row per sequence without new_start_loc
+    assert call(nsl=16, n_new=-1) == 1
+    assert call(nsl=16, n_new=5, k=24) == 1
+    assert call(batch=0, n_new=0) == 0
 
 
 def test_prefill_argument_validation(lib):

@@ -96,21 +96,31 @@ def test_reference_arm_other_ranks_exit_without_work():
     assert not [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
 
 
-def test_one_call_step_is_chosen_only_for_new_token_steps():
-    """bench.py runs a step as one paged_attention_decode_step call exactly
-    when the step's writes are the sequences' new tokens and its fresh blocks
-    are the blocks those tokens open: the rows it picks are those tokens, in
-    sequence order; the recycled-block workload keeps the two-call step."""
+def test_new_token_tail_layout():
+    """Workload.new_token_tail, which bench.py uses to run a step as one
+    paged_attention_decode_step call: it applies exactly when every
+    sequence's writes are its last positions and the fresh blocks are the
+    blocks that open among them, and gives those tokens in sequence and
+    position order, delimited per sequence.  The recycled-block workload
+    has that layout (its 515 blocks are the sequences' last blocks, every
+    valid slot rewritten); a sequence without a write, or a fresh block the
+    tail does not open, has not."""
     from paged_kv_cache_48_gb300 import workload as wl
     W = wl.llama8b_gqa(small=True)
-    rows = bench.new_token_rows(W)
-    assert rows is not None and len(rows) == W.batch
+    rows, start = W.new_token_tail()
+    assert list(start) == list(range(W.batch + 1))
     for b, i in enumerate(rows):
         L = int(W.seq_lens[b])
         assert W.step_slots[i] == W.block_tables[b, (L - 1) // 16] * 16 + (L - 1) % 16
-    assert bench.new_token_rows(wl.fp8_recycle(small=True)) is None
-    # a sequence without a token, or an extra fresh block, falls back too
+    R = wl.fp8_recycle(small=True)
+    rows, start = R.new_token_tail()
+    for b in range(R.batch):
+        L, n = int(R.seq_lens[b]), int(start[b + 1] - start[b])
+        assert n >= 1
+        for k, i in enumerate(rows[start[b]:start[b + 1]]):
+            t = L - n + k
+            assert R.step_slots[i] == R.block_tables[b, t // 16] * 16 + t % 16
     W0 = wl.make_workload("empty", 3, 8, 8, 64, 0, 0, 1, seq_lens=[0, 5, 9])
-    assert bench.new_token_rows(W0) is None
+    assert W0.new_token_tail() is None
     W.fresh_blocks = np.append(W.fresh_blocks, np.int32(W.num_blocks - 1))
-    assert bench.new_token_rows(W) is None
+    assert W.new_token_tail() is None

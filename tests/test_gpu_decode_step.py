@@ -12,7 +12,9 @@ oracle's cache (byte-exact) and attention (|gpu - ref| <= 1e-2 + 1e-2
 64 and 128, group sizes 1, 4, 5, 8 and 16, CTA-shared and warp-owned
 partitions, tokens that open a block and tokens that do not, an empty
 sequence, a table entry outside the pool and a length above the host
-bound.
+bound; tails of several new tokens per sequence (the fp8 recycling step,
+tails that start mid-block or at a block start and cross partitions), and
+a tail longer than its sequence.
 """
 import numpy as np
 import pytest
@@ -179,6 +181,88 @@ def test_step_length_above_bound_writes_nothing():
     paged_kv_zero_and_write(A.step_k[i0:i0 + 1].contiguous(), A.step_v[i0:i0 + 1].contiguous(),
                             A.step_slots[i0:i0 + 1].contiguous(), A.cache,
                             np.zeros(0, np.int32))
+    assert pkv_check()[0] == PKV_OK
+    ka, va = _caches(A)
+    kb, vb = _caches(G)
+    assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+
+
+def _tail_step(W, G, start_loc, pt, max_seq_len=None, tables=None):
+    """The one-call step with the step's rows as the new tokens, delimited
+    per sequence by start_loc (the rows are in sequence and position
+    order)."""
+    return paged_attention_decode_step(
+        G.q, G.step_k, G.step_v, G.cache, G.tables if tables is None else tables,
+        G.seq_lens, W.scale, max_seq_len=W.max_seq_len if max_seq_len is None else max_seq_len,
+        partition_tokens=pt,
+        new_start_loc=torch.from_numpy(np.asarray(start_loc, np.int32)).cuda())
+
+
+def _check_against_two_call(W, start_loc, pt):
+    A = harness.upload(W)
+    out_a = harness.gpu_step(W, A, partition_tokens=pt, fused=True)
+    assert pkv_check()[0] == PKV_OK
+    G = harness.upload(W)
+    out_b = _tail_step(W, G, start_loc, pt)
+    assert pkv_check()[0] == PKV_OK
+    ka, va = _caches(A)
+    kb, vb = _caches(G)
+    assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+    assert torch.equal(out_a, out_b)
+    kc, vc = harness.oracle_cache(W)
+    assert np.array_equal(kb, kc.view(np.uint8).reshape(-1))
+    assert np.array_equal(vb, vc.view(np.uint8).reshape(-1))
+    harness.assert_close(out_b.float().cpu().numpy(), harness.oracle_out(W, kc, vc),
+                         W.kv_dtype)
+
+
+@pytest.mark.parametrize("pt", [0, 64])
+def test_step_recycled_tail_fp8(pt):
+    """The fp8 recycling step (its recycled blocks are each sequence's last
+    four or five, every valid slot rewritten, the new token included) as one
+    call: each sequence's rewritten tail is its new tokens."""
+    W = wl.fp8_recycle(small=True)
+    rows, start = W.new_token_tail()
+    assert np.array_equal(rows, np.arange(W.step_slots.size))
+    _check_against_two_call(W, start, pt)
+
+
+TAILS = [1, 5, 16, 17, 20, 33, 0, 40]
+
+
+@pytest.mark.parametrize("pt,kv_dtype", [(0, "bf16"), (64, "bf16"), (32, "fp8_e4m3")])
+def test_step_tails_of_several_tokens(pt, kv_dtype):
+    """Tails of 0 to 40 tokens: starting mid-block (the block keeps its
+    earlier rows), at a block start (the block opens: rows past the sequence
+    zeroed), across several blocks and across partitions of 32 and 64
+    tokens; a sequence with no new token writes nothing."""
+    base = (wl.llama8b_gqa(small=True) if kv_dtype == "bf16" else
+            wl.make_workload("tails_fp8", 8, 32, 8, 128, 20, 700, 5, kv_dtype="fp8_e4m3"))
+    W = wl.with_step_tail(base, TAILS, seed=11)
+    start = np.concatenate([[0], np.cumsum(np.minimum(TAILS, base.seq_lens))])
+    _check_against_two_call(W, start, pt)
+
+
+def test_step_tail_longer_than_sequence_writes_nothing():
+    """A sequence whose new-token count exceeds its length is reported and
+    writes nothing; the others are written as usual."""
+    base = wl.make_workload("tail_bad", 3, 32, 8, 128, 0, 0, 31, seq_lens=[20, 40, 9])
+    W = wl.with_step_tail(base, [3, 2, 9], seed=4)
+    G = harness.upload(W)
+    # sequence 2 claims 12 new tokens (rows 5 .. 16) but holds 9 positions
+    k = torch.cat([G.step_k, G.step_k[-3:]])
+    v = torch.cat([G.step_v, G.step_v[-3:]])
+    paged_attention_decode_step(G.q, k.contiguous(), v.contiguous(), G.cache, G.tables,
+                                G.seq_lens, W.scale, W.max_seq_len,
+                                new_start_loc=torch.tensor([0, 3, 5, 17], dtype=torch.int32,
+                                                           device="cuda"))
+    st, detail = pkv_check()
+    assert st == PKV_ERR_RANGE and detail == 2
+    # the reference: the rows of sequences 0 and 1 only (their tails open
+    # no block)
+    A = harness.upload(W)
+    paged_kv_zero_and_write(A.step_k[:5].contiguous(), A.step_v[:5].contiguous(),
+                            A.step_slots[:5].contiguous(), A.cache, np.zeros(0, np.int32))
     assert pkv_check()[0] == PKV_OK
     ka, va = _caches(A)
     kb, vb = _caches(G)
