@@ -552,6 +552,45 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Decode step, one new token: the warp writes the token's K and V rows of
+// kv head kvh (token row src) to row `off` of block `blk`, and when the
+// token opens the block (off == 0) zeroes the block's other 15 rows of the
+// head.  The caller fences (fence_proxy_async_global) before the warp's TMA
+// copy of the block.
+template <bool FP8, int D>
+__device__ __forceinline__ void write_one_token(const DecodeParams &p, int blk, int off, int kvh,
+                                                long long src, int lane) {
+  constexpr int ELT = FP8 ? 1 : 2;
+  constexpr int CH = D * ELT / 16;  // 16-byte chunks of one head's row
+  const size_t row_bytes = (size_t)p.num_kv_heads * D * ELT;
+  const size_t head0 = (size_t)blk * 16 * row_bytes + (size_t)kvh * D * ELT;
+  uint8_t *kc = p.k_cache + head0, *vc = p.v_cache + head0;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  const bool is_v = lane >= D / 8;
+  const int vec = is_v ? lane - D / 8 : lane;  // 8 elements
+  if (lane < 2 * (D / 8))
+    v = __ldg(reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) +
+                                              ((size_t)src * p.num_kv_heads + kvh) * D) +
+              vec);
+  if (off == 0) {
+    for (int idx = lane; idx < 2 * 15 * CH; idx += 32) {
+      const int rem = idx % (15 * CH);
+      uint8_t *base = idx < 15 * CH ? kc : vc;
+      *reinterpret_cast<uint4 *>(base + (size_t)(1 + rem / CH) * row_bytes + (rem % CH) * 16) =
+          make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  if (lane < 2 * (D / 8)) {
+    uint8_t *dst = (is_v ? vc : kc) + (size_t)off * row_bytes;
+    if constexpr (FP8) {
+      const float scale = is_v ? p.v_scale : p.k_scale;
+      *reinterpret_cast<uint2 *>(dst + vec * 8) = quant8_e4m3(v, scale, e4m3_recip(scale));
+    } else {
+      *reinterpret_cast<uint4 *>(dst + vec * 16) = v;
+    }
+  }
+}
+
 // Decode step: the warp's part of sequence b's new tokens in block j
 // (physical id blk) of kv head kvh: the rows of new positions (w0 .. L - 1)
 // get the tokens' K and V (position t from token row src0 + t - w0), and a
@@ -752,11 +791,17 @@ paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
     if (ok_new && n_new > 0 && my_n > 0 && i_w < my_n) {
       for (; issued < min(pre, i_w); ++issued) issue(issued);
       const int32_t *trow = p.block_tables + (size_t)b * p.max_blocks;
-      for (int ii = i_w; ii < my_n; ++ii) {
-        const int j = blk0 + j_off + ii * jstep;
-        const int wblk = __ldg(trow + j);
+      if (n_new == 1) {  // the usual decode step: the last block only
+        const int wblk = __ldg(trow + (w0 >> 4));
         if (wblk >= 0 && wblk < p.num_blocks)  // (else reported when issued)
-          write_new_rows<FP8, D>(p, wblk, j, w0, L, src0, kvh, lane);
+          write_one_token<FP8, D>(p, wblk, w0 & 15, kvh, src0, lane);
+      } else {
+        for (int ii = i_w; ii < my_n; ++ii) {
+          const int j = blk0 + j_off + ii * jstep;
+          const int wblk = __ldg(trow + j);
+          if (wblk >= 0 && wblk < p.num_blocks)  // (else reported when issued)
+            write_new_rows<FP8, D>(p, wblk, j, w0, L, src0, kvh, lane);
+        }
       }
       fence_proxy_async_global();
       __syncwarp();
