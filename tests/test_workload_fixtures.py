@@ -127,3 +127,34 @@ def test_prefill_workload_layout(cfg):
     assert W.attention_flops() == sum(
         int(c) * int(h) + int(c) * (int(c) + 1) // 2
         for h, c in zip(W.history, W.chunk)) * W.num_heads * 4 * W.head_dim
+
+
+def test_step_tail_fixture_writes_every_position():
+    """with_step_tail (the decode-step tests' fixture): every position below
+    each sequence's length is written, at set-up or in the step; the step
+    writes exactly the requested tails; the fresh blocks are the blocks that
+    open inside a tail; and new_token_tail recovers the layout whenever
+    every tail is non-empty."""
+    from paged_kv_cache_48_gb300 import workload as wl
+    base = wl.llama8b_gqa(small=True)
+    tails = [1, 5, 16, 17, 20, 33, 0, 40]
+    W = wl.with_step_tail(base, tails, seed=11)
+    bs = W.block_size
+    written = set(W.hist_slots.tolist()) | set(W.step_slots.tolist())
+    step = set(W.step_slots.tolist())
+    opened = set()
+    for b in range(W.batch):
+        L = int(W.seq_lens[b])
+        slot = lambda t: int(W.block_tables[b, t // bs]) * bs + t % bs
+        assert all(slot(t) in written for t in range(L))
+        n = min(tails[b], L)
+        assert {slot(t) for t in range(L - n, L)} <= step
+        opened |= {int(W.block_tables[b, j]) for j in range(-(-(L - n) // bs), (L - 1) // bs + 1)
+                   if n}
+    assert W.step_slots.size == sum(min(t, int(L)) for t, L in zip(tails, W.seq_lens))
+    assert set(W.fresh_blocks.tolist()) == opened
+    assert W.new_token_tail() is None           # sequence 6 has no new token
+    W1 = wl.with_step_tail(base, [3] * base.batch, seed=2)
+    rows, start = W1.new_token_tail()
+    assert list(start) == [3 * b for b in range(base.batch + 1)]
+    assert np.array_equal(rows, np.arange(3 * base.batch))
